@@ -1,0 +1,1 @@
+"""Float64 CPU oracle (test infrastructure only; see oracle.py)."""

@@ -1,0 +1,243 @@
+"""Float64 CPU oracle for blockwise exact attention -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this module.  The CUDA
+library never calls it, and it shares no code with the CUDA path: this file
+only marshals numpy arrays into ``oracle.c`` (plain C, float64), which holds
+all of the arithmetic and documents the definitions it follows.
+
+Inputs are contiguous BSHD arrays: ``q [B,S,Hq,d]``, ``k [B,S,Hkv,d]``,
+``v [B,S,Hkv,dv]``, ``dout [B,S,Hq,dv]``.  They may be float64, float32, or
+bfloat16 bit patterns held in ``uint16`` arrays; the C side widens every
+element exactly to double.  Outputs are float64; ``m`` and ``l`` are
+``[B,Hq,S]`` in natural-log units of ``z = scale * q.k + bias``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+_F64, _F32, _BF16 = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (gcc, OpenMP, no FMA)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+               "-ffp-contract=off", "-fno-fast-math", "-o", _LIB + ".tmp", _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("S", ctypes.c_int32), ("Hq", ctypes.c_int32),
+        ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32), ("dv", ctypes.c_int32),
+        ("scale", ctypes.c_double),
+        ("causal", ctypes.c_int32), ("window_left", ctypes.c_int32),
+        ("window_right", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
+        ("bias", ctypes.c_void_p), ("bias_strides", ctypes.c_int64 * 4),
+        ("block_idx", ctypes.c_void_p), ("sel_block", ctypes.c_int32),
+        ("top_n", ctypes.c_int32), ("local_window", ctypes.c_int32),
+    ]
+
+
+_lib = None
+
+
+def _bind(lib):
+    """Declare the argument types of every exported oracle function."""
+    P = ctypes.c_void_p
+    dp = ctypes.POINTER(_Desc)
+    i32 = ctypes.c_int32
+    lib.ora_fwd.argtypes = [dp, P, P, P, P, P, P]
+    lib.ora_bwd.argtypes = [dp, P, P, P, P, P, P, P, P, P, P]
+    lib.ora_blockwise_fwd.argtypes = [dp, P, P, P, i32, i32, i32, P, P, P]
+    lib.ora_rows.argtypes = [dp, P, P, P, P, i32, P, P, P, P, P]
+    lib.ora_keys.argtypes = [dp, P, P, P, P, i32, i32, i32, P, P, P]
+    lib.ora_select.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32, P]
+    for f in ("ora_fwd", "ora_bwd", "ora_blockwise_fwd", "ora_rows", "ora_keys",
+              "ora_select", "ora_num_threads"):
+        getattr(lib, f).restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle runs on (OMP_NUM_THREADS, else all cores)."""
+    return int(_load().ora_num_threads())
+
+
+def _in(x):
+    """Return (contiguous array, dtype code) for an input tensor."""
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float64:
+        return x, _F64
+    if x.dtype == np.float32:
+        return x, _F32
+    if x.dtype == np.uint16:
+        return x, _BF16
+    raise TypeError(f"oracle inputs must be float64, float32 or bf16 bits (uint16), got {x.dtype}")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _desc(q, k, v, *, causal, window, scale, bias, block_idx, sel_block, top_n,
+          local_window, in_dtype):
+    B, S, Hq, d = q.shape
+    Hkv, dv = k.shape[2], v.shape[3]
+    if k.shape != (B, S, Hkv, d) or v.shape != (B, S, Hkv, dv):
+        raise ValueError("q, k, v shapes disagree")
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    D = _Desc()
+    D.B, D.S, D.Hq, D.Hkv, D.d, D.dv = B, S, Hq, Hkv, d, dv
+    D.scale = float(d ** -0.5 if scale is None else scale)
+    D.causal = int(bool(causal))
+    wl, wr = (-1, -1) if window is None else window
+    D.window_left, D.window_right = int(wl), int(wr)
+    D.in_dtype = in_dtype
+    keep = []
+    if bias is not None:
+        b64 = np.asarray(bias, dtype=np.float64)
+        if b64.ndim != 4:
+            raise ValueError("bias must be 4-D [B|1, Hq|1, S|1, S|1]")
+        full = (B, Hq, S, S)
+        st = []
+        for ax, (n, want) in enumerate(zip(b64.shape, full)):
+            if n not in (1, want):
+                raise ValueError(f"bias dim {ax} must be 1 or {want}")
+        b64 = np.ascontiguousarray(b64)
+        for ax in range(4):
+            st.append(0 if b64.shape[ax] == 1 else b64.strides[ax] // 8)
+        keep.append(b64)
+        D.bias = b64.ctypes.data
+        D.bias_strides[:] = st
+    if block_idx is not None:
+        bi = np.ascontiguousarray(block_idx, dtype=np.int32)
+        if bi.shape != (B, Hq, S // sel_block, top_n):
+            raise ValueError("block_idx must be [B, Hq, S/sel_block, top_n]")
+        keep.append(bi)
+        D.block_idx = bi.ctypes.data
+        D.sel_block, D.top_n, D.local_window = sel_block, top_n, local_window
+    return D, keep
+
+
+def _check(rc, what):
+    if rc:
+        raise RuntimeError(f"oracle {what} failed with code {rc}")
+
+
+def attention_fwd(q, k, v, *, causal=False, window=None, scale=None, bias=None,
+                  block_idx=None, sel_block=32, top_n=8, local_window=32):
+    """One-shot masked softmax attention.  Returns (o, m, l) in float64."""
+    (q, dt), (k, _), (v, _) = _in(q), _in(k), _in(v)
+    D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
+                    block_idx=block_idx, sel_block=sel_block, top_n=top_n,
+                    local_window=local_window, in_dtype=dt)
+    B, S, Hq, _ = q.shape
+    o = np.zeros((B, S, Hq, v.shape[3]))
+    m = np.zeros((B, Hq, S))
+    l = np.zeros((B, Hq, S))
+    _check(_load().ora_fwd(ctypes.byref(D), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(m),
+                           _ptr(l)), "fwd")
+    return o, m, l
+
+
+def attention_bwd(q, k, v, dout, *, causal=False, window=None, scale=None, bias=None,
+                  block_idx=None, sel_block=32, top_n=8, local_window=32):
+    """Analytic gradients.  Returns (dq, dk, dv, o, m, l) in float64."""
+    (q, dt), (k, _), (v, _), (dout, _) = _in(q), _in(k), _in(v), _in(dout)
+    D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
+                    block_idx=block_idx, sel_block=sel_block, top_n=top_n,
+                    local_window=local_window, in_dtype=dt)
+    B, S, Hq, d = q.shape
+    Hkv, dv_ = k.shape[2], v.shape[3]
+    dq = np.zeros((B, S, Hq, d))
+    dk = np.zeros((B, S, Hkv, d))
+    dv = np.zeros((B, S, Hkv, dv_))
+    o = np.zeros((B, S, Hq, dv_))
+    m = np.zeros((B, Hq, S))
+    l = np.zeros((B, Hq, S))
+    _check(_load().ora_bwd(ctypes.byref(D), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq),
+                           _ptr(dk), _ptr(dv), _ptr(o), _ptr(m), _ptr(l)), "bwd")
+    return dq, dk, dv, o, m, l
+
+
+def blockwise_fwd(q, k, v, *, query_chunk, key_chunk, ring_size=1, causal=False,
+                  window=None, scale=None, bias=None):
+    """The pages' blockwise carry, step by step, in ring order.  Returns (o, m, l)."""
+    (q, dt), (k, _), (v, _) = _in(q), _in(k), _in(v)
+    D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
+                    block_idx=None, sel_block=32, top_n=8, local_window=32, in_dtype=dt)
+    B, S, Hq, _ = q.shape
+    o = np.zeros((B, S, Hq, v.shape[3]))
+    m = np.zeros((B, Hq, S))
+    l = np.zeros((B, Hq, S))
+    _check(_load().ora_blockwise_fwd(ctypes.byref(D), _ptr(q), _ptr(k), _ptr(v), query_chunk,
+                                     key_chunk, ring_size, _ptr(o), _ptr(m), _ptr(l)),
+           "blockwise_fwd")
+    return o, m, l
+
+
+def rows(q, k, v, dout, row_list, *, causal=False, window=None, scale=None, bias=None):
+    """O, m, l and dQ of the sampled (b, h, q) rows.  dout may be None (no dQ)."""
+    (q, dt), (k, _), (v, _) = _in(q), _in(k), _in(v)
+    if dout is not None:
+        dout, _ = _in(dout)
+    D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
+                    block_idx=None, sel_block=32, top_n=8, local_window=32, in_dtype=dt)
+    rl = np.ascontiguousarray(np.asarray(row_list, dtype=np.int32).reshape(-1, 3))
+    n = rl.shape[0]
+    o = np.zeros((n, v.shape[3]))
+    m = np.zeros(n)
+    l = np.zeros(n)
+    dq = np.zeros((n, q.shape[3])) if dout is not None else None
+    _check(_load().ora_rows(ctypes.byref(D), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), n,
+                            _ptr(rl), _ptr(o), _ptr(m), _ptr(l), _ptr(dq)), "rows")
+    return o, m, l, dq
+
+
+def keys(q, k, v, dout, b, g, key_list, *, causal=False, window=None, scale=None,
+         bias=None):
+    """dK and dV of the sampled keys of kv head g at batch b."""
+    (q, dt), (k, _), (v, _), (dout, _) = _in(q), _in(k), _in(v), _in(dout)
+    D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
+                    block_idx=None, sel_block=32, top_n=8, local_window=32, in_dtype=dt)
+    kl = np.ascontiguousarray(np.asarray(key_list, dtype=np.int32).reshape(-1))
+    n = kl.shape[0]
+    dk = np.zeros((n, q.shape[3]))
+    dv = np.zeros((n, v.shape[3]))
+    _check(_load().ora_keys(ctypes.byref(D), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), int(b),
+                            int(g), n, _ptr(kl), _ptr(dk), _ptr(dv)), "keys")
+    return dk, dv
+
+
+def select_blocks(q, k, *, block_size=32, top_n=8):
+    """Exact top-n earlier key blocks per query block.  q, k: [B,S,H,d] -> int32 [B,H,S/bs,top_n]."""
+    (q, dt), (k, dt2) = _in(q), _in(k)
+    if dt != dt2 or q.shape != k.shape:
+        raise ValueError("q and k must share shape and dtype")
+    B, S, H, d = q.shape
+    if block_size < 1 or S % block_size:
+        raise ValueError("S must be a multiple of block_size")
+    out = np.zeros((B, H, S // block_size, top_n), dtype=np.int32)
+    _check(_load().ora_select(_ptr(q), _ptr(k), dt, B, S, H, d, block_size, top_n, _ptr(out)),
+           "select")
+    return out

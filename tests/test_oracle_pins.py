@@ -1,0 +1,458 @@
+"""Pins of the float64 oracle against things other than itself.
+
+Every check here runs on the CPU.  The oracle (plain C) is compared with
+  * hand-derived closed forms (tests/golden/closed_form.json),
+  * an independent per-query brute-force loop written below in Python,
+  * a library softmax (scipy) in the unmasked single-query case,
+  * invariants that the attention definition implies,
+  * central finite differences of L = <dO, O> for the gradients,
+  * its own literal blockwise / ring carry, which must equal the one-shot
+    result for every chunking (the pages' own self-test claim: bpt.py,
+    __main__ compares blockwise_attn with a materialised reference).
+A plausible slip in the oracle (a dropped bias term, a wrong sign in the
+backward, a transposed GQA head map, an off-by-one window bound) fails at
+least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+from ring_attention_gb300.inputs import bf16_bits_to_f32, to_bf16_bits
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------
+# independent brute force (pure Python loops; tiny sizes only)
+# --------------------------------------------------------------------------
+def _is_allowed(i, j, causal, window, sel=None, sel_block=None, local_window=None):
+    left, right = window
+    if causal and j > i:
+        return False
+    if left >= 0 and j < i - left:
+        return False
+    if right >= 0 and j > i + right:
+        return False
+    if sel is not None:
+        local = (i - local_window < j <= i)
+        chosen = (j // sel_block) in {int(t) for t in sel if t >= 0}
+        if not (local or chosen):
+            return False
+    return True
+
+
+def brute_force(q, k, v, causal=False, window=(-1, -1), scale=None, bias=None,
+                block_idx=None, sel_block=32, local_window=32):
+    B, S, Hq, d = q.shape
+    Hkv, dv = k.shape[2], v.shape[3]
+    group = Hq // Hkv
+    scale = d ** -0.5 if scale is None else scale
+    full_bias = None if bias is None else np.broadcast_to(np.asarray(bias, np.float64), (B, Hq, S, S))
+    o = np.zeros((B, S, Hq, dv))
+    m = np.full((B, Hq, S), -np.inf)
+    l = np.zeros((B, Hq, S))
+    for b in range(B):
+        for h in range(Hq):
+            kvh = h // group
+            for i in range(S):
+                sel = None if block_idx is None else block_idx[b, h, i // sel_block]
+                keys = [j for j in range(S)
+                        if _is_allowed(i, j, causal, window, sel, sel_block, local_window)]
+                if not keys:
+                    continue
+                z = []
+                for j in keys:
+                    s = 0.0
+                    for c in range(d):
+                        s += float(q[b, i, h, c]) * float(k[b, j, kvh, c])
+                    z.append(scale * s + (0.0 if full_bias is None else float(full_bias[b, h, i, j])))
+                zmax = max(z)
+                w = [math.exp(t - zmax) for t in z]
+                tot = math.fsum(w)
+                for wj, j in zip(w, keys):
+                    o[b, i, h] += (wj / tot) * v[b, j, kvh].astype(np.float64)
+                m[b, h, i] = zmax
+                l[b, h, i] = tot
+    return o, m, l
+
+
+def rnd(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+MASKS = [
+    dict(causal=False, window=(-1, -1)),
+    dict(causal=True, window=(-1, -1)),
+    dict(causal=False, window=(0, 0)),
+    dict(causal=True, window=(3, 0)),
+    dict(causal=False, window=(2, 2)),
+    dict(causal=False, window=(-1, 1)),
+    dict(causal=False, window=(1, -1)),
+]
+
+
+@pytest.mark.parametrize("mask", MASKS, ids=lambda m: f"c{int(m['causal'])}w{m['window'][0]}_{m['window'][1]}")
+@pytest.mark.parametrize("heads", [(1, 1), (4, 2), (4, 1)])
+@pytest.mark.parametrize("bias_kind", ["none", "keys", "full", "rows"])
+def test_fwd_matches_brute_force(ora, mask, heads, bias_kind):
+    Hq, Hkv = heads
+    B, S, d, dv = 2, 9, 5, 3
+    q, k, v = rnd((B, S, Hq, d), 1), rnd((B, S, Hkv, d), 2), rnd((B, S, Hkv, dv), 3)
+    bias = {"none": None,
+            "keys": rnd((1, 1, 1, S), 4),
+            "full": rnd((B, Hq, S, S), 5),
+            "rows": rnd((B, 1, S, 1), 6)}[bias_kind]
+    o, m, l = ora.attention_fwd(q, k, v, bias=bias, scale=0.7, **mask)
+    bo, bm, bl = brute_force(q, k, v, bias=bias, scale=0.7, **mask)
+    np.testing.assert_allclose(o, bo, rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(np.isinf(m), np.isinf(bm))
+    fin = np.isfinite(bm)
+    np.testing.assert_allclose(m[fin], bm[fin], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l, bl, rtol=1e-12, atol=1e-13)
+
+
+def test_default_scale_is_inverse_sqrt_d(ora):
+    q, k, v = rnd((1, 6, 2, 16), 7), rnd((1, 6, 2, 16), 8), rnd((1, 6, 2, 16), 9)
+    o, _, _ = ora.attention_fwd(q, k, v, causal=True)
+    bo, _, _ = brute_force(q, k, v, causal=True, scale=0.25)
+    np.testing.assert_allclose(o, bo, rtol=1e-12, atol=1e-13)
+
+
+def test_row_with_no_allowed_key_is_zero(ora):
+    # window (-1, -1) with causal off but right bound -1 is unbounded; use a
+    # left window that excludes everything before q and causal + right=-1 ...
+    # the simplest empty row: block-selected mode with local_window 0 and no
+    # selected block.
+    B, S, H, d = 1, 8, 1, 4
+    q, k, v = rnd((B, S, H, d), 1), rnd((B, S, H, d), 2), rnd((B, S, H, d), 3)
+    idx = np.full((B, H, S // 4, 2), -1, dtype=np.int32)
+    o, m, l = ora.attention_fwd(q, k, v, causal=True, block_idx=idx, sel_block=4, top_n=2,
+                                local_window=0)
+    assert np.all(o == 0) and np.all(np.isneginf(m)) and np.all(l == 0)
+    dq, dk, dv, *_ = ora.attention_bwd(q, k, v, rnd((B, S, H, d), 4), causal=True, block_idx=idx,
+                                       sel_block=4, top_n=2, local_window=0)
+    assert not dq.any() and not dk.any() and not dv.any()
+
+
+def test_single_query_is_textbook_softmax(ora):
+    # one query, no mask: O = softmax(s q.K^T) V (scipy's softmax)
+    S, d = 11, 6
+    k, v = rnd((1, S, 1, d), 11), rnd((1, S, 1, d), 12)
+    q = np.zeros((1, S, 1, d))
+    q[0, 0, 0] = rnd((d,), 13)
+    o, m, l = ora.attention_fwd(q, k, v, scale=0.5)
+    z = 0.5 * (k[0, :, 0] @ q[0, 0, 0])
+    p = scipy.special.softmax(z)
+    np.testing.assert_allclose(o[0, 0, 0], p @ v[0, :, 0], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(m[0, 0, 0], z.max(), rtol=1e-14)
+    np.testing.assert_allclose(l[0, 0, 0], np.exp(z - z.max()).sum(), rtol=1e-13)
+
+
+def _golden():
+    with open(os.path.join(GOLDEN, "closed_form.json")) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("case", _golden()["cases"], ids=lambda c: c["name"])
+def test_closed_form_fixture(ora, case):
+    a = lambda x: None if x is None else np.array(x, dtype=np.float64)
+    o, m, l = ora.attention_fwd(a(case["q"]), a(case["k"]), a(case["v"]), scale=case["scale"],
+                                causal=case["causal"], window=tuple(case["window"]),
+                                bias=a(case["bias"]))
+    np.testing.assert_allclose(o, a(case["o"]), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(m, a(case["m"]), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(l, a(case["l"]), rtol=0, atol=1e-15)
+
+
+def test_closed_form_gradient_fixture(ora):
+    c = _golden()["grad_case"]
+    a = lambda x: np.array(x, dtype=np.float64)
+    dq, dk, dv, *_ = ora.attention_bwd(a(c["q"]), a(c["k"]), a(c["v"]), a(c["dout"]),
+                                       scale=c["scale"], causal=c["causal"])
+    np.testing.assert_allclose(dq, a(c["dq"]), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dk, a(c["dk"]), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dv, a(c["dv"]), rtol=0, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# the blockwise carry equals the one-shot softmax, for every chunking
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("ring", [1, 2, 4])
+@pytest.mark.parametrize("mask", [dict(causal=True, window=(-1, -1)),
+                                  dict(causal=False, window=(-1, -1)),
+                                  dict(causal=True, window=(5, 0)),
+                                  dict(causal=False, window=(3, 6))],
+                         ids=["causal", "full", "swa5", "win3_6"])
+def test_blockwise_carry_equals_one_shot(ora, ring, mask):
+    B, S, Hq, Hkv, d = 1, 16, 4, 2, 4
+    q, k, v = rnd((B, S, Hq, d), 21), rnd((B, S, Hkv, d), 22), rnd((B, S, Hkv, d), 23)
+    bias = rnd((1, 1, 1, S), 24)
+    ref = ora.attention_fwd(q, k, v, bias=bias, **mask)
+    blk = S // ring
+    chunks = [c for c in range(1, blk + 1) if blk % c == 0]
+    for qc, kc in itertools.product(chunks, chunks):
+        got = ora.blockwise_fwd(q, k, v, query_chunk=qc, key_chunk=kc, ring_size=ring, bias=bias,
+                                **mask)
+        for g, r in zip(got, ref):
+            np.testing.assert_allclose(g, r, rtol=1e-12, atol=1e-12, err_msg=f"qc={qc} kc={kc}")
+
+
+def test_blockwise_padding_bias_tail(ora):
+    # the long-context recipe at toy size: bias -1e9 on the last keys, ring of 4
+    B, S, Hq, Hkv, d = 1, 32, 4, 2, 8
+    q, k, v = rnd((B, S, Hq, d), 31), rnd((B, S, Hkv, d), 32), rnd((B, S, Hkv, d), 33)
+    bias = np.zeros((1, 1, 1, S))
+    bias[..., -4:] = -1e9
+    ref = ora.attention_fwd(q, k, v, causal=True, bias=bias)
+    got = ora.blockwise_fwd(q, k, v, query_chunk=2, key_chunk=4, ring_size=4, causal=True,
+                            bias=bias)
+    for g, r in zip(got, ref):
+        np.testing.assert_allclose(g, r, rtol=1e-12, atol=1e-12)
+    # padded keys carry exactly zero weight for rows that also see real keys
+    o2, _, _ = ora.attention_fwd(q[:, :S - 4], k[:, :S - 4], v[:, :S - 4], causal=True)
+    np.testing.assert_allclose(ref[0][:, :S - 4], o2, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# invariants of the definition
+# --------------------------------------------------------------------------
+def test_constant_value_rows(ora):
+    B, S, Hq, Hkv, d = 2, 12, 4, 2, 6
+    q, k = rnd((B, S, Hq, d), 41), rnd((B, S, Hkv, d), 42)
+    c = rnd((B, 1, Hkv, d), 43)
+    v = np.broadcast_to(c, (B, S, Hkv, d)).copy()
+    o, _, _ = ora.attention_fwd(q, k, v, causal=True, window=(4, 0), bias=rnd((B, Hq, S, S), 44))
+    exp = np.repeat(np.broadcast_to(c, (B, S, Hkv, d)), Hq // Hkv, axis=2)
+    np.testing.assert_allclose(o, exp, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("window", [(3, 0), (2, 2), (-1, -1)])
+def test_uniform_scores_give_window_mean(ora, window):
+    B, S, Hq, Hkv, d = 1, 10, 2, 1, 3
+    q = np.zeros((B, S, Hq, d))
+    k, v = rnd((B, S, Hkv, d), 51), rnd((B, S, Hkv, d), 52)
+    o, _, l = ora.attention_fwd(q, k, v, causal=window[1] == 0, window=window)
+    for i in range(S):
+        lo = 0 if window[0] < 0 else max(0, i - window[0])
+        hi = S - 1 if window[1] < 0 else min(S - 1, i + window[1])
+        if window[1] == 0:
+            hi = min(hi, i)
+        mean = v[0, lo:hi + 1, 0].mean(axis=0)
+        for h in range(Hq):
+            np.testing.assert_allclose(o[0, i, h], mean, rtol=1e-12, atol=1e-13)
+            assert l[0, h, i] == pytest.approx(hi - lo + 1, rel=1e-15)
+
+
+def test_window_00_is_identity_and_gradients(ora):
+    B, S, Hq, Hkv, d = 2, 7, 4, 2, 5
+    q, k, v, do = (rnd((B, S, Hq, d), 61), rnd((B, S, Hkv, d), 62), rnd((B, S, Hkv, d), 63),
+                   rnd((B, S, Hq, d), 64))
+    o, _, l = ora.attention_fwd(q, k, v, window=(0, 0))
+    np.testing.assert_allclose(o, np.repeat(v, 2, axis=2), rtol=0, atol=1e-15)
+    assert np.all(l == 1.0)
+    dq, dk, dv, *_ = ora.attention_bwd(q, k, v, do, window=(0, 0))
+    assert np.abs(dq).max() < 1e-14 and np.abs(dk).max() < 1e-14
+    np.testing.assert_allclose(dv, do.reshape(B, S, Hkv, 2, d).sum(axis=3), rtol=1e-14, atol=1e-14)
+
+
+def test_key_gradients_sum_to_zero(ora):
+    # sum_k P = 1  =>  each row of dS sums to 0  =>  sum_k dK_k = 0 per kv head
+    B, S, Hq, Hkv, d = 2, 13, 4, 2, 6
+    q, k, v, do = (rnd((B, S, Hq, d), 71), rnd((B, S, Hkv, d), 72), rnd((B, S, Hkv, d), 73),
+                   rnd((B, S, Hq, d), 74))
+    for mask in MASKS:
+        _, dk, _, *_ = ora.attention_bwd(q, k, v, do, bias=rnd((1, Hq, S, S), 75), **mask)
+        np.testing.assert_allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+
+
+def test_shift_invariances(ora):
+    B, S, Hq, Hkv, d = 1, 11, 2, 2, 4
+    q, k, v = rnd((B, S, Hq, d), 81), rnd((B, S, Hkv, d), 82), rnd((B, S, Hkv, d), 83)
+    base = ora.attention_fwd(q, k, v, causal=True, window=(5, 0))[0]
+    shifted_k = ora.attention_fwd(q, k + rnd((1, 1, Hkv, d), 84), v, causal=True, window=(5, 0))[0]
+    np.testing.assert_allclose(shifted_k, base, rtol=1e-12, atol=1e-12)
+    row_bias = np.broadcast_to(rnd((B, Hq, S, 1), 85), (B, Hq, S, S))
+    biased = ora.attention_fwd(q, k, v, causal=True, window=(5, 0), bias=row_bias)[0]
+    np.testing.assert_allclose(biased, base, rtol=1e-12, atol=1e-12)
+
+
+def test_gqa_equals_repeated_heads(ora):
+    # GQA reads kv head h // (Hq/Hkv): same as repeating each kv head G times
+    B, S, Hq, Hkv, d = 1, 9, 6, 2, 4
+    q, k, v, do = (rnd((B, S, Hq, d), 91), rnd((B, S, Hkv, d), 92), rnd((B, S, Hkv, d), 93),
+                   rnd((B, S, Hq, d), 94))
+    rk, rv = np.repeat(k, 3, axis=2), np.repeat(v, 3, axis=2)
+    a = ora.attention_bwd(q, k, v, do, causal=True)
+    r = ora.attention_bwd(q, rk, rv, do, causal=True)
+    np.testing.assert_allclose(a[0], r[0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(a[1], r[1].reshape(B, S, Hkv, 3, d).sum(3), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(a[2], r[2].reshape(B, S, Hkv, 3, d).sum(3), rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# gradients: central finite differences of L = <dO, O>
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("cfg", [
+    dict(causal=True, window=(-1, -1), bias=False),
+    dict(causal=True, window=(3, 0), bias=True),
+    dict(causal=False, window=(2, 1), bias=True),
+    dict(causal=False, window=(-1, -1), bias=False),
+], ids=["causal", "swa3_bias", "win2_1_bias", "full"])
+def test_gradients_match_finite_differences(ora, cfg):
+    B, S, Hq, Hkv, d, dv = 1, 8, 4, 2, 3, 2
+    q, k, v, do = (rnd((B, S, Hq, d), 101), rnd((B, S, Hkv, d), 102), rnd((B, S, Hkv, dv), 103),
+                   rnd((B, S, Hq, dv), 104))
+    bias = rnd((B, Hq, S, S), 105) if cfg["bias"] else None
+    kw = dict(causal=cfg["causal"], window=cfg["window"], bias=bias, scale=0.8)
+    dq, dk, dvv, *_ = ora.attention_bwd(q, k, v, do, **kw)
+    h = 1e-6
+
+    def loss(qq, kk, vv):
+        return float((ora.attention_fwd(qq, kk, vv, **kw)[0] * do).sum())
+
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dvv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        err = np.abs(fd - g).max() / max(np.abs(g).max(), 1e-30)
+        assert err < 1e-6, f"d{name}: relative error {err}"
+
+
+# --------------------------------------------------------------------------
+# sampled rows / keys agree with the full evaluation
+# --------------------------------------------------------------------------
+def test_sampled_rows_and_keys_match_full(ora):
+    B, S, Hq, Hkv, d = 2, 20, 4, 2, 5
+    q, k, v, do = (rnd((B, S, Hq, d), 111), rnd((B, S, Hkv, d), 112), rnd((B, S, Hkv, d), 113),
+                   rnd((B, S, Hq, d), 114))
+    bias = rnd((1, 1, 1, S), 115)
+    dq, dk, dv, o, m, l = ora.attention_bwd(q, k, v, do, causal=True, bias=bias)
+    rows = [(0, 0, 0), (1, 3, 19), (0, 2, 7), (1, 1, 12)]
+    ro, rm, rl, rdq = ora.rows(q, k, v, do, rows, causal=True, bias=bias)
+    for t, (b, h, s) in enumerate(rows):
+        np.testing.assert_allclose(ro[t], o[b, s, h], rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(rdq[t], dq[b, s, h], rtol=1e-12, atol=1e-13)
+        assert rm[t] == pytest.approx(m[b, h, s], rel=1e-14)
+        assert rl[t] == pytest.approx(l[b, h, s], rel=1e-13)
+    keys = [0, 5, 19, 11]
+    kdk, kdv = ora.keys(q, k, v, do, 1, 1, keys, causal=True, bias=bias)
+    np.testing.assert_allclose(kdk, dk[1, keys, 1], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(kdv, dv[1, keys, 1], rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# block selection (AnnAttention, select_block) and block-selected attention
+# --------------------------------------------------------------------------
+def brute_select(q, k, block_size, top_n):
+    B, S, H, d = q.shape
+    nblk = S // block_size
+    out = np.full((B, H, nblk, top_n), -1, dtype=np.int32)
+    for b in range(B):
+        for h in range(H):
+            qs, ks = [], []
+            for i in range(nblk):
+                sq, sk = [0.0] * d, [0.0] * d
+                for r in range(block_size):
+                    for c in range(d):
+                        sq[c] += float(q[b, i * block_size + r, h, c])
+                        sk[c] += float(k[b, i * block_size + r, h, c])
+                qs.append(sq)
+                ks.append(sk)
+            for i in range(nblk):
+                scored = []
+                for j in range(i):
+                    s = 0.0
+                    for c in range(d):
+                        s += qs[i][c] * ks[j][c]
+                    scored.append((-s, j))
+                best = sorted(j for _, j in sorted(scored)[:top_n])
+                out[b, h, i, :len(best)] = best
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["f64", "bf16"])
+def test_select_matches_full_sort(ora, dtype):
+    B, S, H, d, bs, n = 2, 64, 2, 8, 4, 3
+    q, k = rnd((B, S, H, d), 121), rnd((B, S, H, d), 122)
+    if dtype == "bf16":
+        qb, kb = to_bf16_bits(q.astype(np.float32)), to_bf16_bits(k.astype(np.float32))
+        got = ora.select_blocks(qb, kb, block_size=bs, top_n=n)
+        exp = brute_select(bf16_bits_to_f32(qb), bf16_bits_to_f32(kb), bs, n)
+    else:
+        got = ora.select_blocks(q, k, block_size=bs, top_n=n)
+        exp = brute_select(q, k, bs, n)
+    np.testing.assert_array_equal(got, exp)
+
+
+def _planted(alpha, bs, d):
+    # first row of every query block = u, of key block j = alpha_j * u; others 0
+    nblk = len(alpha)
+    u = np.array([1.0, 2.0, -1.0, 0.5][:d])
+    q = np.zeros((1, nblk * bs, 1, d))
+    k = np.zeros((1, nblk * bs, 1, d))
+    for j in range(nblk):
+        q[0, j * bs, 0] = u
+        k[0, j * bs, 0] = alpha[j] * u
+    return q, k
+
+
+def test_select_planted_ranking(ora):
+    alpha = [3.0, -1.0, 7.0, 2.0, 5.0, 0.5, 6.0, 4.0, 1.0, -2.0]
+    q, k = _planted(alpha, 4, 4)
+    got = ora.select_blocks(q, k, block_size=4, top_n=3)[0, 0]
+    for i in range(len(alpha)):
+        ranked = sorted(range(i), key=lambda j: -alpha[j])[:3]
+        exp = sorted(ranked) + [-1] * (3 - len(ranked))
+        assert list(got[i]) == exp, f"block {i}"
+
+
+def test_select_ties_keep_lower_block(ora):
+    alpha = [5.0, 3.0, 5.0, 3.0, 5.0, 1.0, 3.0, 0.0]
+    q, k = _planted(alpha, 2, 4)
+    got = ora.select_blocks(q, k, block_size=2, top_n=2)[0, 0]
+    assert list(got[5]) == [0, 2]          # three 5s tie: blocks 0 and 2 win
+    assert list(got[7]) == [0, 2]
+    got4 = ora.select_blocks(q, k, block_size=2, top_n=4)[0, 0]
+    assert list(got4[7]) == [0, 1, 2, 4]   # 5, 5, 5 then the lowest of the 3s
+
+
+def test_select_fewer_candidates_than_top_n(ora):
+    q, k = rnd((1, 24, 1, 4), 131), rnd((1, 24, 1, 4), 132)
+    got = ora.select_blocks(q, k, block_size=4, top_n=8)[0, 0]
+    for i in range(6):
+        assert list(got[i]) == list(range(i)) + [-1] * (8 - i)
+
+
+def test_block_selected_attention_matches_brute_force(ora):
+    B, S, H, d, bs, n, W = 1, 32, 2, 4, 4, 2, 4
+    q, k, v = rnd((B, S, H, d), 141), rnd((B, S, H, d), 142), rnd((B, S, H, d), 143)
+    idx = ora.select_blocks(q, k, block_size=bs, top_n=n)
+    o, m, l = ora.attention_fwd(q, k, v, causal=True, block_idx=idx, sel_block=bs, top_n=n,
+                                local_window=W)
+    bo, bm, bl = brute_force(q, k, v, causal=True, block_idx=idx, sel_block=bs, local_window=W)
+    np.testing.assert_allclose(o, bo, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l, bl, rtol=1e-12, atol=1e-13)
+    # the union counts a key once: a selected block that overlaps the local
+    # window must not double its weight (block i-1 is usually both)
+    assert np.all(l <= W + n * bs)
+
+
+# --------------------------------------------------------------------------
+# the seeded input encoding
+# --------------------------------------------------------------------------
+def test_bf16_round_to_nearest_even():
+    x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 2 ** -7 + 2 ** -9, -2.5,
+                  1.0 + 2 ** -8 + 2 ** -20], dtype=np.float32)
+    got = bf16_bits_to_f32(to_bf16_bits(x))
+    exp = np.array([1.0, 1.0, 1.0 + 2 ** -6, 1.0 + 2 ** -7, -2.5, 1.0 + 2 ** -7], dtype=np.float32)
+    np.testing.assert_array_equal(got, exp)
