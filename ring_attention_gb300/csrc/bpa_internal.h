@@ -1,0 +1,87 @@
+// bpa_internal.h - validated problem description and kernel launchers of libbpa.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "bpa.h"
+
+namespace bpa {
+
+// A validated attention problem (scale resolved, ring geometry derived).
+struct Problem {
+    int B, S, Hq, Hkv, G, d;
+    int dtype;                 // bpa_dtype
+    float scale;
+    int causal, wl, wr;        // window bounds, -1 = unbounded
+    const void* q;
+    const void* k;
+    const void* v;
+    int64_t qs[3], ks[3], vs[3];
+    const float* bias;
+    int64_t bs[4];
+    int ring_n, ring_blk;      // ring_blk = S / ring_n
+    const int32_t* block_idx;
+    int sel_block, top_n, local_window;
+};
+
+struct FwdArgs {
+    Problem P;
+    void* o;            // output (one-shot) - unused by ring steps
+    float* m;           // [B, Hq, S]
+    float* l;           // [B, Hq, S]
+    float* acc;         // ring carry [B, S, Hq, d] float32, or nullptr (one-shot)
+    int ring_idx;       // ring step run by this launch
+    uint32_t* status;   // device status word
+};
+
+struct BwdArgs {
+    Problem P;
+    const void* o;
+    const void* dout;
+    const float* m;
+    const float* l;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* Dvec;        // [B, Hq, Spad] rowsum(dO * O); padding rows hold 0
+    float* lse;         // [B, Hq, Spad] m + log(l) (natural log); +inf on padding / empty rows
+    int Spad;           // S rounded up to 64
+    float* dq_acc;      // [B, S, Hq, d] float32
+    float* dk_acc;      // ring carries [B, S, Hkv, d] float32, or nullptr
+    float* dv_acc;
+    int ring_idx;
+    uint32_t* status;
+};
+
+struct SelectArgs {
+    const void* q;
+    const void* k;
+    int dtype, B, S, H, d;
+    int64_t qs[3], ks[3];
+    int block, top_n;
+    int32_t* out;
+    double* qsum;       // [B, H, nblk, d]
+    double* ksum;
+    uint32_t* status;
+};
+
+// ---- launchers (return the launch error, if any) --------------------------
+cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s);
+cudaError_t launch_bwd_tc(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s);
+cudaError_t launch_gather_fwd(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_ring_init(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_ring_finalize(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
+
+bool fwd_tc_supported(const Problem& P);
+bool bwd_tc_supported(const Problem& P);
+bool gather_supported(const Problem& P);
+
+}  // namespace bpa

@@ -1,0 +1,383 @@
+// simt.cu - CUDA-core attention kernels (float32 path, and any head dim up to 256).
+//
+// The float32 workload needs these: tensor-core tf32 products cannot meet a
+// 1e-5 max-abs bound, so the fp32 path keeps every product and sum in fp32 FMA.
+// They also serve bf16 problems whose head dim the tensor-core kernels do not
+// take.  One warp owns one query row (forward, dQ) or one key row (dK/dV) and
+// walks the allowed keys (queries) 32 at a time, one per lane, folding them
+// into the running (max, numerator, denominator) carry of "bpt.py",
+// _blockwise_attention_fwd / scan_kv_block.
+#include <math.h>
+
+#include "bpa_internal.h"
+#include "common.cuh"
+
+namespace bpa {
+namespace {
+
+constexpr int kMaxD = 256;
+constexpr int kRows = 16;   // rows per CTA
+constexpr int kWarps = 4;   // warps per CTA
+constexpr int kPer = kMaxD / 32;
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T* p);
+template <>
+__device__ __forceinline__ float ldf<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return __bfloat162float(*p);
+}
+template <typename T>
+__device__ __forceinline__ void stf(T* p, float v);
+template <>
+__device__ __forceinline__ void stf<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void stf<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+    *p = __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Keys of the ring super-block query q meets at step `idx` (whole sequence
+// when the problem has no ring or the launch is not a ring step).
+__device__ __forceinline__ void ring_range(const Problem& P, bool ring, int idx, int q, int& lo,
+                                           int& hi) {
+    if (!ring) {
+        lo = 0;
+        hi = P.S - 1;
+        return;
+    }
+    int i = q / P.ring_blk;
+    int j = ((i - idx) % P.ring_n + P.ring_n) % P.ring_n;
+    lo = j * P.ring_blk;
+    hi = lo + P.ring_blk - 1;
+}
+
+__device__ __forceinline__ bool selected(const Problem& P, int b, int h, int q, int kb) {
+    const int nblk = P.S / P.sel_block;
+    const int32_t* sel = P.block_idx + ((static_cast<int64_t>(b) * P.Hq + h) * nblk + q / P.sel_block) * P.top_n;
+    for (int t = 0; t < P.top_n; ++t)
+        if (sel[t] == kb) return true;
+    return false;
+}
+
+__device__ __forceinline__ bool allowed(const Problem& P, int b, int h, int q, int k) {
+    if (P.causal && k > q) return false;
+    if (P.wl >= 0 && k < q - P.wl) return false;
+    if (P.wr >= 0 && k > q + P.wr) return false;
+    if (P.block_idx) {
+        bool local = k <= q && k > q - P.local_window;
+        if (!local && !selected(P, b, h, q, k / P.sel_block)) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ float bias_at(const Problem& P, int b, int h, int q, int k) {
+    if (!P.bias) return 0.f;
+    return P.bias[b * P.bs[0] + h * P.bs[1] + q * P.bs[2] + k * P.bs[3]];
+}
+
+// Forward state of one query row, spread over the warp (lane owns dims lane + 32 i).
+struct RowState {
+    float m, l;
+    float acc[kPer];
+};
+
+template <typename T>
+__device__ void fold_keys(const Problem& P, int b, int h, int g, int q, int klo, int khi,
+                          const float* sq, RowState& st) {
+    const int lane = threadIdx.x & 31;
+    const T* K = static_cast<const T*>(P.k);
+    const T* V = static_cast<const T*>(P.v);
+    for (int k0 = klo; k0 <= khi; k0 += 32) {
+        const int k = k0 + lane;
+        const bool ok = k <= khi && allowed(P, b, h, q, k);
+        float s = -INFINITY;
+        if (ok) {
+            const T* kr = K + b * P.ks[0] + static_cast<int64_t>(k) * P.ks[1] + g * P.ks[2];
+            float dot = 0.f;
+            for (int c = 0; c < P.d; ++c) dot = fmaf(sq[c], ldf(kr + c), dot);
+            s = dot * P.scale + bias_at(P, b, h, q, k);
+        }
+        const float cmax = warp_max(s);
+        const float mnew = fmaxf(st.m, cmax);
+        if (mnew == -INFINITY) continue;  // warp-uniform: nothing allowed yet
+        const float corr = st.m == -INFINITY ? 0.f : expf(st.m - mnew);
+        const float p = ok ? expf(s - mnew) : 0.f;
+        st.l = st.l * corr + warp_sum(p);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) st.acc[i] *= corr;
+        for (int t = 0; t < 32; ++t) {
+            const float pt = __shfl_sync(0xffffffffu, p, t);
+            if (pt == 0.f) continue;  // warp-uniform
+            const T* vr = V + b * P.vs[0] + static_cast<int64_t>(k0 + t) * P.vs[1] + g * P.vs[2];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int c = lane + 32 * i;
+                if (c < P.d) st.acc[i] = fmaf(pt, ldf(vr + c), st.acc[i]);
+            }
+        }
+        st.m = mnew;
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
+    const Problem& P = a.P;
+    const int b = blockIdx.z, h = blockIdx.y, g = h / P.G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ float sq[kWarps][kMaxD];
+    const T* Q = static_cast<const T*>(P.q);
+    const bool ring = a.acc != nullptr;
+    for (int r = warp; r < kRows; r += kWarps) {
+        const int q = blockIdx.x * kRows + r;
+        if (q >= P.S) break;
+        for (int c = lane; c < P.d; c += 32)
+            sq[warp][c] = ldf(Q + b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2] + c);
+        __syncwarp();
+        int lo, hi;
+        ring_range(P, ring, a.ring_idx, q, lo, hi);
+        if (P.causal) hi = min(hi, q);
+        if (P.wr >= 0) hi = min(hi, q + P.wr);
+        if (P.wl >= 0) lo = max(lo, q - P.wl);
+        RowState st;
+        st.m = -INFINITY;
+        st.l = 0.f;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) st.acc[i] = 0.f;
+        if (lo <= hi) {
+            if (!P.block_idx) {
+                fold_keys<T>(P, b, h, g, q, lo, hi, sq[warp], st);
+            } else {
+                // visit each key block once: selected blocks and the blocks of
+                // the local window, in ascending order (a set union)
+                for (int kb = lo / P.sel_block; kb <= hi / P.sel_block; ++kb) {
+                    const int k0 = max(lo, kb * P.sel_block);
+                    const int k1 = min(hi, kb * P.sel_block + P.sel_block - 1);
+                    const bool local = k1 > q - P.local_window && k0 <= q;
+                    if (!local && !selected(P, b, h, q, kb)) continue;
+                    fold_keys<T>(P, b, h, g, q, k0, k1, sq[warp], st);
+                }
+            }
+        }
+        const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * P.S + q;
+        if (!ring) {
+            const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
+            T* O = static_cast<T*>(a.o) + b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int c = lane + 32 * i;
+                if (c < P.d) stf(O + c, st.acc[i] * inv);
+            }
+            if (lane == 0) {
+                a.m[mi] = st.m;
+                a.l[mi] = st.l;
+            }
+        } else {
+            // merge this step's (m, l, numerator) into the carry
+            const float mc = a.m[mi], lc = a.l[mi];
+            const float mn = fmaxf(mc, st.m);
+            if (mn != -INFINITY) {
+                const float fa = mc == -INFINITY ? 0.f : expf(mc - mn);
+                const float fb = st.m == -INFINITY ? 0.f : expf(st.m - mn);
+                float* C = a.acc + ((static_cast<int64_t>(b) * P.S + q) * P.Hq + h) * P.d;
+#pragma unroll
+                for (int i = 0; i < kPer; ++i) {
+                    const int c = lane + 32 * i;
+                    if (c < P.d) C[c] = C[c] * fa + st.acc[i] * fb;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    a.m[mi] = mn;
+                    a.l[mi] = lc * fa + st.l * fb;
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// dQ of one query row per warp:  dQ = scale * sum_k P (dP - D) K_k
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
+    const Problem& P = a.P;
+    const int b = blockIdx.z, h = blockIdx.y, g = h / P.G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ float sq[kWarps][kMaxD];
+    __shared__ float sdo[kWarps][kMaxD];
+    const T* Q = static_cast<const T*>(P.q);
+    const T* K = static_cast<const T*>(P.k);
+    const T* V = static_cast<const T*>(P.v);
+    const T* dO = static_cast<const T*>(a.dout);
+    for (int r = warp; r < kRows; r += kWarps) {
+        const int q = blockIdx.x * kRows + r;
+        if (q >= P.S) break;
+        const int64_t qoff = b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2];
+        for (int c = lane; c < P.d; c += 32) {
+            sq[warp][c] = ldf(Q + qoff + c);
+            sdo[warp][c] = ldf(dO + qoff + c);
+        }
+        __syncwarp();
+        const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * a.Spad + q;
+        const float lse = a.lse[mi], Dq = a.Dvec[mi];
+        float acc[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+        int lo = 0, hi = P.S - 1;
+        if (P.causal) hi = min(hi, q);
+        if (P.wr >= 0) hi = min(hi, q + P.wr);
+        if (P.wl >= 0) lo = max(lo, q - P.wl);
+        if (lse != INFINITY) {
+            for (int k0 = lo; k0 <= hi; k0 += 32) {
+                const int k = k0 + lane;
+                float dS = 0.f;
+                if (k <= hi && allowed(P, b, h, q, k)) {
+                    const T* kr = K + b * P.ks[0] + static_cast<int64_t>(k) * P.ks[1] + g * P.ks[2];
+                    const T* vr = V + b * P.vs[0] + static_cast<int64_t>(k) * P.vs[1] + g * P.vs[2];
+                    float dot = 0.f, dp = 0.f;
+                    for (int c = 0; c < P.d; ++c) {
+                        dot = fmaf(sq[warp][c], ldf(kr + c), dot);
+                        dp = fmaf(sdo[warp][c], ldf(vr + c), dp);
+                    }
+                    const float z = dot * P.scale + bias_at(P, b, h, q, k);
+                    dS = expf(z - lse) * (dp - Dq);
+                }
+                for (int t = 0; t < 32; ++t) {
+                    const float st = __shfl_sync(0xffffffffu, dS, t);
+                    if (st == 0.f) continue;
+                    const T* kr = K + b * P.ks[0] + static_cast<int64_t>(k0 + t) * P.ks[1] + g * P.ks[2];
+#pragma unroll
+                    for (int i = 0; i < kPer; ++i) {
+                        const int c = lane + 32 * i;
+                        if (c < P.d) acc[i] = fmaf(st, ldf(kr + c), acc[i]);
+                    }
+                }
+            }
+        }
+        T* dQ = static_cast<T*>(a.dq) + qoff;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int c = lane + 32 * i;
+            if (c < P.d) stf(dQ + c, acc[i] * P.scale);
+        }
+        __syncwarp();
+    }
+}
+
+// dK, dV of one key row per warp, summed over the q heads of its group:
+//   dK = scale * sum_q dS Q_q,   dV = sum_q P dO_q
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) {
+    const Problem& P = a.P;
+    const int b = blockIdx.z, g = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ float sk[kWarps][kMaxD];
+    __shared__ float sv[kWarps][kMaxD];
+    const T* Q = static_cast<const T*>(P.q);
+    const T* K = static_cast<const T*>(P.k);
+    const T* V = static_cast<const T*>(P.v);
+    const T* dO = static_cast<const T*>(a.dout);
+    for (int r = warp; r < kRows; r += kWarps) {
+        const int k = blockIdx.x * kRows + r;
+        if (k >= P.S) break;
+        const int64_t koff = b * P.ks[0] + static_cast<int64_t>(k) * P.ks[1] + g * P.ks[2];
+        const int64_t voff = b * P.vs[0] + static_cast<int64_t>(k) * P.vs[1] + g * P.vs[2];
+        for (int c = lane; c < P.d; c += 32) {
+            sk[warp][c] = ldf(K + koff + c);
+            sv[warp][c] = ldf(V + voff + c);
+        }
+        __syncwarp();
+        float dk[kPer], dv[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) dk[i] = dv[i] = 0.f;
+        int lo = 0, hi = P.S - 1;  // queries that may see key k
+        if (P.causal) lo = max(lo, k);
+        if (P.wr >= 0) lo = max(lo, k - P.wr);
+        if (P.wl >= 0) hi = min(hi, k + P.wl);
+        for (int h = g * P.G; h < (g + 1) * P.G; ++h) {
+            for (int q0 = lo; q0 <= hi; q0 += 32) {
+                const int q = q0 + lane;
+                float p = 0.f, dS = 0.f;
+                if (q <= hi && allowed(P, b, h, q, k)) {
+                    const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * a.Spad + q;
+                    const float lse = a.lse[mi];
+                    if (lse != INFINITY) {
+                        const int64_t qoff = b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2];
+                        float dot = 0.f, dp = 0.f;
+                        for (int c = 0; c < P.d; ++c) {
+                            dot = fmaf(ldf(Q + qoff + c), sk[warp][c], dot);
+                            dp = fmaf(ldf(dO + qoff + c), sv[warp][c], dp);
+                        }
+                        const float z = dot * P.scale + bias_at(P, b, h, q, k);
+                        p = expf(z - lse);
+                        dS = p * (dp - a.Dvec[mi]);
+                    }
+                }
+                for (int t = 0; t < 32; ++t) {
+                    const float pt = __shfl_sync(0xffffffffu, p, t);
+                    const float st = __shfl_sync(0xffffffffu, dS, t);
+                    if (pt == 0.f && st == 0.f) continue;
+                    const int64_t qoff =
+                        b * P.qs[0] + static_cast<int64_t>(q0 + t) * P.qs[1] + h * P.qs[2];
+#pragma unroll
+                    for (int i = 0; i < kPer; ++i) {
+                        const int c = lane + 32 * i;
+                        if (c < P.d) {
+                            dk[i] = fmaf(st, ldf(Q + qoff + c), dk[i]);
+                            dv[i] = fmaf(pt, ldf(dO + qoff + c), dv[i]);
+                        }
+                    }
+                }
+            }
+        }
+        T* dK = static_cast<T*>(a.dk) + koff;
+        T* dV = static_cast<T*>(a.dv) + voff;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int c = lane + 32 * i;
+            if (c < P.d) {
+                stf(dK + c, dk[i] * P.scale);
+                stf(dV + c, dv[i]);
+            }
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s) {
+    const Problem& P = a.P;
+    dim3 grid((P.S + kRows - 1) / kRows, P.Hq, P.B);
+    if (P.dtype == BPA_FP32)
+        k_fwd_simt<float><<<grid, kWarps * 32, 0, s>>>(a);
+    else
+        k_fwd_simt<__nv_bfloat16><<<grid, kWarps * 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s) {
+    const Problem& P = a.P;
+    dim3 gq((P.S + kRows - 1) / kRows, P.Hq, P.B);
+    dim3 gk((P.S + kRows - 1) / kRows, P.Hkv, P.B);
+    if (P.dtype == BPA_FP32) {
+        k_bwd_dq_simt<float><<<gq, kWarps * 32, 0, s>>>(a);
+        k_bwd_dkdv_simt<float><<<gk, kWarps * 32, 0, s>>>(a);
+    } else {
+        k_bwd_dq_simt<__nv_bfloat16><<<gq, kWarps * 32, 0, s>>>(a);
+        k_bwd_dkdv_simt<__nv_bfloat16><<<gk, kWarps * 32, 0, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace bpa

@@ -1,0 +1,145 @@
+"""The C-ABI library builds, loads and exports what include/bpa.h declares.
+
+Runs without a GPU: only host-side argument validation is exercised (every
+call here fails its checks before anything touches the device).
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bpa.h")
+
+
+@pytest.fixture(scope="module")
+def bpa():
+    from ring_attention_gb300 import build
+    build.build()
+    from ring_attention_gb300 import bpa as mod
+    return mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bpa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("bpa_fwd", "bpa_bwd", "bpa_select_blocks", "bpa_workspace_size", "bpa_check"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(bpa):
+    L = bpa.lib()
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, f"not exported: {missing}"
+    out = subprocess.run(["nm", "-D", "--defined-only", bpa.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (bpa_\w+)", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_descriptor_layout_matches_c(tmp_path, bpa):
+    # compile a host-only probe of the header and compare sizeof / offsetof
+    fields = [f[0] for f in bpa.bpa_attn_desc._fields_]
+    src = tmp_path / "probe.c"
+    body = "\n".join(f'printf("{f} %zu\\n", offsetof(bpa_attn_desc, {f}));' for f in fields)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "bpa.h"\nint main(void){\n'
+                   'printf("size %zu\\n", sizeof(bpa_attn_desc));\n' + body + "\nreturn 0;}\n")
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-o", str(exe), str(src)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                         check=True).stdout.splitlines())
+    assert int(got["size"]) == ctypes.sizeof(bpa.bpa_attn_desc)
+    for f in fields:
+        assert int(got[f]) == getattr(bpa.bpa_attn_desc, f).offset, f
+
+
+def _desc(bpa, **over):
+    D = bpa.bpa_attn_desc()
+    D.struct_size = ctypes.sizeof(bpa.bpa_attn_desc)
+    D.dtype = bpa.BPA_BF16
+    D.B, D.S, D.Hq, D.Hkv, D.d = 2, 256, 8, 2, 128
+    D.q, D.k, D.v = 0x10000, 0x20000, 0x30000    # never dereferenced by host checks
+    D.q_strides[:] = (256 * 8 * 128, 8 * 128, 128)
+    D.k_strides[:] = (256 * 2 * 128, 2 * 128, 128)
+    D.v_strides[:] = (256 * 2 * 128, 2 * 128, 128)
+    D.window_left = D.window_right = -1
+    D.ring_size = 1
+    for k, v in over.items():
+        setattr(D, k, v)
+    return D
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(struct_size=8), 1),
+    (dict(dtype=7), 1),
+    (dict(Hq=6, Hkv=4), 1),
+    (dict(d=512), 2),
+    (dict(S=0), 1),
+    (dict(q=0), 1),
+    (dict(window_left=-2), 1),
+    (dict(ring_size=3), 1),
+    (dict(ring_size=2, query_chunk=100), 1),
+    (dict(ring_size=2, ring_step_begin=2, ring_step_end=2), 1),
+])
+def test_forward_rejects_bad_arguments(bpa, over, status):
+    D = _desc(bpa, **over)
+    st = bpa.lib().bpa_fwd(ctypes.byref(D), 0x40000, 0x50000, 0x60000, 0x70000, 1 << 20, None)
+    assert st == status, bpa.lib().bpa_last_error().decode()
+    assert bpa.lib().bpa_last_error().decode() != ""
+
+
+def test_workspace_is_checked_before_launch(bpa):
+    D = _desc(bpa)
+    L = bpa.lib()
+    need = L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D))
+    assert need >= 256 and need % 256 == 0
+    assert L.bpa_fwd(ctypes.byref(D), 0x40000, 0x50000, 0x60000, None, need, None) == bpa.BPA_ERR_WORKSPACE
+    assert L.bpa_fwd(ctypes.byref(D), 0x40000, 0x50000, 0x60000, 0x70010, need, None) == bpa.BPA_ERR_WORKSPACE
+    assert L.bpa_fwd(ctypes.byref(D), 0x40000, 0x50000, 0x60000, 0x70000, need - 1, None) == bpa.BPA_ERR_WORKSPACE
+
+
+def test_workspace_sizes(bpa):
+    L = bpa.lib()
+    D = _desc(bpa)
+    assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) == 256
+    D2 = _desc(bpa, ring_size=4)
+    assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D2)) == 256 + 4 * 2 * 256 * 8 * 128
+    bw = L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(D))
+    assert bw == 256 + 2 * (4 * 2 * 8 * 256) + 4 * 2 * 256 * 8 * 128
+    assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(_desc(bpa, Hq=3))) == 0
+    assert L.bpa_workspace_size(7, ctypes.byref(D)) == 0
+
+
+def test_backward_rejects_bad_arguments(bpa):
+    L = bpa.lib()
+    D = _desc(bpa, ring_size=2, ring_step_end=1)
+    p = 0x80000
+    st = L.bpa_bwd(ctypes.byref(D), p, p, p, p, p, p, p, p, 1 << 30, None)
+    assert st == bpa.BPA_ERR_INVALID_ARG
+    D = _desc(bpa, block_idx=0x1000, sel_block=32, top_n=8, local_window=32)
+    assert L.bpa_bwd(ctypes.byref(D), p, p, p, p, p, p, p, p, 1 << 30, None) == bpa.BPA_ERR_UNSUPPORTED
+    D = _desc(bpa)
+    assert L.bpa_bwd(ctypes.byref(D), p, 0, p, p, p, p, p, p, 1 << 30, None) == bpa.BPA_ERR_INVALID_ARG
+
+
+def test_select_rejects_bad_arguments(bpa):
+    L = bpa.lib()
+    st = (ctypes.c_int64 * 3)(8192 * 8 * 64, 8 * 64, 64)
+    p = 0x80000
+    assert L.bpa_select_blocks(p, p, 0, 4, 8192, 8, 64, st, st, 33, 8, p, p, 1 << 30, None) == 1
+    assert L.bpa_select_blocks(p, p, 0, 4, 8192, 8, 64, st, st, 32, 0, p, p, 1 << 30, None) == 1
+    assert L.bpa_select_blocks(p, p, 0, 4, 8192, 8, 64, st, st, 32, 8, p, p, 16, None) == 3
+    assert L.bpa_select_workspace_size(4, 8192, 8, 64, 32) == 256 + 2 * 4 * 8 * 256 * 64 * 8
+
+
+def test_status_strings(bpa):
+    L = bpa.lib()
+    assert L.bpa_status_string(5) == b"BPA_ERR_TIMEOUT"
+    assert L.bpa_version() == 1

@@ -1,0 +1,228 @@
+"""GPU parity of libbpa against the float64 oracle on small seeded problems.
+
+Every call goes through the C ABI (ring_attention_gb300.bpa is ctypes
+marshalling only).  Sizes span several 128-row tiles and ragged tails, and
+the mask / bias / GQA / head-dim combinations the method has.
+"""
+import numpy as np
+import pytest
+import torch
+
+from ring_attention_gb300.inputs import draw
+from tests.gpu_util import (BF16_GRAD_REL_L2, BF16_O_MAX_ABS, FP32_MAX_ABS, check_stats, dev, host,
+                            max_abs, rel_l2)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bpa():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from ring_attention_gb300 import build
+    build.build()
+    from ring_attention_gb300 import bpa as mod
+    return mod
+
+
+SHAPES = [  # B, S, Hq, Hkv, d
+    (1, 1, 1, 1, 64),
+    (1, 17, 2, 1, 128),
+    (2, 128, 4, 2, 64),
+    (1, 129, 4, 4, 128),
+    (2, 300, 8, 2, 128),
+    (1, 640, 16, 4, 64),
+]
+MASKS = [
+    dict(causal=True, window=(-1, -1)),
+    dict(causal=False, window=(-1, -1)),
+    dict(causal=True, window=(7, 0)),
+    dict(causal=False, window=(64, 64)),
+    dict(causal=False, window=(0, 0)),
+    dict(causal=True, window=(130, 0)),
+]
+
+
+def _mask_id(m):
+    return f"c{int(m['causal'])}_w{m['window'][0]}_{m['window'][1]}"
+
+
+def _inputs(shape, seed, dtype="bf16", backward=True):
+    B, S, Hq, Hkv, d = shape
+    shapes = [(B, S, Hq, d), (B, S, Hkv, d), (B, S, Hkv, d)] + ([(B, S, Hq, d)] if backward else [])
+    return draw(shapes, seed, dtype)
+
+
+def _bias(kind, B, Hq, S, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "none":
+        return None
+    if kind == "keys":
+        return rng.standard_normal((1, 1, 1, S)).astype(np.float32)
+    return rng.standard_normal((B, Hq, S, S)).astype(np.float32)
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mask", MASKS, ids=_mask_id)
+@pytest.mark.parametrize("bias_kind", ["none", "keys"])
+def test_forward_bf16(bpa, ora, shape, mask, bias_kind):
+    B, S, Hq, Hkv, d = shape
+    q, k, v = _inputs(shape, 11 + S, backward=False)
+    bias = _bias(bias_kind, B, Hq, S, 5)
+    o, m, l = bpa.bpa_fwd(dev(q), dev(k), dev(v), bias=None if bias is None else dev(bias), **mask)
+    torch.cuda.synchronize()
+    oo, om, ol = ora.attention_fwd(q, k, v, bias=bias, **mask)
+    assert max_abs(host(o), oo) <= BF16_O_MAX_ABS
+    check_stats(m, l, om, ol)
+
+
+def test_forward_full_bias_and_strided_views(bpa, ora):
+    # q, k, v as views into one packed [B, S, Hq + 2 Hkv, d] tensor; a full [B, Hq, S, S] bias
+    B, S, Hq, Hkv, d = 2, 200, 4, 2, 128
+    (packed,) = draw([(B, S, Hq + 2 * Hkv, d)], 77, "bf16")
+    bias = _bias("full", B, Hq, S, 78)
+    t = dev(packed)
+    q, k, v = t[:, :, :Hq], t[:, :, Hq:Hq + Hkv], t[:, :, Hq + Hkv:]
+    o, m, l = bpa.bpa_fwd(q, k, v, causal=True, bias=dev(bias))
+    torch.cuda.synchronize()
+    oo, om, ol = ora.attention_fwd(np.ascontiguousarray(packed[:, :, :Hq]),
+                                   np.ascontiguousarray(packed[:, :, Hq:Hq + Hkv]),
+                                   np.ascontiguousarray(packed[:, :, Hq + Hkv:]), causal=True, bias=bias)
+    assert max_abs(host(o), oo) <= BF16_O_MAX_ABS
+    check_stats(m, l, om, ol)
+
+
+@pytest.mark.parametrize("shape", SHAPES[1:], ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mask", [MASKS[0], MASKS[2], MASKS[3]], ids=_mask_id)
+def test_backward_bf16(bpa, ora, shape, mask):
+    B, S, Hq, Hkv, d = shape
+    q, k, v, do = _inputs(shape, 21 + S)
+    bias = _bias("keys", B, Hq, S, 6)
+    tq, tk, tv, tdo, tb = dev(q), dev(k), dev(v), dev(do), dev(bias)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, bias=tb, **mask)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, bias=tb, **mask)
+    torch.cuda.synchronize()
+    rq, rk, rv, *_ = ora.attention_bwd(q, k, v, do, bias=bias, **mask)
+    assert rel_l2(host(dq), rq) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dk), rk) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
+
+
+@pytest.mark.parametrize("mask", [MASKS[0], MASKS[3], MASKS[4]], ids=_mask_id)
+def test_fp32_forward_backward(bpa, ora, mask):
+    shape = (2, 150, 4, 2, 64)
+    q, k, v, do = _inputs(shape, 31, dtype="f32")
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, **mask)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, **mask)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, **mask)
+    assert max_abs(host(o), ro) <= FP32_MAX_ABS
+    assert max_abs(host(dq), rq) <= FP32_MAX_ABS
+    assert max_abs(host(dk), rk) <= FP32_MAX_ABS
+    assert max_abs(host(dv), rv) <= FP32_MAX_ABS
+    check_stats(m, l, rm, rl)
+
+
+@pytest.mark.parametrize("ring", [2, 4, 8])
+def test_ring_forward_equals_one_shot(bpa, ora, ring):
+    B, S, Hq, Hkv, d = 1, 1024, 4, 2, 128
+    q, k, v = _inputs((B, S, Hq, Hkv, d), 41, backward=False)
+    bias = np.zeros((1, 1, 1, S), np.float32)
+    bias[..., -32:] = -1e9
+    o, m, l = bpa.bpa_fwd(dev(q), dev(k), dev(v), causal=True, bias=dev(bias), ring_size=ring,
+                          query_chunk=S // ring // 2, key_chunk=S // ring)
+    torch.cuda.synchronize()
+    oo, om, ol = ora.attention_fwd(q, k, v, causal=True, bias=bias)
+    assert max_abs(host(o), oo) <= BF16_O_MAX_ABS
+    check_stats(m, l, om, ol)
+
+
+def test_ring_sweep_resumes_from_carry(bpa):
+    B, S, Hq, Hkv, d = 1, 1024, 4, 2, 64
+    q, k, v = (dev(x) for x in _inputs((B, S, Hq, Hkv, d), 42, backward=False))
+    full = bpa.bpa_fwd(q, k, v, causal=True, ring_size=8)
+    D = bpa.make_desc(q, k, v, causal=True, ring_size=8)
+    ws = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_FWD, D), q.device)
+    o = torch.empty_like(q)
+    m = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    l = torch.empty_like(m)
+    for steps in ((0, 3), (3, 5), (5, 8)):
+        bpa.bpa_fwd(q, k, v, causal=True, ring_size=8, ring_steps=steps, o=o, m=m, l=l, workspace_buf=ws)
+    torch.cuda.synchronize()
+    bpa.bpa_check(ws)
+    assert torch.equal(o, full[0]) and torch.equal(m, full[1]) and torch.equal(l, full[2])
+
+
+@pytest.mark.parametrize("ring", [2, 4])
+def test_ring_backward(bpa, ora, ring):
+    B, S, Hq, Hkv, d = 1, 512, 4, 2, 128
+    q, k, v, do = _inputs((B, S, Hq, Hkv, d), 43)
+    bias = np.zeros((1, 1, 1, S), np.float32)
+    bias[..., -16:] = -1e9
+    tq, tk, tv, tdo, tb = dev(q), dev(k), dev(v), dev(do), dev(bias)
+    kw = dict(causal=True, bias=tb, ring_size=ring)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, **kw)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, **kw)
+    torch.cuda.synchronize()
+    rq, rk, rv, *_ = ora.attention_bwd(q, k, v, do, causal=True, bias=bias)
+    assert rel_l2(host(dq), rq) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dk), rk) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
+
+
+@pytest.mark.parametrize("dims", [(1, 256, 2, 16, 4, 3), (2, 1024, 4, 64, 32, 8), (1, 96, 1, 8, 32, 64)])
+def test_select_blocks_bit_exact(bpa, ora, dims):
+    B, S, H, d, bs, n = dims
+    q, k = draw([(B, S, H, d), (B, S, H, d)], 51 + S, "bf16")
+    idx = bpa.bpa_select_blocks(dev(q), dev(k), block_size=bs, top_n=n)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), ora.select_blocks(q, k, block_size=bs, top_n=n))
+
+
+def test_select_blocks_ties(bpa, ora):
+    # block sums with many exactly equal scores: ties must keep the lower block
+    B, S, H, d, bs = 1, 256, 1, 8, 8
+    q = np.zeros((B, S, H, d), np.float32)
+    k = np.zeros((B, S, H, d), np.float32)
+    q[0, ::bs, 0, :] = 1.0
+    for j in range(S // bs):
+        k[0, j * bs, 0, :] = float(j % 3)
+    idx = bpa.bpa_select_blocks(dev(q), dev(k), block_size=bs, top_n=5)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), ora.select_blocks(q, k, block_size=bs, top_n=5))
+
+
+def test_block_selected_attention(bpa, ora):
+    B, S, H, d, bs, n = 2, 512, 2, 64, 32, 4
+    q, k, v = draw([(B, S, H, d)] * 3, 61, "bf16")
+    tq, tk, tv = dev(q), dev(k), dev(v)
+    idx = bpa.bpa_select_blocks(tq, tk, block_size=bs, top_n=n)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, causal=True, block_idx=idx, sel_block=bs, top_n=n, local_window=32)
+    torch.cuda.synchronize()
+    ridx = ora.select_blocks(q, k, block_size=bs, top_n=n)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    oo, om, ol = ora.attention_fwd(q, k, v, causal=True, block_idx=ridx, sel_block=bs, top_n=n,
+                                   local_window=32)
+    assert max_abs(host(o), oo) <= BF16_O_MAX_ABS
+    check_stats(m, l, om, ol)
+
+
+def test_bounded_wait_reports_timeout(bpa):
+    ws = bpa.workspace(256, "cuda")
+    bpa.bpa_debug_wait_timeout(ws, 200_000_000)   # 0.2 s
+    torch.cuda.synchronize()
+    with pytest.raises(bpa.BpaError) as e:
+        bpa.bpa_check(ws)
+    assert e.value.status == bpa.BPA_ERR_TIMEOUT
+    # the context is still usable afterwards
+    x = torch.ones(4, device="cuda")
+    assert float((x + 1).sum()) == 8.0
+
+
+def test_status_clean_after_normal_call(bpa):
+    q, k, v = (dev(x) for x in _inputs((1, 256, 2, 2, 128), 71, backward=False))
+    D = bpa.make_desc(q, k, v, causal=True)
+    ws = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_FWD, D), q.device)
+    bpa.bpa_fwd(q, k, v, causal=True, workspace_buf=ws)
+    torch.cuda.synchronize()
+    bpa.bpa_check(ws)
