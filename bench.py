@@ -1,0 +1,365 @@
+#!/usr/bin/env python
+"""Attention forward + backward throughput on GB300, TFLOP/s over unmasked score entries.
+
+One step = bpa_fwd + bpa_bwd over one batch of the GQA causal workload
+(B=2, S=4096, Hq=32, Hkv=8, d=128, bf16, seed 1), inputs resident in HBM.
+FLOPs count only allowed (query, key) entries: 4*d per entry forward
+(Q K^T and P V), 10*d backward (the five contractions, recompute included).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank runs its own replica of the workload
+(independent batches, no collective on the data path) -> "scaling": "weak".
+--impl reference times the float64 CPU oracle on the host cores (rank 0).
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from ring_attention_gb300.inputs import WORKLOADS, GQA_CAUSAL, make_inputs, unmasked_entries  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s (unmasked FLOPs) and % of GB300 BF16 tensor peak"
+FLUSH_BYTES = 256 << 20     # > 129 MB L2: written between timed steps
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def flops(w, entries):
+    return 4.0 * w.d * entries, 10.0 * w.d * entries
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel (else None)."""
+    src = {"k_bwd_tc": "bwd_tc.cu", "k_fwd_tc": "fwd_tc.cu"}[kernel]
+    path = os.path.join(ROOT, "ring_attention_gb300", "csrc", src)
+    digest = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    table = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(table):
+        return None
+    for line in open(table):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == digest:
+            return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.idx)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.2)
+        self.out = ""
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_sample(w, budget_s: float):
+    """Time the float64 oracle (fwd + bwd) on the largest S (power of two, same
+    recipe, B=1) that fits the budget.  Returns (TFLOP/s, seconds, description, cores)."""
+    from oracle import oracle
+    oracle.build()
+    S = 64
+    best = None
+    while S <= w.S:
+        q, k, v, do, bias = make_inputs(w, B=1, S=S)
+        t0 = time.perf_counter()
+        oracle.attention_bwd(q, k, v, do, causal=w.causal, window=w.window, bias=bias)
+        dt = time.perf_counter() - t0
+        ent = unmasked_entries(w, S) // w.B
+        f_fwd, f_bwd = flops(w, ent)
+        best = ((f_fwd + f_bwd) / dt / 1e12, dt, S)
+        if dt * 4.5 > budget_s:    # doubling S roughly quadruples the causal work
+            break
+        S *= 2
+    tf, dt, S = best
+    desc = (f"float64 oracle fwd+bwd on B=1, S={S}, Hq={w.Hq}, Hkv={w.Hkv}, d={w.d} of the same recipe "
+            f"(seed {w.seed}); {dt:.2f} s")
+    return tf, dt, desc, oracle.num_threads(), S
+
+
+def run_reference(args, w):
+    """Reference arm: the float64 CPU oracle, as it stands, on bounded samples."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import oracle
+    oracle.build()
+    per_step = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    # pick the sample size once, then run warmup + timed steps on it
+    tf, dt, desc, cores, S = cpu_oracle_sample(w, per_step)
+    q, k, v, do, bias = make_inputs(w, B=1, S=S)
+    ent = unmasked_entries(w, S) // w.B
+    f = sum(flops(w, ent))
+    for _ in range(args.warmup):
+        oracle.attention_bwd(q, k, v, do, causal=w.causal, window=w.window, bias=bias)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention_bwd(q, k, v, do, causal=w.causal, window=w.window, bias=bias)
+    el = time.perf_counter() - t0
+    val = f * args.steps / el / 1e12
+    sample = f"each step: float64 oracle fwd+bwd on B=1, S={S} of the workload's recipe ({ent} unmasked entries)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "sample": sample},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=GQA_CAUSAL.name, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from ring_attention_gb300 import build as _build
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    from ring_attention_gb300 import bpa
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---- inputs (each rank: its own replica of the workload) -------------
+    q_np, k_np, v_np, do_np, bias_np = make_inputs(w)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    q, k, v, do = to_dev(q_np), to_dev(k_np), to_dev(v_np), to_dev(do_np)
+    bias = to_dev(bias_np) if bias_np is not None else None
+    kw = dict(causal=w.causal, window=w.window, bias=bias, query_chunk=w.query_chunk, key_chunk=w.key_chunk,
+              ring_size=w.ring_size)
+    D = bpa.make_desc(q, k, v, **kw)
+    ws_f = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_FWD, D), dev)
+    ws_b = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_BWD, D), dev)
+    o = torch.empty_like(q)
+    m = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+    l = torch.empty_like(m)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(ev_f=None, ev_b=None):
+        bpa.bpa_set_phase_events(ev_f)
+        bpa.bpa_fwd(q, k, v, o=o, m=m, l=l, workspace_buf=ws_f, **kw)
+        bpa.bpa_set_phase_events(ev_b)
+        bpa.bpa_bwd(q, k, v, o, do, m, l, dq=dq, dk=dk, dv=dv, workspace_buf=ws_b, **kw)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    bpa.bpa_check(ws_f)
+    bpa.bpa_check(ws_b)
+
+    # ---- timed region ---------------------------------------------------
+    K = args.steps
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(E(), E()) for _ in range(K)]
+    evf = [[E() for _ in range(3)] for _ in range(K)]
+    evb = [[E() for _ in range(4)] for _ in range(K)]
+    for e in [x for row in evf + evb for x in row]:
+        e.record()   # creates the CUDA event; the library re-records it at its phase boundary
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(K):
+            ev[i][0].record()
+            step(evf[i], evb[i])
+            ev[i][1].record()
+            flush.zero_()          # L2 flush between steps (not timed)
+        torch.cuda.synchronize()
+        barrier()
+        wall = time.perf_counter() - wall0
+    bpa.bpa_check(ws_f)
+    bpa.bpa_check(ws_b)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evf]
+    bwd_main_ms = [e[1].elapsed_time(e[2]) for e in evb]
+    bwd_pre_ms = [e[0].elapsed_time(e[1]) for e in evb]
+    bwd_post_ms = [e[2].elapsed_time(e[3]) for e in evb]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    entries = unmasked_entries(w)
+    f_fwd, f_bwd = flops(w, entries)
+    value = (f_fwd + f_bwd) * K * world / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / K
+    peaks, peaks_kind = load_peaks()
+    peak_tf = float(peaks["bf16_tflops"])
+    fwd_tf = f_fwd / (statistics.mean(fwd_ms) * 1e-3) / 1e12
+    bwd_main_tf = f_bwd / (statistics.mean(bwd_main_ms) * 1e-3) / 1e12
+    bwd_tf = f_bwd / (statistics.mean([a + b + c for a, b, c in zip(bwd_pre_ms, bwd_main_ms, bwd_post_ms)]) * 1e-3) / 1e12
+    traffic = kernel_traffic("k_bwd_tc")
+
+    # ---- end to end through the public API: pinned host -> device -> host --
+    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q, k, v, do)]
+    for h, t in zip(h_in, (q, k, v, do)):
+        h.copy_(t)
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, dq, dk, dv)]
+    d_in = [torch.empty_like(t) for t in (q, k, v, do)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def e2e_step():
+        for d_, h in zip(d_in, h_in):
+            d_.copy_(h, non_blocking=True)
+        bpa.bpa_fwd(d_in[0], d_in[1], d_in[2], o=o, m=m, l=l, workspace_buf=ws_f, **kw)
+        bpa.bpa_bwd(d_in[0], d_in[1], d_in[2], o, d_in[3], m, l, dq=dq, dk=dk, dv=dv, workspace_buf=ws_b, **kw)
+        for h, d_ in zip(h_out, (o, dq, dk, dv)):
+            h.copy_(d_, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = E(), E()
+    e0.record()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = (f_fwd + f_bwd) * args.e2e_steps * world / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, dt, desc, cores, _ = cpu_oracle_sample(w, 20.0)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "S": w.S, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                       "causal": w.causal, "window": list(w.window), "unmasked_entries": entries,
+                       "flops_per_step": f_fwd + f_bwd, "l2": "flushed between timed steps (256 MiB write)",
+                       "parallelism": f"replicas x{world}"},
+            "pct_of_peak": {"fwd": 100 * fwd_tf / peak_tf, "bwd": 100 * bwd_tf / peak_tf,
+                            "step": 100 * value / world / peak_tf, "peak": f"bf16_tflops ({peaks_kind})"},
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+            "roofline": {"kernel": "k_bwd_tc (backward main kernel)", "bound": "tensor",
+                         "achieved": bwd_main_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": bwd_main_tf / peak_tf,
+                         "peak_kind": f"bf16_tflops, burst ({peaks_kind})",
+                         "traffic": traffic},
+            "roofline_fwd": {"kernel": "k_fwd_tc", "bound": "tensor", "achieved": fwd_tf, "peak": peak_tf,
+                             "unit": "TFLOP/s", "frac": fwd_tf / peak_tf},
+            "kernel_ms": {"fwd": statistics.mean(fwd_ms), "bwd_pre": statistics.mean(bwd_pre_ms),
+                          "bwd_main": statistics.mean(bwd_main_ms), "bwd_post": statistics.mean(bwd_post_ms)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 4 * K,
+            "clocks": clocks.summary(),
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

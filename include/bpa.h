@@ -178,6 +178,16 @@ const char* bpa_last_error(void);
 /* BPA_VERSION of the library. */
 int32_t bpa_version(void);
 
+/* Instrumentation: the next bpa_fwd or bpa_bwd call made on this host
+ * thread records the given CUDA events (cudaEvent_t values) on its stream
+ * at its phase boundaries, then forgets them.  bpa_fwd: [0] before the
+ * first kernel, [1] after the attention kernel(s) (every ring step), [2] at
+ * the end (after the ring finalize).  bpa_bwd: [0] before the pre-pass,
+ * [1] after it, [2] after the main kernel(s), [3] at the end.  Events past n
+ * are not recorded; n <= 0 or events == NULL clears the hook.  Timing only:
+ * nothing else changes. */
+void bpa_set_phase_events(void* const* events, int32_t n);
+
 /* Diagnostic for failure detection: launches one CTA whose bounded wait on a
  * barrier that nothing ever completes must give up after limit_ns
  * (0 < limit_ns <= 5e9) and record BPA_ERR_TIMEOUT in the workspace's status

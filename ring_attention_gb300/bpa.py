@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.bpa_version.argtypes, L.bpa_version.restype = [], i32
         L.bpa_debug_wait_timeout.argtypes = [P, sz, ctypes.c_uint64, P]
         L.bpa_debug_wait_timeout.restype = ctypes.c_int
+        L.bpa_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
+        L.bpa_set_phase_events.restype = None
         _lib = L
     return _lib
 
@@ -157,7 +159,7 @@ def bpa_fwd(q, k, v, *, o=None, m=None, l=None, workspace_buf=None, stream=None,
     D = make_desc(q, k, v, **kw)
     B, S, Hq, _ = q.shape
     if o is None:
-        o = torch.empty(q.shape[:3] + (v.shape[3],), dtype=q.dtype, device=q.device)
+        o = torch.empty_strided(q.shape[:3] + (v.shape[3],), q.stride(), dtype=q.dtype, device=q.device)
     if m is None:
         m = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
     if l is None:
@@ -177,9 +179,9 @@ def bpa_fwd(q, k, v, *, o=None, m=None, l=None, workspace_buf=None, stream=None,
 def bpa_bwd(q, k, v, o, dout, m, l, *, dq=None, dk=None, dv=None, workspace_buf=None, stream=None, **kw):
     """Backward pass.  Returns (dq, dk, dv) with the dtypes and strides of q, k, v."""
     D = make_desc(q, k, v, **kw)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device) if dq is None else dq
+    dk = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device) if dk is None else dk
+    dv = torch.empty_strided(v.shape, v.stride(), dtype=v.dtype, device=v.device) if dv is None else dv
     for name, a, b in (("o", o, q), ("dout", dout, q), ("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
         if a.stride() != b.stride() or a.dtype != b.dtype:
             raise ValueError(f"{name} must share dtype and strides with its input")
@@ -218,6 +220,16 @@ def bpa_select_blocks(q, k, *, block_size=32, top_n=8, out=None, workspace_buf=N
 def bpa_check(workspace_buf: torch.Tensor) -> None:
     """Raises BpaError if a kernel of the last call on this workspace reported a fault."""
     _raise_if(lib().bpa_check(workspace_buf.data_ptr()), "bpa_check")
+
+
+def bpa_set_phase_events(events) -> None:
+    """Record these torch.cuda.Event objects at the phase boundaries of the next
+    bpa_fwd / bpa_bwd call on this thread (None clears the hook)."""
+    if events is None:
+        lib().bpa_set_phase_events(None, 0)
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    lib().bpa_set_phase_events(arr, len(events))
 
 
 def bpa_debug_wait_timeout(workspace_buf: torch.Tensor, limit_ns: int, stream=None) -> None:

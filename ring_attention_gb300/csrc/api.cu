@@ -19,6 +19,23 @@ namespace {
 
 thread_local char g_last_error[512] = "";
 
+// phase-event hook (bpa_set_phase_events): consumed by the next fwd / bwd call
+thread_local cudaEvent_t g_phase_events[8];
+thread_local int g_phase_n = 0;
+
+struct PhaseMarks {
+    cudaEvent_t ev[8];
+    int n = 0;
+    PhaseMarks() {
+        n = g_phase_n;
+        for (int i = 0; i < n; ++i) ev[i] = g_phase_events[i];
+        g_phase_n = 0;
+    }
+    void mark(int i, cudaStream_t s) const {
+        if (i < n && ev[i]) cudaEventRecord(ev[i], s);
+    }
+};
+
 bpa_status fail(bpa_status st, const char* fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -236,8 +253,10 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
     if ((st = check_ws(workspace, workspace_bytes, L.total)) != BPA_OK) return st;
     cudaStream_t s = as_stream(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const PhaseMarks marks;
     cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    marks.mark(0, s);
 
     FwdArgs a;
     memset(&a, 0, sizeof a);
@@ -249,6 +268,8 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
 
     if (P.block_idx) {
         e = gather_supported(P) ? launch_gather_fwd(a, s) : launch_fwd_simt(a, s);
+        marks.mark(1, s);
+        marks.mark(2, s);
         return e == cudaSuccess ? BPA_OK : cuda_fail(e, "block-selected forward launch");
     }
 
@@ -261,6 +282,8 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
     }
     if (n == 1) {
         e = tc ? launch_fwd_tc(a, maps, s) : launch_fwd_simt(a, s);
+        marks.mark(1, s);
+        marks.mark(2, s);
         return e == cudaSuccess ? BPA_OK : cuda_fail(e, "forward launch");
     }
     a.acc = reinterpret_cast<float*>(ws + L.acc);
@@ -270,7 +293,9 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
         e = tc ? launch_fwd_tc(a, maps, s) : launch_fwd_simt(a, s);
         if (e != cudaSuccess) return cuda_fail(e, "ring step launch");
     }
+    marks.mark(1, s);
     if (end == n && (e = launch_ring_finalize(a, s)) != cudaSuccess) return cuda_fail(e, "ring finalize");
+    marks.mark(2, s);
     return BPA_OK;
 }
 
@@ -290,8 +315,10 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
     if ((st = check_ws(workspace, workspace_bytes, L.total)) != BPA_OK) return st;
     cudaStream_t s = as_stream(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const PhaseMarks marks;
     cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, s);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    marks.mark(0, s);
 
     BwdArgs a;
     memset(&a, 0, sizeof a);
@@ -319,11 +346,15 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
     }
     if (!tc) {
         if ((e = launch_bwd_pre(a, s)) != cudaSuccess) return cuda_fail(e, "backward pre-pass");
+        marks.mark(1, s);
         e = launch_bwd_simt(a, s);
+        marks.mark(2, s);
+        marks.mark(3, s);
         return e == cudaSuccess ? BPA_OK : cuda_fail(e, "backward launch");
     }
     a.dq_acc = reinterpret_cast<float*>(ws + L.dq);
     if ((e = launch_bwd_pre(a, s)) != cudaSuccess) return cuda_fail(e, "backward pre-pass");
+    marks.mark(1, s);
     if (n == 1) {
         if ((e = launch_bwd_tc(a, maps, s)) != cudaSuccess) return cuda_fail(e, "backward launch");
     } else {
@@ -338,7 +369,9 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
             if ((e = launch_bwd_tc(a, maps, s)) != cudaSuccess) return cuda_fail(e, "ring backward step");
         }
     }
+    marks.mark(2, s);
     e = launch_bwd_post(a, s);
+    marks.mark(3, s);
     return e == cudaSuccess ? BPA_OK : cuda_fail(e, "backward post-pass");
 }
 
@@ -401,6 +434,14 @@ bpa_status bpa_check(const void* workspace) {
     if (h.flags & ST_TIMEOUT) return fail(BPA_ERR_TIMEOUT, "a kernel wait gave up (site 0x%x)", h.where);
     if (h.flags & ST_CHECK) return fail(BPA_ERR_DEVICE_CHECK, "a device-side check failed (site 0x%x)", h.where);
     return BPA_OK;
+}
+
+void bpa_set_phase_events(void* const* events, int32_t n) {
+    g_phase_n = 0;
+    if (!events || n <= 0) return;
+    if (n > 8) n = 8;
+    for (int i = 0; i < n; ++i) g_phase_events[i] = static_cast<cudaEvent_t>(events[i]);
+    g_phase_n = n;
 }
 
 // Diagnostic: launches one CTA whose bounded wait can never complete, so that

@@ -1,11 +1,493 @@
-// bwd_tc.cu - blockwise attention backward on the 5th-generation tensor cores.
+// bwd_tc.cu - blockwise attention backward on the 5th-generation tensor cores (bf16, d = 128).
+//
+// Recomputes the scores of every allowed (query tile, key tile) pair from
+// the saved row statistics and accumulates the gradients ("bpt.py",
+// _blockwise_attention_bwd / scan_kv_block):
+//     P = exp(S - lse),  dP = dO V^T,  dS = P (dP - D),
+//     dV += P^T dO,  dK += scale dS^T Q,  dQ += scale dS K
+// One CTA owns one 128-key tile of one (batch, kv head) and walks every q
+// head of the group and every 64-row query tile the mask allows, so dK and
+// dV accumulate in TMEM for the whole group with no atomics; dQ partial
+// tiles are added to a float32 accumulator in global memory.
+// The scores are computed transposed (S^T = K Q^T, keys on the TMEM lanes),
+// so that P^T and dS^T come out of the softmax warps already laid out as the
+// A operands of the dV and dK products.
+// TMEM (512 columns): S^T x2 [0,128), dP^T [128,192), dQ^T [192,256),
+// dK [256,384), dV [384,512).
+// Roles (320 threads):
+//   warps 0-3  thread r owns key row r: P, dS from S^T, dP^T -> shared memory;
+//              at the end dK (scaled) -> output;
+//   warps 4-7  thread r owns channel r of dQ^T: TMEM -> global float32
+//              accumulator (red.add); at the end dV -> output;
+//   warp 8     TMA producer: K, V once; Q, dO (+ lse, D) per query tile;
+//   warp 9     MMA issuer, TMEM owner.
+#include <math.h>
+
 #include "bpa_internal.h"
 #include "common.cuh"
 
 namespace bpa {
+namespace {
 
-bool bwd_tc_supported(const Problem&) { return false; }
+constexpr int D = 128;        // head dim
+constexpr int BK = 128;       // keys per CTA
+constexpr int BQ = 64;        // queries per tile
+constexpr int NS = 2;         // Q / dO stages
+constexpr int kThreads = 320;
 
-cudaError_t launch_bwd_tc(const BwdArgs&, const CUtensorMap*, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int SUBK = BK * 128;    // one 64-channel slab of the key tile
+constexpr int SUBQ = BQ * 128;    // one 64-channel slab of a query tile
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + BK * D * 2;
+constexpr int OFF_Q = OFF_V + BK * D * 2;
+constexpr int OFF_DO = OFF_Q + NS * BQ * D * 2;
+constexpr int OFF_P = OFF_DO + NS * BQ * D * 2;     // P^T  [128 keys][64 q] bf16, x2
+constexpr int OFF_DS = OFF_P + 2 * BK * BQ * 2;     // dS^T [128 keys][64 q] bf16, x2
+constexpr int OFF_ST = OFF_DS + 2 * BK * BQ * 2;    // per stage: lse[64], D[64] float
+constexpr int OFF_BAR = OFF_ST + NS * 512;
+constexpr int SMEM = OFF_BAR + 256 + 1024;
+constexpr int PT_BYTES = BK * BQ * 2;
+
+// barrier slots
+constexpr int B_KV = 0, B_QF = 1, B_QE = 1 + NS, B_S = 1 + 2 * NS, B_DP = 3 + 2 * NS, B_DS = 4 + 2 * NS,
+              B_DQF = 5 + 2 * NS, B_DQE = 6 + 2 * NS, B_PF = 7 + 2 * NS, B_KVD = 9 + 2 * NS,
+              B_FIN = 10 + 2 * NS, NBAR = 11 + 2 * NS;
+
+constexpr uint32_t IDESC_S = idesc_bf16_f32(BK, BQ, 0, 0);     // S^T, dP^T: both K-major
+constexpr uint32_t IDESC_KV = idesc_bf16_f32(BK, D, 0, 1);     // dV, dK: A K-major, B MN-major
+constexpr uint32_t IDESC_Q = idesc_bf16_f32(D, BQ, 1, 1);      // dQ^T: both MN-major
+
+struct Work {
+    int b, hkv, k0;
+    int q_lo, q_hi;      // query rows that may see this key tile (ring block included)
+    int qt_lo, n_qt, n_it;
+};
+
+__device__ __forceinline__ Work decode(const BwdArgs& a) {
+    const Problem& P = a.P;
+    int r = blockIdx.x;
+    Work w;
+    w.b = r % P.B;
+    r /= P.B;
+    w.hkv = r % P.Hkv;
+    const int kt = r / P.Hkv;    // lowest key tiles (most causal work) first
+    w.k0 = kt * BK;
+    const int k_last = min(w.k0 + BK - 1, P.S - 1);
+    int lo = 0, hi = P.S - 1;
+    if (a.dk_acc) {   // ring step: the query block that meets this key block now
+        const int j = w.k0 / P.ring_blk;
+        const int iq = (j + a.ring_idx) % P.ring_n;
+        lo = iq * P.ring_blk;
+        hi = lo + P.ring_blk - 1;
+    }
+    if (P.causal) lo = max(lo, w.k0);
+    if (P.wr >= 0) lo = max(lo, w.k0 - P.wr);
+    if (P.wl >= 0) hi = min(hi, k_last + P.wl);
+    w.q_lo = lo;
+    w.q_hi = hi;
+    w.qt_lo = lo / BQ;
+    w.n_qt = lo <= hi ? hi / BQ - w.qt_lo + 1 : 0;
+    w.n_it = w.n_qt * P.G;
+    return w;
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
+    int never = 0;
+    mbar_wait(bar, parity, &never, status, 0xD1);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_bwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+             const BwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t bar0 = sb + OFF_BAR;
+    auto BAR = [&](int i) { return bar0 + 8u * i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 8 * NBAR);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const float* st_smem = reinterpret_cast<const float*>(smem + OFF_ST);
+
+    const Problem& P = a.P;
+    const Work W = decode(a);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(B_KV), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(BAR(B_QF + s), 1);
+            mbar_init(BAR(B_QE + s), 1);
+        }
+        mbar_init(BAR(B_S + 0), 1);
+        mbar_init(BAR(B_S + 1), 1);
+        mbar_init(BAR(B_DP), 1);
+        mbar_init(BAR(B_DS), 128);
+        mbar_init(BAR(B_DQF), 1);
+        mbar_init(BAR(B_DQE), 128);
+        mbar_init(BAR(B_PF + 0), 1);
+        mbar_init(BAR(B_PF + 1), 1);
+        mbar_init(BAR(B_KVD), 1);
+        mbar_init(BAR(B_FIN), 1);
+        *abort_flag = (a.status && (*reinterpret_cast<volatile uint32_t*>(a.status) & ST_TIMEOUT)) ? 1 : 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tDP = tmem + 128, tDQ = tmem + 192, tDK = tmem + 256, tDV = tmem + 384;
+    const bool skip = *abort_flag != 0;
+    const int n_it = skip ? 0 : W.n_it;
+
+    auto iter_head = [&](int it) { return W.hkv * P.G + it / W.n_qt; };
+    auto iter_q0 = [&](int it) { return (W.qt_lo + it % W.n_qt) * BQ; };
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && n_it > 0) {
+            tma_prefetch(&tmQ);
+            tma_prefetch(&tmK);
+            tma_prefetch(&tmV);
+            tma_prefetch(&tmDO);
+            mbar_expect_tx(BAR(B_KV), 2 * BK * D * 2);
+            for (int sub = 0; sub < 2; ++sub) {
+                tma_load_4d(sb + OFF_K + sub * SUBK, &tmK, BAR(B_KV), sub * 64, W.hkv, W.k0, W.b);
+                tma_load_4d(sb + OFF_V + sub * SUBK, &tmV, BAR(B_KV), sub * 64, W.hkv, W.k0, W.b);
+            }
+            int n_issued = 0;
+            for (int it = 0; it < n_it; ++it) {
+                const int st = it % NS, use = it / NS;
+                if (use > 0 && !mbar_wait(BAR(B_QE + st), (use - 1) & 1, abort_flag, a.status, 0x40)) break;
+                const int h = iter_head(it), q0 = iter_q0(it);
+                mbar_expect_tx(BAR(B_QF + st), 2 * BQ * D * 2 + 512);
+                for (int sub = 0; sub < 2; ++sub) {
+                    tma_load_4d(sb + OFF_Q + st * BQ * D * 2 + sub * SUBQ, &tmQ, BAR(B_QF + st), sub * 64, h,
+                                q0, W.b);
+                    tma_load_4d(sb + OFF_DO + st * BQ * D * 2 + sub * SUBQ, &tmDO, BAR(B_QF + st), sub * 64,
+                                h, q0, W.b);
+                }
+                const int64_t row = (static_cast<int64_t>(W.b) * P.Hq + h) * a.Spad + q0;
+                bulk_load(sb + OFF_ST + st * 512, a.lse + row, 256, BAR(B_QF + st));
+                bulk_load(sb + OFF_ST + st * 512 + 256, a.Dvec + row, 256, BAR(B_QF + st));
+                n_issued = it + 1;
+            }
+            drain_wait(BAR(B_KV), 0, a.status);
+            for (int s = 0; s < NS; ++s) {
+                const int uses = (n_issued - s + NS - 1) / NS;
+                if (uses > 0) drain_wait(BAR(B_QF + s), (uses - 1) & 1, a.status);
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n_it > 0) {
+            bool ok = mbar_wait(BAR(B_KV), 0, abort_flag, a.status, 0x50);
+            for (int it = 0; ok && it <= n_it; ++it) {
+                if (it < n_it) {
+                    const int st = it % NS;
+                    if (!mbar_wait(BAR(B_QF + st), (it / NS) & 1, abort_flag, a.status, 0x51)) break;
+                    tc_fence_after();
+                    const uint32_t qb = sb + OFF_Q + st * BQ * D * 2;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
+                        const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
+                        tc_mma_ss(tS + (it & 1) * BQ, sdesc_sw128(sb + OFF_K + offk, 16, 1024),
+                                  sdesc_sw128(qb + offq, 16, 1024), IDESC_S, kk > 0);
+                    }
+                    tc_commit(BAR(B_S + (it & 1)));
+                }
+                if (it > 0) {
+                    const int p = it - 1, pst = p % NS, buf = p & 1;
+                    if (!mbar_wait(BAR(B_DS), p & 1, abort_flag, a.status, 0x52)) break;
+                    tc_fence_after();
+                    const uint32_t pb = sb + OFF_P + buf * PT_BYTES, db = sb + OFF_DS + buf * PT_BYTES;
+                    const uint32_t qb = sb + OFF_Q + pst * BQ * D * 2, dob = sb + OFF_DO + pst * BQ * D * 2;
+#pragma unroll
+                    for (int kk = 0; kk < BQ / 16; ++kk) {
+                        const uint32_t acc = (p > 0 || kk > 0) ? 1u : 0u;
+                        tc_mma_ss(tDV, sdesc_sw128(pb + kk * 32, 16, 1024), sdesc_sw128(dob + kk * 2048, SUBQ, 1024),
+                                  IDESC_KV, acc);
+                        tc_mma_ss(tDK, sdesc_sw128(db + kk * 32, 16, 1024), sdesc_sw128(qb + kk * 2048, SUBQ, 1024),
+                                  IDESC_KV, acc);
+                    }
+                    if (p > 0 && !mbar_wait(BAR(B_DQE), (p - 1) & 1, abort_flag, a.status, 0x53)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma_ss(tDQ, sdesc_sw128(sb + OFF_K + kk * 2048, SUBK, 1024),
+                                  sdesc_sw128(db + kk * 2048, 16, 1024), IDESC_Q, kk > 0);
+                    tc_commit(BAR(B_DQF));
+                    tc_commit(BAR(B_PF + buf));
+                    tc_commit(BAR(B_QE + pst));
+                    if (p == n_it - 1) tc_commit(BAR(B_KVD));
+                }
+                if (it < n_it) {
+                    const int st = it % NS;
+                    const uint32_t dob = sb + OFF_DO + st * BQ * D * 2;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
+                        const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
+                        tc_mma_ss(tDP, sdesc_sw128(sb + OFF_V + offk, 16, 1024),
+                                  sdesc_sw128(dob + offq, 16, 1024), IDESC_S, kk > 0);
+                    }
+                    tc_commit(BAR(B_DP));
+                }
+            }
+            tc_commit(BAR(B_FIN));
+            drain_wait(BAR(B_FIN), 0, a.status);
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ P / dS (key rows)
+        const int r = threadIdx.x;
+        const int k = W.k0 + r;
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        int qmin = W.q_lo, qmax = min(W.q_hi, P.S - 1);
+        if (P.causal) qmin = max(qmin, k);
+        if (P.wr >= 0) qmin = max(qmin, k - P.wr);
+        if (P.wl >= 0) qmax = min(qmax, k + P.wl);
+        if (k >= P.S) qmax = -1;
+        const float sl2 = P.scale * kLog2e;
+        bool aborted = false;
+        for (int it = 0; it < n_it; ++it) {
+            const int h = iter_head(it), q0 = iter_q0(it), st = it % NS, buf = it & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_S + buf), (it >> 1) & 1, abort_flag, a.status, 0x60))) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            float p[BQ];
+#pragma unroll
+            for (int c = 0; c < BQ / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tS + buf * BQ + c * 32 + lane_base, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) p[c * 32 + i] = __uint_as_float(v[i]) * sl2;
+            }
+            // the lse / D of this tile came with the Q tile: observe that copy's barrier
+            // (it cannot have moved on: the stage is refilled only after this tile's dS)
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_QF + st), (it / NS) & 1, abort_flag, a.status, 0x64))) {
+                aborted = true;
+                break;
+            }
+            const float* lse = st_smem + st * 128;
+            const float* Dq = lse + 64;
+            if (P.bias) {
+                const float* brow = P.bias + W.b * P.bs[0] + h * P.bs[1] + static_cast<int64_t>(min(k, P.S - 1)) * P.bs[3];
+#pragma unroll
+                for (int c = 0; c < BQ; ++c) {
+                    const int q = min(q0 + c, P.S - 1);
+                    p[c] = fmaf(brow[q * P.bs[2]], kLog2e, p[c]);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < BQ; ++c) p[c] = ex2(p[c] - lse[c] * kLog2e);
+            const bool edge = q0 < qmin || q0 + BQ - 1 > qmax;
+            if (__any_sync(0xffffffffu, edge)) {
+#pragma unroll
+                for (int c = 0; c < BQ; ++c) {
+                    const int q = q0 + c;
+                    if (q < qmin || q > qmax) p[c] = 0.f;
+                }
+            }
+            // the P^T / dS^T buffer is free once the MMAs of two tiles ago are done
+            if (it >= 2 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_PF + buf), ((it - 2) >> 1) & 1, abort_flag,
+                                                              a.status, 0x61))) {
+                aborted = true;
+                break;
+            }
+            const uint32_t pb = sb + OFF_P + buf * PT_BYTES, db = sb + OFF_DS + buf * PT_BYTES;
+#pragma unroll
+            for (int cc = 0; cc < BQ / 8; ++cc)
+                st_shared_v4(pb + sw128_offset(r, cc), pack_bf16(p[cc * 8 + 0], p[cc * 8 + 1]),
+                             pack_bf16(p[cc * 8 + 2], p[cc * 8 + 3]), pack_bf16(p[cc * 8 + 4], p[cc * 8 + 5]),
+                             pack_bf16(p[cc * 8 + 6], p[cc * 8 + 7]));
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DP), it & 1, abort_flag, a.status, 0x62))) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < BQ / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tDP + c * 32 + lane_base, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) p[c * 32 + i] *= __uint_as_float(v[i]) - Dq[c * 32 + i];
+            }
+#pragma unroll
+            for (int cc = 0; cc < BQ / 8; ++cc)
+                st_shared_v4(db + sw128_offset(r, cc), pack_bf16(p[cc * 8 + 0], p[cc * 8 + 1]),
+                             pack_bf16(p[cc * 8 + 2], p[cc * 8 + 3]), pack_bf16(p[cc * 8 + 4], p[cc * 8 + 5]),
+                             pack_bf16(p[cc * 8 + 6], p[cc * 8 + 7]));
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(BAR(B_DS));
+        }
+        // ---- epilogue: dK = scale * acc
+        if (!aborted && !skip) {
+            if (n_it > 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_KVD), 0, abort_flag, a.status, 0x63))) aborted = true;
+                tc_fence_after();
+            }
+            if (!aborted) {
+                const int kk = min(k, P.S - 1);
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.dk) + W.b * P.ks[0] +
+                                     static_cast<int64_t>(kk) * P.ks[1] + W.hkv * P.ks[2];
+                float* carry = a.dk_acc ? a.dk_acc + ((static_cast<int64_t>(W.b) * P.S + kk) * P.Hkv + W.hkv) * D
+                                        : nullptr;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    if (n_it > 0) {
+                        tmem_ld32(tDK + c * 32 + lane_base, v);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
+                    }
+                    if (k < P.S) {
+                        if (carry) {
+                            if (n_it > 0) {
+                                float4* dst = reinterpret_cast<float4*>(carry + c * 32);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    float4 x = dst[i];
+                                    x.x += __uint_as_float(v[4 * i + 0]) * P.scale;
+                                    x.y += __uint_as_float(v[4 * i + 1]) * P.scale;
+                                    x.z += __uint_as_float(v[4 * i + 2]) * P.scale;
+                                    x.w += __uint_as_float(v[4 * i + 3]) * P.scale;
+                                    dst[i] = x;
+                                }
+                            }
+                        } else {
+                            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[i] = make_uint4(
+                                    pack_bf16(__uint_as_float(v[8 * i + 0]) * P.scale, __uint_as_float(v[8 * i + 1]) * P.scale),
+                                    pack_bf16(__uint_as_float(v[8 * i + 2]) * P.scale, __uint_as_float(v[8 * i + 3]) * P.scale),
+                                    pack_bf16(__uint_as_float(v[8 * i + 4]) * P.scale, __uint_as_float(v[8 * i + 5]) * P.scale),
+                                    pack_bf16(__uint_as_float(v[8 * i + 6]) * P.scale, __uint_as_float(v[8 * i + 7]) * P.scale));
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ dQ (channel rows)
+        const int ch = threadIdx.x - 128;     // channel of dQ^T == TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
+        bool aborted = false;
+        for (int it = 0; it < n_it; ++it) {
+            const int h = iter_head(it), q0 = iter_q0(it);
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DQF), it & 1, abort_flag, a.status, 0x70))) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tDQ + lane_base, v0);
+            tmem_ld32(tDQ + 32 + lane_base, v1);
+            tc_fence_before();
+            mbar_arrive(BAR(B_DQE));
+            float* base = a.dq_acc + ((static_cast<int64_t>(W.b) * P.S + q0) * P.Hq + h) * D + ch;
+            const int64_t qstride = static_cast<int64_t>(P.Hq) * D;
+            const int nq = min(BQ, P.S - q0);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (c < nq) atomicAdd(base + c * qstride, __uint_as_float(v0[c]) * P.scale);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                if (c + 32 < nq) atomicAdd(base + (c + 32) * qstride, __uint_as_float(v1[c]) * P.scale);
+        }
+        // ---- epilogue: dV
+        if (!aborted && !skip) {
+            if (n_it > 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_KVD), 0, abort_flag, a.status, 0x71))) aborted = true;
+                tc_fence_after();
+            }
+            if (!aborted) {
+                const int k = W.k0 + ch;
+                const int kk = min(k, P.S - 1);
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.dv) + W.b * P.vs[0] +
+                                     static_cast<int64_t>(kk) * P.vs[1] + W.hkv * P.vs[2];
+                float* carry = a.dv_acc ? a.dv_acc + ((static_cast<int64_t>(W.b) * P.S + kk) * P.Hkv + W.hkv) * D
+                                        : nullptr;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    if (n_it > 0) {
+                        tmem_ld32(tDV + c * 32 + lane_base, v);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
+                    }
+                    if (k < P.S) {
+                        if (carry) {
+                            if (n_it > 0) {
+                                float4* dst = reinterpret_cast<float4*>(carry + c * 32);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    float4 x = dst[i];
+                                    x.x += __uint_as_float(v[4 * i + 0]);
+                                    x.y += __uint_as_float(v[4 * i + 1]);
+                                    x.z += __uint_as_float(v[4 * i + 2]);
+                                    x.w += __uint_as_float(v[4 * i + 3]);
+                                    dst[i] = x;
+                                }
+                            }
+                        } else {
+                            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[i] = make_uint4(pack_bf16(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1])),
+                                                    pack_bf16(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                                                    pack_bf16(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                                                    pack_bf16(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool bwd_tc_supported(const Problem& P) {
+    if (P.dtype != BPA_BF16 || P.d != D || P.block_idx) return false;
+    if (P.ring_n > 1 && P.ring_blk % BK) return false;
+    return true;
+}
+
+cudaError_t launch_bwd_tc(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(k_bwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    const int nkt = (a.P.S + BK - 1) / BK;
+    const int grid = nkt * a.P.Hkv * a.P.B;
+    k_bwd_tc<<<grid, kThreads, SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
+    return cudaGetLastError();
+}
 
 }  // namespace bpa
