@@ -163,6 +163,36 @@ bpa_status bpa_select_blocks(const void* q, const void* k, int32_t dtype, int32_
                              int32_t* block_idx_out, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/* Block selection for callers that cannot provide device scratch memory.
+ * (An addition of this library; the pages have no counterpart.)
+ * Same inputs, output and arithmetic as bpa_select_blocks, minus the
+ * workspace: the scratch is a fixed 16 MiB buffer compiled into the
+ * library (a __device__ array that every GPU loading the library keeps
+ * until the process exits).  It is for programs that must not call
+ * cudaMalloc themselves: a plain host program without a device allocator,
+ * where cudaMalloc could synchronise the device and stall other streams,
+ * or an embedder that forbids device allocations after start-up.  This
+ * entry point allocates nothing and calls no allocating routine.
+ *   - Limit: problems whose bpa_select_workspace_size exceeds
+ *     bpa_select_noalloc_max_bytes() (16 MiB; e.g. B*H*(S/block_size)*d
+ *     up to about one million) are rejected with BPA_ERR_UNSUPPORTED
+ *     before anything is launched; use bpa_select_blocks for them.
+ *   - The first call on each device looks up the buffer's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on that device.
+ *   - All calls share the one buffer, which keeps the last call's contents:
+ *     each call clears the status word and overwrites every block sum it
+ *     reads.  Calls whose kernels overlap on the GPU (different streams, or
+ *     host threads without ordering between them) race on the buffer:
+ *     order them on one stream.
+ *   - Errors come back through the returned code and bpa_last_error(). */
+size_t bpa_select_noalloc_max_bytes(void);
+bpa_status bpa_select_blocks_noalloc(const void* q, const void* k, int32_t dtype, int32_t B,
+                                     int32_t S, int32_t H, int32_t d,
+                                     const int64_t q_strides[3], const int64_t k_strides[3],
+                                     int32_t block_size, int32_t top_n,
+                                     int32_t* block_idx_out, void* stream);
+
 /* Reads the status word of a workspace used by an earlier call (blocking
  * copy; synchronise the stream first).  BPA_OK, BPA_ERR_TIMEOUT or
  * BPA_ERR_DEVICE_CHECK; BPA_ERR_CUDA if the copy itself fails. */

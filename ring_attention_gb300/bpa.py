@@ -77,6 +77,10 @@ def lib() -> ctypes.CDLL:
         L.bpa_version.argtypes, L.bpa_version.restype = [], i32
         L.bpa_debug_wait_timeout.argtypes = [P, sz, ctypes.c_uint64, P]
         L.bpa_debug_wait_timeout.restype = ctypes.c_int
+        L.bpa_select_noalloc_max_bytes.argtypes, L.bpa_select_noalloc_max_bytes.restype = [], sz
+        L.bpa_select_blocks_noalloc.argtypes = [P, P, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int64),
+                                                ctypes.POINTER(ctypes.c_int64), i32, i32, P, P]
+        L.bpa_select_blocks_noalloc.restype = ctypes.c_int
         L.bpa_set_phase_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         L.bpa_set_phase_events.restype = None
         _lib = L
@@ -214,6 +218,22 @@ def bpa_select_blocks(q, k, *, block_size=32, top_n=8, out=None, workspace_buf=N
                                  block_size, top_n, out.data_ptr(), ws.data_ptr(), ws.numel(),
                                  _stream_ptr(stream))
     _raise_if(st, "bpa_select_blocks")
+    return out
+
+
+def bpa_select_blocks_noalloc(q, k, *, block_size=32, top_n=8, out=None, stream=None):
+    """bpa_select_blocks without a workspace: the library's built-in scratch buffer is used."""
+    B, S, H, d = q.shape
+    if k.shape != q.shape or k.dtype != q.dtype:
+        raise ValueError("q and k must share shape and dtype")
+    qs = (ctypes.c_int64 * 3)(*_bshd_strides(q, "q"))
+    ks = (ctypes.c_int64 * 3)(*_bshd_strides(k, "k"))
+    nblk = S // block_size if block_size > 0 else 0
+    if out is None:
+        out = torch.empty((B, H, nblk, top_n), dtype=torch.int32, device=q.device)
+    st = lib().bpa_select_blocks_noalloc(q.data_ptr(), k.data_ptr(), _dtype_code(q), B, S, H, d, qs, ks,
+                                         block_size, top_n, out.data_ptr(), _stream_ptr(stream))
+    _raise_if(st, "bpa_select_blocks_noalloc")
     return out
 
 

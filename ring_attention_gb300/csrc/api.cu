@@ -211,6 +211,11 @@ cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 }  // namespace
 
+namespace bpa {
+// Lets other translation units of the library report an error through bpa_last_error.
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+}  // namespace bpa
+
 extern "C" {
 
 int32_t bpa_version(void) { return BPA_VERSION; }

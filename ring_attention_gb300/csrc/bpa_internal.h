@@ -80,6 +80,8 @@ cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 
+void set_last_error(const char* msg);
+
 bool fwd_tc_supported(const Problem& P);
 bool bwd_tc_supported(const Problem& P);
 bool gather_supported(const Problem& P);
