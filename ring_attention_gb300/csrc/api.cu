@@ -143,7 +143,8 @@ BwdLayout bwd_layout(const Problem& P) {
     L.D = kHeader;
     L.lse = L.D + round256(rows * sizeof(float));
     L.dq = L.lse + round256(rows * sizeof(float));
-    const size_t nq = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hq * P.d;
+    // dQ accumulator, head-major [B, Hq, Spad, d] (one 64-row tile is contiguous)
+    const size_t nq = sizeof(float) * P.B * static_cast<size_t>(L.Spad) * P.Hq * P.d;
     const size_t nk = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.d;
     L.dk = L.dq + round256(nq);
     L.dv = L.dk + (P.ring_n > 1 ? round256(nk) : 0);

@@ -97,7 +97,7 @@ __global__ void k_bwd_pre(const BwdArgs a, int zero_dq) {
         }
     }
     if (zero_dq) {
-        const int64_t n4 = static_cast<int64_t>(P.B) * P.S * P.Hq * P.d / 4;
+        const int64_t n4 = static_cast<int64_t>(P.B) * a.Spad * P.Hq * P.d / 4;
         float4* z = reinterpret_cast<float4*>(a.dq_acc);
         const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
         for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4; i += stride)
@@ -105,20 +105,84 @@ __global__ void k_bwd_pre(const BwdArgs a, int zero_dq) {
     }
 }
 
-// float32 [B, S, H, d] accumulator -> dtype tensor with strides st
-template <typename T>
-__global__ void k_cast_out(const float* src, T* dst, int B, int S, int H, int d, int64_t s0,
-                           int64_t s1, int64_t s2, float mul) {
-    const int64_t total = static_cast<int64_t>(B) * S * H * d;
+// bf16 rows, d % 8 == 0 and d / 8 a power of two (<= 32): each thread loads 16 bytes
+// of O and of dO; the d/8 threads of a row reduce with shuffles.
+__global__ void k_bwd_pre_bf16v(const BwdArgs a, int zero_dq) {
+    const Problem& P = a.P;
+    const int tpr = P.d / 8;                       // threads per row
+    const int rpw = 32 / tpr;                      // rows per warp and step
+    const int lane = threadIdx.x & 31, sub = lane % tpr;
+    const int64_t rows = static_cast<int64_t>(P.B) * P.Hq * a.Spad;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int64_t warp_id = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5);
+    // the loop bound is uniform across the warp, so the shuffles see every lane
+    for (int64_t rbase = warp_id * rpw; rbase < rows; rbase += warps * rpw) {
+        const int64_t r = rbase + lane / tpr;
+        const bool live = r < rows;
+        const int64_t rr = live ? r : 0;
+        const int q = static_cast<int>(rr % a.Spad);
+        const int64_t bh = rr / a.Spad;
+        const int h = static_cast<int>(bh % P.Hq);
+        const int b = static_cast<int>(bh / P.Hq);
+        float s = 0.f;
+        if (live && q < P.S) {
+            const int64_t off = b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2] + sub * 8;
+            const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o) + off);
+            const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + off);
+            const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 x = __bfloat1622float2(o2[i]), y = __bfloat1622float2(g2[i]);
+                s = fmaf(x.x, y.x, s);
+                s = fmaf(x.y, y.y, s);
+            }
+        }
+        for (int o = tpr >> 1; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o, tpr);
+        if (live && sub == 0) {
+            float lse = INFINITY;
+            if (q < P.S) {
+                const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * P.S + q;
+                const float lv = a.l[mi];
+                if (lv > 0.f) lse = a.m[mi] + logf(lv);
+            }
+            a.Dvec[r] = q < P.S ? s : 0.f;
+            a.lse[r] = lse;
+        }
+    }
+    if (zero_dq) {
+        const int64_t n4 = static_cast<int64_t>(P.B) * a.Spad * P.Hq * P.d / 4;
+        float4* z = reinterpret_cast<float4*>(a.dq_acc);
+        const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+        for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4; i += nthreads)
+            z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// float32 [B, S, H, d] accumulator -> bf16 tensor with strides (s0, s1, s2); d % 8 == 0:
+// 8 consecutive channels per thread (two 16-byte loads, one 16-byte store).
+// src_rows > 0: the source is head-major [B, H, src_rows, d]; else [B, S, H, d].
+__global__ void k_cast_out_bf16v(const float* src, __nv_bfloat16* dst, int B, int S, int H, int d, int64_t s0,
+                                 int64_t s1, int64_t s2, int src_rows) {
+    const int g8 = d / 8;
+    const int64_t total = static_cast<int64_t>(B) * S * H * g8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total; i += stride) {
-        const int c = static_cast<int>(i % d);
-        int64_t r = i / d;
-        const int h = static_cast<int>(r % H);
-        r /= H;
-        const int q = static_cast<int>(r % S);
-        const int b = static_cast<int>(r / S);
-        stf(dst + b * s0 + static_cast<int64_t>(q) * s1 + h * s2 + c, src[i] * mul);
+        const int c = static_cast<int>(i % g8) * 8;
+        const int64_t row = i / g8;                 // (b * S + q) * H + h
+        const int h = static_cast<int>(row % H);
+        const int64_t bq = row / H;
+        const int q = static_cast<int>(bq % S);
+        const int b = static_cast<int>(bq / S);
+        const int64_t so = src_rows > 0 ? ((static_cast<int64_t>(b) * H + h) * src_rows + q) * d + c : i * 8;
+        const float4 x = *reinterpret_cast<const float4*>(src + so);
+        const float4 y = *reinterpret_cast<const float4*>(src + so + 4);
+        uint4 w;
+        w.x = pack_bf16(x.x, x.y);
+        w.y = pack_bf16(x.z, x.w);
+        w.z = pack_bf16(y.x, y.y);
+        w.w = pack_bf16(y.z, y.w);
+        *reinterpret_cast<uint4*>(dst + b * s0 + static_cast<int64_t>(q) * s1 + h * s2 + c) = w;
     }
 }
 
@@ -167,7 +231,14 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t s) {
     const Problem& P = a.P;
     const int64_t rows = static_cast<int64_t>(P.B) * P.Hq * a.Spad;
     const int zero = a.dq_acc != nullptr;
-    if (P.dtype == BPA_FP32)
+    const int tpr = P.d / 8;
+    const bool vec_ok = ((reinterpret_cast<uintptr_t>(a.o) | reinterpret_cast<uintptr_t>(a.dout)) & 15u) == 0 &&
+                        ((P.qs[0] | P.qs[1] | P.qs[2]) & 7) == 0;
+    if (P.dtype == BPA_BF16 && vec_ok && P.d % 8 == 0 && tpr <= 32 && (tpr & (tpr - 1)) == 0) {
+        const int threads = 256;   // a multiple of every tpr
+        const int64_t work = rows * tpr;
+        k_bwd_pre_bf16v<<<grid_for(work, threads), threads, 0, s>>>(a, zero);
+    } else if (P.dtype == BPA_FP32)
         k_bwd_pre<float><<<grid_for(rows * 32, 256), 256, 0, s>>>(a, zero);
     else
         k_bwd_pre<__nv_bfloat16><<<grid_for(rows * 32, 256), 256, 0, s>>>(a, zero);
@@ -179,18 +250,22 @@ cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t s) {
     const int64_t nq = static_cast<int64_t>(P.B) * P.S * P.Hq * P.d;
     const int64_t nk = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.d;
     if (P.dtype != BPA_BF16) return cudaErrorInvalidValue;
-    k_cast_out<__nv_bfloat16><<<grid_for(nq, 256), 256, 0, s>>>(
-        a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), P.B, P.S, P.Hq, P.d, P.qs[0], P.qs[1], P.qs[2],
-        1.f);
-    if (a.dk_acc) {
-        k_cast_out<__nv_bfloat16><<<grid_for(nk, 256), 256, 0, s>>>(
-            a.dk_acc, static_cast<__nv_bfloat16*>(a.dk), P.B, P.S, P.Hkv, P.d, P.ks[0], P.ks[1],
-            P.ks[2], 1.f);
-        k_cast_out<__nv_bfloat16><<<grid_for(nk, 256), 256, 0, s>>>(
-            a.dv_acc, static_cast<__nv_bfloat16*>(a.dv), P.B, P.S, P.Hkv, P.d, P.vs[0], P.vs[1],
-            P.vs[2], 1.f);
+    const bool vec_ok =
+        ((reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) | reinterpret_cast<uintptr_t>(a.dv)) &
+         15u) == 0 &&
+        ((P.qs[0] | P.qs[1] | P.qs[2] | P.ks[0] | P.ks[1] | P.ks[2] | P.vs[0] | P.vs[1] | P.vs[2]) & 7) == 0;
+    if (vec_ok && P.d % 8 == 0) {
+        k_cast_out_bf16v<<<grid_for(nq / 8, 256), 256, 0, s>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), P.B,
+                                                               P.S, P.Hq, P.d, P.qs[0], P.qs[1], P.qs[2], a.Spad);
+        if (a.dk_acc) {
+            k_cast_out_bf16v<<<grid_for(nk / 8, 256), 256, 0, s>>>(
+                a.dk_acc, static_cast<__nv_bfloat16*>(a.dk), P.B, P.S, P.Hkv, P.d, P.ks[0], P.ks[1], P.ks[2], 0);
+            k_cast_out_bf16v<<<grid_for(nk / 8, 256), 256, 0, s>>>(
+                a.dv_acc, static_cast<__nv_bfloat16*>(a.dv), P.B, P.S, P.Hkv, P.d, P.vs[0], P.vs[1], P.vs[2], 0);
+        }
+        return cudaGetLastError();
     }
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;   // the tensor-core backward always meets the vector conditions
 }
 
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {

@@ -48,7 +48,7 @@ struct BwdArgs {
     float* Dvec;        // [B, Hq, Spad] rowsum(dO * O); padding rows hold 0
     float* lse;         // [B, Hq, Spad] m + log(l) (natural log); +inf on padding / empty rows
     int Spad;           // S rounded up to 64
-    float* dq_acc;      // [B, S, Hq, d] float32
+    float* dq_acc;      // [B, Hq, Spad, d] float32 (head-major: a 64-row tile is contiguous)
     float* dk_acc;      // ring carries [B, S, Hkv, d] float32, or nullptr
     float* dv_acc;
     int ring_idx;

@@ -12,13 +12,18 @@
 // The scores are computed transposed (S^T = K Q^T, keys on the TMEM lanes),
 // so that P^T and dS^T come out of the softmax warps already laid out as the
 // A operands of the dV and dK products.
-// TMEM (512 columns): S^T x2 [0,128), dP^T [128,192), dQ^T [192,256),
-// dK [256,384), dV [384,512).
+// TMEM (512 columns): S^T [0,64), dP^T x2 [64,192), dQ^T [192,256),
+// dK [256,384), dV [384,512).  dP^T is double-buffered so that S^T and dP^T
+// of tile it are computed while the softmax warps still work on tile it-1.
+// dQ partial tiles go to a head-major float32 accumulator [B, Hq, S', 128]
+// (S' = S rounded up to 64), where one 64 x 128 tile is one contiguous 32 KB
+// block: the dQ warps stage it in shared memory and add it with one bulk
+// reduction.
 // Roles (320 threads):
 //   warps 0-3  thread r owns key row r: P, dS from S^T, dP^T -> shared memory;
 //              at the end dK (scaled) -> output;
-//   warps 4-7  thread r owns channel r of dQ^T: TMEM -> global float32
-//              accumulator (red.add); at the end dV -> output;
+//   warps 4-7  thread r owns channel r of dQ^T: TMEM -> shared staging ->
+//              global float32 accumulator (bulk reduce-add); at the end dV -> output;
 //   warp 8     TMA producer: K, V once; Q, dO (+ lse, D) per query tile;
 //   warp 9     MMA issuer, TMEM owner.
 #include <math.h>
@@ -44,14 +49,15 @@ constexpr int OFF_DO = OFF_Q + NS * BQ * D * 2;
 constexpr int OFF_P = OFF_DO + NS * BQ * D * 2;     // P^T  [128 keys][64 q] bf16, x2
 constexpr int OFF_DS = OFF_P + 2 * BK * BQ * 2;     // dS^T [128 keys][64 q] bf16, x2
 constexpr int OFF_ST = OFF_DS + 2 * BK * BQ * 2;    // per stage: lse[64], D[64] float
-constexpr int OFF_BAR = OFF_ST + NS * 512;
+constexpr int OFF_DQ = OFF_ST + NS * 512;           // dQ staging [64 q][128 ch] float32
+constexpr int OFF_BAR = OFF_DQ + BQ * D * 4;
 constexpr int SMEM = OFF_BAR + 256 + 1024;
 constexpr int PT_BYTES = BK * BQ * 2;
 
 // barrier slots
-constexpr int B_KV = 0, B_QF = 1, B_QE = 1 + NS, B_S = 1 + 2 * NS, B_DP = 3 + 2 * NS, B_DS = 4 + 2 * NS,
-              B_DQF = 5 + 2 * NS, B_DQE = 6 + 2 * NS, B_PF = 7 + 2 * NS, B_KVD = 9 + 2 * NS,
-              B_FIN = 10 + 2 * NS, NBAR = 11 + 2 * NS;
+constexpr int B_KV = 0, B_QF = 1, B_QE = 1 + NS, B_S = 1 + 2 * NS, B_SF = 2 + 2 * NS, B_DP = 3 + 2 * NS,
+              B_DS = 5 + 2 * NS, B_DQF = 6 + 2 * NS, B_DQE = 7 + 2 * NS, B_PF = 8 + 2 * NS, B_KVD = 10 + 2 * NS,
+              B_FIN = 11 + 2 * NS, B_STW = 12 + 2 * NS, B_STF = 13 + 2 * NS, NBAR = 14 + 2 * NS;
 
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BK, BQ, 0, 0);     // S^T, dP^T: both K-major
 constexpr uint32_t IDESC_KV = idesc_bf16_f32(BK, D, 0, 1);     // dV, dK: A K-major, B MN-major
@@ -120,9 +126,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(B_QF + s), 1);
             mbar_init(BAR(B_QE + s), 1);
         }
-        mbar_init(BAR(B_S + 0), 1);
-        mbar_init(BAR(B_S + 1), 1);
-        mbar_init(BAR(B_DP), 1);
+        mbar_init(BAR(B_S), 1);
+        mbar_init(BAR(B_SF), 128);
+        mbar_init(BAR(B_DP + 0), 1);
+        mbar_init(BAR(B_DP + 1), 1);
         mbar_init(BAR(B_DS), 128);
         mbar_init(BAR(B_DQF), 1);
         mbar_init(BAR(B_DQE), 128);
@@ -130,6 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR(B_PF + 1), 1);
         mbar_init(BAR(B_KVD), 1);
         mbar_init(BAR(B_FIN), 1);
+        mbar_init(BAR(B_STW), 128);
+        mbar_init(BAR(B_STF), 1);
         *abort_flag = (a.status && (*reinterpret_cast<volatile uint32_t*>(a.status) & ST_TIMEOUT)) ? 1 : 0;
         fence_mbar_init();
     }
@@ -141,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tDP = tmem + 128, tDQ = tmem + 192, tDK = tmem + 256, tDV = tmem + 384;
+    const uint32_t tS = tmem, tDP = tmem + 64, tDQ = tmem + 192, tDK = tmem + 256, tDV = tmem + 384;
     const bool skip = *abort_flag != 0;
     const int n_it = skip ? 0 : W.n_it;
 
@@ -187,20 +196,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n_it > 0) {
             bool ok = mbar_wait(BAR(B_KV), 0, abort_flag, a.status, 0x50);
+            // order per tile it: S_it (once S_it-1 has been read), dP_it, then dV / dK / dQ
+            // of tile it-1 (once its dS is ready)
             for (int it = 0; ok && it <= n_it; ++it) {
                 if (it < n_it) {
                     const int st = it % NS;
                     if (!mbar_wait(BAR(B_QF + st), (it / NS) & 1, abort_flag, a.status, 0x51)) break;
+                    if (it > 0 && !mbar_wait(BAR(B_SF), (it - 1) & 1, abort_flag, a.status, 0x54)) break;
                     tc_fence_after();
-                    const uint32_t qb = sb + OFF_Q + st * BQ * D * 2;
+                    const uint32_t qb = sb + OFF_Q + st * BQ * D * 2, dob = sb + OFF_DO + st * BQ * D * 2;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
                         const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
-                        tc_mma_ss(tS + (it & 1) * BQ, sdesc_sw128(sb + OFF_K + offk, 16, 1024),
-                                  sdesc_sw128(qb + offq, 16, 1024), IDESC_S, kk > 0);
+                        tc_mma_ss(tS, sdesc_sw128(sb + OFF_K + offk, 16, 1024), sdesc_sw128(qb + offq, 16, 1024),
+                                  IDESC_S, kk > 0);
                     }
-                    tc_commit(BAR(B_S + (it & 1)));
+                    tc_commit(BAR(B_S));
+                    // dP^T buffer (it & 1) last held tile it-2, whose dS was waited for below
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
+                        const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
+                        tc_mma_ss(tDP + (it & 1) * BQ, sdesc_sw128(sb + OFF_V + offk, 16, 1024),
+                                  sdesc_sw128(dob + offq, 16, 1024), IDESC_S, kk > 0);
+                    }
+                    tc_commit(BAR(B_DP + (it & 1)));
                 }
                 if (it > 0) {
                     const int p = it - 1, pst = p % NS, buf = p & 1;
@@ -227,18 +248,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_commit(BAR(B_QE + pst));
                     if (p == n_it - 1) tc_commit(BAR(B_KVD));
                 }
-                if (it < n_it) {
-                    const int st = it % NS;
-                    const uint32_t dob = sb + OFF_DO + st * BQ * D * 2;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
-                        const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
-                        tc_mma_ss(tDP, sdesc_sw128(sb + OFF_V + offk, 16, 1024),
-                                  sdesc_sw128(dob + offq, 16, 1024), IDESC_S, kk > 0);
-                    }
-                    tc_commit(BAR(B_DP));
-                }
             }
             tc_commit(BAR(B_FIN));
             drain_wait(BAR(B_FIN), 0, a.status);
@@ -257,19 +266,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool aborted = false;
         for (int it = 0; it < n_it; ++it) {
             const int h = iter_head(it), q0 = iter_q0(it), st = it % NS, buf = it & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_S + buf), (it >> 1) & 1, abort_flag, a.status, 0x60))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_S), it & 1, abort_flag, a.status, 0x60))) {
                 aborted = true;
                 break;
             }
             tc_fence_after();
             float p[BQ];
+            {
+                uint32_t v[64];
+                tmem_ld64(tS + lane_base, v);
 #pragma unroll
-            for (int c = 0; c < BQ / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tS + buf * BQ + c * 32 + lane_base, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) p[c * 32 + i] = __uint_as_float(v[i]) * sl2;
+                for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(v[i]) * sl2;
             }
+            tc_fence_before();
+            mbar_arrive(BAR(B_SF));   // S^T may be overwritten by the next tile
             // the lse / D of this tile came with the Q tile: observe that copy's barrier
             // (it cannot have moved on: the stage is refilled only after this tile's dS)
             if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_QF + st), (it / NS) & 1, abort_flag, a.status, 0x64))) {
@@ -308,17 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st_shared_v4(pb + sw128_offset(r, cc), pack_bf16(p[cc * 8 + 0], p[cc * 8 + 1]),
                              pack_bf16(p[cc * 8 + 2], p[cc * 8 + 3]), pack_bf16(p[cc * 8 + 4], p[cc * 8 + 5]),
                              pack_bf16(p[cc * 8 + 6], p[cc * 8 + 7]));
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DP), it & 1, abort_flag, a.status, 0x62))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DP + buf), (it >> 1) & 1, abort_flag, a.status, 0x62))) {
                 aborted = true;
                 break;
             }
             tc_fence_after();
+            {
+                uint32_t v[64];
+                tmem_ld64(tDP + buf * BQ + lane_base, v);
 #pragma unroll
-            for (int c = 0; c < BQ / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tDP + c * 32 + lane_base, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) p[c * 32 + i] *= __uint_as_float(v[i]) - Dq[c * 32 + i];
+                for (int i = 0; i < 64; ++i) p[i] *= __uint_as_float(v[i]) - Dq[i];
             }
 #pragma unroll
             for (int cc = 0; cc < BQ / 8; ++cc)
@@ -390,21 +399,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            uint32_t v0[32], v1[32];
-            tmem_ld32(tDQ + lane_base, v0);
-            tmem_ld32(tDQ + 32 + lane_base, v1);
+            uint32_t v[64];
+            tmem_ld64(tDQ + lane_base, v);
             tc_fence_before();
             mbar_arrive(BAR(B_DQE));
-            float* base = a.dq_acc + ((static_cast<int64_t>(W.b) * P.S + q0) * P.Hq + h) * D + ch;
-            const int64_t qstride = static_cast<int64_t>(P.Hq) * D;
-            const int nq = min(BQ, P.S - q0);
+            // staging buffer: the bulk reduction of the previous tile must have read it
+            if (it > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_STF), (it - 1) & 1, abort_flag, a.status, 0x72))) {
+                aborted = true;
+                break;
+            }
+            const uint32_t stg = sb + OFF_DQ + ch * 4;
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-                if (c < nq) atomicAdd(base + c * qstride, __uint_as_float(v0[c]) * P.scale);
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-                if (c + 32 < nq) atomicAdd(base + (c + 32) * qstride, __uint_as_float(v1[c]) * P.scale);
+            for (int c = 0; c < 64; ++c) st_shared_f32(stg + c * (D * 4), __uint_as_float(v[c]) * P.scale);
+            fence_proxy_async_smem();
+            mbar_arrive(BAR(B_STW));
+            if (ch == 0) {
+                if (!mbar_wait(BAR(B_STW), it & 1, abort_flag, a.status, 0x73)) {
+                    aborted = true;
+                } else {
+                    // rows q0 .. q0+63 of head h: one contiguous block of the accumulator
+                    float* tile = a.dq_acc + ((static_cast<int64_t>(W.b) * P.Hq + h) * a.Spad + q0) * D;
+                    bulk_reduce_add_f32(tile, sb + OFF_DQ, BQ * D * 4);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                    mbar_arrive(BAR(B_STF));
+                }
+            }
+            if (__any_sync(0xffffffffu, aborted)) {
+                aborted = true;
+                break;
+            }
         }
+        if (ch == 0) bulk_wait_all();
         // ---- epilogue: dV
         if (!aborted && !skip) {
             if (n_it > 0) {
