@@ -37,7 +37,7 @@ namespace {
 constexpr int D = 128;        // head dim
 constexpr int BK = 128;       // keys per CTA
 constexpr int BQ = 64;        // queries per tile
-constexpr int NS = 2;         // Q / dO stages
+constexpr int NS = 3;         // Q / dO stages
 constexpr int kThreads = 320;
 
 constexpr int SUBK = BK * 128;    // one 64-channel slab of the key tile
@@ -46,9 +46,10 @@ constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + BK * D * 2;
 constexpr int OFF_Q = OFF_V + BK * D * 2;
 constexpr int OFF_DO = OFF_Q + NS * BQ * D * 2;
-constexpr int OFF_P = OFF_DO + NS * BQ * D * 2;     // P^T  [128 keys][64 q] bf16, x2
-constexpr int OFF_DS = OFF_P + 2 * BK * BQ * 2;     // dS^T [128 keys][64 q] bf16, x2
-constexpr int OFF_ST = OFF_DS + 2 * BK * BQ * 2;    // per stage: lse[64], D[64] float
+constexpr int NPB = 1;        // P^T / dS^T buffers
+constexpr int OFF_P = OFF_DO + NS * BQ * D * 2;     // P^T  [128 keys][64 q] bf16, x NPB
+constexpr int OFF_DS = OFF_P + NPB * BK * BQ * 2;   // dS^T [128 keys][64 q] bf16, x NPB
+constexpr int OFF_ST = OFF_DS + NPB * BK * BQ * 2;  // per stage: lse[64], D[64] float
 constexpr int OFF_DQ = OFF_ST + NS * 512;           // dQ staging [64 q][128 ch] float32
 constexpr int OFF_BAR = OFF_DQ + BQ * D * 4;
 constexpr int SMEM = OFF_BAR + 256 + 1024;
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_commit(BAR(B_DP + (it & 1)));
                 }
                 if (it > 0) {
-                    const int p = it - 1, pst = p % NS, buf = p & 1;
+                    const int p = it - 1, pst = p % NS, buf = p % NPB;
                     if (!mbar_wait(BAR(B_DS), p & 1, abort_flag, a.status, 0x52)) break;
                     tc_fence_after();
                     const uint32_t pb = sb + OFF_P + buf * PT_BYTES, db = sb + OFF_DS + buf * PT_BYTES;
@@ -306,13 +307,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (q < qmin || q > qmax) p[c] = 0.f;
                 }
             }
-            // the P^T / dS^T buffer is free once the MMAs of two tiles ago are done
-            if (it >= 2 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_PF + buf), ((it - 2) >> 1) & 1, abort_flag,
-                                                              a.status, 0x61))) {
+            // the P^T / dS^T buffer is free once the MMAs of the previous tile that read it are done
+            if (it >= NPB && !__all_sync(0xffffffffu, mbar_wait(BAR(B_PF + it % NPB), ((it - NPB) / NPB) & 1,
+                                                                abort_flag, a.status, 0x61))) {
                 aborted = true;
                 break;
             }
-            const uint32_t pb = sb + OFF_P + buf * PT_BYTES, db = sb + OFF_DS + buf * PT_BYTES;
+            const uint32_t pb = sb + OFF_P + (it % NPB) * PT_BYTES, db = sb + OFF_DS + (it % NPB) * PT_BYTES;
 #pragma unroll
             for (int cc = 0; cc < BQ / 8; ++cc)
                 st_shared_v4(pb + sw128_offset(r, cc), pack_bf16(p[cc * 8 + 0], p[cc * 8 + 1]),
