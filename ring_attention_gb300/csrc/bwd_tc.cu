@@ -197,6 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n_it > 0) {
             bool ok = mbar_wait(BAR(B_KV), 0, abort_flag, a.status, 0x50);
+            // descriptors of the resident K / V tile (K-major, and K as an MN-major A operand)
+            const uint64_t kd0 = sdesc_sw128(sb + OFF_K, 16, 1024), vd0 = sdesc_sw128(sb + OFF_V, 16, 1024);
+            const uint64_t kmn0 = sdesc_sw128(sb + OFF_K, SUBK, 1024);
             // order per tile it: S_it (once S_it-1 has been read), dP_it, then dV / dK / dQ
             // of tile it-1 (once its dS is ready)
             for (int it = 0; ok && it <= n_it; ++it) {
@@ -205,13 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(BAR(B_QF + st), (it / NS) & 1, abort_flag, a.status, 0x51)) break;
                     if (it > 0 && !mbar_wait(BAR(B_SF), (it - 1) & 1, abort_flag, a.status, 0x54)) break;
                     tc_fence_after();
-                    const uint32_t qb = sb + OFF_Q + st * BQ * D * 2, dob = sb + OFF_DO + st * BQ * D * 2;
+                    const uint64_t qd = sdesc_sw128(sb + OFF_Q + st * BQ * D * 2, 16, 1024);
+                    const uint64_t dod = sdesc_sw128(sb + OFF_DO + st * BQ * D * 2, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
                         const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
-                        tc_mma_ss(tS, sdesc_sw128(sb + OFF_K + offk, 16, 1024), sdesc_sw128(qb + offq, 16, 1024),
-                                  IDESC_S, kk > 0);
+                        tc_mma_ss(tS, sdesc_advance(kd0, offk), sdesc_advance(qd, offq), IDESC_S, kk > 0);
                     }
                     tc_commit(BAR(B_S));
                     // dP^T buffer (it & 1) last held tile it-2, whose dS was waited for below
@@ -219,8 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
                         const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
-                        tc_mma_ss(tDP + (it & 1) * BQ, sdesc_sw128(sb + OFF_V + offk, 16, 1024),
-                                  sdesc_sw128(dob + offq, 16, 1024), IDESC_S, kk > 0);
+                        tc_mma_ss(tDP + (it & 1) * BQ, sdesc_advance(vd0, offk), sdesc_advance(dod, offq), IDESC_S,
+                                  kk > 0);
                     }
                     tc_commit(BAR(B_DP + (it & 1)));
                 }
@@ -228,22 +231,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int p = it - 1, pst = p % NS, buf = p % NPB;
                     if (!mbar_wait(BAR(B_DS), p & 1, abort_flag, a.status, 0x52)) break;
                     tc_fence_after();
-                    const uint32_t pb = sb + OFF_P + buf * PT_BYTES, db = sb + OFF_DS + buf * PT_BYTES;
-                    const uint32_t qb = sb + OFF_Q + pst * BQ * D * 2, dob = sb + OFF_DO + pst * BQ * D * 2;
+                    const uint64_t pd = sdesc_sw128(sb + OFF_P + buf * PT_BYTES, 16, 1024);
+                    const uint64_t dsd = sdesc_sw128(sb + OFF_DS + buf * PT_BYTES, 16, 1024);
+                    const uint64_t qmn = sdesc_sw128(sb + OFF_Q + pst * BQ * D * 2, SUBQ, 1024);
+                    const uint64_t domn = sdesc_sw128(sb + OFF_DO + pst * BQ * D * 2, SUBQ, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BQ / 16; ++kk) {
                         const uint32_t acc = (p > 0 || kk > 0) ? 1u : 0u;
-                        tc_mma_ss(tDV, sdesc_sw128(pb + kk * 32, 16, 1024), sdesc_sw128(dob + kk * 2048, SUBQ, 1024),
-                                  IDESC_KV, acc);
-                        tc_mma_ss(tDK, sdesc_sw128(db + kk * 32, 16, 1024), sdesc_sw128(qb + kk * 2048, SUBQ, 1024),
-                                  IDESC_KV, acc);
+                        tc_mma_ss(tDV, sdesc_advance(pd, kk * 32), sdesc_advance(domn, kk * 2048), IDESC_KV, acc);
+                        tc_mma_ss(tDK, sdesc_advance(dsd, kk * 32), sdesc_advance(qmn, kk * 2048), IDESC_KV, acc);
                     }
                     if (p > 0 && !mbar_wait(BAR(B_DQE), (p - 1) & 1, abort_flag, a.status, 0x53)) break;
                     tc_fence_after();
+                    const uint64_t dsmn = sdesc_sw128(sb + OFF_DS + buf * PT_BYTES, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        tc_mma_ss(tDQ, sdesc_sw128(sb + OFF_K + kk * 2048, SUBK, 1024),
-                                  sdesc_sw128(db + kk * 2048, 16, 1024), IDESC_Q, kk > 0);
+                        tc_mma_ss(tDQ, sdesc_advance(kmn0, kk * 2048), sdesc_advance(dsmn, kk * 2048), IDESC_Q, kk > 0);
                     tc_commit(BAR(B_DQF));
                     tc_commit(BAR(B_PF + buf));
                     tc_commit(BAR(B_QE + pst));

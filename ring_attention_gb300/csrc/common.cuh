@@ -214,6 +214,11 @@ BPA_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return d;
 }
 
+// A descriptor advanced by `bytes` within the same shared-memory window: the
+// start-address field holds addr >> 4 in its low 14 bits and shared memory is
+// below 256 KB, so the advance is a plain add that cannot carry out of the field.
+BPA_DEV uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // 32 lanes x 32 columns of 32-bit TMEM -> registers, then wait for the load.
 BPA_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -241,6 +246,17 @@ BPA_DEV void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
         : "r"(taddr)
         : "memory");
 }
+
+// registers -> 32 lanes x 16 columns of TMEM (no wait: the caller waits once).
+BPA_DEV void tmem_st16_nowait(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+BPA_DEV void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // registers -> 32 lanes x 32 columns of TMEM, then wait for the store.
 BPA_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -279,6 +295,31 @@ BPA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uin
 // 128-byte-swizzled [rows][128 B] tile whose base is 1024-byte aligned.
 BPA_DEV uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// ---- packed float32 pairs (Blackwell f32x2 instructions) --------------------
+BPA_DEV uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+BPA_DEV void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+BPA_DEV uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {   // a * b + c, per lane
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+BPA_DEV uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+BPA_DEV float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 constexpr float kLog2e = 1.4426950408889634f;

@@ -1,25 +1,32 @@
 // fwd_tc.cu - blockwise attention forward on the 5th-generation tensor cores (bf16, d = 64 / 128).
 //
-// One CTA owns one 128-row query tile of one (batch, q head) and walks the
-// 128-key tiles its mask allows, folding each into a running
-// (max, numerator, denominator) carry ("bpt.py", _blockwise_attention_fwd /
-// scan_kv_block):
+// One CTA owns two consecutive 128-row query tiles of one (batch, q head)
+// and walks the 128-key tiles their masks allow, folding each into a running
+// (max, numerator, denominator) carry per query row ("bpt.py",
+// _blockwise_attention_fwd / scan_kv_block):
 //     m' = max(m, rowmax S);  P = exp(S - m');  num = num * exp(m - m') + P V;
 //     den = den * exp(m - m') + rowsum P
-// Roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t (TMEM lane t); reads S from
-//              TMEM, applies scale / bias / mask, keeps the row statistics,
-//              writes P (bf16) to shared memory, rescales O when needed;
-//   warp 4     TMA producer: Q once, then K / V tiles through an NS-stage ring;
-//   warp 5     MMA issuer (one thread): S = Q K^T into a double-buffered TMEM
-//              tile, O += P V into a TMEM accumulator; owns the TMEM allocation.
-// The numerator is rescaled lazily: the reference max only moves when a row's
-// max grows by more than kTau (log2 units), which is exact in real arithmetic
-// because numerator and denominator share the reference.
-// Fully masked tiles are never visited (the key range is cut by position);
-// only tiles that straddle a mask edge apply the elementwise mask.
-// Every wait is bounded (see common.cuh); on a timeout the CTA drains its
-// in-flight copies and MMAs, frees TMEM and returns.
+// Both query tiles share every K / V tile that is loaded.
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [384,384+d).
+// P (bf16, two per 32-bit column) is written back over the first 64 columns
+// of its S tile and read from there by the P V product (A operand in TMEM).
+// Roles (320 threads):
+//   warps 0-3  softmax of query tile 0: thread t owns row t (TMEM lane t);
+//   warps 4-7  softmax of query tile 1;
+//   warp 8     TMA producer: Q0, Q1 once, then K / V tiles through their rings;
+//   warp 9     MMA issuer (one thread), TMEM owner.  Issue order per key tile j:
+//              [P0(j) ready] P0 V -> O0, S0(j+1) = Q0 K^T ; [P1(j) ready] P1 V -> O1,
+//              S1(j+1): the tensor core works on one tile while the other tile's
+//              softmax runs.  The products of a tile execute in issue order, so
+//              when S_i(j+1) completes, P_i(j) V has consumed P_i(j) and O_i holds
+//              every key tile up to j.
+// The numerator is rescaled lazily: the reference max of a row only moves when
+// its max grows by more than kTau (log2 units); exact in real arithmetic because
+// numerator and denominator share the reference.
+// Fully masked tiles are never visited (key ranges are cut by position); only
+// tiles that straddle a mask edge apply the elementwise mask.
+// Every wait is bounded (common.cuh); on a timeout the CTA drains its in-flight
+// copies and MMAs, frees TMEM and returns.
 #include <math.h>
 
 #include "bpa_internal.h"
@@ -29,39 +36,44 @@ namespace bpa {
 namespace {
 
 constexpr int BM = 128;       // query rows per tile
+constexpr int NQT = 2;        // query tiles per CTA
 constexpr int BN = 128;       // keys per tile
 constexpr float kTau = 8.f;   // lazy-rescale threshold, log2 units
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 
 template <int D>
 struct FwdCfg {
-    static constexpr int NS = D == 128 ? 2 : 4;    // K/V pipeline stages
-    static constexpr int Q_BYTES = BM * D * 2;
+    // K and V flow through separate rings: K tile j is needed one product
+    // earlier than V tile j and is released earlier, so it gets more stages.
+    static constexpr int NSK = D == 128 ? 3 : 4;   // K stages
+    static constexpr int NSV = D == 128 ? 2 : 4;   // V stages
+    static constexpr int Q_BYTES = BM * D * 2;     // one query tile
     static constexpr int KV_BYTES = BN * D * 2;
-    static constexpr int P_BYTES = BM * BN * 2;
     static constexpr int SUB = 128 * 128;          // one 64-column slab of 128 rows
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + Q_BYTES;
-    static constexpr int OFF_V = OFF_K + NS * KV_BYTES;
-    static constexpr int OFF_P = OFF_V + NS * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_K = OFF_Q + NQT * Q_BYTES;
+    static constexpr int OFF_V = OFF_K + NSK * KV_BYTES;
+    static constexpr int OFF_BAR = OFF_V + NSV * KV_BYTES;
     static constexpr int SMEM = OFF_BAR + 256 + 1024;   // + slack to align the base to 1024
-    // barrier slots
-    static constexpr int B_Q = 0, B_K = 1, B_V = 1 + NS, B_E = 1 + 2 * NS, B_S = 1 + 3 * NS,
-                         B_P = 3 + 3 * NS, B_PV = 5 + 3 * NS, B_FIN = 7 + 3 * NS,
-                         NBAR = 8 + 3 * NS;
+    // barrier slots: K full / empty, V full / empty, S, P, O per query tile
+    static constexpr int B_Q = 0, B_KF = 1, B_KE = 1 + NSK, B_VF = 1 + 2 * NSK, B_VE = 1 + 2 * NSK + NSV,
+                         B_S = 1 + 2 * NSK + 2 * NSV, B_P = B_S + 2, B_O = B_S + 4, B_FIN = B_S + 6,
+                         NBAR = B_S + 7;
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);   // Q, K both K-major
-    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 0, 1);   // P K-major, V MN-major
+    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 0, 1);   // P (TMEM), V MN-major
 };
 
 struct Tile {
-    int b, h, hkv, q0, kt_lo, n_kv;
-    int rlo, rhi;   // key range of this launch (ring super-block or whole sequence)
+    int b, h, hkv, q0;       // q0: first row of query tile 0
+    int rlo, rhi;            // key range of this launch (ring super-block or whole sequence)
+    int kt0;                 // first key tile visited by the CTA
+    int n;                   // key tiles visited by the CTA
+    int lo[NQT], hi[NQT];    // per query tile: visited step range [lo, hi] (empty if lo > hi)
 };
 
 __device__ __forceinline__ Tile decode_tile(const FwdArgs& a) {
     const Problem& P = a.P;
-    const int nqt = (P.S + BM - 1) / BM;
+    const int nqp = (P.S + NQT * BM - 1) / (NQT * BM);
     int r = blockIdx.x;
     const int gi = r % P.G;
     r /= P.G;
@@ -69,10 +81,9 @@ __device__ __forceinline__ Tile decode_tile(const FwdArgs& a) {
     t.hkv = r % P.Hkv;
     r /= P.Hkv;
     t.b = r % P.B;
-    const int qt = nqt - 1 - r / P.B;   // heaviest (causal) tiles first
+    const int qp = nqp - 1 - r / P.B;   // heaviest (causal) query pairs first
     t.h = t.hkv * P.G + gi;
-    t.q0 = qt * BM;
-    const int q_last = min(t.q0 + BM - 1, P.S - 1);
+    t.q0 = qp * NQT * BM;
     t.rlo = 0;
     t.rhi = P.S - 1;
     if (a.acc) {
@@ -81,12 +92,33 @@ __device__ __forceinline__ Tile decode_tile(const FwdArgs& a) {
         t.rlo = j * P.ring_blk;
         t.rhi = t.rlo + P.ring_blk - 1;
     }
-    int lo = t.rlo, hi = t.rhi;
-    if (P.causal) hi = min(hi, q_last);
-    if (P.wr >= 0) hi = min(hi, q_last + P.wr);
-    if (P.wl >= 0) lo = max(lo, t.q0 - P.wl);
-    t.kt_lo = lo / BN;
-    t.n_kv = lo <= hi ? hi / BN - t.kt_lo + 1 : 0;
+    int ktlo[NQT], kthi[NQT];
+    int ulo = 1 << 30, uhi = -1;
+#pragma unroll
+    for (int i = 0; i < NQT; ++i) {
+        const int qa = t.q0 + i * BM, qb = min(qa + BM - 1, P.S - 1);
+        int lo = t.rlo, hi = t.rhi;
+        if (qa >= P.S) hi = -1;
+        if (P.causal) hi = min(hi, qb);
+        if (P.wr >= 0) hi = min(hi, qb + P.wr);
+        if (P.wl >= 0) lo = max(lo, qa - P.wl);
+        if (lo <= hi) {
+            ktlo[i] = lo / BN;
+            kthi[i] = hi / BN;
+            ulo = min(ulo, ktlo[i]);
+            uhi = max(uhi, kthi[i]);
+        } else {
+            ktlo[i] = 1;
+            kthi[i] = 0;
+        }
+    }
+    t.kt0 = uhi >= 0 ? ulo : 0;
+    t.n = uhi >= 0 ? uhi - ulo + 1 : 0;
+#pragma unroll
+    for (int i = 0; i < NQT; ++i) {
+        t.lo[i] = ktlo[i] - t.kt0;
+        t.hi[i] = kthi[i] - t.kt0;
+    }
     return t;
 }
 
@@ -94,6 +126,87 @@ __device__ __forceinline__ Tile decode_tile(const FwdArgs& a) {
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
     int never = 0;
     mbar_wait(bar, parity, &never, status, 0xD0);
+}
+
+// Softmax passes over one 128-column row of S in TMEM, specialised on whether
+// an additive bias is present and whether the tile straddles a mask edge, so
+// that interior tiles run branch-free.  Scores are in log2 units:
+// x = S * scale * log2(e) + bias * log2(e), -inf where masked.
+struct RowCtx {
+    uint32_t tS;            // TMEM address of this thread's row of S
+    float sl2;              // scale * log2(e)
+    const float* bias_row;  // bias of this row (broadcast dims have stride 0)
+    int64_t bs3;            // bias stride along keys
+    int k0, kmin, kmax, S;  // first key of the tile, allowed keys of the row, length
+};
+
+template <bool BIAS, bool EDGE>
+__device__ __forceinline__ float score_at(const RowCtx& R, uint32_t raw, int i) {
+    float x = __uint_as_float(raw) * R.sl2;
+    if (BIAS) x = fmaf(R.bias_row[min(R.k0 + i, R.S - 1) * R.bs3], kLog2e, x);
+    if (EDGE) x = (R.k0 + i < R.kmin || R.k0 + i > R.kmax) ? -INFINITY : x;
+    return x;
+}
+
+// Two passes over the 128-column row of S.  S is read from TMEM twice rather
+// than held in registers: 128 live scores do not fit the 168 registers a
+// thread has with 10 warps.  Interior tiles use packed float32-pair
+// arithmetic and a 3-input max.
+
+// pass 1: the row max of the scores
+template <bool BIAS, bool EDGE>
+__device__ __forceinline__ float row_max(const RowCtx& R) {
+    float mt = -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < BN / 64; ++cc) {
+        uint32_t r[64];
+        tmem_ld64(R.tS + cc * 64, r);
+        if (!BIAS && !EDGE) {
+            float m2 = -INFINITY;   // scale > 0: max of raw S, scaled once
+#pragma unroll
+            for (int i = 0; i < 32; ++i) m2 = fmax3(m2, __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            mt = fmaxf(mt, m2 * R.sl2);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) mt = fmaxf(mt, score_at<BIAS, EDGE>(R, r[i], cc * 64 + i));
+        }
+    }
+    return mt;
+}
+
+// pass 2: P = exp2(x - mref) as bf16 pairs written over the first 64 columns
+// of the row's S (chunk cc reads S columns [64cc, 64cc+64) and writes P
+// columns [32cc, 32cc+32)); returns the row sum of P in float32
+template <bool BIAS, bool EDGE>
+__device__ __forceinline__ float row_exp(const RowCtx& R, float mref) {
+    uint64_t rs2 = 0;   // two float32 partial sums
+    const uint64_t sl2x2 = f2_pack(R.sl2, R.sl2), negm2 = f2_pack(-mref, -mref);
+#pragma unroll
+    for (int cc = 0; cc < BN / 64; ++cc) {
+        uint32_t r[64];
+        tmem_ld64(R.tS + cc * 64, r);
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            uint64_t p2;
+            if (!BIAS && !EDGE) {
+                float x0, x1;
+                f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2, negm2), x0, x1);
+                p2 = f2_pack(ex2(x0), ex2(x1));
+            } else {
+                p2 = f2_pack(ex2(score_at<BIAS, EDGE>(R, r[2 * i], cc * 64 + 2 * i) - mref),
+                             ex2(score_at<BIAS, EDGE>(R, r[2 * i + 1], cc * 64 + 2 * i + 1) - mref));
+            }
+            rs2 = fadd2(rs2, p2);
+            float p0, p1;
+            f2_unpack(p2, p0, p1);
+            pk[i] = pack_bf16(p0, p1);
+        }
+        tmem_st32(R.tS + cc * 32, pk);
+    }
+    float a, b;
+    f2_unpack(rs2, a, b);
+    return a + b;
 }
 
 template <int D>
@@ -116,22 +229,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(C::B_Q), 1);
-        for (int s = 0; s < C::NS; ++s) {
-            mbar_init(BAR(C::B_K + s), 1);
-            mbar_init(BAR(C::B_V + s), 1);
-            mbar_init(BAR(C::B_E + s), 1);
+        for (int s = 0; s < C::NSK; ++s) {
+            mbar_init(BAR(C::B_KF + s), 1);
+            mbar_init(BAR(C::B_KE + s), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int s = 0; s < C::NSV; ++s) {
+            mbar_init(BAR(C::B_VF + s), 1);
+            mbar_init(BAR(C::B_VE + s), 1);
+        }
+        for (int i = 0; i < NQT; ++i) {
             mbar_init(BAR(C::B_S + i), 1);
             mbar_init(BAR(C::B_P + i), 128);
-            mbar_init(BAR(C::B_PV + i), 1);
+            mbar_init(BAR(C::B_O + i), 1);
         }
         mbar_init(BAR(C::B_FIN), 1);
         // a CTA that starts after another one gave up does no work
         *abort_flag = (a.status && (*reinterpret_cast<volatile uint32_t*>(a.status) & ST_TIMEOUT)) ? 1 : 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -139,88 +255,129 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS0 = tmem, tO = tmem + 256;
-    const int n_kv = *abort_flag ? 0 : T.n_kv;
     const bool skip = *abort_flag != 0;
+    const int n = skip ? 0 : T.n;
+    auto active = [&](int i, int j) { return j >= T.lo[i] && j <= T.hi[i]; };
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && n_kv > 0) {
+        if (lane == 0 && n > 0) {
             tma_prefetch(&tmQ);
             tma_prefetch(&tmK);
             tma_prefetch(&tmV);
-            mbar_expect_tx(BAR(C::B_Q), C::Q_BYTES);
-            for (int sub = 0; sub < D / 64; ++sub)
-                tma_load_4d(sb + C::OFF_Q + sub * C::SUB, &tmQ, BAR(C::B_Q), sub * 64, T.h, T.q0, T.b);
-            int n_issued = 0;   // tiles whose loads were issued
-            for (int j = 0; j < n_kv; ++j) {
-                const int st = j % C::NS, use = j / C::NS;
-                if (use > 0 && !mbar_wait(BAR(C::B_E + st), (use - 1) & 1, abort_flag, a.status, 0x10))
-                    break;
-                const int k0 = (T.kt_lo + j) * BN;
-                mbar_expect_tx(BAR(C::B_K + st), C::KV_BYTES);
+            mbar_expect_tx(BAR(C::B_Q), NQT * C::Q_BYTES);
+            for (int i = 0; i < NQT; ++i)
                 for (int sub = 0; sub < D / 64; ++sub)
-                    tma_load_4d(sb + C::OFF_K + st * C::KV_BYTES + sub * C::SUB, &tmK, BAR(C::B_K + st),
-                                sub * 64, T.hkv, k0, T.b);
-                mbar_expect_tx(BAR(C::B_V + st), C::KV_BYTES);
+                    tma_load_4d(sb + C::OFF_Q + i * C::Q_BYTES + sub * C::SUB, &tmQ, BAR(C::B_Q), sub * 64, T.h,
+                                T.q0 + i * BM, T.b);
+            // K runs one tile ahead of V: K0, K1, V0, K2, V1, ...
+            int nk = 0, nv = 0;   // tiles issued
+            bool ok = true;
+            auto load_k = [&](int j) {
+                const int st = j % C::NSK, use = j / C::NSK;
+                if (use > 0 && !mbar_wait(BAR(C::B_KE + st), (use - 1) & 1, abort_flag, a.status, 0x10)) return false;
+                mbar_expect_tx(BAR(C::B_KF + st), C::KV_BYTES);
                 for (int sub = 0; sub < D / 64; ++sub)
-                    tma_load_4d(sb + C::OFF_V + st * C::KV_BYTES + sub * C::SUB, &tmV, BAR(C::B_V + st),
-                                sub * 64, T.hkv, k0, T.b);
-                n_issued = j + 1;
+                    tma_load_4d(sb + C::OFF_K + st * C::KV_BYTES + sub * C::SUB, &tmK, BAR(C::B_KF + st), sub * 64,
+                                T.hkv, (T.kt0 + j) * BN, T.b);
+                nk = j + 1;
+                return true;
+            };
+            auto load_v = [&](int j) {
+                const int st = j % C::NSV, use = j / C::NSV;
+                if (use > 0 && !mbar_wait(BAR(C::B_VE + st), (use - 1) & 1, abort_flag, a.status, 0x11)) return false;
+                mbar_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
+                for (int sub = 0; sub < D / 64; ++sub)
+                    tma_load_4d(sb + C::OFF_V + st * C::KV_BYTES + sub * C::SUB, &tmV, BAR(C::B_VF + st), sub * 64,
+                                T.hkv, (T.kt0 + j) * BN, T.b);
+                nv = j + 1;
+                return true;
+            };
+            for (int j = 0; ok && j <= n; ++j) {
+                if (j < n) ok = load_k(j);
+                if (ok && j > 0) ok = load_v(j - 1);
             }
             // drain: every copy issued must land before the CTA may exit
             drain_wait(BAR(C::B_Q), 0, a.status);
-            for (int s = 0; s < C::NS; ++s) {
-                const int uses = (n_issued - s + C::NS - 1) / C::NS;   // loads issued into stage s
-                if (uses > 0) {
-                    drain_wait(BAR(C::B_K + s), (uses - 1) & 1, a.status);
-                    drain_wait(BAR(C::B_V + s), (uses - 1) & 1, a.status);
-                }
+            for (int s = 0; s < C::NSK; ++s) {
+                const int uses = (nk - s + C::NSK - 1) / C::NSK;
+                if (uses > 0) drain_wait(BAR(C::B_KF + s), (uses - 1) & 1, a.status);
+            }
+            for (int s = 0; s < C::NSV; ++s) {
+                const int uses = (nv - s + C::NSV - 1) / C::NSV;
+                if (uses > 0) drain_wait(BAR(C::B_VF + s), (uses - 1) & 1, a.status);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_kv > 0) {
-            auto issue_s = [&](int j) {
-                const int st = j % C::NS;
-                const uint32_t q_base = sb + C::OFF_Q, k_base = sb + C::OFF_K + st * C::KV_BYTES;
-                const uint32_t d_tmem = tS0 + (j & 1) * BN;
+        if (lane == 0 && n > 0) {
+            int cnt[NQT] = {0, 0};    // products P_i V issued per query tile
+            // descriptors are built once per tile and advanced by immediates
+            auto issue_s = [&](int i, int j) {
+                const int st = j % C::NSK;
+                const uint64_t qd = sdesc_sw128(sb + C::OFF_Q + i * C::Q_BYTES, 16, 1024);
+                const uint64_t kd = sdesc_sw128(sb + C::OFF_K + st * C::KV_BYTES, 16, 1024);
+                const uint32_t d_tmem = tmem + i * BN;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * C::SUB + (kk & 3) * 32;
-                    tc_mma_ss(d_tmem, sdesc_sw128(q_base + off, 16, 1024),
-                              sdesc_sw128(k_base + off, 16, 1024), C::IDESC_S, kk > 0);
+                    tc_mma_ss(d_tmem, sdesc_advance(qd, off), sdesc_advance(kd, off), C::IDESC_S, kk > 0);
                 }
-                tc_commit(BAR(C::B_S + (j & 1)));
+                tc_commit(BAR(C::B_S + i));
+            };
+            auto issue_pv = [&](int i, int j, bool first) {
+                const int st = j % C::NSV;
+                const uint64_t vd = sdesc_sw128(sb + C::OFF_V + st * C::KV_BYTES, C::SUB, 1024);
+                const uint32_t t_p = tmem + i * BN, t_o = tmem + 256 + i * 128;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    tc_mma_ts(t_o, t_p + kk * 8, sdesc_advance(vd, kk * 2048), C::IDESC_PV, (!first || kk > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, a.status, 0x20) &&
-                      mbar_wait(BAR(C::B_K), 0, abort_flag, a.status, 0x21);
+                      mbar_wait(BAR(C::B_KF), 0, abort_flag, a.status, 0x21);
             if (ok) {
                 tc_fence_after();
-                issue_s(0);
+                for (int i = 0; i < NQT; ++i)
+                    if (active(i, 0)) issue_s(i, 0);
+                tc_commit(BAR(C::B_KE));   // K_0 is no longer read once both S(0) are done
             }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                if (j + 1 < n_kv) {
-                    const int st1 = (j + 1) % C::NS;
-                    if (!mbar_wait(BAR(C::B_K + st1), ((j + 1) / C::NS) & 1, abort_flag, a.status, 0x22))
-                        break;
-                    tc_fence_after();
-                    issue_s(j + 1);
+            for (int j = 0; ok && j < n; ++j) {
+                const bool next = j + 1 < n;
+                // every K / V copy is observed here, so a stage is never refilled while a copy is in flight
+                if (!mbar_wait(BAR(C::B_VF + j % C::NSV), (j / C::NSV) & 1, abort_flag, a.status, 0x23)) break;
+                bool k_ready = false;
+                auto wait_k_next = [&]() {
+                    const int k1 = j + 1;
+                    if (!mbar_wait(BAR(C::B_KF + k1 % C::NSK), (k1 / C::NSK) & 1, abort_flag, a.status, 0x22)) return false;
+                    k_ready = true;
+                    return true;
+                };
+                for (int i = 0; i < NQT; ++i) {
+                    if (active(i, j)) {
+                        if (!mbar_wait(BAR(C::B_P + i), cnt[i] & 1, abort_flag, a.status, 0x24)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(i, j, cnt[i] == 0);
+                        ++cnt[i];
+                        if (j == T.hi[i]) tc_commit(BAR(C::B_O + i));
+                    }
+                    if (next && active(i, j + 1)) {
+                        if (!k_ready) {
+                            if (!wait_k_next()) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        issue_s(i, j + 1);
+                    }
                 }
-                const int st = j % C::NS;
-                if (!mbar_wait(BAR(C::B_V + st), (j / C::NS) & 1, abort_flag, a.status, 0x23)) break;
-                if (!mbar_wait(BAR(C::B_P + (j & 1)), (j >> 1) & 1, abort_flag, a.status, 0x24)) break;
-                tc_fence_after();
-                const uint32_t p_base = sb + C::OFF_P + (j & 1) * C::P_BYTES;
-                const uint32_t v_base = sb + C::OFF_V + st * C::KV_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t ad = sdesc_sw128(p_base + (kk >> 2) * C::SUB + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(v_base + kk * 2048, C::SUB, 1024);
-                    tc_mma_ss(tO, ad, bd, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(BAR(C::B_E + st));
-                tc_commit(BAR(C::B_PV + (j & 1)));
+                if (ok && next && !k_ready && !wait_k_next()) ok = false;
+                if (!ok) break;
+                tc_commit(BAR(C::B_VE + j % C::NSV));             // V_j is no longer read
+                if (next) tc_commit(BAR(C::B_KE + (j + 1) % C::NSK));   // nor K_{j+1}, once its S are done
             }
             // drain: all MMAs issued by this thread complete before TMEM is freed
             tc_commit(BAR(C::B_FIN));
@@ -228,9 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax (rows)
-        const int t = threadIdx.x;            // row within the tile == TMEM lane
-        const int q = T.q0 + t;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const int qt = warp >> 2;             // query tile of this warpgroup
+        const int t = threadIdx.x & 127;      // row within the tile == TMEM lane
+        const int q = T.q0 + qt * BM + t;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + qt * BN + lane_base, tO = tmem + 256 + qt * 128 + lane_base;
         int kmin = T.rlo, kmax = min(T.rhi, P.S - 1);
         if (P.causal) kmax = min(kmax, q);
         if (P.wr >= 0) kmax = min(kmax, q + P.wr);
@@ -242,100 +401,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                    : nullptr;
         float m_used = -INFINITY, m_true = -INFINITY, lsum = 0.f;
         bool aborted = false;
-        for (int j = 0; j < n_kv; ++j) {
-            const int bsel = j & 1;
-            const int k0 = (T.kt_lo + j) * BN;
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_S + bsel), (j >> 1) & 1, abort_flag, a.status, 0x30))) {
+        const int jlo = T.lo[qt], jhi = skip ? -1 : T.hi[qt];
+        int c = 0;
+        for (int j = jlo; j <= jhi; ++j, ++c) {
+            const int k0 = (T.kt0 + j) * BN;
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_S + qt), c & 1, abort_flag, a.status, 0x30))) {
                 aborted = true;
                 break;
             }
             tc_fence_after();
-            float s[BN];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tS0 + bsel * BN + c * 32 + lane_base, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]) * sl2;
+            const bool edge = __any_sync(0xffffffffu, k0 < kmin || k0 + BN - 1 > kmax);
+            const RowCtx R{tS, sl2, bias_row, P.bs[3], k0, kmin, kmax, P.S};
+            const int mode = (bias_row ? 2 : 0) | (edge ? 1 : 0);
+            float mt;
+            switch (mode) {
+                case 0: mt = row_max<false, false>(R); break;
+                case 1: mt = row_max<false, true>(R); break;
+                case 2: mt = row_max<true, false>(R); break;
+                default: mt = row_max<true, true>(R); break;
             }
-            if (bias_row) {
-#pragma unroll
-                for (int i = 0; i < BN; ++i) {
-                    const int k = min(k0 + i, P.S - 1);
-                    s[i] = fmaf(bias_row[k * P.bs[3]], kLog2e, s[i]);
-                }
-            }
-            const bool edge = k0 < kmin || k0 + BN - 1 > kmax;
-            if (__any_sync(0xffffffffu, edge)) {
-#pragma unroll
-                for (int i = 0; i < BN; ++i) {
-                    const int k = k0 + i;
-                    if (k < kmin || k > kmax) s[i] = -INFINITY;
-                }
-            }
-            float mt = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < BN; ++i) mt = fmaxf(mt, s[i]);
             m_true = fmaxf(m_true, mt);
+            // lazy rescale: the reference max only moves when the tile max exceeds it by kTau
             float fac = 1.f;
             bool o_resc = false;
             if (mt > m_used + kTau) {
                 fac = m_used == -INFINITY ? 0.f : ex2(m_used - mt);
-                o_resc = j > 0 && m_used != -INFINITY;
+                o_resc = c > 0 && m_used != -INFINITY;
                 m_used = mt;
                 lsum *= fac;
             }
             if (__any_sync(0xffffffffu, o_resc)) {
-                // O must hold every earlier P V before it is rescaled
-                if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_PV + ((j - 1) & 1)), ((j - 1) >> 1) & 1,
-                                                       abort_flag, a.status, 0x31))) {
-                    aborted = true;
-                    break;
-                }
-                tc_fence_after();
+                // S(j) is complete, so every earlier P V has been added to O
                 const float f = o_resc ? fac : 1.f;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t r[32];
-                    tmem_ld32(tO + c * 32 + lane_base, r);
+                    tmem_ld32(tO + cc * 32, r);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-                    tmem_st32(tO + c * 32 + lane_base, r);
+                    tmem_st32(tO + cc * 32, r);
                 }
             }
             const float mref = m_used == -INFINITY ? 0.f : m_used;
-            float rs = 0.f;
-#pragma unroll
-            for (int i = 0; i < BN; ++i) {
-                s[i] = ex2(s[i] - mref);
-                rs += s[i];
+            float rs;
+            switch (mode) {
+                case 0: rs = row_exp<false, false>(R, mref); break;
+                case 1: rs = row_exp<false, true>(R, mref); break;
+                case 2: rs = row_exp<true, false>(R, mref); break;
+                default: rs = row_exp<true, true>(R, mref); break;
             }
             lsum += rs;
-            // the P buffer is free once the P V that read it two tiles ago is done
-            if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(BAR(C::B_PV + bsel), ((j - 2) >> 1) & 1,
-                                                              abort_flag, a.status, 0x32))) {
-                aborted = true;
-                break;
-            }
-            const uint32_t p_base = sb + C::OFF_P + bsel * C::P_BYTES;
-#pragma unroll
-            for (int cc = 0; cc < BN / 8; ++cc) {
-                const uint32_t addr = p_base + (cc >> 3) * C::SUB + sw128_offset(t, cc & 7);
-                st_shared_v4(addr, pack_bf16(s[cc * 8 + 0], s[cc * 8 + 1]),
-                             pack_bf16(s[cc * 8 + 2], s[cc * 8 + 3]),
-                             pack_bf16(s[cc * 8 + 4], s[cc * 8 + 5]),
-                             pack_bf16(s[cc * 8 + 6], s[cc * 8 + 7]));
-            }
-            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(BAR(C::B_P + bsel));
+            mbar_arrive(BAR(C::B_P + qt));
         }
 
         // ------------------------------------------------------------ epilogue
-        const int64_t mi = (static_cast<int64_t>(T.b) * P.Hq + T.h) * P.S + q;
-        if (!aborted && n_kv > 0 &&
-            __all_sync(0xffffffffu, mbar_wait(BAR(C::B_PV + ((n_kv - 1) & 1)), ((n_kv - 1) >> 1) & 1,
-                                              abort_flag, a.status, 0x33))) {
+        const int qc = min(q, P.S - 1);
+        const int64_t mi = (static_cast<int64_t>(T.b) * P.Hq + T.h) * P.S + qc;
+        const bool has_work = jlo <= jhi;
+        if (!aborted && has_work &&
+            __all_sync(0xffffffffu, mbar_wait(BAR(C::B_O + qt), 0, abort_flag, a.status, 0x33))) {
             tc_fence_after();
             // statistics relative to the true row max
             const float rel = m_true == -INFINITY ? 0.f : ex2(m_used - m_true);
@@ -344,13 +469,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!a.acc) {
                 const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
                 __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.qs[0] +
-                                   static_cast<int64_t>(q) * P.qs[1] + T.h * P.qs[2];
+                                   static_cast<int64_t>(qc) * P.qs[1] + T.h * P.qs[2];
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t r[32];
-                    tmem_ld32(tO + c * 32 + lane_base, r);
+                    tmem_ld32(tO + cc * 32, r);
                     if (q < P.S) {
-                        uint4* dst = reinterpret_cast<uint4*>(O + c * 32);
+                        uint4* dst = reinterpret_cast<uint4*>(O + cc * 32);
 #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4) {
                             uint4 w;
@@ -376,13 +501,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float mn = fmaxf(mc, m_nat);
                 const float fa = mc == -INFINITY ? 0.f : ex2((mc - mn) * kLog2e);
                 const float fb = m_nat == -INFINITY ? 0.f : ex2((m_nat - mn) * kLog2e) * rel;
-                float* Cr = a.acc + ((static_cast<int64_t>(T.b) * P.S + q) * P.Hq + T.h) * D;
+                float* Cr = a.acc + ((static_cast<int64_t>(T.b) * P.S + qc) * P.Hq + T.h) * D;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t r[32];
-                    tmem_ld32(tO + c * 32 + lane_base, r);
+                    tmem_ld32(tO + cc * 32, r);
                     if (q < P.S && mn != -INFINITY) {
-                        float4* dst = reinterpret_cast<float4*>(Cr + c * 32);
+                        float4* dst = reinterpret_cast<float4*>(Cr + cc * 32);
 #pragma unroll
                         for (int v4 = 0; v4 < 8; ++v4) {
                             float4 x = dst[v4];
@@ -399,11 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     a.l[mi] = lc * fa + lsum * fb;
                 }
             }
-        } else if (!aborted && !skip && n_kv == 0 && !a.acc && q < P.S) {
+        } else if (!aborted && !skip && !has_work && !a.acc && q < P.S) {
             // no key allowed for this tile: O = 0, m = -inf, l = 0
             __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.qs[0] +
                                static_cast<int64_t>(q) * P.qs[1] + T.h * P.qs[2];
-            for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(O + c) = make_uint4(0, 0, 0, 0);
+            for (int cc = 0; cc < D; cc += 8) *reinterpret_cast<uint4*>(O + cc) = make_uint4(0, 0, 0, 0);
             a.m[mi] = -INFINITY;
             a.l[mi] = 0.f;
         }
@@ -412,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -431,8 +556,8 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    const int nqt = (a.P.S + BM - 1) / BM;
-    const int grid = nqt * a.P.Hq * a.P.B;
+    const int nqp = (a.P.S + NQT * BM - 1) / (NQT * BM);
+    const int grid = nqp * a.P.Hq * a.P.B;
     k_fwd_tc<D><<<grid, kThreads, C::SMEM, s>>>(maps[0], maps[1], maps[2], a);
     return cudaGetLastError();
 }
@@ -441,7 +566,7 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
 
 bool fwd_tc_supported(const Problem& P) {
     if (P.dtype != BPA_BF16 || (P.d != 64 && P.d != 128) || P.block_idx) return false;
-    if (P.ring_n > 1 && P.ring_blk % BM) return false;
+    if (P.ring_n > 1 && P.ring_blk % (NQT * BM)) return false;
     return true;
 }
 
