@@ -142,6 +142,98 @@ def cpu_oracle_sample(w, budget_s: float):
     return tf, dt, desc, oracle.num_threads(), S
 
 
+def time_extra_workloads(bpa, dev, peak_tf):
+    """Secondary workloads (not the headline): device-timed per-call times.
+    Inputs are drawn on the device from seeded generators (timing only; the
+    parity tests use the numpy recipe)."""
+    import torch
+    from ring_attention_gb300.inputs import BLOCK_SEL, GQA_SWA, RING_LONG, TINY_F32
+
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    out = {}
+
+    def rnd(shape, dtype, seed):
+        g = torch.Generator(device=dev)
+        g.manual_seed(seed)
+        return torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(dtype)
+
+    def fwd_bwd(w, steps, warmup):
+        dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        q = rnd((w.B, w.S, w.Hq, w.d), dt, w.seed)
+        k = rnd((w.B, w.S, w.Hkv, w.d), dt, w.seed + 1)
+        v = rnd((w.B, w.S, w.Hkv, w.d), dt, w.seed + 2)
+        do = rnd((w.B, w.S, w.Hq, w.d), dt, w.seed + 3)
+        bias = None
+        if w.pad_tail:
+            bias = torch.zeros((1, 1, 1, w.S), device=dev, dtype=torch.float32)
+            bias[..., w.S - w.pad_tail:] = -1e9
+        kw = dict(causal=w.causal, window=w.window, bias=bias, query_chunk=w.query_chunk, key_chunk=w.key_chunk,
+                  ring_size=w.ring_size)
+        D = bpa.make_desc(q, k, v, **kw)
+        wsf = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_FWD, D), dev)
+        wsb = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_BWD, D), dev)
+        o, m, l = bpa.bpa_fwd(q, k, v, workspace_buf=wsf, **kw)
+        dq, dk, dv = bpa.bpa_bwd(q, k, v, o, do, m, l, workspace_buf=wsb, **kw)
+        tf, tb = [], []
+        for it in range(warmup + steps):
+            a, b, c = E(), E(), E()
+            a.record()
+            bpa.bpa_fwd(q, k, v, o=o, m=m, l=l, workspace_buf=wsf, **kw)
+            b.record()
+            bpa.bpa_bwd(q, k, v, o, do, m, l, dq=dq, dk=dk, dv=dv, workspace_buf=wsb, **kw)
+            c.record()
+            torch.cuda.synchronize()
+            if it >= warmup:
+                tf.append(a.elapsed_time(b))
+                tb.append(b.elapsed_time(c))
+        bpa.bpa_check(wsf)
+        bpa.bpa_check(wsb)
+        ent = unmasked_entries(w)
+        f_fwd, f_bwd = flops(w, ent)
+        mf, mb = statistics.mean(tf), statistics.mean(tb)
+        el = 2 if dt == torch.bfloat16 else 4
+        fwd_bytes = el * w.B * w.S * w.d * (2 * w.Hq + 2 * w.Hkv)             # Q, K, V read, O written
+        bwd_bytes = el * w.B * w.S * w.d * (4 * w.Hq + 4 * w.Hkv)             # Q, K, V, O, dO read; dQ, dK, dV written
+        res = {"fwd_ms": mf, "bwd_ms": mb, "fwd_tflops": f_fwd / mf / 1e9, "bwd_tflops": f_bwd / mb / 1e9,
+               "fwd_pct_peak": 100 * f_fwd / mf / 1e9 / peak_tf, "bwd_pct_peak": 100 * f_bwd / mb / 1e9 / peak_tf,
+               "fwd_min_bytes_gbs": fwd_bytes / mf / 1e6, "bwd_min_bytes_gbs": bwd_bytes / mb / 1e6,
+               "unmasked_entries": ent, "steps": steps}
+        del q, k, v, do, o, dq, dk, dv, wsf, wsb
+        torch.cuda.empty_cache()
+        return res
+
+    out[GQA_SWA.name] = fwd_bwd(GQA_SWA, 20, 3)
+    out[TINY_F32.name] = fwd_bwd(TINY_F32, 20, 3)
+    out[RING_LONG.name] = fwd_bwd(RING_LONG, 2, 1)
+
+    w = BLOCK_SEL
+    q = rnd((w.B, w.S, w.Hq, w.d), torch.bfloat16, w.seed)
+    k = rnd((w.B, w.S, w.Hkv, w.d), torch.bfloat16, w.seed + 1)
+    v = rnd((w.B, w.S, w.Hkv, w.d), torch.bfloat16, w.seed + 2)
+    idx = bpa.bpa_select_blocks(q, k, block_size=w.sel_block, top_n=w.top_n)
+    kw = dict(causal=True, block_idx=idx, sel_block=w.sel_block, top_n=w.top_n, local_window=w.local_window)
+    o, m, l = bpa.bpa_fwd(q, k, v, **kw)
+    ts, ta = [], []
+    for it in range(23):
+        a, b, c = E(), E(), E()
+        a.record()
+        bpa.bpa_select_blocks(q, k, block_size=w.sel_block, top_n=w.top_n, out=idx)
+        b.record()
+        bpa.bpa_fwd(q, k, v, o=o, m=m, l=l, **kw)
+        c.record()
+        torch.cuda.synchronize()
+        if it >= 3:
+            ts.append(a.elapsed_time(b))
+            ta.append(b.elapsed_time(c))
+    # algorithmic bytes: Q, K, V read once and O written once (the gathered re-reads come from L2)
+    qkvo = 2 * w.B * w.S * w.d * (2 * w.Hq + 2 * w.Hkv)
+    nb = (idx >= 0).sum().item()
+    out[w.name] = {"select_ms": statistics.mean(ts), "attention_ms": statistics.mean(ta),
+                   "attention_min_bytes_gbs": qkvo / statistics.mean(ta) / 1e6,
+                   "selected_blocks": int(nb), "steps": 20}
+    return out
+
+
 def run_reference(args, w):
     """Reference arm: the float64 CPU oracle, as it stands, on bounded samples."""
     rank = int(os.environ.get("RANK", "0"))
@@ -182,6 +274,7 @@ def main():
     ap.add_argument("--workload", default=GQA_CAUSAL.name, choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -325,6 +418,10 @@ def main():
         e2e_ms = float(t.item())
     e2e_val = (f_fwd + f_bwd) * args.e2e_steps * world / (e2e_ms * 1e-3) / 1e12
 
+    extra = None
+    if rank == 0 and not args.no_extra:
+        extra = time_extra_workloads(bpa, dev, peak_tf)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, desc, cores, _ = cpu_oracle_sample(w, 20.0)
@@ -355,6 +452,7 @@ def main():
             "gpu_launches": 4 * K,
             "clocks": clocks.summary(),
             "wall_s_timed_region": wall,
+            "extra": extra,
         }
         print(json.dumps(line))
     if world > 1:
