@@ -294,10 +294,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* Dq = lse + 64;
             if (P.bias) {
                 const float* brow = P.bias + W.b * P.bs[0] + h * P.bs[1] + static_cast<int64_t>(min(k, P.S - 1)) * P.bs[3];
+                if (P.bs[2] == 0) {   // the bias does not depend on the query: one value per key row
+                    const float bk = brow[0] * kLog2e;
 #pragma unroll
-                for (int c = 0; c < BQ; ++c) {
-                    const int q = min(q0 + c, P.S - 1);
-                    p[c] = fmaf(brow[q * P.bs[2]], kLog2e, p[c]);
+                    for (int c = 0; c < BQ; ++c) p[c] += bk;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BQ; ++c) {
+                        const int q = min(q0 + c, P.S - 1);
+                        p[c] = fmaf(brow[q * P.bs[2]], kLog2e, p[c]);
+                    }
                 }
             }
 #pragma unroll

@@ -53,7 +53,8 @@ struct FwdCfg {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQT * Q_BYTES;
     static constexpr int OFF_V = OFF_K + NSK * KV_BYTES;
-    static constexpr int OFF_BAR = OFF_V + NSV * KV_BYTES;
+    static constexpr int OFF_KB = OFF_V + NSV * KV_BYTES;   // per K stage: the tile's 128 key-bias values
+    static constexpr int OFF_BAR = OFF_KB + NSK * BN * 4;
     static constexpr int SMEM = OFF_BAR + 256 + 1024;   // + slack to align the base to 1024
     // barrier slots: K full / empty, V full / empty, S, P, O per query tile
     static constexpr int B_Q = 0, B_KF = 1, B_KE = 1 + NSK, B_VF = 1 + 2 * NSK, B_VE = 1 + 2 * NSK + NSV,
@@ -137,13 +138,16 @@ struct RowCtx {
     float sl2;              // scale * log2(e)
     const float* bias_row;  // bias of this row (broadcast dims have stride 0)
     int64_t bs3;            // bias stride along keys
+    const float* kbias;     // key-only bias: the tile's 128 values in shared memory
     int k0, kmin, kmax, S;  // first key of the tile, allowed keys of the row, length
 };
 
-template <bool BIAS, bool EDGE>
+// BIAS: 0 none, 1 key-only bias staged in shared memory, 2 general bias read from global memory
+template <int BIAS, bool EDGE>
 __device__ __forceinline__ float score_at(const RowCtx& R, uint32_t raw, int i) {
     float x = __uint_as_float(raw) * R.sl2;
-    if (BIAS) x = fmaf(R.bias_row[min(R.k0 + i, R.S - 1) * R.bs3], kLog2e, x);
+    if (BIAS == 1) x = fmaf(R.kbias[i], kLog2e, x);
+    if (BIAS == 2) x = fmaf(R.bias_row[min(R.k0 + i, R.S - 1) * R.bs3], kLog2e, x);
     if (EDGE) x = (R.k0 + i < R.kmin || R.k0 + i > R.kmax) ? -INFINITY : x;
     return x;
 }
@@ -154,14 +158,29 @@ __device__ __forceinline__ float score_at(const RowCtx& R, uint32_t raw, int i) 
 // arithmetic and a 3-input max.
 
 // pass 1: the row max of the scores
-template <bool BIAS, bool EDGE>
+template <int BIAS, bool EDGE>
 __device__ __forceinline__ float row_max(const RowCtx& R) {
     float mt = -INFINITY;
+    const uint64_t sl2x2 = f2_pack(R.sl2, R.sl2), l2e2 = f2_pack(kLog2e, kLog2e);
 #pragma unroll
     for (int cc = 0; cc < BN / 64; ++cc) {
         uint32_t r[64];
         tmem_ld64(R.tS + cc * 64, r);
-        if (!BIAS && !EDGE) {
+        if (BIAS == 1 && !EDGE) {
+            float m2 = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 bq = reinterpret_cast<const float4*>(R.kbias + cc * 64)[i];
+                float x0, x1, x2, x3;
+                f2_unpack(ffma2(f2_pack(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), sl2x2,
+                                fmul2(f2_pack(bq.x, bq.y), l2e2)), x0, x1);
+                f2_unpack(ffma2(f2_pack(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), sl2x2,
+                                fmul2(f2_pack(bq.z, bq.w), l2e2)), x2, x3);
+                m2 = fmax3(m2, x0, x1);
+                m2 = fmax3(m2, x2, x3);
+            }
+            mt = fmaxf(mt, m2);
+        } else if (!BIAS && !EDGE) {
             float m2 = -INFINITY;   // scale > 0: max of raw S, scaled once
 #pragma unroll
             for (int i = 0; i < 32; ++i) m2 = fmax3(m2, __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
@@ -177,7 +196,7 @@ __device__ __forceinline__ float row_max(const RowCtx& R) {
 // pass 2: P = exp2(x - mref) as bf16 pairs written over the first 64 columns
 // of the row's S (chunk cc reads S columns [64cc, 64cc+64) and writes P
 // columns [32cc, 32cc+32)); returns the row sum of P in float32
-template <bool BIAS, bool EDGE>
+template <int BIAS, bool EDGE>
 __device__ __forceinline__ float row_exp(const RowCtx& R, float mref) {
     uint64_t rs2 = 0;   // two float32 partial sums
     const uint64_t sl2x2 = f2_pack(R.sl2, R.sl2), negm2 = f2_pack(-mref, -mref);
@@ -189,7 +208,14 @@ __device__ __forceinline__ float row_exp(const RowCtx& R, float mref) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             uint64_t p2;
-            if (!BIAS && !EDGE) {
+            if (BIAS == 1 && !EDGE) {
+                const float2 bp = reinterpret_cast<const float2*>(R.kbias + cc * 64)[i];
+                float x0, x1;   // S * scale_log2 + (bias * log2e - mref)
+                f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2,
+                                ffma2(f2_pack(bp.x, bp.y), f2_pack(kLog2e, kLog2e), negm2)),
+                          x0, x1);
+                p2 = f2_pack(ex2(x0), ex2(x1));
+            } else if (!BIAS && !EDGE) {
                 float x0, x1;
                 f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2, negm2), x0, x1);
                 p2 = f2_pack(ex2(x0), ex2(x1));
@@ -258,6 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool skip = *abort_flag != 0;
     const int n = skip ? 0 : T.n;
     auto active = [&](int i, int j) { return j >= T.lo[i] && j <= T.hi[i]; };
+    // a bias that does not depend on the query row (and is contiguous along keys)
+    // is staged per key tile in shared memory by the producer
+    const bool key_bias = P.bias && P.bs[2] == 0 && P.bs[3] == 1 && (P.S % BN) == 0 &&
+                          ((reinterpret_cast<uintptr_t>(P.bias) | ((P.bs[0] | P.bs[1]) * 4)) & 15) == 0;
+    const float* kbias_src = key_bias ? P.bias + T.b * P.bs[0] + T.h * P.bs[1] : nullptr;
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
@@ -276,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto load_k = [&](int j) {
                 const int st = j % C::NSK, use = j / C::NSK;
                 if (use > 0 && !mbar_wait(BAR(C::B_KE + st), (use - 1) & 1, abort_flag, a.status, 0x10)) return false;
-                mbar_expect_tx(BAR(C::B_KF + st), C::KV_BYTES);
+                mbar_expect_tx(BAR(C::B_KF + st), C::KV_BYTES + (key_bias ? BN * 4 : 0));
+                if (key_bias)
+                    bulk_load(sb + C::OFF_KB + st * BN * 4, kbias_src + (T.kt0 + j) * BN, BN * 4, BAR(C::B_KF + st));
                 for (int sub = 0; sub < D / 64; ++sub)
                     tma_load_4d(sb + C::OFF_K + st * C::KV_BYTES + sub * C::SUB, &tmK, BAR(C::B_KF + st), sub * 64,
                                 T.hkv, (T.kt0 + j) * BN, T.b);
@@ -339,7 +372,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 for (int i = 0; i < NQT; ++i)
                     if (active(i, 0)) issue_s(i, 0);
-                tc_commit(BAR(C::B_KE));   // K_0 is no longer read once both S(0) are done
             }
             for (int j = 0; ok && j < n; ++j) {
                 const bool next = j + 1 < n;
@@ -376,8 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (ok && next && !k_ready && !wait_k_next()) ok = false;
                 if (!ok) break;
-                tc_commit(BAR(C::B_VE + j % C::NSV));             // V_j is no longer read
-                if (next) tc_commit(BAR(C::B_KE + (j + 1) % C::NSK));   // nor K_{j+1}, once its S are done
+                // K_j (and its staged bias) and V_j are released together: both softmax
+                // warpgroups have finished step j (their P(j) arrivals were waited for above)
+                tc_commit(BAR(C::B_VE + j % C::NSV));
+                tc_commit(BAR(C::B_KE + j % C::NSK));
             }
             // drain: all MMAs issued by this thread complete before TMEM is freed
             tc_commit(BAR(C::B_FIN));
@@ -411,14 +445,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const bool edge = __any_sync(0xffffffffu, k0 < kmin || k0 + BN - 1 > kmax);
-            const RowCtx R{tS, sl2, bias_row, P.bs[3], k0, kmin, kmax, P.S};
-            const int mode = (bias_row ? 2 : 0) | (edge ? 1 : 0);
+            const float* kb_tile = reinterpret_cast<const float*>(smem + C::OFF_KB + (j % C::NSK) * BN * 4);
+            // the staged key bias arrived with K_j: observe that copy's barrier (the stage
+            // cannot be refilled before this warpgroup's P(j) arrival)
+            if (key_bias && !__all_sync(0xffffffffu, mbar_wait(BAR(C::B_KF + j % C::NSK), (j / C::NSK) & 1, abort_flag,
+                                                               a.status, 0x34))) {
+                aborted = true;
+                break;
+            }
+            const RowCtx R{tS, sl2, bias_row, P.bs[3], kb_tile, k0, kmin, kmax, P.S};
+            // mode = bias kind (0 none, 1 staged key bias, 2 general) * 2 + edge
+            const int mode = (bias_row ? (key_bias ? 2 : 4) : 0) | (edge ? 1 : 0);
             float mt;
             switch (mode) {
-                case 0: mt = row_max<false, false>(R); break;
-                case 1: mt = row_max<false, true>(R); break;
-                case 2: mt = row_max<true, false>(R); break;
-                default: mt = row_max<true, true>(R); break;
+                case 0: mt = row_max<0, false>(R); break;
+                case 1: mt = row_max<0, true>(R); break;
+                case 2: mt = row_max<1, false>(R); break;
+                case 3: mt = row_max<1, true>(R); break;
+                case 4: mt = row_max<2, false>(R); break;
+                default: mt = row_max<2, true>(R); break;
             }
             m_true = fmaxf(m_true, mt);
             // lazy rescale: the reference max only moves when the tile max exceeds it by kTau
@@ -445,10 +490,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mref = m_used == -INFINITY ? 0.f : m_used;
             float rs;
             switch (mode) {
-                case 0: rs = row_exp<false, false>(R, mref); break;
-                case 1: rs = row_exp<false, true>(R, mref); break;
-                case 2: rs = row_exp<true, false>(R, mref); break;
-                default: rs = row_exp<true, true>(R, mref); break;
+                case 0: rs = row_exp<0, false>(R, mref); break;
+                case 1: rs = row_exp<0, true>(R, mref); break;
+                case 2: rs = row_exp<1, false>(R, mref); break;
+                case 3: rs = row_exp<1, true>(R, mref); break;
+                case 4: rs = row_exp<2, false>(R, mref); break;
+                default: rs = row_exp<2, true>(R, mref); break;
             }
             lsum += rs;
             tc_fence_before();
