@@ -29,6 +29,8 @@
 // copies and MMAs, frees TMEM and returns.
 #include <math.h>
 
+#include <algorithm>
+
 #include "bpa_internal.h"
 #include "common.cuh"
 
@@ -36,22 +38,28 @@ namespace bpa {
 namespace {
 
 constexpr int BM = 128;       // query rows per tile
-constexpr int NQT = 2;        // query tiles per CTA
 constexpr int BN = 128;       // keys per tile
 constexpr float kTau = 8.f;   // lazy-rescale threshold, log2 units
-constexpr int kThreads = 320;
 
-template <int D>
+// NQ query tiles per CTA.  NQ = 2: two softmax warpgroups share every K / V
+// tile (long key ranges).  NQ = 1: a smaller CTA (192 threads, 256 TMEM
+// columns, < 113 KB of shared memory) so that two run on an SM and one CTA's
+// loads and stores overlap the other's products (short key ranges, e.g. a
+// narrow sliding window).
+template <int D, int NQ>
 struct FwdCfg {
+    static constexpr int kThreads = NQ * 128 + 64;
+    static constexpr int kTmemCols = NQ * 256;
+    static constexpr int kProducer = 4 * NQ, kMma = 4 * NQ + 1;   // warp indices
     // K and V flow through separate rings: K tile j is needed one product
-    // earlier than V tile j and is released earlier, so it gets more stages.
-    static constexpr int NSK = D == 128 ? 3 : 4;   // K stages
-    static constexpr int NSV = D == 128 ? 2 : 4;   // V stages
+    // earlier than V tile j, so it gets more stages where space allows.
+    static constexpr int NSK = NQ == 2 ? (D == 128 ? 3 : 4) : (D == 128 ? 1 : 2);   // K stages
+    static constexpr int NSV = NQ == 2 ? (D == 128 ? 2 : 4) : (D == 128 ? 1 : 2);   // V stages
     static constexpr int Q_BYTES = BM * D * 2;     // one query tile
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int SUB = 128 * 128;          // one 64-column slab of 128 rows
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + NQT * Q_BYTES;
+    static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + NSK * KV_BYTES;
     static constexpr int OFF_KB = OFF_V + NSV * KV_BYTES;   // per K stage: the tile's 128 key-bias values
     static constexpr int OFF_BAR = OFF_KB + NSK * BN * 4;
@@ -62,6 +70,7 @@ struct FwdCfg {
                          NBAR = B_S + 7;
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);   // Q, K both K-major
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 0, 1);   // P (TMEM), V MN-major
+    static_assert(NQ == 2 || 2 * SMEM <= 233472, "two single-tile CTAs must fit an SM");
 };
 
 struct Tile {
@@ -69,12 +78,13 @@ struct Tile {
     int rlo, rhi;            // key range of this launch (ring super-block or whole sequence)
     int kt0;                 // first key tile visited by the CTA
     int n;                   // key tiles visited by the CTA
-    int lo[NQT], hi[NQT];    // per query tile: visited step range [lo, hi] (empty if lo > hi)
+    int lo[2], hi[2];        // per query tile: visited step range [lo, hi] (empty if lo > hi)
 };
 
+template <int NQ>
 __device__ __forceinline__ Tile decode_tile(const FwdArgs& a) {
     const Problem& P = a.P;
-    const int nqp = (P.S + NQT * BM - 1) / (NQT * BM);
+    const int nqp = (P.S + NQ * BM - 1) / (NQ * BM);
     int r = blockIdx.x;
     const int gi = r % P.G;
     r /= P.G;
@@ -84,7 +94,7 @@ __device__ __forceinline__ Tile decode_tile(const FwdArgs& a) {
     t.b = r % P.B;
     const int qp = nqp - 1 - r / P.B;   // heaviest (causal) query pairs first
     t.h = t.hkv * P.G + gi;
-    t.q0 = qp * NQT * BM;
+    t.q0 = qp * NQ * BM;
     t.rlo = 0;
     t.rhi = P.S - 1;
     if (a.acc) {
@@ -93,10 +103,10 @@ __device__ __forceinline__ Tile decode_tile(const FwdArgs& a) {
         t.rlo = j * P.ring_blk;
         t.rhi = t.rlo + P.ring_blk - 1;
     }
-    int ktlo[NQT], kthi[NQT];
+    int ktlo[2] = {1, 1}, kthi[2] = {0, 0};
     int ulo = 1 << 30, uhi = -1;
 #pragma unroll
-    for (int i = 0; i < NQT; ++i) {
+    for (int i = 0; i < NQ; ++i) {
         const int qa = t.q0 + i * BM, qb = min(qa + BM - 1, P.S - 1);
         int lo = t.rlo, hi = t.rhi;
         if (qa >= P.S) hi = -1;
@@ -116,7 +126,7 @@ __device__ __forceinline__ Tile decode_tile(const FwdArgs& a) {
     t.kt0 = uhi >= 0 ? ulo : 0;
     t.n = uhi >= 0 ? uhi - ulo + 1 : 0;
 #pragma unroll
-    for (int i = 0; i < NQT; ++i) {
+    for (int i = 0; i < 2; ++i) {
         t.lo[i] = ktlo[i] - t.kt0;
         t.hi[i] = kthi[i] - t.kt0;
     }
@@ -235,11 +245,11 @@ __device__ __forceinline__ float row_exp(const RowCtx& R, float mref) {
     return a + b;
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int NQ>
+__global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
     k_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, NQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -250,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const Problem& P = a.P;
-    const Tile T = decode_tile(a);
+    const Tile T = decode_tile<NQ>(a);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -263,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(C::B_VF + s), 1);
             mbar_init(BAR(C::B_VE + s), 1);
         }
-        for (int i = 0; i < NQT; ++i) {
+        for (int i = 0; i < NQ; ++i) {
             mbar_init(BAR(C::B_S + i), 1);
             mbar_init(BAR(C::B_P + i), 128);
             mbar_init(BAR(C::B_O + i), 1);
@@ -273,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = (a.status && (*reinterpret_cast<volatile uint32_t*>(a.status) & ST_TIMEOUT)) ? 1 : 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
+    if (warp == C::kMma) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -290,61 +300,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                           ((reinterpret_cast<uintptr_t>(P.bias) | ((P.bs[0] | P.bs[1]) * 4)) & 15) == 0;
     const float* kbias_src = key_bias ? P.bias + T.b * P.bs[0] + T.h * P.bs[1] : nullptr;
 
-    if (warp == 8) {
+    if (warp == C::kProducer) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && n > 0) {
-            tma_prefetch(&tmQ);
-            tma_prefetch(&tmK);
-            tma_prefetch(&tmV);
-            mbar_expect_tx(BAR(C::B_Q), NQT * C::Q_BYTES);
-            for (int i = 0; i < NQT; ++i)
-                for (int sub = 0; sub < D / 64; ++sub)
-                    tma_load_4d(sb + C::OFF_Q + i * C::Q_BYTES + sub * C::SUB, &tmQ, BAR(C::B_Q), sub * 64, T.h,
-                                T.q0 + i * BM, T.b);
-            // K runs one tile ahead of V: K0, K1, V0, K2, V1, ...
-            int nk = 0, nv = 0;   // tiles issued
-            bool ok = true;
-            auto load_k = [&](int j) {
-                const int st = j % C::NSK, use = j / C::NSK;
-                if (use > 0 && !mbar_wait(BAR(C::B_KE + st), (use - 1) & 1, abort_flag, a.status, 0x10)) return false;
-                mbar_expect_tx(BAR(C::B_KF + st), C::KV_BYTES + (key_bias ? BN * 4 : 0));
-                if (key_bias)
-                    bulk_load(sb + C::OFF_KB + st * BN * 4, kbias_src + (T.kt0 + j) * BN, BN * 4, BAR(C::B_KF + st));
-                for (int sub = 0; sub < D / 64; ++sub)
-                    tma_load_4d(sb + C::OFF_K + st * C::KV_BYTES + sub * C::SUB, &tmK, BAR(C::B_KF + st), sub * 64,
-                                T.hkv, (T.kt0 + j) * BN, T.b);
-                nk = j + 1;
-                return true;
-            };
-            auto load_v = [&](int j) {
-                const int st = j % C::NSV, use = j / C::NSV;
-                if (use > 0 && !mbar_wait(BAR(C::B_VE + st), (use - 1) & 1, abort_flag, a.status, 0x11)) return false;
-                mbar_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
-                for (int sub = 0; sub < D / 64; ++sub)
-                    tma_load_4d(sb + C::OFF_V + st * C::KV_BYTES + sub * C::SUB, &tmV, BAR(C::B_VF + st), sub * 64,
-                                T.hkv, (T.kt0 + j) * BN, T.b);
-                nv = j + 1;
-                return true;
-            };
-            for (int j = 0; ok && j <= n; ++j) {
-                if (j < n) ok = load_k(j);
-                if (ok && j > 0) ok = load_v(j - 1);
-            }
-            // drain: every copy issued must land before the CTA may exit
-            drain_wait(BAR(C::B_Q), 0, a.status);
-            for (int s = 0; s < C::NSK; ++s) {
-                const int uses = (nk - s + C::NSK - 1) / C::NSK;
-                if (uses > 0) drain_wait(BAR(C::B_KF + s), (uses - 1) & 1, a.status);
-            }
-            for (int s = 0; s < C::NSV; ++s) {
-                const int uses = (nv - s + C::NSV - 1) / C::NSV;
-                if (uses > 0) drain_wait(BAR(C::B_VF + s), (uses - 1) & 1, a.status);
+        // lane 0 streams Q and the K ring (plus the staged key bias), lane 1 the
+        // V ring: two independent loops, so no stage count can order them into a wait cycle
+        if (lane < 2 && n > 0) {
+            if (lane == 0) {
+                tma_prefetch(&tmQ);
+                tma_prefetch(&tmK);
+                mbar_expect_tx(BAR(C::B_Q), NQ * C::Q_BYTES);
+                for (int i = 0; i < NQ; ++i)
+                    for (int sub = 0; sub < D / 64; ++sub)
+                        tma_load_4d(sb + C::OFF_Q + i * C::Q_BYTES + sub * C::SUB, &tmQ, BAR(C::B_Q), sub * 64, T.h,
+                                    T.q0 + i * BM, T.b);
+                int nk = 0;
+                for (int j = 0; j < n; ++j) {
+                    const int st = j % C::NSK, use = j / C::NSK;
+                    if (use > 0 && !mbar_wait(BAR(C::B_KE + st), (use - 1) & 1, abort_flag, a.status, 0x10)) break;
+                    mbar_expect_tx(BAR(C::B_KF + st), C::KV_BYTES + (key_bias ? BN * 4 : 0));
+                    if (key_bias)
+                        bulk_load(sb + C::OFF_KB + st * BN * 4, kbias_src + (T.kt0 + j) * BN, BN * 4, BAR(C::B_KF + st));
+                    for (int sub = 0; sub < D / 64; ++sub)
+                        tma_load_4d(sb + C::OFF_K + st * C::KV_BYTES + sub * C::SUB, &tmK, BAR(C::B_KF + st), sub * 64,
+                                    T.hkv, (T.kt0 + j) * BN, T.b);
+                    nk = j + 1;
+                }
+                // drain: every copy issued must land before the CTA may exit
+                drain_wait(BAR(C::B_Q), 0, a.status);
+                for (int s = 0; s < C::NSK; ++s) {
+                    const int uses = (nk - s + C::NSK - 1) / C::NSK;
+                    if (uses > 0) drain_wait(BAR(C::B_KF + s), (uses - 1) & 1, a.status);
+                }
+            } else {
+                tma_prefetch(&tmV);
+                int nv = 0;
+                for (int j = 0; j < n; ++j) {
+                    const int st = j % C::NSV, use = j / C::NSV;
+                    if (use > 0 && !mbar_wait(BAR(C::B_VE + st), (use - 1) & 1, abort_flag, a.status, 0x11)) break;
+                    mbar_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
+                    for (int sub = 0; sub < D / 64; ++sub)
+                        tma_load_4d(sb + C::OFF_V + st * C::KV_BYTES + sub * C::SUB, &tmV, BAR(C::B_VF + st), sub * 64,
+                                    T.hkv, (T.kt0 + j) * BN, T.b);
+                    nv = j + 1;
+                }
+                for (int s = 0; s < C::NSV; ++s) {
+                    const int uses = (nv - s + C::NSV - 1) / C::NSV;
+                    if (uses > 0) drain_wait(BAR(C::B_VF + s), (uses - 1) & 1, a.status);
+                }
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == C::kMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
-            int cnt[NQT] = {0, 0};    // products P_i V issued per query tile
+            int cnt[2] = {0, 0};      // products P_i V issued per query tile
             // descriptors are built once per tile and advanced by immediates
             auto issue_s = [&](int i, int j) {
                 const int st = j % C::NSK;
@@ -361,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_pv = [&](int i, int j, bool first) {
                 const int st = j % C::NSV;
                 const uint64_t vd = sdesc_sw128(sb + C::OFF_V + st * C::KV_BYTES, C::SUB, 1024);
-                const uint32_t t_p = tmem + i * BN, t_o = tmem + 256 + i * 128;
+                const uint32_t t_p = tmem + i * BN, t_o = tmem + NQ * BN + i * 128;
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     tc_mma_ts(t_o, t_p + kk * 8, sdesc_advance(vd, kk * 2048), C::IDESC_PV, (!first || kk > 0) ? 1u : 0u);
@@ -370,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       mbar_wait(BAR(C::B_KF), 0, abort_flag, a.status, 0x21);
             if (ok) {
                 tc_fence_after();
-                for (int i = 0; i < NQT; ++i)
+                for (int i = 0; i < NQ; ++i)
                     if (active(i, 0)) issue_s(i, 0);
             }
             for (int j = 0; ok && j < n; ++j) {
@@ -384,11 +392,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     k_ready = true;
                     return true;
                 };
-                for (int i = 0; i < NQT; ++i) {
+                const int last = active(NQ - 1, j) ? NQ - 1 : 0;   // last query tile active at step j
+                bool k_released = false;
+                for (int i = 0; i < NQ; ++i) {
                     if (active(i, j)) {
                         if (!mbar_wait(BAR(C::B_P + i), cnt[i] & 1, abort_flag, a.status, 0x24)) {
                             ok = false;
                             break;
+                        }
+                        // every softmax of step j is done (S(j) and the staged bias are no longer
+                        // read): release K_j's stage before S(j+1) may need a free one
+                        if (i == last) {
+                            tc_commit(BAR(C::B_KE + j % C::NSK));
+                            k_released = true;
                         }
                         tc_fence_after();
                         issue_pv(i, j, cnt[i] == 0);
@@ -408,10 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (ok && next && !k_ready && !wait_k_next()) ok = false;
                 if (!ok) break;
-                // K_j (and its staged bias) and V_j are released together: both softmax
-                // warpgroups have finished step j (their P(j) arrivals were waited for above)
-                tc_commit(BAR(C::B_VE + j % C::NSV));
-                tc_commit(BAR(C::B_KE + j % C::NSK));
+                if (!k_released) tc_commit(BAR(C::B_KE + j % C::NSK));   // (a step no tile used)
+                tc_commit(BAR(C::B_VE + j % C::NSV));   // V_j is no longer read
             }
             // drain: all MMAs issued by this thread complete before TMEM is freed
             tc_commit(BAR(C::B_FIN));
@@ -423,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = threadIdx.x & 127;      // row within the tile == TMEM lane
         const int q = T.q0 + qt * BM + t;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + qt * BN + lane_base, tO = tmem + 256 + qt * 128 + lane_base;
+        const uint32_t tS = tmem + qt * BN + lane_base, tO = tmem + NQ * BN + qt * 128 + lane_base;
         int kmin = T.rlo, kmax = min(T.rhi, P.S - 1);
         if (P.causal) kmax = min(kmax, q);
         if (P.wr >= 0) kmax = min(kmax, q + P.wr);
@@ -584,41 +598,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == C::kMma) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
-template <int D>
+template <int D, int NQ>
 cudaError_t launch(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, NQ>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(k_fwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        e = cudaFuncSetAttribute(k_fwd_tc<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    const int nqp = (a.P.S + NQT * BM - 1) / (NQT * BM);
+    const int nqp = (a.P.S + NQ * BM - 1) / (NQ * BM);
     const int grid = nqp * a.P.Hq * a.P.B;
-    k_fwd_tc<D><<<grid, kThreads, C::SMEM, s>>>(maps[0], maps[1], maps[2], a);
+    k_fwd_tc<D, NQ><<<grid, C::kThreads, C::SMEM, s>>>(maps[0], maps[1], maps[2], a);
     return cudaGetLastError();
+}
+
+// Key tiles one 128-row query tile visits at most (window and causal bounds).
+int key_tiles_per_query_tile(const Problem& P) {
+    const int64_t left = P.wl >= 0 ? P.wl : P.S, right = P.causal ? 0 : (P.wr >= 0 ? P.wr : P.S);
+    const int64_t span = std::min<int64_t>(P.S, left + right + BM);
+    return static_cast<int>((span + BN - 1) / BN) + 1;
 }
 
 }  // namespace
 
 bool fwd_tc_supported(const Problem& P) {
     if (P.dtype != BPA_BF16 || (P.d != 64 && P.d != 128) || P.block_idx) return false;
-    if (P.ring_n > 1 && P.ring_blk % (NQT * BM)) return false;
+    if (P.ring_n > 1 && P.ring_blk % BM) return false;
     return true;
 }
 
 cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
-    return a.P.d == 128 ? launch<128>(a, maps, s) : launch<64>(a, maps, s);
+    const Problem& P = a.P;
+    // short key ranges: single-tile CTAs, two per SM; a ring block must hold whole CTAs
+    const bool single = key_tiles_per_query_tile(P) <= 4 || P.S <= BM || (P.ring_n > 1 && P.ring_blk % (2 * BM));
+    if (P.d == 128) return single ? launch<128, 1>(a, maps, s) : launch<128, 2>(a, maps, s);
+    return single ? launch<64, 1>(a, maps, s) : launch<64, 2>(a, maps, s);
 }
 
 }  // namespace bpa

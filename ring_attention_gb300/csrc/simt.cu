@@ -106,6 +106,7 @@ __device__ void fold_keys(const Problem& P, int b, int h, int g, int q, int klo,
         if (ok) {
             const T* kr = K + b * P.ks[0] + static_cast<int64_t>(k) * P.ks[1] + g * P.ks[2];
             float dot = 0.f;
+#pragma unroll 8
             for (int c = 0; c < P.d; ++c) dot = fmaf(sq[c], ldf(kr + c), dot);
             s = dot * P.scale + bias_at(P, b, h, q, k);
         }
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
                     const T* kr = K + b * P.ks[0] + static_cast<int64_t>(k) * P.ks[1] + g * P.ks[2];
                     const T* vr = V + b * P.vs[0] + static_cast<int64_t>(k) * P.vs[1] + g * P.vs[2];
                     float dot = 0.f, dp = 0.f;
+#pragma unroll 8
                     for (int c = 0; c < P.d; ++c) {
                         dot = fmaf(sq[warp][c], ldf(kr + c), dot);
                         dp = fmaf(sdo[warp][c], ldf(vr + c), dp);
@@ -314,6 +316,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
                     if (lse != INFINITY) {
                         const int64_t qoff = b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2];
                         float dot = 0.f, dp = 0.f;
+#pragma unroll 8
                         for (int c = 0; c < P.d; ++c) {
                             dot = fmaf(ldf(Q + qoff + c), sk[warp][c], dot);
                             dp = fmaf(ldf(dO + qoff + c), sv[warp][c], dp);
