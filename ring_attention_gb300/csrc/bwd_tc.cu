@@ -15,15 +15,18 @@
 // TMEM (512 columns): S^T [0,64), dP^T x2 [64,192), dQ^T [192,256),
 // dK [256,384), dV [384,512).  dP^T is double-buffered so that S^T and dP^T
 // of tile it are computed while the softmax warps still work on tile it-1.
-// dQ partial tiles go to a head-major float32 accumulator [B, Hq, S', 128]
-// (S' = S rounded up to 64), where one 64 x 128 tile is one contiguous 32 KB
-// block: the dQ warps stage it in shared memory and add it with one bulk
-// reduction.
+// Two softmax warpgroups split the 64 query columns of a tile (32 each).
+// Once a warpgroup has read its 32 dP^T columns, it writes there its P^T
+// (16 columns of bf16 pairs) and dS^T (16 columns), the TMEM A operands of
+// the dV and dK products; dS^T also goes to shared memory, where it is the
+// B operand of dQ^T.  The same warpgroup then drains its 32 columns of the
+// previous tile's dQ^T (channels on the lanes) straight into a head-major
+// float32 accumulator [B, Hq, S', 128] (S' = S rounded up to 64) with
+// coalesced reductions: one warp instruction adds one 128-byte row segment.
 // Roles (320 threads):
-//   warps 0-3  thread r owns key row r: P, dS from S^T, dP^T -> shared memory;
-//              at the end dK (scaled) -> output;
-//   warps 4-7  thread r owns channel r of dQ^T: TMEM -> shared staging ->
-//              global float32 accumulator (bulk reduce-add); at the end dV -> output;
+//   warps 0-3  query columns 0-31 of each tile, warps 4-7 columns 32-63;
+//              thread (warp % 4) * 32 + lane owns key row / dQ channel of that TMEM lane;
+//              at the end warps 0-3 write dK (scaled), warps 4-7 dV;
 //   warp 8     TMA producer: K, V once; Q, dO (+ lse, D) per query tile;
 //   warp 9     MMA issuer, TMEM owner.
 #include <math.h>
@@ -37,8 +40,9 @@ namespace {
 constexpr int D = 128;        // head dim
 constexpr int BK = 128;       // keys per CTA
 constexpr int BQ = 64;        // queries per tile
-constexpr int NS = 3;         // Q / dO stages
+constexpr int NS = 4;         // Q / dO stages
 constexpr int kThreads = 320;
+constexpr int kSoftmax = 256;    // threads of the two softmax warpgroups
 
 constexpr int SUBK = BK * 128;    // one 64-channel slab of the key tile
 constexpr int SUBQ = BQ * 128;    // one 64-channel slab of a query tile
@@ -46,22 +50,20 @@ constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + BK * D * 2;
 constexpr int OFF_Q = OFF_V + BK * D * 2;
 constexpr int OFF_DO = OFF_Q + NS * BQ * D * 2;
-constexpr int NPB = 1;        // P^T / dS^T buffers
-constexpr int OFF_P = OFF_DO + NS * BQ * D * 2;     // P^T  [128 keys][64 q] bf16, x NPB
-constexpr int OFF_DS = OFF_P + NPB * BK * BQ * 2;   // dS^T [128 keys][64 q] bf16, x NPB
-constexpr int OFF_ST = OFF_DS + NPB * BK * BQ * 2;  // per stage: lse[64], D[64] float
-constexpr int OFF_DQ = OFF_ST + NS * 512;           // dQ staging [64 q][128 ch] float32
-constexpr int OFF_BAR = OFF_DQ + BQ * D * 4;
+constexpr int OFF_DS = OFF_DO + NS * BQ * D * 2;    // dS^T [128 keys][64 q] bf16
+constexpr int OFF_ST = OFF_DS + BK * BQ * 2;        // per stage: lse[64], D[64] float
+constexpr int OFF_BAR = OFF_ST + NS * 512;
 constexpr int SMEM = OFF_BAR + 256 + 1024;
-constexpr int PT_BYTES = BK * BQ * 2;
+static_assert(SMEM <= 232448, "shared memory");
 
 // barrier slots
 constexpr int B_KV = 0, B_QF = 1, B_QE = 1 + NS, B_S = 1 + 2 * NS, B_SF = 2 + 2 * NS, B_DP = 3 + 2 * NS,
-              B_DS = 5 + 2 * NS, B_DQF = 6 + 2 * NS, B_DQE = 7 + 2 * NS, B_PF = 8 + 2 * NS, B_KVD = 10 + 2 * NS,
-              B_FIN = 11 + 2 * NS, B_STW = 12 + 2 * NS, B_STF = 13 + 2 * NS, NBAR = 14 + 2 * NS;
+              B_DS = 5 + 2 * NS, B_DQF = 6 + 2 * NS, B_DQE = 7 + 2 * NS, B_PF = 8 + 2 * NS, B_KVD = 9 + 2 * NS,
+              B_FIN = 10 + 2 * NS, NBAR = 11 + 2 * NS;
+static_assert(8 * NBAR + 8 <= 256, "barrier area");
 
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BK, BQ, 0, 0);     // S^T, dP^T: both K-major
-constexpr uint32_t IDESC_KV = idesc_bf16_f32(BK, D, 0, 1);     // dV, dK: A K-major, B MN-major
+constexpr uint32_t IDESC_KV = idesc_bf16_f32(BK, D, 0, 1);     // dV, dK: A from TMEM, B MN-major
 constexpr uint32_t IDESC_Q = idesc_bf16_f32(D, BQ, 1, 1);      // dQ^T: both MN-major
 
 struct Work {
@@ -128,18 +130,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(B_QE + s), 1);
         }
         mbar_init(BAR(B_S), 1);
-        mbar_init(BAR(B_SF), 128);
+        mbar_init(BAR(B_SF), kSoftmax);
         mbar_init(BAR(B_DP + 0), 1);
         mbar_init(BAR(B_DP + 1), 1);
-        mbar_init(BAR(B_DS), 128);
+        mbar_init(BAR(B_DS), kSoftmax);
         mbar_init(BAR(B_DQF), 1);
-        mbar_init(BAR(B_DQE), 128);
-        mbar_init(BAR(B_PF + 0), 1);
-        mbar_init(BAR(B_PF + 1), 1);
+        mbar_init(BAR(B_DQE), kSoftmax);
+        mbar_init(BAR(B_PF), 1);
         mbar_init(BAR(B_KVD), 1);
         mbar_init(BAR(B_FIN), 1);
-        mbar_init(BAR(B_STW), 128);
-        mbar_init(BAR(B_STF), 1);
         *abort_flag = (a.status && (*reinterpret_cast<volatile uint32_t*>(a.status) & ST_TIMEOUT)) ? 1 : 0;
         fence_mbar_init();
     }
@@ -155,8 +154,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool skip = *abort_flag != 0;
     const int n_it = skip ? 0 : W.n_it;
 
-    auto iter_head = [&](int it) { return W.hkv * P.G + it / W.n_qt; };
-    auto iter_q0 = [&](int it) { return (W.qt_lo + it % W.n_qt) * BQ; };
+    // Query tiles from the last one down, the group's q heads innermost: the CTAs of one
+    // (batch, kv head) then walk the same query tiles at about the same time, so a Q / dO
+    // tile and its dQ accumulator rows are fetched once into L2 and shared.
+    auto iter_head = [&](int it) { return W.hkv * P.G + it % P.G; };
+    auto iter_q0 = [&](int it) { return (W.qt_lo + W.n_qt - 1 - it / P.G) * BQ; };
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
@@ -200,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // descriptors of the resident K / V tile (K-major, and K as an MN-major A operand)
             const uint64_t kd0 = sdesc_sw128(sb + OFF_K, 16, 1024), vd0 = sdesc_sw128(sb + OFF_V, 16, 1024);
             const uint64_t kmn0 = sdesc_sw128(sb + OFF_K, SUBK, 1024);
+            const uint64_t dsmn = sdesc_sw128(sb + OFF_DS, 16, 1024);
             // order per tile it: S_it (once S_it-1 has been read), dP_it, then dV / dK / dQ
             // of tile it-1 (once its dS is ready)
             for (int it = 0; ok && it <= n_it; ++it) {
@@ -218,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_commit(BAR(B_S));
                     // dP^T buffer (it & 1) last held tile it-2, whose dS was waited for below
+                    // (and whose P^T / dS^T pairs were consumed by MMAs issued before this one)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
@@ -228,27 +232,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_commit(BAR(B_DP + (it & 1)));
                 }
                 if (it > 0) {
-                    const int p = it - 1, pst = p % NS, buf = p % NPB;
+                    const int p = it - 1, pst = p % NS;
                     if (!mbar_wait(BAR(B_DS), p & 1, abort_flag, a.status, 0x52)) break;
                     tc_fence_after();
-                    const uint64_t pd = sdesc_sw128(sb + OFF_P + buf * PT_BYTES, 16, 1024);
-                    const uint64_t dsd = sdesc_sw128(sb + OFF_DS + buf * PT_BYTES, 16, 1024);
                     const uint64_t qmn = sdesc_sw128(sb + OFF_Q + pst * BQ * D * 2, SUBQ, 1024);
                     const uint64_t domn = sdesc_sw128(sb + OFF_DO + pst * BQ * D * 2, SUBQ, 1024);
+                    // bf16 pairs of query columns 16 kk .. 16 kk + 15: warpgroup kk / 2 wrote P^T at
+                    // columns 32 (kk / 2) + 8 (kk % 2) of the dP^T buffer and dS^T 16 columns further
+                    const uint32_t tPD = tDP + (p & 1) * BQ;
 #pragma unroll
                     for (int kk = 0; kk < BQ / 16; ++kk) {
                         const uint32_t acc = (p > 0 || kk > 0) ? 1u : 0u;
-                        tc_mma_ss(tDV, sdesc_advance(pd, kk * 32), sdesc_advance(domn, kk * 2048), IDESC_KV, acc);
-                        tc_mma_ss(tDK, sdesc_advance(dsd, kk * 32), sdesc_advance(qmn, kk * 2048), IDESC_KV, acc);
+                        const uint32_t tp = tPD + (kk >> 1) * 32 + (kk & 1) * 8;
+                        tc_mma_ts(tDV, tp, sdesc_advance(domn, kk * 2048), IDESC_KV, acc);
+                        tc_mma_ts(tDK, tp + 16, sdesc_advance(qmn, kk * 2048), IDESC_KV, acc);
                     }
                     if (p > 0 && !mbar_wait(BAR(B_DQE), (p - 1) & 1, abort_flag, a.status, 0x53)) break;
                     tc_fence_after();
-                    const uint64_t dsmn = sdesc_sw128(sb + OFF_DS + buf * PT_BYTES, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         tc_mma_ss(tDQ, sdesc_advance(kmn0, kk * 2048), sdesc_advance(dsmn, kk * 2048), IDESC_Q, kk > 0);
                     tc_commit(BAR(B_DQF));
-                    tc_commit(BAR(B_PF + buf));
+                    tc_commit(BAR(B_PF));
                     tc_commit(BAR(B_QE + pst));
                     if (p == n_it - 1) tc_commit(BAR(B_KVD));
                 }
@@ -256,11 +261,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(BAR(B_FIN));
             drain_wait(BAR(B_FIN), 0, a.status);
         }
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ P / dS (key rows)
-        const int r = threadIdx.x;
+    } else {
+        // ------------------------------------------------------------ P, dS, dQ (two warpgroups)
+        const int wg = warp >> 2, quarter = warp & 3;
+        const int r = quarter * 32 + lane;    // key row of S^T / dP^T, channel of dQ^T: the TMEM lane
+        const int cq = wg * 32;               // this warpgroup's query columns of a tile
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const int k = W.k0 + r;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         int qmin = W.q_lo, qmax = min(W.q_hi, P.S - 1);
         if (P.causal) qmin = max(qmin, k);
         if (P.wr >= 0) qmin = max(qmin, k - P.wr);
@@ -268,19 +275,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (k >= P.S) qmax = -1;
         const float sl2 = P.scale * kLog2e;
         bool aborted = false;
+
+        // dQ^T of tile t, columns cq .. cq+31, added to rows q0+cq .. of the accumulator
+        auto drain_dq = [&](int t) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DQF), t & 1, abort_flag, a.status, 0x70))) return false;
+            tc_fence_after();
+            uint32_t v[32];
+            tmem_ld32(tDQ + cq + lane_base, v);
+            tc_fence_before();
+            mbar_arrive(BAR(B_DQE));
+            float* dst = a.dq_acc + ((static_cast<int64_t>(W.b) * P.Hq + iter_head(t)) * a.Spad + iter_q0(t) + cq) * D + r;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) atomicAdd(dst + c * D, __uint_as_float(v[c]) * P.scale);
+            return true;
+        };
+
         for (int it = 0; it < n_it; ++it) {
-            const int h = iter_head(it), q0 = iter_q0(it), st = it % NS, buf = it & 1;
+            const int h = iter_head(it), q0 = iter_q0(it) + cq, st = it % NS, buf = it & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_S), it & 1, abort_flag, a.status, 0x60))) {
                 aborted = true;
                 break;
             }
             tc_fence_after();
-            float p[BQ];
+            float p[32];
             {
-                uint32_t v[64];
-                tmem_ld64(tS + lane_base, v);
+                uint32_t v[32];
+                tmem_ld32(tS + cq + lane_base, v);
 #pragma unroll
-                for (int i = 0; i < 64; ++i) p[i] = __uint_as_float(v[i]) * sl2;
+                for (int i = 0; i < 32; ++i) p[i] = __uint_as_float(v[i]) * sl2;
             }
             tc_fence_before();
             mbar_arrive(BAR(B_SF));   // S^T may be overwritten by the next tile
@@ -290,65 +312,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 aborted = true;
                 break;
             }
-            const float* lse = st_smem + st * 128;
-            const float* Dq = lse + 64;
+            const float* lse = st_smem + st * 128 + cq;
+            const float* Dq = st_smem + st * 128 + 64 + cq;
             if (P.bias) {
                 const float* brow = P.bias + W.b * P.bs[0] + h * P.bs[1] + static_cast<int64_t>(min(k, P.S - 1)) * P.bs[3];
                 if (P.bs[2] == 0) {   // the bias does not depend on the query: one value per key row
                     const float bk = brow[0] * kLog2e;
 #pragma unroll
-                    for (int c = 0; c < BQ; ++c) p[c] += bk;
+                    for (int c = 0; c < 32; ++c) p[c] += bk;
                 } else {
 #pragma unroll
-                    for (int c = 0; c < BQ; ++c) {
+                    for (int c = 0; c < 32; ++c) {
                         const int q = min(q0 + c, P.S - 1);
                         p[c] = fmaf(brow[q * P.bs[2]], kLog2e, p[c]);
                     }
                 }
             }
 #pragma unroll
-            for (int c = 0; c < BQ; ++c) p[c] = ex2(p[c] - lse[c] * kLog2e);
-            const bool edge = q0 < qmin || q0 + BQ - 1 > qmax;
+            for (int c = 0; c < 32; ++c) p[c] = ex2(p[c] - lse[c] * kLog2e);
+            const bool edge = q0 < qmin || q0 + 31 > qmax;
             if (__any_sync(0xffffffffu, edge)) {
 #pragma unroll
-                for (int c = 0; c < BQ; ++c) {
+                for (int c = 0; c < 32; ++c) {
                     const int q = q0 + c;
                     if (q < qmin || q > qmax) p[c] = 0.f;
                 }
             }
-            // the P^T / dS^T buffer is free once the MMAs of the previous tile that read it are done
-            if (it >= NPB && !__all_sync(0xffffffffu, mbar_wait(BAR(B_PF + it % NPB), ((it - NPB) / NPB) & 1,
-                                                                abort_flag, a.status, 0x61))) {
+            // the dS^T buffer is free once the dQ product of the previous tile has read it
+            if (it > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_PF), (it - 1) & 1, abort_flag, a.status, 0x61))) {
                 aborted = true;
                 break;
             }
-            const uint32_t pb = sb + OFF_P + (it % NPB) * PT_BYTES, db = sb + OFF_DS + (it % NPB) * PT_BYTES;
-#pragma unroll
-            for (int cc = 0; cc < BQ / 8; ++cc)
-                st_shared_v4(pb + sw128_offset(r, cc), pack_bf16(p[cc * 8 + 0], p[cc * 8 + 1]),
-                             pack_bf16(p[cc * 8 + 2], p[cc * 8 + 3]), pack_bf16(p[cc * 8 + 4], p[cc * 8 + 5]),
-                             pack_bf16(p[cc * 8 + 6], p[cc * 8 + 7]));
             if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DP + buf), (it >> 1) & 1, abort_flag, a.status, 0x62))) {
                 aborted = true;
                 break;
             }
             tc_fence_after();
+            // this warpgroup's 32 dP^T columns; once read, P^T pairs take the first 16 of them
+            // and dS^T pairs the other 16
+            const uint32_t tcol = tDP + buf * BQ + cq + lane_base;
+            uint32_t ppk[16], dpk[16];
             {
-                uint32_t v[64];
-                tmem_ld64(tDP + buf * BQ + lane_base, v);
+                uint32_t v[32];
+                tmem_ld32(tcol, v);
 #pragma unroll
-                for (int i = 0; i < 64; ++i) p[i] *= __uint_as_float(v[i]) - Dq[i];
+                for (int i = 0; i < 16; ++i) {
+                    ppk[i] = pack_bf16(p[2 * i], p[2 * i + 1]);
+                    dpk[i] = pack_bf16(p[2 * i] * (__uint_as_float(v[2 * i]) - Dq[2 * i]),
+                                       p[2 * i + 1] * (__uint_as_float(v[2 * i + 1]) - Dq[2 * i + 1]));
+                }
             }
+            tmem_st16_nowait(tcol, ppk);
+            tmem_st16_nowait(tcol + 16, dpk);
+            const uint32_t db = sb + OFF_DS;
 #pragma unroll
-            for (int cc = 0; cc < BQ / 8; ++cc)
-                st_shared_v4(db + sw128_offset(r, cc), pack_bf16(p[cc * 8 + 0], p[cc * 8 + 1]),
-                             pack_bf16(p[cc * 8 + 2], p[cc * 8 + 3]), pack_bf16(p[cc * 8 + 4], p[cc * 8 + 5]),
-                             pack_bf16(p[cc * 8 + 6], p[cc * 8 + 7]));
+            for (int cc = 0; cc < 4; ++cc)
+                st_shared_v4(db + sw128_offset(r, wg * 4 + cc), dpk[4 * cc], dpk[4 * cc + 1], dpk[4 * cc + 2],
+                             dpk[4 * cc + 3]);
+            tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(BAR(B_DS));
+            if (it > 0 && !drain_dq(it - 1)) {
+                aborted = true;
+                break;
+            }
         }
-        // ---- epilogue: dK = scale * acc
+        if (!aborted && n_it > 0 && !drain_dq(n_it - 1)) aborted = true;
+        // ---- epilogue: warps 0-3 dK = scale * acc, warps 4-7 dV = acc
         if (!aborted && !skip) {
             if (n_it > 0) {
                 if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_KVD), 0, abort_flag, a.status, 0x63))) aborted = true;
@@ -356,15 +387,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!aborted) {
                 const int kk = min(k, P.S - 1);
-                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.dk) + W.b * P.ks[0] +
-                                     static_cast<int64_t>(kk) * P.ks[1] + W.hkv * P.ks[2];
-                float* carry = a.dk_acc ? a.dk_acc + ((static_cast<int64_t>(W.b) * P.S + kk) * P.Hkv + W.hkv) * D
-                                        : nullptr;
+                const float f = wg == 0 ? P.scale : 1.f;
+                const uint32_t tacc = wg == 0 ? tDK : tDV;
+                __nv_bfloat16* out = wg == 0 ? static_cast<__nv_bfloat16*>(a.dk) + W.b * P.ks[0] +
+                                                   static_cast<int64_t>(kk) * P.ks[1] + W.hkv * P.ks[2]
+                                             : static_cast<__nv_bfloat16*>(a.dv) + W.b * P.vs[0] +
+                                                   static_cast<int64_t>(kk) * P.vs[1] + W.hkv * P.vs[2];
+                float* carry_base = wg == 0 ? a.dk_acc : a.dv_acc;
+                float* carry = carry_base
+                                   ? carry_base + ((static_cast<int64_t>(W.b) * P.S + kk) * P.Hkv + W.hkv) * D
+                                   : nullptr;
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t v[32];
                     if (n_it > 0) {
-                        tmem_ld32(tDK + c * 32 + lane_base, v);
+                        tmem_ld32(tacc + c * 32 + lane_base, v);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0u;
@@ -376,10 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int i = 0; i < 8; ++i) {
                                     float4 x = dst[i];
-                                    x.x += __uint_as_float(v[4 * i + 0]) * P.scale;
-                                    x.y += __uint_as_float(v[4 * i + 1]) * P.scale;
-                                    x.z += __uint_as_float(v[4 * i + 2]) * P.scale;
-                                    x.w += __uint_as_float(v[4 * i + 3]) * P.scale;
+                                    x.x += __uint_as_float(v[4 * i + 0]) * f;
+                                    x.y += __uint_as_float(v[4 * i + 1]) * f;
+                                    x.z += __uint_as_float(v[4 * i + 2]) * f;
+                                    x.w += __uint_as_float(v[4 * i + 3]) * f;
                                     dst[i] = x;
                                 }
                             }
@@ -388,103 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 4; ++i)
                                 dst[i] = make_uint4(
-                                    pack_bf16(__uint_as_float(v[8 * i + 0]) * P.scale, __uint_as_float(v[8 * i + 1]) * P.scale),
-                                    pack_bf16(__uint_as_float(v[8 * i + 2]) * P.scale, __uint_as_float(v[8 * i + 3]) * P.scale),
-                                    pack_bf16(__uint_as_float(v[8 * i + 4]) * P.scale, __uint_as_float(v[8 * i + 5]) * P.scale),
-                                    pack_bf16(__uint_as_float(v[8 * i + 6]) * P.scale, __uint_as_float(v[8 * i + 7]) * P.scale));
-                        }
-                    }
-                }
-            }
-        }
-    } else {
-        // ------------------------------------------------------------ dQ (channel rows)
-        const int ch = threadIdx.x - 128;     // channel of dQ^T == TMEM lane
-        const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
-        bool aborted = false;
-        for (int it = 0; it < n_it; ++it) {
-            const int h = iter_head(it), q0 = iter_q0(it);
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DQF), it & 1, abort_flag, a.status, 0x70))) {
-                aborted = true;
-                break;
-            }
-            tc_fence_after();
-            uint32_t v[64];
-            tmem_ld64(tDQ + lane_base, v);
-            tc_fence_before();
-            mbar_arrive(BAR(B_DQE));
-            // staging buffer: the bulk reduction of the previous tile must have read it
-            if (it > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_STF), (it - 1) & 1, abort_flag, a.status, 0x72))) {
-                aborted = true;
-                break;
-            }
-            const uint32_t stg = sb + OFF_DQ + ch * 4;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) st_shared_f32(stg + c * (D * 4), __uint_as_float(v[c]) * P.scale);
-            fence_proxy_async_smem();
-            mbar_arrive(BAR(B_STW));
-            if (ch == 0) {
-                if (!mbar_wait(BAR(B_STW), it & 1, abort_flag, a.status, 0x73)) {
-                    aborted = true;
-                } else {
-                    // rows q0 .. q0+63 of head h: one contiguous block of the accumulator
-                    float* tile = a.dq_acc + ((static_cast<int64_t>(W.b) * P.Hq + h) * a.Spad + q0) * D;
-                    bulk_reduce_add_f32(tile, sb + OFF_DQ, BQ * D * 4);
-                    bulk_commit();
-                    bulk_wait_read_all();
-                    mbar_arrive(BAR(B_STF));
-                }
-            }
-            if (__any_sync(0xffffffffu, aborted)) {
-                aborted = true;
-                break;
-            }
-        }
-        if (ch == 0) bulk_wait_all();
-        // ---- epilogue: dV
-        if (!aborted && !skip) {
-            if (n_it > 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_KVD), 0, abort_flag, a.status, 0x71))) aborted = true;
-                tc_fence_after();
-            }
-            if (!aborted) {
-                const int k = W.k0 + ch;
-                const int kk = min(k, P.S - 1);
-                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.dv) + W.b * P.vs[0] +
-                                     static_cast<int64_t>(kk) * P.vs[1] + W.hkv * P.vs[2];
-                float* carry = a.dv_acc ? a.dv_acc + ((static_cast<int64_t>(W.b) * P.S + kk) * P.Hkv + W.hkv) * D
-                                        : nullptr;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t v[32];
-                    if (n_it > 0) {
-                        tmem_ld32(tDV + c * 32 + lane_base, v);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0u;
-                    }
-                    if (k < P.S) {
-                        if (carry) {
-                            if (n_it > 0) {
-                                float4* dst = reinterpret_cast<float4*>(carry + c * 32);
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    float4 x = dst[i];
-                                    x.x += __uint_as_float(v[4 * i + 0]);
-                                    x.y += __uint_as_float(v[4 * i + 1]);
-                                    x.z += __uint_as_float(v[4 * i + 2]);
-                                    x.w += __uint_as_float(v[4 * i + 3]);
-                                    dst[i] = x;
-                                }
-                            }
-                        } else {
-                            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                dst[i] = make_uint4(pack_bf16(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1])),
-                                                    pack_bf16(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
-                                                    pack_bf16(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
-                                                    pack_bf16(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+                                    pack_bf16(__uint_as_float(v[8 * i + 0]) * f, __uint_as_float(v[8 * i + 1]) * f),
+                                    pack_bf16(__uint_as_float(v[8 * i + 2]) * f, __uint_as_float(v[8 * i + 3]) * f),
+                                    pack_bf16(__uint_as_float(v[8 * i + 4]) * f, __uint_as_float(v[8 * i + 5]) * f),
+                                    pack_bf16(__uint_as_float(v[8 * i + 6]) * f, __uint_as_float(v[8 * i + 7]) * f));
                         }
                     }
                 }

@@ -118,9 +118,11 @@ __device__ void fold_keys(const Problem& P, int b, int h, int g, int q, int klo,
         st.l = st.l * corr + warp_sum(p);
 #pragma unroll
         for (int i = 0; i < kPer; ++i) st.acc[i] *= corr;
+        const int nt = min(32, khi - k0 + 1);   // keys of this chunk inside the range
+#pragma unroll 8
         for (int t = 0; t < 32; ++t) {
             const float pt = __shfl_sync(0xffffffffu, p, t);
-            if (pt == 0.f) continue;  // warp-uniform
+            if (t >= nt) continue;
             const T* vr = V + b * P.vs[0] + static_cast<int64_t>(k0 + t) * P.vs[1] + g * P.vs[2];
 #pragma unroll
             for (int i = 0; i < kPer; ++i) {
@@ -254,9 +256,11 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
                     const float z = dot * P.scale + bias_at(P, b, h, q, k);
                     dS = expf(z - lse) * (dp - Dq);
                 }
+                const int nt = min(32, hi - k0 + 1);
+#pragma unroll 8
                 for (int t = 0; t < 32; ++t) {
                     const float st = __shfl_sync(0xffffffffu, dS, t);
-                    if (st == 0.f) continue;
+                    if (t >= nt) continue;
                     const T* kr = K + b * P.ks[0] + static_cast<int64_t>(k0 + t) * P.ks[1] + g * P.ks[2];
 #pragma unroll
                     for (int i = 0; i < kPer; ++i) {
@@ -326,10 +330,12 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
                         dS = p * (dp - a.Dvec[mi]);
                     }
                 }
+                const int nt = min(32, hi - q0 + 1);
+#pragma unroll 8
                 for (int t = 0; t < 32; ++t) {
                     const float pt = __shfl_sync(0xffffffffu, p, t);
                     const float st = __shfl_sync(0xffffffffu, dS, t);
-                    if (pt == 0.f && st == 0.f) continue;
+                    if (t >= nt) continue;
                     const int64_t qoff =
                         b * P.qs[0] + static_cast<int64_t>(q0 + t) * P.qs[1] + h * P.qs[2];
 #pragma unroll
