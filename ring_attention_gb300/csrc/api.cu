@@ -143,7 +143,7 @@ BwdLayout bwd_layout(const Problem& P) {
     L.D = kHeader;
     L.lse = L.D + round256(rows * sizeof(float));
     L.dq = L.lse + round256(rows * sizeof(float));
-    // dQ accumulator, head-major [B, Hq, Spad, d] (one 64-row tile is contiguous)
+    // dQ accumulator [B, Hq, Spad / 4, d, 4]: four consecutive queries of one channel side by side
     const size_t nq = sizeof(float) * P.B * static_cast<size_t>(L.Spad) * P.Hq * P.d;
     const size_t nk = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.d;
     L.dk = L.dq + round256(nq);

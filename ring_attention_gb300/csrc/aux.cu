@@ -161,9 +161,8 @@ __global__ void k_bwd_pre_bf16v(const BwdArgs a, int zero_dq) {
 
 // float32 [B, S, H, d] accumulator -> bf16 tensor with strides (s0, s1, s2); d % 8 == 0:
 // 8 consecutive channels per thread (two 16-byte loads, one 16-byte store).
-// src_rows > 0: the source is head-major [B, H, src_rows, d]; else [B, S, H, d].
 __global__ void k_cast_out_bf16v(const float* src, __nv_bfloat16* dst, int B, int S, int H, int d, int64_t s0,
-                                 int64_t s1, int64_t s2, int src_rows) {
+                                 int64_t s1, int64_t s2) {
     const int g8 = d / 8;
     const int64_t total = static_cast<int64_t>(B) * S * H * g8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -174,7 +173,7 @@ __global__ void k_cast_out_bf16v(const float* src, __nv_bfloat16* dst, int B, in
         const int64_t bq = row / H;
         const int q = static_cast<int>(bq % S);
         const int b = static_cast<int>(bq / S);
-        const int64_t so = src_rows > 0 ? ((static_cast<int64_t>(b) * H + h) * src_rows + q) * d + c : i * 8;
+        const int64_t so = i * 8;
         const float4 x = *reinterpret_cast<const float4*>(src + so);
         const float4 y = *reinterpret_cast<const float4*>(src + so + 4);
         uint4 w;
@@ -183,6 +182,39 @@ __global__ void k_cast_out_bf16v(const float* src, __nv_bfloat16* dst, int B, in
         w.z = pack_bf16(y.x, y.y);
         w.w = pack_bf16(y.z, y.w);
         *reinterpret_cast<uint4*>(dst + b * s0 + static_cast<int64_t>(q) * s1 + h * s2 + c) = w;
+    }
+}
+
+// float32 dQ accumulator of the tensor-core backward, [B, H, src_rows / 4, d, 4] (four
+// consecutive queries of one channel side by side) -> bf16 tensor with strides (s0, s1, s2);
+// d % 32 == 0.  One warp per group of four queries: lane l loads channels l, l+32, ... (512
+// contiguous bytes per load), neighbouring lanes swap halves so that each holds a channel pair
+// for two of the queries, and a store writes 64 contiguous bytes of a row.
+__global__ void k_cast_dq4_bf16(const float* src, __nv_bfloat16* dst, int B, int S, int H, int d, int64_t s0,
+                                int64_t s1, int64_t s2, int src_rows) {
+    const int lane = threadIdx.x & 31, r4 = src_rows / 4, n4 = (S + 3) / 4;
+    const bool even = (lane & 1) == 0;
+    const int64_t groups = static_cast<int64_t>(B) * H * n4;
+    const int64_t wstride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); g < groups;
+         g += wstride) {
+        const int q4 = static_cast<int>(g % n4);
+        const int64_t bh = g / n4;
+        const int h = static_cast<int>(bh % H);
+        const int b = static_cast<int>(bh / H);
+        const float4* in = reinterpret_cast<const float4*>(src + (bh * r4 + q4) * static_cast<int64_t>(d) * 4);
+        const int qa = q4 * 4 + (even ? 0 : 2);   // the two rows this lane writes: qa, qa + 1
+        __nv_bfloat16* out = dst + b * s0 + h * s2;
+        for (int c0 = 0; c0 < d; c0 += 32) {
+            const float4 x = in[c0 + lane];
+            const float y0 = __shfl_xor_sync(0xffffffffu, even ? x.z : x.x, 1);
+            const float y1 = __shfl_xor_sync(0xffffffffu, even ? x.w : x.y, 1);
+            const int c = c0 + lane - (even ? 0 : 1);   // first channel of this lane's pair
+            const uint32_t w0 = even ? pack_bf16(x.x, y0) : pack_bf16(y0, x.z);
+            const uint32_t w1 = even ? pack_bf16(x.y, y1) : pack_bf16(y1, x.w);
+            if (qa < S) *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(qa) * s1 + c) = w0;
+            if (qa + 1 < S) *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(qa + 1) * s1 + c) = w1;
+        }
     }
 }
 
@@ -254,14 +286,15 @@ cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t s) {
         ((reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) | reinterpret_cast<uintptr_t>(a.dv)) &
          15u) == 0 &&
         ((P.qs[0] | P.qs[1] | P.qs[2] | P.ks[0] | P.ks[1] | P.ks[2] | P.vs[0] | P.vs[1] | P.vs[2]) & 7) == 0;
-    if (vec_ok && P.d % 8 == 0) {
-        k_cast_out_bf16v<<<grid_for(nq / 8, 256), 256, 0, s>>>(a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), P.B,
-                                                               P.S, P.Hq, P.d, P.qs[0], P.qs[1], P.qs[2], a.Spad);
+    if (vec_ok && P.d % 32 == 0) {
+        const int64_t dq_threads = static_cast<int64_t>(P.B) * P.Hq * ((P.S + 3) / 4) * 32;   // a warp per 4 rows
+        k_cast_dq4_bf16<<<grid_for(dq_threads, 256), 256, 0, s>>>(
+            a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), P.B, P.S, P.Hq, P.d, P.qs[0], P.qs[1], P.qs[2], a.Spad);
         if (a.dk_acc) {
             k_cast_out_bf16v<<<grid_for(nk / 8, 256), 256, 0, s>>>(
-                a.dk_acc, static_cast<__nv_bfloat16*>(a.dk), P.B, P.S, P.Hkv, P.d, P.ks[0], P.ks[1], P.ks[2], 0);
+                a.dk_acc, static_cast<__nv_bfloat16*>(a.dk), P.B, P.S, P.Hkv, P.d, P.ks[0], P.ks[1], P.ks[2]);
             k_cast_out_bf16v<<<grid_for(nk / 8, 256), 256, 0, s>>>(
-                a.dv_acc, static_cast<__nv_bfloat16*>(a.dv), P.B, P.S, P.Hkv, P.d, P.vs[0], P.vs[1], P.vs[2], 0);
+                a.dv_acc, static_cast<__nv_bfloat16*>(a.dv), P.B, P.S, P.Hkv, P.d, P.vs[0], P.vs[1], P.vs[2]);
         }
         return cudaGetLastError();
     }

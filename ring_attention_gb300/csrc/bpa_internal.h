@@ -48,7 +48,7 @@ struct BwdArgs {
     float* Dvec;        // [B, Hq, Spad] rowsum(dO * O); padding rows hold 0
     float* lse;         // [B, Hq, Spad] m + log(l) (natural log); +inf on padding / empty rows
     int Spad;           // S rounded up to 64
-    float* dq_acc;      // [B, Hq, Spad, d] float32 (head-major: a 64-row tile is contiguous)
+    float* dq_acc;      // [B, Hq, Spad / 4, d, 4] float32 (four consecutive queries of a channel together)
     float* dk_acc;      // ring carries [B, S, Hkv, d] float32, or nullptr
     float* dv_acc;
     int ring_idx;

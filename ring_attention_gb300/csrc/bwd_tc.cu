@@ -20,9 +20,12 @@
 // (16 columns of bf16 pairs) and dS^T (16 columns), the TMEM A operands of
 // the dV and dK products; dS^T also goes to shared memory, where it is the
 // B operand of dQ^T.  The same warpgroup then drains its 32 columns of the
-// previous tile's dQ^T (channels on the lanes) straight into a head-major
-// float32 accumulator [B, Hq, S', 128] (S' = S rounded up to 64) with
-// coalesced reductions: one warp instruction adds one 128-byte row segment.
+// previous tile's dQ^T (channels on the lanes) straight into a float32
+// accumulator with coalesced 16-byte reductions.  The accumulator of one
+// (batch, q head) is laid out [S'/4][128 channels][4 queries] (S' = S rounded
+// up to 64), so a warp's reduction covers 512 contiguous bytes.
+// Consecutive products into one TMEM accumulator wait on each other, so the
+// independent S^T and dP^T products are issued interleaved (as are dV, dK).
 // Roles (320 threads):
 //   warps 0-3  query columns 0-31 of each tile, warps 4-7 columns 32-63;
 //              thread (warp % 4) * 32 + lane owns key row / dQ channel of that TMEM lane;
@@ -213,22 +216,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint64_t qd = sdesc_sw128(sb + OFF_Q + st * BQ * D * 2, 16, 1024);
                     const uint64_t dod = sdesc_sw128(sb + OFF_DO + st * BQ * D * 2, 16, 1024);
+                    // S^T and dP^T are independent accumulations: interleaved, each waits less on
+                    // its own previous step.  The dP^T buffer (it & 1) last held tile it-2, whose dS
+                    // was waited for below (and whose P^T / dS^T pairs were consumed by MMAs issued
+                    // before these).
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
                         const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
                         tc_mma_ss(tS, sdesc_advance(kd0, offk), sdesc_advance(qd, offq), IDESC_S, kk > 0);
-                    }
-                    tc_commit(BAR(B_S));
-                    // dP^T buffer (it & 1) last held tile it-2, whose dS was waited for below
-                    // (and whose P^T / dS^T pairs were consumed by MMAs issued before this one)
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
-                        const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
                         tc_mma_ss(tDP + (it & 1) * BQ, sdesc_advance(vd0, offk), sdesc_advance(dod, offq), IDESC_S,
                                   kk > 0);
                     }
+                    tc_commit(BAR(B_S));
                     tc_commit(BAR(B_DP + (it & 1)));
                 }
                 if (it > 0) {
@@ -276,7 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = P.scale * kLog2e;
         bool aborted = false;
 
-        // dQ^T of tile t, columns cq .. cq+31, added to rows q0+cq .. of the accumulator
+        // dQ^T of tile t, query columns cq .. cq+31, added to the accumulator [S'/4][128][4] of
+        // its (batch, q head): four consecutive queries of this thread's channel are one 16-byte
+        // reduction, and a warp's 32 channels are 512 contiguous bytes
         auto drain_dq = [&](int t) -> bool {
             if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DQF), t & 1, abort_flag, a.status, 0x70))) return false;
             tc_fence_after();
@@ -284,9 +286,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tDQ + cq + lane_base, v);
             tc_fence_before();
             mbar_arrive(BAR(B_DQE));
-            float* dst = a.dq_acc + ((static_cast<int64_t>(W.b) * P.Hq + iter_head(t)) * a.Spad + iter_q0(t) + cq) * D + r;
+            float* dst = a.dq_acc + (static_cast<int64_t>(W.b) * P.Hq + iter_head(t)) * a.Spad * D +
+                         (static_cast<int64_t>((iter_q0(t) + cq) >> 2) * D + r) * 4;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) atomicAdd(dst + c * D, __uint_as_float(v[c]) * P.scale);
+            for (int j = 0; j < 8; ++j)
+                red_add_v4(dst + j * (4 * D), __uint_as_float(v[4 * j]) * P.scale,
+                           __uint_as_float(v[4 * j + 1]) * P.scale, __uint_as_float(v[4 * j + 2]) * P.scale,
+                           __uint_as_float(v[4 * j + 3]) * P.scale);
             return true;
         };
 

@@ -127,6 +127,12 @@ BPA_DEV void bulk_reduce_add_f32(float* dst, uint32_t src, uint32_t bytes) {
                  "r"(src), "r"(bytes)
                  : "memory");
 }
+// dst[0..3] += (x, y, z, w) in global memory (16-byte aligned), no return value.
+BPA_DEV void red_add_v4(float* dst, float x, float y, float z, float w) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(reinterpret_cast<uint64_t>(dst)), "f"(x),
+                 "f"(y), "f"(z), "f"(w)
+                 : "memory");
+}
 BPA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Waits until every committed bulk operation has finished reading its shared source.
 BPA_DEV void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
