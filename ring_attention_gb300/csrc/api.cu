@@ -271,6 +271,11 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
     a.m = m;
     a.l = l;
     a.status = reinterpret_cast<uint32_t*>(ws);
+    // work-item counters of the tensor-core forward: words 2..63 of the (cleared) status
+    // header, one per launch; a word is cleared again before it is reused
+    uint32_t* counters = a.status + 2;
+    constexpr int kCounters = static_cast<int>(kHeader / 4) - 2;
+    a.sched = counters;
 
     if (P.block_idx) {
         e = gather_supported(P) ? launch_gather_fwd(a, s) : launch_fwd_simt(a, s);
@@ -296,6 +301,10 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
     if (begin == 0 && (e = launch_ring_init(a, s)) != cudaSuccess) return cuda_fail(e, "ring carry init");
     for (int idx = begin; idx < end; ++idx) {
         a.ring_idx = idx;
+        const int li = idx - begin;
+        a.sched = counters + li % kCounters;
+        if (tc && li >= kCounters && (e = cudaMemsetAsync(a.sched, 0, sizeof(uint32_t), s)) != cudaSuccess)
+            return cuda_fail(e, "clearing a work counter");
         e = tc ? launch_fwd_tc(a, maps, s) : launch_fwd_simt(a, s);
         if (e != cudaSuccess) return cuda_fail(e, "ring step launch");
     }

@@ -34,6 +34,7 @@ struct FwdArgs {
     float* acc;         // ring carry [B, S, Hq, d] float32, or nullptr (one-shot)
     int ring_idx;       // ring step run by this launch
     uint32_t* status;   // device status word
+    uint32_t* sched;    // work-item counter of the tensor-core forward; zero before each launch
 };
 
 struct BwdArgs {

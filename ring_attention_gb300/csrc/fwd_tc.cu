@@ -63,11 +63,14 @@ struct FwdCfg {
     static constexpr int OFF_V = OFF_K + NSK * KV_BYTES;
     static constexpr int OFF_KB = OFF_V + NSV * KV_BYTES;   // per K stage: the tile's 128 key-bias values
     static constexpr int OFF_BAR = OFF_KB + NSK * BN * 4;
-    static constexpr int SMEM = OFF_BAR + 256 + 1024;   // + slack to align the base to 1024
-    // barrier slots: K full / empty, V full / empty, S, P, O per query tile
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;   // + slack to align the base to 1024
+    // barrier slots: Q full / empty; K full / empty, V full / empty; S, P, O full, O empty per
+    // query tile; work item published / read (two slots)
     static constexpr int B_Q = 0, B_KF = 1, B_KE = 1 + NSK, B_VF = 1 + 2 * NSK, B_VE = 1 + 2 * NSK + NSV,
                          B_S = 1 + 2 * NSK + 2 * NSV, B_P = B_S + 2, B_O = B_S + 4, B_FIN = B_S + 6,
-                         NBAR = B_S + 7;
+                         B_QE = B_S + 7, B_OE = B_S + 8, B_IF = B_S + 10, B_IE = B_S + 12, NBAR = B_S + 14;
+    static_assert(8 * NBAR + 16 <= 512, "barrier area");
+    static_assert(SMEM <= 232448, "shared memory");
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);   // Q, K both K-major
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 0, 1);   // P (TMEM), V MN-major
     static_assert(NQ == 2 || 2 * SMEM <= 233472, "two single-tile CTAs must fit an SM");
@@ -81,11 +84,12 @@ struct Tile {
     int lo[2], hi[2];        // per query tile: visited step range [lo, hi] (empty if lo > hi)
 };
 
+// Work item `item` (heaviest causal query pairs first) -> its query tiles and key range.
 template <int NQ>
-__device__ __forceinline__ Tile decode_tile(const FwdArgs& a) {
+__device__ __forceinline__ Tile decode_tile(const FwdArgs& a, int item) {
     const Problem& P = a.P;
     const int nqp = (P.S + NQ * BM - 1) / (NQ * BM);
-    int r = blockIdx.x;
+    int r = item;
     const int gi = r % P.G;
     r /= P.G;
     Tile t;
@@ -245,6 +249,51 @@ __device__ __forceinline__ float row_exp(const RowCtx& R, float mref) {
     return a + b;
 }
 
+// One pass over the row for tiles after the first: P = exp2(x - mref) for the
+// reference the row already has, kept in registers as bf16 pairs (pk[i] holds
+// columns 2i, 2i+1), together with the tile max `mt` and the row sum of P.  The
+// caller writes pk over S only when no row of the warp has to move its
+// reference (mt > reference + kTau); otherwise it recomputes P with row_exp.
+template <int BIAS, bool EDGE>
+__device__ __forceinline__ float row_exp_1p(const RowCtx& R, float mref, uint32_t (&pk)[BN / 2], float& mt) {
+    uint64_t rs2 = 0;   // two float32 partial sums
+    float mx = -INFINITY;
+    const uint64_t sl2x2 = f2_pack(R.sl2, R.sl2), negm2 = f2_pack(-mref, -mref);
+#pragma unroll
+    for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t cur[32];
+        tmem_ld32(R.tS + cc * 32, cur);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int col = cc * 32 + 2 * i;
+            const float s0 = __uint_as_float(cur[2 * i]), s1 = __uint_as_float(cur[2 * i + 1]);
+            float x0, x1;   // x - mref
+            if (!BIAS && !EDGE) {
+                mx = fmax3(mx, s0, s1);   // scale > 0: max of raw S, scaled once
+                f2_unpack(ffma2(f2_pack(s0, s1), sl2x2, negm2), x0, x1);
+            } else if (BIAS == 1 && !EDGE) {
+                const float2 bp = *reinterpret_cast<const float2*>(R.kbias + col);
+                f2_unpack(ffma2(f2_pack(s0, s1), sl2x2, ffma2(f2_pack(bp.x, bp.y), f2_pack(kLog2e, kLog2e), negm2)),
+                          x0, x1);
+                mx = fmax3(mx, x0, x1);
+            } else {
+                x0 = score_at<BIAS, EDGE>(R, cur[2 * i], col) - mref;
+                x1 = score_at<BIAS, EDGE>(R, cur[2 * i + 1], col + 1) - mref;
+                mx = fmax3(mx, x0, x1);
+            }
+            const uint64_t p2 = f2_pack(ex2(x0), ex2(x1));
+            rs2 = fadd2(rs2, p2);
+            float p0, p1;
+            f2_unpack(p2, p0, p1);
+            pk[cc * 16 + i] = pack_bf16(p0, p1);
+        }
+    }
+    mt = (!BIAS && !EDGE) ? mx * R.sl2 : mx + mref;
+    float a, b;
+    f2_unpack(rs2, a, b);
+    return a + b;
+}
+
 template <int D, int NQ>
 __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
     k_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -260,11 +309,13 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const Problem& P = a.P;
-    const Tile T = decode_tile<NQ>(a);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int* item_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);   // two slots
+    const int n_items = ((P.S + NQ * BM - 1) / (NQ * BM)) * P.Hq * P.B;
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(C::B_Q), 1);
+        mbar_init(BAR(C::B_QE), 1);
         for (int s = 0; s < C::NSK; ++s) {
             mbar_init(BAR(C::B_KF + s), 1);
             mbar_init(BAR(C::B_KE + s), 1);
@@ -277,6 +328,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
             mbar_init(BAR(C::B_S + i), 1);
             mbar_init(BAR(C::B_P + i), 128);
             mbar_init(BAR(C::B_O + i), 1);
+            mbar_init(BAR(C::B_OE + i), 128);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(BAR(C::B_IF + s), 1);
+            mbar_init(BAR(C::B_IE + s), 2 + 4 * NQ);   // V lane, MMA lane, one lane per softmax warp
         }
         mbar_init(BAR(C::B_FIN), 1);
         // a CTA that starts after another one gave up does no work
@@ -292,140 +348,217 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const bool skip = *abort_flag != 0;
-    const int n = skip ? 0 : T.n;
-    auto active = [&](int i, int j) { return j >= T.lo[i] && j <= T.hi[i]; };
     // a bias that does not depend on the query row (and is contiguous along keys)
     // is staged per key tile in shared memory by the producer
     const bool key_bias = P.bias && P.bs[2] == 0 && P.bs[3] == 1 && (P.S % BN) == 0 &&
                           ((reinterpret_cast<uintptr_t>(P.bias) | ((P.bs[0] | P.bs[1]) * 4)) & 15) == 0;
-    const float* kbias_src = key_bias ? P.bias + T.b * P.bs[0] + T.h * P.bs[1] : nullptr;
+
+    // Work items are handed out dynamically (heaviest first): producer lane 0 takes the next
+    // one from the global counter and publishes it in slot k % 2; every other role reads it.
+    // A value >= n_items ends the loop.  Items whose tiles see no key carry no barrier phases.
+    auto read_item = [&](int k, bool arrive) -> int {
+        const int sl = k & 1;
+        if (!mbar_wait(BAR(C::B_IF + sl), (k >> 1) & 1, abort_flag, a.status, 0x0F)) return n_items;
+        const int item = item_slot[sl];
+        __syncwarp(__activemask());
+        if (arrive) mbar_arrive(BAR(C::B_IE + sl));
+        return item;
+    };
 
     if (warp == C::kProducer) {
         // ------------------------------------------------------------ producer
-        // lane 0 streams Q and the K ring (plus the staged key bias), lane 1 the
-        // V ring: two independent loops, so no stage count can order them into a wait cycle
-        if (lane < 2 && n > 0) {
-            if (lane == 0) {
-                tma_prefetch(&tmQ);
-                tma_prefetch(&tmK);
+        // lane 0 fetches the work items and streams Q and the K ring (plus the staged key
+        // bias), lane 1 the V ring: two independent loops, so no stage count can order them
+        // into a wait cycle.  Ring positions continue across items.
+        if (lane == 0) {
+            tma_prefetch(&tmQ);
+            tma_prefetch(&tmK);
+            int kw = 0, gk = 0;
+            for (int k = 0;; ++k) {
+                if (k >= 2 && !mbar_wait(BAR(C::B_IE + (k & 1)), ((k >> 1) - 1) & 1, abort_flag, a.status, 0x0E)) break;
+                int item = skip ? n_items : static_cast<int>(atomicAdd(a.sched, 1u));
+                if (item > n_items) item = n_items;
+                item_slot[k & 1] = item;
+                mbar_arrive(BAR(C::B_IF + (k & 1)));
+                if (item >= n_items) break;
+                const Tile T = decode_tile<NQ>(a, item);
+                if (T.n == 0) continue;
+                // Q buffers are free once the previous item's S products are done
+                if (kw > 0 && !mbar_wait(BAR(C::B_QE), (kw - 1) & 1, abort_flag, a.status, 0x12)) break;
                 mbar_expect_tx(BAR(C::B_Q), NQ * C::Q_BYTES);
                 for (int i = 0; i < NQ; ++i)
                     for (int sub = 0; sub < D / 64; ++sub)
                         tma_load_4d(sb + C::OFF_Q + i * C::Q_BYTES + sub * C::SUB, &tmQ, BAR(C::B_Q), sub * 64, T.h,
                                     T.q0 + i * BM, T.b);
-                int nk = 0;
-                for (int j = 0; j < n; ++j) {
-                    const int st = j % C::NSK, use = j / C::NSK;
-                    if (use > 0 && !mbar_wait(BAR(C::B_KE + st), (use - 1) & 1, abort_flag, a.status, 0x10)) break;
+                ++kw;
+                const float* kbias_src = key_bias ? P.bias + T.b * P.bs[0] + T.h * P.bs[1] : nullptr;
+                bool ok = true;
+                for (int j = 0; j < T.n; ++j, ++gk) {
+                    const int st = gk % C::NSK, use = gk / C::NSK;
+                    if (use > 0 && !mbar_wait(BAR(C::B_KE + st), (use - 1) & 1, abort_flag, a.status, 0x10)) {
+                        ok = false;
+                        break;
+                    }
                     mbar_expect_tx(BAR(C::B_KF + st), C::KV_BYTES + (key_bias ? BN * 4 : 0));
                     if (key_bias)
                         bulk_load(sb + C::OFF_KB + st * BN * 4, kbias_src + (T.kt0 + j) * BN, BN * 4, BAR(C::B_KF + st));
                     for (int sub = 0; sub < D / 64; ++sub)
                         tma_load_4d(sb + C::OFF_K + st * C::KV_BYTES + sub * C::SUB, &tmK, BAR(C::B_KF + st), sub * 64,
                                     T.hkv, (T.kt0 + j) * BN, T.b);
-                    nk = j + 1;
                 }
-                // drain: every copy issued must land before the CTA may exit
-                drain_wait(BAR(C::B_Q), 0, a.status);
-                for (int s = 0; s < C::NSK; ++s) {
-                    const int uses = (nk - s + C::NSK - 1) / C::NSK;
-                    if (uses > 0) drain_wait(BAR(C::B_KF + s), (uses - 1) & 1, a.status);
-                }
-            } else {
-                tma_prefetch(&tmV);
-                int nv = 0;
-                for (int j = 0; j < n; ++j) {
-                    const int st = j % C::NSV, use = j / C::NSV;
-                    if (use > 0 && !mbar_wait(BAR(C::B_VE + st), (use - 1) & 1, abort_flag, a.status, 0x11)) break;
+                if (!ok) break;
+            }
+            // drain: every copy issued must land before the CTA may exit
+            if (kw > 0) drain_wait(BAR(C::B_Q), (kw - 1) & 1, a.status);
+            for (int s = 0; s < C::NSK; ++s) {
+                const int uses = (gk - s + C::NSK - 1) / C::NSK;
+                if (uses > 0) drain_wait(BAR(C::B_KF + s), (uses - 1) & 1, a.status);
+            }
+        } else if (lane == 1) {
+            tma_prefetch(&tmV);
+            int gv = 0;
+            for (int k = 0;; ++k) {
+                const int item = read_item(k, true);
+                if (item >= n_items) break;
+                const Tile T = decode_tile<NQ>(a, item);
+                bool ok = true;
+                for (int j = 0; j < T.n; ++j, ++gv) {
+                    const int st = gv % C::NSV, use = gv / C::NSV;
+                    if (use > 0 && !mbar_wait(BAR(C::B_VE + st), (use - 1) & 1, abort_flag, a.status, 0x11)) {
+                        ok = false;
+                        break;
+                    }
                     mbar_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
                     for (int sub = 0; sub < D / 64; ++sub)
                         tma_load_4d(sb + C::OFF_V + st * C::KV_BYTES + sub * C::SUB, &tmV, BAR(C::B_VF + st), sub * 64,
                                     T.hkv, (T.kt0 + j) * BN, T.b);
-                    nv = j + 1;
                 }
-                for (int s = 0; s < C::NSV; ++s) {
-                    const int uses = (nv - s + C::NSV - 1) / C::NSV;
-                    if (uses > 0) drain_wait(BAR(C::B_VF + s), (uses - 1) & 1, a.status);
-                }
+                if (!ok) break;
+            }
+            for (int s = 0; s < C::NSV; ++s) {
+                const int uses = (gv - s + C::NSV - 1) / C::NSV;
+                if (uses > 0) drain_wait(BAR(C::B_VF + s), (uses - 1) & 1, a.status);
             }
         }
     } else if (warp == C::kMma) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n > 0) {
-            int cnt[2] = {0, 0};      // products P_i V issued per query tile
-            // descriptors are built once per tile and advanced by immediates
-            auto issue_s = [&](int i, int j) {
-                const int st = j % C::NSK;
-                const uint64_t qd = sdesc_sw128(sb + C::OFF_Q + i * C::Q_BYTES, 16, 1024);
-                const uint64_t kd = sdesc_sw128(sb + C::OFF_K + st * C::KV_BYTES, 16, 1024);
-                const uint32_t d_tmem = tmem + i * BN;
+        if (lane == 0) {
+            int np[2] = {0, 0};       // products P_i V consumed per query tile (P barrier phases)
+            int kw = 0, gk = 0, gv = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int item = read_item(k, true);
+                if (item >= n_items) break;
+                const Tile T = decode_tile<NQ>(a, item);
+                const int n = T.n;
+                if (n == 0) continue;
+                auto active = [&](int i, int j) { return j >= T.lo[i] && j <= T.hi[i]; };
+                // descriptors are built once per tile and advanced by immediates
+                auto issue_s = [&](int i, int j) {
+                    const int st = (gk + j) % C::NSK;
+                    const uint64_t qd = sdesc_sw128(sb + C::OFF_Q + i * C::Q_BYTES, 16, 1024);
+                    const uint64_t kd = sdesc_sw128(sb + C::OFF_K + st * C::KV_BYTES, 16, 1024);
+                    const uint32_t d_tmem = tmem + i * BN;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::SUB + (kk & 3) * 32;
-                    tc_mma_ss(d_tmem, sdesc_advance(qd, off), sdesc_advance(kd, off), C::IDESC_S, kk > 0);
-                }
-                tc_commit(BAR(C::B_S + i));
-            };
-            auto issue_pv = [&](int i, int j, bool first) {
-                const int st = j % C::NSV;
-                const uint64_t vd = sdesc_sw128(sb + C::OFF_V + st * C::KV_BYTES, C::SUB, 1024);
-                const uint32_t t_p = tmem + i * BN, t_o = tmem + NQ * BN + i * 128;
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * C::SUB + (kk & 3) * 32;
+                        tc_mma_ss(d_tmem, sdesc_advance(qd, off), sdesc_advance(kd, off), C::IDESC_S, kk > 0);
+                    }
+                    tc_commit(BAR(C::B_S + i));
+                };
+                auto issue_pv = [&](int i, int j, bool first) {
+                    const int st = (gv + j) % C::NSV;
+                    const uint64_t vd = sdesc_sw128(sb + C::OFF_V + st * C::KV_BYTES, C::SUB, 1024);
+                    const uint32_t t_p = tmem + i * BN, t_o = tmem + NQ * BN + i * 128;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    tc_mma_ts(t_o, t_p + kk * 8, sdesc_advance(vd, kk * 2048), C::IDESC_PV, (!first || kk > 0) ? 1u : 0u);
-            };
-            bool ok = mbar_wait(BAR(C::B_Q), 0, abort_flag, a.status, 0x20) &&
-                      mbar_wait(BAR(C::B_KF), 0, abort_flag, a.status, 0x21);
-            if (ok) {
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc_mma_ts(t_o, t_p + kk * 8, sdesc_advance(vd, kk * 2048), C::IDESC_PV,
+                                  (!first || kk > 0) ? 1u : 0u);
+                };
+                auto wait_k = [&](int j) {
+                    const int pos = gk + j;
+                    return mbar_wait(BAR(C::B_KF + pos % C::NSK), (pos / C::NSK) & 1, abort_flag, a.status, 0x22);
+                };
+                // O_i of the previous item must have been read by its epilogue before this
+                // item's first P_i V overwrites it (waited once per item, in order)
+                bool oe_seen[2] = {kw == 0, kw == 0};
+                auto wait_oe = [&](int i) {
+                    if (oe_seen[i]) return true;
+                    oe_seen[i] = true;
+                    return mbar_wait(BAR(C::B_OE + i), (kw - 1) & 1, abort_flag, a.status, 0x25);
+                };
+                ok = mbar_wait(BAR(C::B_Q), kw & 1, abort_flag, a.status, 0x20) && wait_k(0);
+                if (!ok) break;
                 tc_fence_after();
+                // the S tiles still hold the previous item's P; its P V products were issued first
                 for (int i = 0; i < NQ; ++i)
                     if (active(i, 0)) issue_s(i, 0);
-            }
-            for (int j = 0; ok && j < n; ++j) {
-                const bool next = j + 1 < n;
-                // every K / V copy is observed here, so a stage is never refilled while a copy is in flight
-                if (!mbar_wait(BAR(C::B_VF + j % C::NSV), (j / C::NSV) & 1, abort_flag, a.status, 0x23)) break;
-                bool k_ready = false;
-                auto wait_k_next = [&]() {
-                    const int k1 = j + 1;
-                    if (!mbar_wait(BAR(C::B_KF + k1 % C::NSK), (k1 / C::NSK) & 1, abort_flag, a.status, 0x22)) return false;
-                    k_ready = true;
-                    return true;
-                };
-                const int last = active(NQ - 1, j) ? NQ - 1 : 0;   // last query tile active at step j
-                bool k_released = false;
-                for (int i = 0; i < NQ; ++i) {
-                    if (active(i, j)) {
-                        if (!mbar_wait(BAR(C::B_P + i), cnt[i] & 1, abort_flag, a.status, 0x24)) {
-                            ok = false;
-                            break;
-                        }
-                        // every softmax of step j is done (S(j) and the staged bias are no longer
-                        // read): release K_j's stage before S(j+1) may need a free one
-                        if (i == last) {
-                            tc_commit(BAR(C::B_KE + j % C::NSK));
-                            k_released = true;
-                        }
-                        tc_fence_after();
-                        issue_pv(i, j, cnt[i] == 0);
-                        ++cnt[i];
-                        if (j == T.hi[i]) tc_commit(BAR(C::B_O + i));
+                if (n == 1) tc_commit(BAR(C::B_QE));
+                int pv_item[2] = {0, 0};
+                for (int j = 0; ok && j < n; ++j) {
+                    const bool next = j + 1 < n;
+                    // every K / V copy is observed here, so a stage is never refilled while a copy is in flight
+                    const int vpos = gv + j;
+                    if (!mbar_wait(BAR(C::B_VF + vpos % C::NSV), (vpos / C::NSV) & 1, abort_flag, a.status, 0x23)) {
+                        ok = false;
+                        break;
                     }
-                    if (next && active(i, j + 1)) {
-                        if (!k_ready) {
-                            if (!wait_k_next()) {
+                    bool k_ready = false;
+                    const int last = active(NQ - 1, j) ? NQ - 1 : 0;   // last query tile active at step j
+                    bool k_released = false;
+                    for (int i = 0; i < NQ; ++i) {
+                        if (active(i, j)) {
+                            if (!mbar_wait(BAR(C::B_P + i), np[i] & 1, abort_flag, a.status, 0x24) || !wait_oe(i)) {
                                 ok = false;
                                 break;
                             }
+                            // every softmax of step j is done (S(j) and the staged bias are no longer
+                            // read): release K_j's stage before S(j+1) may need a free one
+                            if (i == last) {
+                                tc_commit(BAR(C::B_KE + (gk + j) % C::NSK));
+                                k_released = true;
+                            }
                             tc_fence_after();
+                            issue_pv(i, j, pv_item[i] == 0);
+                            ++np[i];
+                            ++pv_item[i];
+                            if (j == T.hi[i]) tc_commit(BAR(C::B_O + i));
                         }
-                        issue_s(i, j + 1);
+                        if (next && active(i, j + 1)) {
+                            if (!k_ready) {
+                                if (!wait_k(j + 1)) {
+                                    ok = false;
+                                    break;
+                                }
+                                k_ready = true;
+                                tc_fence_after();
+                            }
+                            issue_s(i, j + 1);
+                        }
+                    }
+                    if (!ok) break;
+                    if (next && !k_ready && !wait_k(j + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (j + 2 == n) tc_commit(BAR(C::B_QE));   // every S of this item is issued
+                    if (!k_released) tc_commit(BAR(C::B_KE + (gk + j) % C::NSK));   // (a step no tile used)
+                    tc_commit(BAR(C::B_VE + vpos % C::NSV));   // V_j is no longer read
+                }
+                if (!ok) break;
+                // a query tile without keys in this item still completes its O phase
+                for (int i = 0; i < NQ; ++i) {
+                    if (T.lo[i] > T.hi[i]) {
+                        if (!wait_oe(i)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_commit(BAR(C::B_O + i));
                     }
                 }
-                if (ok && next && !k_ready && !wait_k_next()) ok = false;
-                if (!ok) break;
-                if (!k_released) tc_commit(BAR(C::B_KE + j % C::NSK));   // (a step no tile used)
-                tc_commit(BAR(C::B_VE + j % C::NSV));   // V_j is no longer read
+                gk += n;
+                gv += n;
+                ++kw;
             }
             // drain: all MMAs issued by this thread complete before TMEM is freed
             tc_commit(BAR(C::B_FIN));
@@ -435,34 +568,40 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
         // ------------------------------------------------------------ softmax (rows)
         const int qt = warp >> 2;             // query tile of this warpgroup
         const int t = threadIdx.x & 127;      // row within the tile == TMEM lane
-        const int q = T.q0 + qt * BM + t;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + qt * BN + lane_base, tO = tmem + NQ * BN + qt * 128 + lane_base;
-        int kmin = T.rlo, kmax = min(T.rhi, P.S - 1);
-        if (P.causal) kmax = min(kmax, q);
-        if (P.wr >= 0) kmax = min(kmax, q + P.wr);
-        if (P.wl >= 0) kmin = max(kmin, q - P.wl);
-        if (q >= P.S) kmax = -1;              // padding row: nothing allowed
         const float sl2 = P.scale * kLog2e;
-        const float* bias_row =
-            P.bias ? P.bias + T.b * P.bs[0] + T.h * P.bs[1] + static_cast<int64_t>(min(q, P.S - 1)) * P.bs[2]
-                   : nullptr;
-        float m_used = -INFINITY, m_true = -INFINITY, lsum = 0.f;
         bool aborted = false;
-        const int jlo = T.lo[qt], jhi = skip ? -1 : T.hi[qt];
-        int c = 0;
-        for (int j = jlo; j <= jhi; ++j, ++c) {
+        int cs = 0, kw = 0, gk = 0;           // S_qt tiles seen, items with work, K ring position
+        for (int k = 0; !aborted; ++k) {
+            const int item = read_item(k, lane == 0);
+            if (item >= n_items) break;
+            const Tile T = decode_tile<NQ>(a, item);
+            const int q = T.q0 + qt * BM + t;
+            int kmin = T.rlo, kmax = min(T.rhi, P.S - 1);
+            if (P.causal) kmax = min(kmax, q);
+            if (P.wr >= 0) kmax = min(kmax, q + P.wr);
+            if (P.wl >= 0) kmin = max(kmin, q - P.wl);
+            if (q >= P.S) kmax = -1;              // padding row: nothing allowed
+            const float* bias_row =
+                P.bias ? P.bias + T.b * P.bs[0] + T.h * P.bs[1] + static_cast<int64_t>(min(q, P.S - 1)) * P.bs[2]
+                       : nullptr;
+            float m_used = -INFINITY, m_true = -INFINITY, lsum = 0.f;
+            const int jlo = T.lo[qt], jhi = T.n > 0 ? T.hi[qt] : -1;
+            int c = 0;                            // tiles of this item so far
+            for (int j = jlo; j <= jhi; ++j, ++c, ++cs) {
             const int k0 = (T.kt0 + j) * BN;
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_S + qt), c & 1, abort_flag, a.status, 0x30))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_S + qt), cs & 1, abort_flag, a.status, 0x30))) {
                 aborted = true;
                 break;
             }
             tc_fence_after();
             const bool edge = __any_sync(0xffffffffu, k0 < kmin || k0 + BN - 1 > kmax);
-            const float* kb_tile = reinterpret_cast<const float*>(smem + C::OFF_KB + (j % C::NSK) * BN * 4);
+            const int kpos = gk + j;   // position of K_j in the K ring
+            const float* kb_tile = reinterpret_cast<const float*>(smem + C::OFF_KB + (kpos % C::NSK) * BN * 4);
             // the staged key bias arrived with K_j: observe that copy's barrier (the stage
             // cannot be refilled before this warpgroup's P(j) arrival)
-            if (key_bias && !__all_sync(0xffffffffu, mbar_wait(BAR(C::B_KF + j % C::NSK), (j / C::NSK) & 1, abort_flag,
+            if (key_bias && !__all_sync(0xffffffffu, mbar_wait(BAR(C::B_KF + kpos % C::NSK), (kpos / C::NSK) & 1, abort_flag,
                                                                a.status, 0x34))) {
                 aborted = true;
                 break;
@@ -470,6 +609,30 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
             const RowCtx R{tS, sl2, bias_row, P.bs[3], kb_tile, k0, kmin, kmax, P.S};
             // mode = bias kind (0 none, 1 staged key bias, 2 general) * 2 + edge
             const int mode = (bias_row ? (key_bias ? 2 : 4) : 0) | (edge ? 1 : 0);
+            // after the first tile: one pass with the reference the row already has, P kept in
+            // registers; stored if no row of the warp has to move its reference
+            if (c > 0) {
+                const float mref0 = m_used == -INFINITY ? 0.f : m_used;
+                float mt1, rs1;
+                uint32_t pk[BN / 2];
+                switch (mode) {
+                    case 0: rs1 = row_exp_1p<0, false>(R, mref0, pk, mt1); break;
+                    case 1: rs1 = row_exp_1p<0, true>(R, mref0, pk, mt1); break;
+                    case 2: rs1 = row_exp_1p<1, false>(R, mref0, pk, mt1); break;
+                    case 3: rs1 = row_exp_1p<1, true>(R, mref0, pk, mt1); break;
+                    case 4: rs1 = row_exp_1p<2, false>(R, mref0, pk, mt1); break;
+                    default: rs1 = row_exp_1p<2, true>(R, mref0, pk, mt1); break;
+                }
+                if (!__any_sync(0xffffffffu, mt1 > m_used + kTau)) {
+                    m_true = fmaxf(m_true, mt1);
+                    tmem_st64(tS, pk);
+                    lsum += rs1;
+                    tc_fence_before();
+                    mbar_arrive(BAR(C::B_P + qt));
+                    continue;
+                }
+            }
+            // first tile, or a warp where some row moves its reference: two passes
             float mt;
             switch (mode) {
                 case 0: mt = row_max<0, false>(R); break;
@@ -514,84 +677,101 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
             lsum += rs;
             tc_fence_before();
             mbar_arrive(BAR(C::B_P + qt));
-        }
-
-        // ------------------------------------------------------------ epilogue
-        const int qc = min(q, P.S - 1);
-        const int64_t mi = (static_cast<int64_t>(T.b) * P.Hq + T.h) * P.S + qc;
-        const bool has_work = jlo <= jhi;
-        if (!aborted && has_work &&
-            __all_sync(0xffffffffu, mbar_wait(BAR(C::B_O + qt), 0, abort_flag, a.status, 0x33))) {
-            tc_fence_after();
-            // statistics relative to the true row max
-            const float rel = m_true == -INFINITY ? 0.f : ex2(m_used - m_true);
-            const float l_true = lsum * rel;
-            const float m_nat = m_true * kLn2;
-            if (!a.acc) {
-                const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-                __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.qs[0] +
-                                   static_cast<int64_t>(qc) * P.qs[1] + T.h * P.qs[2];
-#pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + cc * 32, r);
-                    if (q < P.S) {
-                        uint4* dst = reinterpret_cast<uint4*>(O + cc * 32);
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            uint4 w;
-                            w.x = pack_bf16(__uint_as_float(r[v4 * 8 + 0]) * inv, __uint_as_float(r[v4 * 8 + 1]) * inv);
-                            w.y = pack_bf16(__uint_as_float(r[v4 * 8 + 2]) * inv, __uint_as_float(r[v4 * 8 + 3]) * inv);
-                            w.z = pack_bf16(__uint_as_float(r[v4 * 8 + 4]) * inv, __uint_as_float(r[v4 * 8 + 5]) * inv);
-                            w.w = pack_bf16(__uint_as_float(r[v4 * 8 + 6]) * inv, __uint_as_float(r[v4 * 8 + 7]) * inv);
-                            dst[v4] = w;
-                        }
-                    }
-                }
-                if (q < P.S) {
-                    a.m[mi] = m_nat;
-                    a.l[mi] = l_true;
-                }
-            } else {
-                // merge into the ring carry: (m_c, l_c, acc) with (m_nat, l_true, O * rel)
-                float mc = -INFINITY, lc = 0.f;
-                if (q < P.S) {
-                    mc = a.m[mi];
-                    lc = a.l[mi];
-                }
-                const float mn = fmaxf(mc, m_nat);
-                const float fa = mc == -INFINITY ? 0.f : ex2((mc - mn) * kLog2e);
-                const float fb = m_nat == -INFINITY ? 0.f : ex2((m_nat - mn) * kLog2e) * rel;
-                float* Cr = a.acc + ((static_cast<int64_t>(T.b) * P.S + qc) * P.Hq + T.h) * D;
-#pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t r[32];
-                    tmem_ld32(tO + cc * 32, r);
-                    if (q < P.S && mn != -INFINITY) {
-                        float4* dst = reinterpret_cast<float4*>(Cr + cc * 32);
-#pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4) {
-                            float4 x = dst[v4];
-                            x.x = x.x * fa + __uint_as_float(r[v4 * 4 + 0]) * fb;
-                            x.y = x.y * fa + __uint_as_float(r[v4 * 4 + 1]) * fb;
-                            x.z = x.z * fa + __uint_as_float(r[v4 * 4 + 2]) * fb;
-                            x.w = x.w * fa + __uint_as_float(r[v4 * 4 + 3]) * fb;
-                            dst[v4] = x;
-                        }
-                    }
-                }
-                if (q < P.S && mn != -INFINITY) {
-                    a.m[mi] = mn;
-                    a.l[mi] = lc * fa + lsum * fb;
-                }
             }
-        } else if (!aborted && !skip && !has_work && !a.acc && q < P.S) {
-            // no key allowed for this tile: O = 0, m = -inf, l = 0
-            __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.qs[0] +
-                               static_cast<int64_t>(q) * P.qs[1] + T.h * P.qs[2];
-            for (int cc = 0; cc < D; cc += 8) *reinterpret_cast<uint4*>(O + cc) = make_uint4(0, 0, 0, 0);
-            a.m[mi] = -INFINITY;
-            a.l[mi] = 0.f;
+            if (aborted) break;
+            if (T.n > 0) {
+                // the MMA issuer completes one O phase per item and query tile
+                if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_O + qt), kw & 1, abort_flag, a.status, 0x33))) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+            }
+
+            // -------------------------------------------------------- epilogue
+            const int qc = min(q, P.S - 1);
+            const int64_t mi = (static_cast<int64_t>(T.b) * P.Hq + T.h) * P.S + qc;
+            const bool has_work = jlo <= jhi;
+            if (!aborted && has_work) {
+                tc_fence_after();
+                // statistics relative to the true row max
+                const float rel = m_true == -INFINITY ? 0.f : ex2(m_used - m_true);
+                const float l_true = lsum * rel;
+                const float m_nat = m_true * kLn2;
+                if (!a.acc) {
+                    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                    __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.qs[0] +
+                                       static_cast<int64_t>(qc) * P.qs[1] + T.h * P.qs[2];
+    #pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + cc * 32, r);
+                        if (q < P.S) {
+                            uint4* dst = reinterpret_cast<uint4*>(O + cc * 32);
+    #pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4) {
+                                uint4 w;
+                                w.x = pack_bf16(__uint_as_float(r[v4 * 8 + 0]) * inv, __uint_as_float(r[v4 * 8 + 1]) * inv);
+                                w.y = pack_bf16(__uint_as_float(r[v4 * 8 + 2]) * inv, __uint_as_float(r[v4 * 8 + 3]) * inv);
+                                w.z = pack_bf16(__uint_as_float(r[v4 * 8 + 4]) * inv, __uint_as_float(r[v4 * 8 + 5]) * inv);
+                                w.w = pack_bf16(__uint_as_float(r[v4 * 8 + 6]) * inv, __uint_as_float(r[v4 * 8 + 7]) * inv);
+                                dst[v4] = w;
+                            }
+                        }
+                    }
+                    if (q < P.S) {
+                        a.m[mi] = m_nat;
+                        a.l[mi] = l_true;
+                    }
+                } else {
+                    // merge into the ring carry: (m_c, l_c, acc) with (m_nat, l_true, O * rel)
+                    float mc = -INFINITY, lc = 0.f;
+                    if (q < P.S) {
+                        mc = a.m[mi];
+                        lc = a.l[mi];
+                    }
+                    const float mn = fmaxf(mc, m_nat);
+                    const float fa = mc == -INFINITY ? 0.f : ex2((mc - mn) * kLog2e);
+                    const float fb = m_nat == -INFINITY ? 0.f : ex2((m_nat - mn) * kLog2e) * rel;
+                    float* Cr = a.acc + ((static_cast<int64_t>(T.b) * P.S + qc) * P.Hq + T.h) * D;
+    #pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + cc * 32, r);
+                        if (q < P.S && mn != -INFINITY) {
+                            float4* dst = reinterpret_cast<float4*>(Cr + cc * 32);
+    #pragma unroll
+                            for (int v4 = 0; v4 < 8; ++v4) {
+                                float4 x = dst[v4];
+                                x.x = x.x * fa + __uint_as_float(r[v4 * 4 + 0]) * fb;
+                                x.y = x.y * fa + __uint_as_float(r[v4 * 4 + 1]) * fb;
+                                x.z = x.z * fa + __uint_as_float(r[v4 * 4 + 2]) * fb;
+                                x.w = x.w * fa + __uint_as_float(r[v4 * 4 + 3]) * fb;
+                                dst[v4] = x;
+                            }
+                        }
+                    }
+                    if (q < P.S && mn != -INFINITY) {
+                        a.m[mi] = mn;
+                        a.l[mi] = lc * fa + lsum * fb;
+                    }
+                }
+            } else if (!aborted && !has_work && !a.acc && q < P.S) {
+                // no key allowed for this tile: O = 0, m = -inf, l = 0
+                __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.qs[0] +
+                                   static_cast<int64_t>(q) * P.qs[1] + T.h * P.qs[2];
+                for (int cc = 0; cc < D; cc += 8) *reinterpret_cast<uint4*>(O + cc) = make_uint4(0, 0, 0, 0);
+                a.m[mi] = -INFINITY;
+                a.l[mi] = 0.f;
+            }
+
+            if (T.n > 0) {
+                // O_qt has been read: the next item's first P V may overwrite it
+                tc_fence_before();
+                mbar_arrive(BAR(C::B_OE + qt));
+                ++kw;
+                gk += T.n;
+            }
         }
     }
 
@@ -617,8 +797,17 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
+    // persistent CTAs (one per SM, two for single-tile CTAs) take work items from a counter
+    static int sm_count[64] = {};
+    int sms = dev >= 0 && dev < 64 ? sm_count[dev] : 0;
+    if (sms <= 0) {
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) sm_count[dev] = sms;
+    }
     const int nqp = (a.P.S + NQ * BM - 1) / (NQ * BM);
-    const int grid = nqp * a.P.Hq * a.P.B;
+    const int64_t items = static_cast<int64_t>(nqp) * a.P.Hq * a.P.B;
+    const int grid = static_cast<int>(std::min<int64_t>(items, static_cast<int64_t>(sms) * (NQ == 1 ? 2 : 1)));
     k_fwd_tc<D, NQ><<<grid, C::kThreads, C::SMEM, s>>>(maps[0], maps[1], maps[2], a);
     return cudaGetLastError();
 }
