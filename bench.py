@@ -444,7 +444,7 @@ def main():
                          "peak_kind": f"bf16_tflops, burst ({peaks_kind})",
                          "traffic": traffic},
             "roofline_fwd": {"kernel": "k_fwd_tc", "bound": "tensor", "achieved": fwd_tf, "peak": peak_tf,
-                             "unit": "TFLOP/s", "frac": fwd_tf / peak_tf},
+                             "unit": "TFLOP/s", "frac": fwd_tf / peak_tf, "traffic": kernel_traffic("k_fwd_tc")},
             "kernel_ms": {"fwd": statistics.mean(fwd_ms), "bwd_pre": statistics.mean(bwd_pre_ms),
                           "bwd_main": statistics.mean(bwd_main_ms), "bwd_post": statistics.mean(bwd_post_ms)},
             "cpu_baseline": cpu,
