@@ -31,7 +31,8 @@
 //              thread (warp % 4) * 32 + lane owns key row / dQ channel of that TMEM lane;
 //              at the end warps 0-3 write dK (scaled), warps 4-7 dV;
 //   warp 8     TMA producer: K, V once; Q, dO (+ lse, D) per query tile;
-//   warp 9     MMA issuer, TMEM owner.
+//   warp 9     MMA issuer (the whole warp runs the loop with warp-uniform operands, one
+//              elected lane issues: cheaper per product than a lone lane), TMEM owner.
 #include <math.h>
 
 #include "bpa_internal.h"
@@ -200,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_it > 0) {
-            bool ok = mbar_wait(BAR(B_KV), 0, abort_flag, a.status, 0x50);
+        if (n_it > 0) {   // the whole warp runs the loop; one elected lane issues
+            bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_KV), 0, abort_flag, a.status, 0x50));
             // descriptors of the resident K / V tile (K-major, and K as an MN-major A operand)
             const uint64_t kd0 = sdesc_sw128(sb + OFF_K, 16, 1024), vd0 = sdesc_sw128(sb + OFF_V, 16, 1024);
             const uint64_t kmn0 = sdesc_sw128(sb + OFF_K, SUBK, 1024);
@@ -211,8 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int it = 0; ok && it <= n_it; ++it) {
                 if (it < n_it) {
                     const int st = it % NS;
-                    if (!mbar_wait(BAR(B_QF + st), (it / NS) & 1, abort_flag, a.status, 0x51)) break;
-                    if (it > 0 && !mbar_wait(BAR(B_SF), (it - 1) & 1, abort_flag, a.status, 0x54)) break;
+                    if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_QF + st), (it / NS) & 1, abort_flag, a.status, 0x51))) break;
+                    if (it > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_SF), (it - 1) & 1, abort_flag, a.status, 0x54))) break;
                     tc_fence_after();
                     const uint64_t qd = sdesc_sw128(sb + OFF_Q + st * BQ * D * 2, 16, 1024);
                     const uint64_t dod = sdesc_sw128(sb + OFF_DO + st * BQ * D * 2, 16, 1024);
@@ -224,16 +225,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
                         const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
-                        tc_mma_ss(tS, sdesc_advance(kd0, offk), sdesc_advance(qd, offq), IDESC_S, kk > 0);
-                        tc_mma_ss(tDP + (it & 1) * BQ, sdesc_advance(vd0, offk), sdesc_advance(dod, offq), IDESC_S,
+                        tc_mma_ss_w(tS, sdesc_advance(kd0, offk), sdesc_advance(qd, offq), IDESC_S, kk > 0);
+                        tc_mma_ss_w(tDP + (it & 1) * BQ, sdesc_advance(vd0, offk), sdesc_advance(dod, offq), IDESC_S,
                                   kk > 0);
                     }
-                    tc_commit(BAR(B_S));
-                    tc_commit(BAR(B_DP + (it & 1)));
+                    tc_commit_w(BAR(B_S));
+                    tc_commit_w(BAR(B_DP + (it & 1)));
                 }
                 if (it > 0) {
                     const int p = it - 1, pst = p % NS;
-                    if (!mbar_wait(BAR(B_DS), p & 1, abort_flag, a.status, 0x52)) break;
+                    if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DS), p & 1, abort_flag, a.status, 0x52))) break;
                     tc_fence_after();
                     const uint64_t qmn = sdesc_sw128(sb + OFF_Q + pst * BQ * D * 2, SUBQ, 1024);
                     const uint64_t domn = sdesc_sw128(sb + OFF_DO + pst * BQ * D * 2, SUBQ, 1024);
@@ -244,21 +245,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < BQ / 16; ++kk) {
                         const uint32_t acc = (p > 0 || kk > 0) ? 1u : 0u;
                         const uint32_t tp = tPD + (kk >> 1) * 32 + (kk & 1) * 8;
-                        tc_mma_ts(tDV, tp, sdesc_advance(domn, kk * 2048), IDESC_KV, acc);
-                        tc_mma_ts(tDK, tp + 16, sdesc_advance(qmn, kk * 2048), IDESC_KV, acc);
+                        tc_mma_ts_w(tDV, tp, sdesc_advance(domn, kk * 2048), IDESC_KV, acc);
+                        tc_mma_ts_w(tDK, tp + 16, sdesc_advance(qmn, kk * 2048), IDESC_KV, acc);
                     }
-                    if (p > 0 && !mbar_wait(BAR(B_DQE), (p - 1) & 1, abort_flag, a.status, 0x53)) break;
+                    if (p > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_DQE), (p - 1) & 1, abort_flag, a.status, 0x53))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        tc_mma_ss(tDQ, sdesc_advance(kmn0, kk * 2048), sdesc_advance(dsmn, kk * 2048), IDESC_Q, kk > 0);
-                    tc_commit(BAR(B_DQF));
-                    tc_commit(BAR(B_PF));
-                    tc_commit(BAR(B_QE + pst));
-                    if (p == n_it - 1) tc_commit(BAR(B_KVD));
+                        tc_mma_ss_w(tDQ, sdesc_advance(kmn0, kk * 2048), sdesc_advance(dsmn, kk * 2048), IDESC_Q, kk > 0);
+                    tc_commit_w(BAR(B_DQF));
+                    tc_commit_w(BAR(B_PF));
+                    tc_commit_w(BAR(B_QE + pst));
+                    if (p == n_it - 1) tc_commit_w(BAR(B_KVD));
                 }
             }
-            tc_commit(BAR(B_FIN));
+            tc_commit_w(BAR(B_FIN));
             drain_wait(BAR(B_FIN), 0, a.status);
         }
     } else {

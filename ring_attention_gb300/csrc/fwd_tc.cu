@@ -14,7 +14,8 @@
 //   warps 0-3  softmax of query tile 0: thread t owns row t (TMEM lane t);
 //   warps 4-7  softmax of query tile 1;
 //   warp 8     TMA producer: Q0, Q1 once, then K / V tiles through their rings;
-//   warp 9     MMA issuer (one thread), TMEM owner.  Issue order per key tile j:
+//   warp 9     MMA issuer (the whole warp runs the loop with warp-uniform operands, one
+//              elected lane issues: cheaper per product than a lone lane), TMEM owner.  Issue order per key tile j:
 //              [P0(j) ready] P0 V -> O0, S0(j+1) = Q0 K^T ; [P1(j) ready] P1 V -> O1,
 //              S1(j+1): the tensor core works on one tile while the other tile's
 //              softmax runs.  The products of a tile execute in issue order, so
@@ -442,12 +443,12 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
         }
     } else if (warp == C::kMma) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        {   // the whole warp runs the loop with warp-uniform operands; one elected lane issues
             int np[2] = {0, 0};       // products P_i V consumed per query tile (P barrier phases)
             int kw = 0, gk = 0, gv = 0;
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const int item = read_item(k, true);
+                const int item = __shfl_sync(0xffffffffu, read_item(k, lane == 0), 0);   // warp-uniform
                 if (item >= n_items) break;
                 const Tile T = decode_tile<NQ>(a, item);
                 const int n = T.n;
@@ -462,9 +463,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * C::SUB + (kk & 3) * 32;
-                        tc_mma_ss(d_tmem, sdesc_advance(qd, off), sdesc_advance(kd, off), C::IDESC_S, kk > 0);
+                        tc_mma_ss_w(d_tmem, sdesc_advance(qd, off), sdesc_advance(kd, off), C::IDESC_S, kk > 0);
                     }
-                    tc_commit(BAR(C::B_S + i));
+                    tc_commit_w(BAR(C::B_S + i));
                 };
                 auto issue_pv = [&](int i, int j, bool first) {
                     const int st = (gv + j) % C::NSV;
@@ -472,34 +473,34 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                     const uint32_t t_p = tmem + i * BN, t_o = tmem + NQ * BN + i * 128;
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        tc_mma_ts(t_o, t_p + kk * 8, sdesc_advance(vd, kk * 2048), C::IDESC_PV,
+                        tc_mma_ts_w(t_o, t_p + kk * 8, sdesc_advance(vd, kk * 2048), C::IDESC_PV,
                                   (!first || kk > 0) ? 1u : 0u);
                 };
-                auto wait_k = [&](int j) {
+                auto wait_k = [&](int j) -> bool {
                     const int pos = gk + j;
-                    return mbar_wait(BAR(C::B_KF + pos % C::NSK), (pos / C::NSK) & 1, abort_flag, a.status, 0x22);
+                    return __all_sync(0xffffffffu, mbar_wait(BAR(C::B_KF + pos % C::NSK), (pos / C::NSK) & 1, abort_flag, a.status, 0x22)) != 0;
                 };
                 // O_i of the previous item must have been read by its epilogue before this
                 // item's first P_i V overwrites it (waited once per item, in order)
                 bool oe_seen[2] = {kw == 0, kw == 0};
-                auto wait_oe = [&](int i) {
+                auto wait_oe = [&](int i) -> bool {
                     if (oe_seen[i]) return true;
                     oe_seen[i] = true;
-                    return mbar_wait(BAR(C::B_OE + i), (kw - 1) & 1, abort_flag, a.status, 0x25);
+                    return __all_sync(0xffffffffu, mbar_wait(BAR(C::B_OE + i), (kw - 1) & 1, abort_flag, a.status, 0x25)) != 0;
                 };
-                ok = mbar_wait(BAR(C::B_Q), kw & 1, abort_flag, a.status, 0x20) && wait_k(0);
+                ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_Q), kw & 1, abort_flag, a.status, 0x20)) && wait_k(0);
                 if (!ok) break;
                 tc_fence_after();
                 // the S tiles still hold the previous item's P; its P V products were issued first
                 for (int i = 0; i < NQ; ++i)
                     if (active(i, 0)) issue_s(i, 0);
-                if (n == 1) tc_commit(BAR(C::B_QE));
+                if (n == 1) tc_commit_w(BAR(C::B_QE));
                 int pv_item[2] = {0, 0};
                 for (int j = 0; ok && j < n; ++j) {
                     const bool next = j + 1 < n;
                     // every K / V copy is observed here, so a stage is never refilled while a copy is in flight
                     const int vpos = gv + j;
-                    if (!mbar_wait(BAR(C::B_VF + vpos % C::NSV), (vpos / C::NSV) & 1, abort_flag, a.status, 0x23)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_VF + vpos % C::NSV), (vpos / C::NSV) & 1, abort_flag, a.status, 0x23))) {
                         ok = false;
                         break;
                     }
@@ -508,21 +509,21 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                     bool k_released = false;
                     for (int i = 0; i < NQ; ++i) {
                         if (active(i, j)) {
-                            if (!mbar_wait(BAR(C::B_P + i), np[i] & 1, abort_flag, a.status, 0x24) || !wait_oe(i)) {
+                            if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_P + i), np[i] & 1, abort_flag, a.status, 0x24)) || !wait_oe(i)) {
                                 ok = false;
                                 break;
                             }
                             // every softmax of step j is done (S(j) and the staged bias are no longer
                             // read): release K_j's stage before S(j+1) may need a free one
                             if (i == last) {
-                                tc_commit(BAR(C::B_KE + (gk + j) % C::NSK));
+                                tc_commit_w(BAR(C::B_KE + (gk + j) % C::NSK));
                                 k_released = true;
                             }
                             tc_fence_after();
                             issue_pv(i, j, pv_item[i] == 0);
                             ++np[i];
                             ++pv_item[i];
-                            if (j == T.hi[i]) tc_commit(BAR(C::B_O + i));
+                            if (j == T.hi[i]) tc_commit_w(BAR(C::B_O + i));
                         }
                         if (next && active(i, j + 1)) {
                             if (!k_ready) {
@@ -541,9 +542,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                         ok = false;
                         break;
                     }
-                    if (j + 2 == n) tc_commit(BAR(C::B_QE));   // every S of this item is issued
-                    if (!k_released) tc_commit(BAR(C::B_KE + (gk + j) % C::NSK));   // (a step no tile used)
-                    tc_commit(BAR(C::B_VE + vpos % C::NSV));   // V_j is no longer read
+                    if (j + 2 == n) tc_commit_w(BAR(C::B_QE));   // every S of this item is issued
+                    if (!k_released) tc_commit_w(BAR(C::B_KE + (gk + j) % C::NSK));   // (a step no tile used)
+                    tc_commit_w(BAR(C::B_VE + vpos % C::NSV));   // V_j is no longer read
                 }
                 if (!ok) break;
                 // a query tile without keys in this item still completes its O phase
@@ -553,7 +554,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                             ok = false;
                             break;
                         }
-                        tc_commit(BAR(C::B_O + i));
+                        tc_commit_w(BAR(C::B_O + i));
                     }
                 }
                 gk += n;
@@ -561,7 +562,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                 ++kw;
             }
             // drain: all MMAs issued by this thread complete before TMEM is freed
-            tc_commit(BAR(C::B_FIN));
+            tc_commit_w(BAR(C::B_FIN));
             drain_wait(BAR(C::B_FIN), 0, a.status);
         }
     } else {
