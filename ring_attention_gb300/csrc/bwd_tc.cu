@@ -26,13 +26,17 @@
 // up to 64), so a warp's reduction covers 512 contiguous bytes.
 // Consecutive products into one TMEM accumulator wait on each other, so the
 // independent S^T and dP^T products are issued interleaved (as are dV, dK).
-// Roles (320 threads):
+// Roles (352 threads):
 //   warps 0-3  query columns 0-31 of each tile, warps 4-7 columns 32-63;
 //              thread (warp % 4) * 32 + lane owns key row / dQ channel of that TMEM lane;
 //              at the end warps 0-3 write dK (scaled), warps 4-7 dV;
 //   warp 8     TMA producer: K, V once; Q, dO (+ lse, D) per query tile;
-//   warp 9     MMA issuer (the whole warp runs the loop with warp-uniform operands, one
-//              elected lane issues: cheaper per product than a lone lane), TMEM owner.
+//   warp 9     MMA issuer A: S^T and dP^T products; TMEM owner;
+//   warp 10    MMA issuer B: dV, dK and dQ^T products.  Two issuers halve the per-thread
+//              issue and wait chain; their shared resources are handed over by barriers
+//              (a dP^T buffer returns to A once B's dV / dK have read its pairs; a Q / dO
+//              stage is released by a commit from each).  Each issuer is a whole warp
+//              running the loop with warp-uniform operands, one elected lane issuing.
 #include <math.h>
 
 #include "bpa_internal.h"
@@ -45,7 +49,7 @@ constexpr int D = 128;        // head dim
 constexpr int BK = 128;       // keys per CTA
 constexpr int BQ = 64;        // queries per tile
 constexpr int NS = 4;         // Q / dO stages
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmax = 256;    // threads of the two softmax warpgroups
 
 constexpr int SUBK = BK * 128;    // one 64-channel slab of the key tile
@@ -63,7 +67,7 @@ static_assert(SMEM <= 232448, "shared memory");
 // barrier slots
 constexpr int B_KV = 0, B_QF = 1, B_QE = 1 + NS, B_S = 1 + 2 * NS, B_SF = 2 + 2 * NS, B_DP = 3 + 2 * NS,
               B_DS = 5 + 2 * NS, B_DQF = 6 + 2 * NS, B_DQE = 7 + 2 * NS, B_PF = 8 + 2 * NS, B_KVD = 9 + 2 * NS,
-              B_FIN = 10 + 2 * NS, NBAR = 11 + 2 * NS;
+              B_FIN = 10 + 2 * NS, B_PRF = 11 + 2 * NS /* x2 */, B_FINB = 13 + 2 * NS, NBAR = 14 + 2 * NS;
 static_assert(8 * NBAR + 8 <= 256, "barrier area");
 
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BK, BQ, 0, 0);     // S^T, dP^T: both K-major
@@ -131,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR(B_KV), 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(BAR(B_QF + s), 1);
-            mbar_init(BAR(B_QE + s), 1);
+            mbar_init(BAR(B_QE + s), 2);   // both MMA issuers read the stage
         }
         mbar_init(BAR(B_S), 1);
         mbar_init(BAR(B_SF), kSoftmax);
@@ -143,6 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR(B_PF), 1);
         mbar_init(BAR(B_KVD), 1);
         mbar_init(BAR(B_FIN), 1);
+        mbar_init(BAR(B_FINB), 1);
+        mbar_init(BAR(B_PRF + 0), 1);
+        mbar_init(BAR(B_PRF + 1), 1);
         *abort_flag = (a.status && (*reinterpret_cast<volatile uint32_t*>(a.status) & ST_TIMEOUT)) ? 1 : 0;
         fence_mbar_init();
     }
@@ -200,67 +207,73 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 9) {
-        // ------------------------------------------------------------ MMA issuer
-        if (n_it > 0) {   // the whole warp runs the loop; one elected lane issues
+        // ------------------------------------------------------------ MMA issuer A: S^T, dP^T
+        // The whole warp runs the loop with warp-uniform operands; one elected lane issues.
+        if (n_it > 0) {
             bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_KV), 0, abort_flag, a.status, 0x50));
-            // descriptors of the resident K / V tile (K-major, and K as an MN-major A operand)
             const uint64_t kd0 = sdesc_sw128(sb + OFF_K, 16, 1024), vd0 = sdesc_sw128(sb + OFF_V, 16, 1024);
-            const uint64_t kmn0 = sdesc_sw128(sb + OFF_K, SUBK, 1024);
-            const uint64_t dsmn = sdesc_sw128(sb + OFF_DS, 16, 1024);
-            // order per tile it: S_it (once S_it-1 has been read), dP_it, then dV / dK / dQ
-            // of tile it-1 (once its dS is ready)
-            for (int it = 0; ok && it <= n_it; ++it) {
-                if (it < n_it) {
-                    const int st = it % NS;
-                    if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_QF + st), (it / NS) & 1, abort_flag, a.status, 0x51))) break;
-                    if (it > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_SF), (it - 1) & 1, abort_flag, a.status, 0x54))) break;
-                    tc_fence_after();
-                    const uint64_t qd = sdesc_sw128(sb + OFF_Q + st * BQ * D * 2, 16, 1024);
-                    const uint64_t dod = sdesc_sw128(sb + OFF_DO + st * BQ * D * 2, 16, 1024);
-                    // S^T and dP^T are independent accumulations: interleaved, each waits less on
-                    // its own previous step.  The dP^T buffer (it & 1) last held tile it-2, whose dS
-                    // was waited for below (and whose P^T / dS^T pairs were consumed by MMAs issued
-                    // before these).
+            for (int it = 0; ok && it < n_it; ++it) {
+                const int st = it % NS, buf = it & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_QF + st), (it / NS) & 1, abort_flag, a.status, 0x51))) break;
+                // S^T(it-1) has been read; the P^T / dS^T pairs of tile it-2 in this dP^T buffer
+                // have been consumed by issuer B's dV / dK products
+                if (it > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_SF), (it - 1) & 1, abort_flag, a.status, 0x54))) break;
+                if (it > 1 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_PRF + buf), ((it >> 1) - 1) & 1, abort_flag,
+                                                                  a.status, 0x55)))
+                    break;
+                tc_fence_after();
+                const uint64_t qd = sdesc_sw128(sb + OFF_Q + st * BQ * D * 2, 16, 1024);
+                const uint64_t dod = sdesc_sw128(sb + OFF_DO + st * BQ * D * 2, 16, 1024);
+                // S^T and dP^T are independent accumulations: interleaved, each waits less on
+                // its own previous step
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
-                        const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
-                        tc_mma_ss_w(tS, sdesc_advance(kd0, offk), sdesc_advance(qd, offq), IDESC_S, kk > 0);
-                        tc_mma_ss_w(tDP + (it & 1) * BQ, sdesc_advance(vd0, offk), sdesc_advance(dod, offq), IDESC_S,
-                                  kk > 0);
-                    }
-                    tc_commit_w(BAR(B_S));
-                    tc_commit_w(BAR(B_DP + (it & 1)));
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
+                    const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
+                    tc_mma_ss_w(tS, sdesc_advance(kd0, offk), sdesc_advance(qd, offq), IDESC_S, kk > 0);
+                    tc_mma_ss_w(tDP + buf * BQ, sdesc_advance(vd0, offk), sdesc_advance(dod, offq), IDESC_S, kk > 0);
                 }
-                if (it > 0) {
-                    const int p = it - 1, pst = p % NS;
-                    if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DS), p & 1, abort_flag, a.status, 0x52))) break;
-                    tc_fence_after();
-                    const uint64_t qmn = sdesc_sw128(sb + OFF_Q + pst * BQ * D * 2, SUBQ, 1024);
-                    const uint64_t domn = sdesc_sw128(sb + OFF_DO + pst * BQ * D * 2, SUBQ, 1024);
-                    // bf16 pairs of query columns 16 kk .. 16 kk + 15: warpgroup kk / 2 wrote P^T at
-                    // columns 32 (kk / 2) + 8 (kk % 2) of the dP^T buffer and dS^T 16 columns further
-                    const uint32_t tPD = tDP + (p & 1) * BQ;
-#pragma unroll
-                    for (int kk = 0; kk < BQ / 16; ++kk) {
-                        const uint32_t acc = (p > 0 || kk > 0) ? 1u : 0u;
-                        const uint32_t tp = tPD + (kk >> 1) * 32 + (kk & 1) * 8;
-                        tc_mma_ts_w(tDV, tp, sdesc_advance(domn, kk * 2048), IDESC_KV, acc);
-                        tc_mma_ts_w(tDK, tp + 16, sdesc_advance(qmn, kk * 2048), IDESC_KV, acc);
-                    }
-                    if (p > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_DQE), (p - 1) & 1, abort_flag, a.status, 0x53))) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        tc_mma_ss_w(tDQ, sdesc_advance(kmn0, kk * 2048), sdesc_advance(dsmn, kk * 2048), IDESC_Q, kk > 0);
-                    tc_commit_w(BAR(B_DQF));
-                    tc_commit_w(BAR(B_PF));
-                    tc_commit_w(BAR(B_QE + pst));
-                    if (p == n_it - 1) tc_commit_w(BAR(B_KVD));
-                }
+                tc_commit_w(BAR(B_S));
+                tc_commit_w(BAR(B_DP + buf));
+                tc_commit_w(BAR(B_QE + st));   // this issuer's reads of the Q / dO stage
             }
             tc_commit_w(BAR(B_FIN));
             drain_wait(BAR(B_FIN), 0, a.status);
+        }
+    } else if (warp == 10) {
+        // ------------------------------------------------------------ MMA issuer B: dV, dK, dQ^T
+        if (n_it > 0) {
+            const uint64_t kmn0 = sdesc_sw128(sb + OFF_K, SUBK, 1024);
+            const uint64_t dsmn = sdesc_sw128(sb + OFF_DS, 16, 1024);
+            for (int p = 0; p < n_it; ++p) {
+                const int pst = p % NS, buf = p & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DS), p & 1, abort_flag, a.status, 0x52))) break;
+                tc_fence_after();
+                const uint64_t qmn = sdesc_sw128(sb + OFF_Q + pst * BQ * D * 2, SUBQ, 1024);
+                const uint64_t domn = sdesc_sw128(sb + OFF_DO + pst * BQ * D * 2, SUBQ, 1024);
+                // bf16 pairs of query columns 16 kk .. 16 kk + 15: warpgroup kk / 2 wrote P^T at
+                // columns 32 (kk / 2) + 8 (kk % 2) of the dP^T buffer and dS^T 16 columns further
+                const uint32_t tPD = tDP + buf * BQ;
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk) {
+                    const uint32_t acc = (p > 0 || kk > 0) ? 1u : 0u;
+                    const uint32_t tp = tPD + (kk >> 1) * 32 + (kk & 1) * 8;
+                    tc_mma_ts_w(tDV, tp, sdesc_advance(domn, kk * 2048), IDESC_KV, acc);
+                    tc_mma_ts_w(tDK, tp + 16, sdesc_advance(qmn, kk * 2048), IDESC_KV, acc);
+                }
+                tc_commit_w(BAR(B_PRF + buf));   // the pairs have been read: issuer A may reuse the buffer
+                tc_commit_w(BAR(B_QE + pst));
+                if (p > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_DQE), (p - 1) & 1, abort_flag, a.status, 0x53))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    tc_mma_ss_w(tDQ, sdesc_advance(kmn0, kk * 2048), sdesc_advance(dsmn, kk * 2048), IDESC_Q, kk > 0);
+                tc_commit_w(BAR(B_DQF));
+                tc_commit_w(BAR(B_PF));
+                if (p == n_it - 1) tc_commit_w(BAR(B_KVD));
+            }
+            tc_commit_w(BAR(B_FINB));
+            drain_wait(BAR(B_FINB), 0, a.status);
         }
     } else {
         // ------------------------------------------------------------ P, dS, dQ (two warpgroups)
