@@ -115,15 +115,17 @@ __global__ void k_bwd_pre_bf16v(const BwdArgs a, int zero_dq) {
     const int64_t rows = static_cast<int64_t>(P.B) * P.Hq * a.Spad;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     const int64_t warp_id = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5);
-    // the loop bound is uniform across the warp, so the shuffles see every lane
-    for (int64_t rbase = warp_id * rpw; rbase < rows; rbase += warps * rpw) {
-        const int64_t r = rbase + lane / tpr;
-        const bool live = r < rows;
-        const int64_t rr = live ? r : 0;
-        const int q = static_cast<int>(rr % a.Spad);
-        const int64_t bh = rr / a.Spad;
-        const int h = static_cast<int>(bh % P.Hq);
-        const int b = static_cast<int>(bh / P.Hq);
+    // the loop bound is uniform across the warp, so the shuffles see every lane; row indices
+    // fit 32 bits (the launcher checks), so no 64-bit division is needed
+    const int nrows = static_cast<int>(rows), spad = a.Spad;
+    for (int rbase = static_cast<int>(warp_id) * rpw; rbase < nrows; rbase += static_cast<int>(warps) * rpw) {
+        const int r = rbase + lane / tpr;
+        const bool live = r < nrows;
+        const int rr = live ? r : 0;
+        const int q = rr % spad;
+        const int bh = rr / spad;
+        const int h = bh % P.Hq;
+        const int b = bh / P.Hq;
         float s = 0.f;
         if (live && q < P.S) {
             const int64_t off = b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2] + sub * 8;
@@ -142,7 +144,7 @@ __global__ void k_bwd_pre_bf16v(const BwdArgs a, int zero_dq) {
         if (live && sub == 0) {
             float lse = INFINITY;
             if (q < P.S) {
-                const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * P.S + q;
+                const int64_t mi = static_cast<int64_t>(bh) * P.S + q;
                 const float lv = a.l[mi];
                 if (lv > 0.f) lse = a.m[mi] + logf(lv);
             }
@@ -194,19 +196,17 @@ __global__ void k_cast_dq4_bf16(const float* src, __nv_bfloat16* dst, int B, int
                                 int64_t s1, int64_t s2, int src_rows) {
     const int lane = threadIdx.x & 31, r4 = src_rows / 4, n4 = (S + 3) / 4;
     const bool even = (lane & 1) == 0;
-    const int64_t groups = static_cast<int64_t>(B) * H * n4;
-    const int64_t wstride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); g < groups;
-         g += wstride) {
-        const int q4 = static_cast<int>(g % n4);
-        const int64_t bh = g / n4;
-        const int h = static_cast<int>(bh % H);
-        const int b = static_cast<int>(bh / H);
-        const float4* in = reinterpret_cast<const float4*>(src + (bh * r4 + q4) * static_cast<int64_t>(d) * 4);
+    const int groups = B * H * n4;   // < 2^31 (the launcher checks): 32-bit index arithmetic
+    const int wstride = gridDim.x * (blockDim.x >> 5);
+    for (int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < groups; g += wstride) {
+        const int q4 = g % n4;
+        const int bh = g / n4;
+        const int h = bh % H;
+        const int b = bh / H;
+        const float4* in = reinterpret_cast<const float4*>(src + (static_cast<int64_t>(bh) * r4 + q4) * d * 4);
         const int qa = q4 * 4 + (even ? 0 : 2);   // the two rows this lane writes: qa, qa + 1
         __nv_bfloat16* out = dst + b * s0 + h * s2;
-        for (int c0 = 0; c0 < d; c0 += 32) {
-            const float4 x = in[c0 + lane];
+        auto emit = [&](const float4& x, int c0) {
             const float y0 = __shfl_xor_sync(0xffffffffu, even ? x.z : x.x, 1);
             const float y1 = __shfl_xor_sync(0xffffffffu, even ? x.w : x.y, 1);
             const int c = c0 + lane - (even ? 0 : 1);   // first channel of this lane's pair
@@ -214,6 +214,15 @@ __global__ void k_cast_dq4_bf16(const float* src, __nv_bfloat16* dst, int B, int
             const uint32_t w1 = even ? pack_bf16(x.y, y1) : pack_bf16(y1, x.w);
             if (qa < S) *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(qa) * s1 + c) = w0;
             if (qa + 1 < S) *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(qa + 1) * s1 + c) = w1;
+        };
+        if (d == 128) {   // the tensor-core backward's head dim: the four loads go out together
+            float4 xs[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) xs[g] = in[g * 32 + lane];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) emit(xs[g], g * 32);
+        } else {
+            for (int c0 = 0; c0 < d; c0 += 32) emit(in[c0 + lane], c0);
         }
     }
 }
@@ -266,7 +275,7 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t s) {
     const int tpr = P.d / 8;
     const bool vec_ok = ((reinterpret_cast<uintptr_t>(a.o) | reinterpret_cast<uintptr_t>(a.dout)) & 15u) == 0 &&
                         ((P.qs[0] | P.qs[1] | P.qs[2]) & 7) == 0;
-    if (P.dtype == BPA_BF16 && vec_ok && P.d % 8 == 0 && tpr <= 32 && (tpr & (tpr - 1)) == 0) {
+    if (P.dtype == BPA_BF16 && vec_ok && P.d % 8 == 0 && tpr <= 32 && (tpr & (tpr - 1)) == 0 && rows < (1ll << 31)) {
         const int threads = 256;   // a multiple of every tpr
         const int64_t work = rows * tpr;
         k_bwd_pre_bf16v<<<grid_for(work, threads), threads, 0, s>>>(a, zero);
@@ -279,14 +288,13 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t s) {
 
 cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t s) {
     const Problem& P = a.P;
-    const int64_t nq = static_cast<int64_t>(P.B) * P.S * P.Hq * P.d;
     const int64_t nk = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.d;
     if (P.dtype != BPA_BF16) return cudaErrorInvalidValue;
     const bool vec_ok =
         ((reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) | reinterpret_cast<uintptr_t>(a.dv)) &
          15u) == 0 &&
         ((P.qs[0] | P.qs[1] | P.qs[2] | P.ks[0] | P.ks[1] | P.ks[2] | P.vs[0] | P.vs[1] | P.vs[2]) & 7) == 0;
-    if (vec_ok && P.d % 32 == 0) {
+    if (vec_ok && P.d % 32 == 0 && static_cast<int64_t>(P.B) * P.Hq * ((P.S + 3) / 4) < (1ll << 31)) {
         const int64_t dq_threads = static_cast<int64_t>(P.B) * P.Hq * ((P.S + 3) / 4) * 32;   // a warp per 4 rows
         k_cast_dq4_bf16<<<grid_for(dq_threads, 256), 256, 0, s>>>(
             a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), P.B, P.S, P.Hq, P.d, P.qs[0], P.qs[1], P.qs[2], a.Spad);
