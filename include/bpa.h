@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define BPA_VERSION 1
+#define BPA_VERSION 2
 
 typedef enum {
     BPA_OK = 0,
@@ -75,11 +75,11 @@ typedef enum { BPA_OP_FWD = 0, BPA_OP_BWD = 1 } bpa_op;
 typedef struct bpa_attn_desc {
     uint32_t struct_size;      /* = sizeof(bpa_attn_desc) */
     int32_t dtype;             /* bpa_dtype of q, k, v, o, dout, dq, dk, dv */
-    int32_t B, S, Hq, Hkv, d;  /* Sq = Sk = S; Hq % Hkv == 0; 1 <= d <= 256 */
+    int32_t B, S, Hq, Hkv, d;  /* Sq = Sk = S; Hq % Hkv == 0; 1 <= d <= 256 (head dim of q, k) */
     const void* q;             /* [B, S, Hq, d] */
     const void* k;             /* [B, S, Hkv, d] */
-    const void* v;             /* [B, S, Hkv, d] */
-    int64_t q_strides[3];      /* (b, s, h) strides of q, o, dout, dq */
+    const void* v;             /* [B, S, Hkv, dv] */
+    int64_t q_strides[3];      /* (b, s, h) strides of q, dq (and of o, dout unless o_strides is set) */
     int64_t k_strides[3];      /* (b, s, h) strides of k, dk */
     int64_t v_strides[3];      /* (b, s, h) strides of v, dv */
     float scale;               /* <= 0 selects d^-0.5 */
@@ -97,15 +97,22 @@ typedef struct bpa_attn_desc {
     int32_t sel_block;         /*   bpa_select_blocks (-1 entries are ignored); forward only */
     int32_t top_n;
     int32_t local_window;      /* keys q - local_window + 1 .. q are always allowed */
+    /* Fields below were added in descriptor version 2 (bpa_version() >= 2).  A caller
+     * that sets struct_size = offsetof(bpa_attn_desc, dv) (version 1) gets dv = d and
+     * o_strides = q_strides.  Separate value head dims follow "JAX: Single-GPU Attention
+     * with TransformerEngine", section 4 (DeepSeek-style MLA head dimensions: q, k with
+     * head dim d, v and the output with head dim dv). */
+    int32_t dv;                /* head dim of v, o, dout and the dv gradient; 0 selects d; <= 256 */
+    int64_t o_strides[3];      /* (b, s, h) strides of o and dout; all 0 selects q_strides */
 } bpa_attn_desc;
 
 /* Bytes of workspace bpa_fwd (op = BPA_OP_FWD) or bpa_bwd (op = BPA_OP_BWD)
  * needs for this problem, a multiple of 256.  0 if the descriptor is invalid.
  * Forward: a status header, plus, when ring_size > 1, the float32 running
- * numerator [B, S, Hq, d].  Backward: the header, D = rowsum(dO * O) and
+ * numerator [B, S, Hq, dv].  Backward: the header, D = rowsum(dO * O) and
  * the log-sum-exp [B, Hq, S'] (S' = S rounded up to 64), the float32 dQ
- * accumulator [B, S, Hq, d], plus, when ring_size > 1, float32 dK and dV
- * carries [B, S, Hkv, d]. */
+ * accumulator [B, Hq, S', d], plus, when ring_size > 1, float32 dK and dV
+ * carries [B, S, Hkv, d] and [B, S, Hkv, dv]. */
 size_t bpa_workspace_size(int32_t op, const bpa_attn_desc* desc);
 
 /* Forward pass.
@@ -113,7 +120,7 @@ size_t bpa_workspace_size(int32_t op, const bpa_attn_desc* desc);
  * running max, exp correction, numerator and denominator) and
  * _ring_attention_fwd (ring order: query block i meets KV block
  * (i - idx) mod n at step idx; output = numerator / denominator).
- * Writes o [B, S, Hq, d] (dtype of the inputs) and m, l [B, Hq, S].
+ * Writes o [B, S, Hq, dv] (dtype of the inputs, strides o_strides) and m, l [B, Hq, S].
  * With ring_size = n > 1 the sequence is cut into n query blocks and n KV
  * super-blocks; steps [ring_step_begin, ring_step_end) run, carrying the
  * float32 numerator in the workspace and the running max / denominator in
@@ -135,7 +142,8 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l,
  * in ring order like the forward pass, the float32 dK / dV carries stand
  * in for the gradients that travel around the ring, and all steps run in
  * one call (ring_step_begin / ring_step_end must select the whole sweep).
- * dq, dk, dv have the dtype of the inputs and the strides of q, k, v.
+ * dq, dk, dv have the dtype of the inputs and the strides of q, k, v; o and
+ * dout are [B, S, Hq, dv] with o_strides.
  * Block-selected mode is not supported (BPA_ERR_UNSUPPORTED). */
 bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout,
                    const float* m, const float* l, void* dq, void* dk, void* dv,

@@ -43,6 +43,7 @@ class bpa_attn_desc(ctypes.Structure):
         ("ring_step_end", ctypes.c_int32),
         ("block_idx", ctypes.c_void_p), ("sel_block", ctypes.c_int32),
         ("top_n", ctypes.c_int32), ("local_window", ctypes.c_int32),
+        ("dv", ctypes.c_int32), ("o_strides", ctypes.c_int64 * 3),
     ]
 
 
@@ -114,10 +115,11 @@ def _stream_ptr(stream) -> int:
     return s.cuda_stream
 
 
-def make_desc(q, k, v, *, causal=False, window=(-1, -1), scale=None, bias=None, query_chunk=0,
+def make_desc(q, k, v, *, o=None, causal=False, window=(-1, -1), scale=None, bias=None, query_chunk=0,
               key_chunk=0, ring_size=1, ring_steps=None, block_idx=None, sel_block=0, top_n=0,
               local_window=0) -> bpa_attn_desc:
-    """Fill a bpa_attn_desc from torch tensors (no data is touched)."""
+    """Fill a bpa_attn_desc from torch tensors (no data is touched).  The value head dim
+    is v's last dim; o (the output, or dout, which shares its strides) sets o_strides."""
     B, S, Hq, d = q.shape
     Hkv = k.shape[2]
     D = bpa_attn_desc()
@@ -128,6 +130,11 @@ def make_desc(q, k, v, *, causal=False, window=(-1, -1), scale=None, bias=None, 
     D.q_strides[:] = _bshd_strides(q, "q")
     D.k_strides[:] = _bshd_strides(k, "k")
     D.v_strides[:] = _bshd_strides(v, "v")
+    D.dv = v.shape[3]
+    if o is not None:
+        if o.shape[:3] != q.shape[:3] or o.shape[3] != v.shape[3]:
+            raise ValueError("o / dout must be [B, S, Hq, dv]")
+        D.o_strides[:] = _bshd_strides(o, "o")
     D.scale = 0.0 if scale is None else float(scale)
     D.causal = int(bool(causal))
     wl, wr = (-1, -1) if window is None else window
@@ -159,17 +166,21 @@ def workspace(nbytes: int, device) -> torch.Tensor:
 
 
 def bpa_fwd(q, k, v, *, o=None, m=None, l=None, workspace_buf=None, stream=None, **kw):
-    """Forward pass.  Returns (o, m, l); m and l are float32 [B, Hq, S]."""
-    D = make_desc(q, k, v, **kw)
+    """Forward pass.  Returns (o, m, l): o [B, S, Hq, dv] (v's head dim); m and l are
+    float32 [B, Hq, S]."""
     B, S, Hq, _ = q.shape
     if o is None:
-        o = torch.empty_strided(q.shape[:3] + (v.shape[3],), q.stride(), dtype=q.dtype, device=q.device)
+        if v.shape[3] == q.shape[3]:
+            o = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+        else:
+            o = torch.empty(q.shape[:3] + (v.shape[3],), dtype=q.dtype, device=q.device)
+    D = make_desc(q, k, v, o=o, **kw)
     if m is None:
         m = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
     if l is None:
         l = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
-    if o.stride() != q.stride():
-        raise ValueError("o must have the strides of q")
+    if o.dtype != q.dtype:
+        raise ValueError("o must have the dtype of q")
     need = bpa_workspace_size(BPA_OP_FWD, D)
     if need == 0:
         _raise_if(BPA_ERR_INVALID_ARG, "bpa_workspace_size")
@@ -181,12 +192,17 @@ def bpa_fwd(q, k, v, *, o=None, m=None, l=None, workspace_buf=None, stream=None,
 
 
 def bpa_bwd(q, k, v, o, dout, m, l, *, dq=None, dk=None, dv=None, workspace_buf=None, stream=None, **kw):
-    """Backward pass.  Returns (dq, dk, dv) with the dtypes and strides of q, k, v."""
-    D = make_desc(q, k, v, **kw)
+    """Backward pass.  Returns (dq, dk, dv) with the dtypes and strides of q, k, v;
+    o and dout are [B, S, Hq, dv] with common strides."""
+    D = make_desc(q, k, v, o=o, **kw)
     dq = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device) if dq is None else dq
     dk = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device) if dk is None else dk
     dv = torch.empty_strided(v.shape, v.stride(), dtype=v.dtype, device=v.device) if dv is None else dv
-    for name, a, b in (("o", o, q), ("dout", dout, q), ("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+    for name, a, b in (("o", o, q), ("dout", dout, o), ("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if name == "o":
+            if a.dtype != b.dtype:
+                raise ValueError("o must have the dtype of q")
+            continue
         if a.stride() != b.stride() or a.dtype != b.dtype:
             raise ValueError(f"{name} must share dtype and strides with its input")
     need = bpa_workspace_size(BPA_OP_BWD, D)

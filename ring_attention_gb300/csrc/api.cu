@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stddef.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
@@ -57,9 +58,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ---- descriptor validation ---------------------------------------------------
 bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     if (!d) return fail(BPA_ERR_INVALID_ARG, "desc is NULL");
-    if (d->struct_size != sizeof(bpa_attn_desc))
-        return fail(BPA_ERR_INVALID_ARG, "desc->struct_size is %u, expected %zu", d->struct_size,
-                    sizeof(bpa_attn_desc));
+    const size_t v1_size = offsetof(bpa_attn_desc, dv);   // descriptor version 1: no dv, o_strides
+    if (d->struct_size != sizeof(bpa_attn_desc) && d->struct_size != v1_size)
+        return fail(BPA_ERR_INVALID_ARG, "desc->struct_size is %u, expected %zu (or %zu)", d->struct_size,
+                    sizeof(bpa_attn_desc), v1_size);
+    const bool v2 = d->struct_size == sizeof(bpa_attn_desc);
     if (d->dtype != BPA_BF16 && d->dtype != BPA_FP32)
         return fail(BPA_ERR_INVALID_ARG, "unknown dtype %d", d->dtype);
     if (d->B < 1 || d->S < 1 || d->Hq < 1 || d->Hkv < 1 || d->d < 1)
@@ -67,6 +70,10 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     if (d->Hq % d->Hkv)
         return fail(BPA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", d->Hq, d->Hkv);
     if (d->d > 256) return fail(BPA_ERR_UNSUPPORTED, "head dim %d > 256", d->d);
+    const int dv = v2 && d->dv ? d->dv : d->d;
+    if (dv < 1) return fail(BPA_ERR_INVALID_ARG, "dv must be >= 1 (or 0 for d)");
+    if (dv > 256) return fail(BPA_ERR_UNSUPPORTED, "value head dim %d > 256", dv);
+    const bool own_os = v2 && (d->o_strides[0] | d->o_strides[1] | d->o_strides[2]) != 0;
     if (need_qkv && (!d->q || !d->k || !d->v)) return fail(BPA_ERR_INVALID_ARG, "q, k or v is NULL");
     if (d->window_left < -1 || d->window_right < -1)
         return fail(BPA_ERR_INVALID_ARG, "window bounds must be >= -1");
@@ -78,7 +85,7 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
         return fail(BPA_ERR_INVALID_ARG, "query_chunk (%d) / key_chunk (%d) must divide S / ring_size = %d",
                     d->query_chunk, d->key_chunk, blk);
     for (int i = 0; i < 3; ++i)
-        if (d->q_strides[i] < 0 || d->k_strides[i] < 0 || d->v_strides[i] < 0)
+        if (d->q_strides[i] < 0 || d->k_strides[i] < 0 || d->v_strides[i] < 0 || (own_os && d->o_strides[i] < 0))
             return fail(BPA_ERR_INVALID_ARG, "strides must be non-negative");
     if (d->bias)
         for (int i = 0; i < 4; ++i)
@@ -96,6 +103,7 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     P.Hkv = d->Hkv;
     P.G = d->Hq / d->Hkv;
     P.d = d->d;
+    P.dv = dv;
     P.dtype = d->dtype;
     P.scale = d->scale > 0.f ? d->scale : 1.f / sqrtf(static_cast<float>(d->d));
     P.causal = d->causal != 0;
@@ -108,6 +116,7 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
         P.qs[i] = d->q_strides[i];
         P.ks[i] = d->k_strides[i];
         P.vs[i] = d->v_strides[i];
+        P.os[i] = own_os ? d->o_strides[i] : d->q_strides[i];
     }
     P.bias = d->bias;
     for (int i = 0; i < 4; ++i) P.bs[i] = d->bias ? d->bias_strides[i] : 0;
@@ -127,7 +136,7 @@ struct FwdLayout {
 FwdLayout fwd_layout(const Problem& P) {
     FwdLayout L;
     L.acc = kHeader;
-    size_t acc_bytes = P.ring_n > 1 ? round256(sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hq * P.d) : 0;
+    size_t acc_bytes = P.ring_n > 1 ? round256(sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hq * P.dv) : 0;
     L.total = L.acc + acc_bytes;
     return L;
 }
@@ -146,9 +155,10 @@ BwdLayout bwd_layout(const Problem& P) {
     // dQ accumulator [B, Hq, Spad / 4, d, 4]: four consecutive queries of one channel side by side
     const size_t nq = sizeof(float) * P.B * static_cast<size_t>(L.Spad) * P.Hq * P.d;
     const size_t nk = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.d;
+    const size_t nv = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.dv;
     L.dk = L.dq + round256(nq);
     L.dv = L.dk + (P.ring_n > 1 ? round256(nk) : 0);
-    L.total = L.dv + (P.ring_n > 1 ? round256(nk) : 0);
+    L.total = L.dv + (P.ring_n > 1 ? round256(nv) : 0);
     return L;
 }
 
@@ -204,7 +214,7 @@ bool make_map(CUtensorMap* map, const void* base, int d, int H, int S, int B, co
 bool tma_layout_ok(const Problem& P) {
     if (!aligned16(P.q) || !aligned16(P.k) || !aligned16(P.v)) return false;
     for (int i = 0; i < 3; ++i)
-        if ((P.qs[i] | P.ks[i] | P.vs[i]) & 7) return false;
+        if ((P.qs[i] | P.ks[i] | P.vs[i] | P.os[i]) & 7) return false;
     return true;
 }
 
@@ -289,7 +299,7 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
     if (tc) {
         tc = make_map(&maps[0], P.q, P.d, P.Hq, P.S, P.B, P.qs, 128) &&
              make_map(&maps[1], P.k, P.d, P.Hkv, P.S, P.B, P.ks, 128) &&
-             make_map(&maps[2], P.v, P.d, P.Hkv, P.S, P.B, P.vs, 128);
+             make_map(&maps[2], P.v, P.dv, P.Hkv, P.S, P.B, P.vs, 128);
     }
     if (n == 1) {
         e = tc ? launch_fwd_tc(a, maps, s) : launch_fwd_simt(a, s);
@@ -356,8 +366,8 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
     if (tc) {
         tc = make_map(&maps[0], P.q, P.d, P.Hq, P.S, P.B, P.qs, 64) &&
              make_map(&maps[1], P.k, P.d, P.Hkv, P.S, P.B, P.ks, 128) &&
-             make_map(&maps[2], P.v, P.d, P.Hkv, P.S, P.B, P.vs, 128) &&
-             make_map(&maps[3], dout, P.d, P.Hq, P.S, P.B, P.qs, 64);
+             make_map(&maps[2], P.v, P.dv, P.Hkv, P.S, P.B, P.vs, 128) &&
+             make_map(&maps[3], dout, P.dv, P.Hq, P.S, P.B, P.os, 64);
     }
     if (!tc) {
         if ((e = launch_bwd_pre(a, s)) != cudaSuccess) return cuda_fail(e, "backward pre-pass");
@@ -376,8 +386,9 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
         a.dk_acc = reinterpret_cast<float*>(ws + L.dk);
         a.dv_acc = reinterpret_cast<float*>(ws + L.dv);
         const size_t nk = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.d;
+        const size_t nv = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.dv;
         if ((e = cudaMemsetAsync(a.dk_acc, 0, nk, s)) != cudaSuccess ||
-            (e = cudaMemsetAsync(a.dv_acc, 0, nk, s)) != cudaSuccess)
+            (e = cudaMemsetAsync(a.dv_acc, 0, nv, s)) != cudaSuccess)
             return cuda_fail(e, "clearing the dK / dV carries");
         for (int idx = 0; idx < n; ++idx) {
             a.ring_idx = idx;

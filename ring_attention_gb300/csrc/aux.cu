@@ -47,7 +47,7 @@ __global__ void k_ring_init(float* acc, float* m, float* l, int64_t n_acc, int64
 template <typename T>
 __global__ void k_ring_finalize(const FwdArgs a) {
     const Problem& P = a.P;
-    const int groups = (P.d + 7) / 8;
+    const int groups = (P.dv + 7) / 8;
     const int64_t total = static_cast<int64_t>(P.B) * P.S * P.Hq * groups;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total; i += stride) {
@@ -59,9 +59,9 @@ __global__ void k_ring_finalize(const FwdArgs a) {
         const int b = static_cast<int>(r / P.S);
         const float lv = a.l[(static_cast<int64_t>(b) * P.Hq + h) * P.S + q];
         const float inv = lv > 0.f ? 1.f / lv : 0.f;
-        const float* C = a.acc + ((static_cast<int64_t>(b) * P.S + q) * P.Hq + h) * P.d;
-        T* O = static_cast<T*>(a.o) + b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2];
-        for (int c = gi * 8; c < min(P.d, gi * 8 + 8); ++c) stf(O + c, C[c] * inv);
+        const float* C = a.acc + ((static_cast<int64_t>(b) * P.S + q) * P.Hq + h) * P.dv;
+        T* O = static_cast<T*>(a.o) + b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2];
+        for (int c = gi * 8; c < min(P.dv, gi * 8 + 8); ++c) stf(O + c, C[c] * inv);
     }
 }
 
@@ -79,11 +79,11 @@ __global__ void k_bwd_pre(const BwdArgs a, int zero_dq) {
         const int b = static_cast<int>(r / (static_cast<int64_t>(a.Spad) * P.Hq));
         float D = 0.f, lse = INFINITY;
         if (q < P.S) {
-            const int64_t off = b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2];
+            const int64_t off = b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2];
             const T* O = static_cast<const T*>(a.o) + off;
             const T* dO = static_cast<const T*>(a.dout) + off;
             float s = 0.f;
-            for (int c = lane; c < P.d; c += 32) s = fmaf(ldf(O + c), ldf(dO + c), s);
+            for (int c = lane; c < P.dv; c += 32) s = fmaf(ldf(O + c), ldf(dO + c), s);
 #pragma unroll
             for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
             D = s;
@@ -109,7 +109,7 @@ __global__ void k_bwd_pre(const BwdArgs a, int zero_dq) {
 // of O and of dO; the d/8 threads of a row reduce with shuffles.
 __global__ void k_bwd_pre_bf16v(const BwdArgs a, int zero_dq) {
     const Problem& P = a.P;
-    const int tpr = P.d / 8;                       // threads per row
+    const int tpr = P.dv / 8;                      // threads per row (O, dO have dv channels)
     const int rpw = 32 / tpr;                      // rows per warp and step
     const int lane = threadIdx.x & 31, sub = lane % tpr;
     const int64_t rows = static_cast<int64_t>(P.B) * P.Hq * a.Spad;
@@ -128,7 +128,7 @@ __global__ void k_bwd_pre_bf16v(const BwdArgs a, int zero_dq) {
         const int b = bh / P.Hq;
         float s = 0.f;
         if (live && q < P.S) {
-            const int64_t off = b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2] + sub * 8;
+            const int64_t off = b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2] + sub * 8;
             const uint4 o = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o) + off);
             const uint4 g = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + off);
             const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
@@ -252,7 +252,7 @@ int grid_for(int64_t work, int threads) {
 
 cudaError_t launch_ring_init(const FwdArgs& a, cudaStream_t s) {
     const Problem& P = a.P;
-    const int64_t n_acc = static_cast<int64_t>(P.B) * P.S * P.Hq * P.d;
+    const int64_t n_acc = static_cast<int64_t>(P.B) * P.S * P.Hq * P.dv;
     const int64_t n_rows = static_cast<int64_t>(P.B) * P.Hq * P.S;
     k_ring_init<<<grid_for(n_acc, 256), 256, 0, s>>>(a.acc, a.m, a.l, n_acc, n_rows);
     return cudaGetLastError();
@@ -260,7 +260,7 @@ cudaError_t launch_ring_init(const FwdArgs& a, cudaStream_t s) {
 
 cudaError_t launch_ring_finalize(const FwdArgs& a, cudaStream_t s) {
     const Problem& P = a.P;
-    const int64_t work = static_cast<int64_t>(P.B) * P.S * P.Hq * ((P.d + 7) / 8);
+    const int64_t work = static_cast<int64_t>(P.B) * P.S * P.Hq * ((P.dv + 7) / 8);
     if (P.dtype == BPA_FP32)
         k_ring_finalize<float><<<grid_for(work, 256), 256, 0, s>>>(a);
     else
@@ -272,10 +272,10 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t s) {
     const Problem& P = a.P;
     const int64_t rows = static_cast<int64_t>(P.B) * P.Hq * a.Spad;
     const int zero = a.dq_acc != nullptr;
-    const int tpr = P.d / 8;
+    const int tpr = P.dv / 8;
     const bool vec_ok = ((reinterpret_cast<uintptr_t>(a.o) | reinterpret_cast<uintptr_t>(a.dout)) & 15u) == 0 &&
-                        ((P.qs[0] | P.qs[1] | P.qs[2]) & 7) == 0;
-    if (P.dtype == BPA_BF16 && vec_ok && P.d % 8 == 0 && tpr <= 32 && (tpr & (tpr - 1)) == 0 && rows < (1ll << 31)) {
+                        ((P.os[0] | P.os[1] | P.os[2]) & 7) == 0;
+    if (P.dtype == BPA_BF16 && vec_ok && P.dv % 8 == 0 && tpr <= 32 && (tpr & (tpr - 1)) == 0 && rows < (1ll << 31)) {
         const int threads = 256;   // a multiple of every tpr
         const int64_t work = rows * tpr;
         k_bwd_pre_bf16v<<<grid_for(work, threads), threads, 0, s>>>(a, zero);
@@ -289,20 +289,21 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t s) {
 cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t s) {
     const Problem& P = a.P;
     const int64_t nk = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.d;
+    const int64_t nv = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.dv;
     if (P.dtype != BPA_BF16) return cudaErrorInvalidValue;
     const bool vec_ok =
         ((reinterpret_cast<uintptr_t>(a.dq) | reinterpret_cast<uintptr_t>(a.dk) | reinterpret_cast<uintptr_t>(a.dv)) &
          15u) == 0 &&
         ((P.qs[0] | P.qs[1] | P.qs[2] | P.ks[0] | P.ks[1] | P.ks[2] | P.vs[0] | P.vs[1] | P.vs[2]) & 7) == 0;
-    if (vec_ok && P.d % 32 == 0 && static_cast<int64_t>(P.B) * P.Hq * ((P.S + 3) / 4) < (1ll << 31)) {
+    if (vec_ok && P.d % 32 == 0 && P.dv % 8 == 0 && static_cast<int64_t>(P.B) * P.Hq * ((P.S + 3) / 4) < (1ll << 31)) {
         const int64_t dq_threads = static_cast<int64_t>(P.B) * P.Hq * ((P.S + 3) / 4) * 32;   // a warp per 4 rows
         k_cast_dq4_bf16<<<grid_for(dq_threads, 256), 256, 0, s>>>(
             a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), P.B, P.S, P.Hq, P.d, P.qs[0], P.qs[1], P.qs[2], a.Spad);
         if (a.dk_acc) {
             k_cast_out_bf16v<<<grid_for(nk / 8, 256), 256, 0, s>>>(
                 a.dk_acc, static_cast<__nv_bfloat16*>(a.dk), P.B, P.S, P.Hkv, P.d, P.ks[0], P.ks[1], P.ks[2]);
-            k_cast_out_bf16v<<<grid_for(nk / 8, 256), 256, 0, s>>>(
-                a.dv_acc, static_cast<__nv_bfloat16*>(a.dv), P.B, P.S, P.Hkv, P.d, P.vs[0], P.vs[1], P.vs[2]);
+            k_cast_out_bf16v<<<grid_for(nv / 8, 256), 256, 0, s>>>(
+                a.dv_acc, static_cast<__nv_bfloat16*>(a.dv), P.B, P.S, P.Hkv, P.dv, P.vs[0], P.vs[1], P.vs[2]);
         }
         return cudaGetLastError();
     }

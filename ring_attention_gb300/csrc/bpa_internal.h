@@ -12,6 +12,7 @@ namespace bpa {
 // A validated attention problem (scale resolved, ring geometry derived).
 struct Problem {
     int B, S, Hq, Hkv, G, d;
+    int dv;                    // head dim of v, o, dout (== d unless separate value head dims)
     int dtype;                 // bpa_dtype
     float scale;
     int causal, wl, wr;        // window bounds, -1 = unbounded
@@ -19,6 +20,7 @@ struct Problem {
     const void* k;
     const void* v;
     int64_t qs[3], ks[3], vs[3];
+    int64_t os[3];             // strides of o and dout
     const float* bias;
     int64_t bs[4];
     int ring_n, ring_blk;      // ring_blk = S / ring_n
@@ -31,7 +33,7 @@ struct FwdArgs {
     void* o;            // output (one-shot) - unused by ring steps
     float* m;           // [B, Hq, S]
     float* l;           // [B, Hq, S]
-    float* acc;         // ring carry [B, S, Hq, d] float32, or nullptr (one-shot)
+    float* acc;         // ring carry [B, S, Hq, dv] float32, or nullptr (one-shot)
     int ring_idx;       // ring step run by this launch
     uint32_t* status;   // device status word
     uint32_t* sched;    // work-item counter of the tensor-core forward; zero before each launch

@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 bool bwd_tc_supported(const Problem& P) {
-    if (P.dtype != BPA_BF16 || P.d != D || P.block_idx) return false;
+    if (P.dtype != BPA_BF16 || P.d != D || P.dv != D || P.block_idx) return false;
     if (P.ring_n > 1 && P.ring_blk % BK) return false;
     return true;
 }

@@ -701,8 +701,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                 const float m_nat = m_true * kLn2;
                 if (!a.acc) {
                     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-                    __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.qs[0] +
-                                       static_cast<int64_t>(qc) * P.qs[1] + T.h * P.qs[2];
+                    __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.os[0] +
+                                       static_cast<int64_t>(qc) * P.os[1] + T.h * P.os[2];
     #pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t r[32];
@@ -759,8 +759,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                 }
             } else if (!aborted && !has_work && !a.acc && q < P.S) {
                 // no key allowed for this tile: O = 0, m = -inf, l = 0
-                __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.qs[0] +
-                                   static_cast<int64_t>(q) * P.qs[1] + T.h * P.qs[2];
+                __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.os[0] +
+                                   static_cast<int64_t>(q) * P.os[1] + T.h * P.os[2];
                 for (int cc = 0; cc < D; cc += 8) *reinterpret_cast<uint4*>(O + cc) = make_uint4(0, 0, 0, 0);
                 a.m[mi] = -INFINITY;
                 a.l[mi] = 0.f;
@@ -823,7 +823,7 @@ int key_tiles_per_query_tile(const Problem& P) {
 }  // namespace
 
 bool fwd_tc_supported(const Problem& P) {
-    if (P.dtype != BPA_BF16 || (P.d != 64 && P.d != 128) || P.block_idx) return false;
+    if (P.dtype != BPA_BF16 || (P.d != 64 && P.d != 128) || P.dv != P.d || P.block_idx) return false;
     if (P.ring_n > 1 && P.ring_blk % BM) return false;
     return true;
 }

@@ -253,14 +253,14 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
     }
 
     // ---- epilogue: O = num / den, m, l
-    __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + b * P.qs[0] + h * P.qs[2];
+    __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + b * P.os[0] + h * P.os[2];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int q = BS * i + mt * 16 + g + hh * 8;
             const float inv = lrow[mt][hh] > 0.f ? 1.f / lrow[mt][hh] : 0.f;
-            __nv_bfloat16* orow = O + static_cast<int64_t>(q) * P.qs[1];
+            __nv_bfloat16* orow = O + static_cast<int64_t>(q) * P.os[1];
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
                 *reinterpret_cast<uint32_t*>(orow + nt * 8 + 2 * t) =
@@ -276,13 +276,15 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
 }  // namespace
 
 bool gather_supported(const Problem& P) {
-    if (P.dtype != BPA_BF16 || P.d != D || !P.block_idx || P.sel_block != BS) return false;
+    if (P.dtype != BPA_BF16 || P.d != D || P.dv != D || !P.block_idx || P.sel_block != BS) return false;
     if (P.top_n + 3 > kMaxList || P.local_window > 2 * BS) return false;
     if (P.ring_n != 1 || P.bias) return false;
     // 16-byte rows for the staged copies, 4-byte fragment loads
     if ((reinterpret_cast<uintptr_t>(P.q) | reinterpret_cast<uintptr_t>(P.k) | reinterpret_cast<uintptr_t>(P.v)) & 15)
         return false;
-    if ((P.qs[0] | P.qs[1] | P.qs[2] | P.ks[0] | P.ks[1] | P.ks[2] | P.vs[0] | P.vs[1] | P.vs[2]) & 7) return false;
+    if ((P.qs[0] | P.qs[1] | P.qs[2] | P.ks[0] | P.ks[1] | P.ks[2] | P.vs[0] | P.vs[1] | P.vs[2] | P.os[0] | P.os[1] |
+         P.os[2]) & 7)
+        return false;
     return true;
 }
 

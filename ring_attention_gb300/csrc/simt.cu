@@ -127,7 +127,7 @@ __device__ void fold_keys(const Problem& P, int b, int h, int g, int q, int klo,
 #pragma unroll
             for (int i = 0; i < kPer; ++i) {
                 const int c = lane + 32 * i;
-                if (c < P.d) st.acc[i] = fmaf(pt, ldf(vr + c), st.acc[i]);
+                if (c < P.dv) st.acc[i] = fmaf(pt, ldf(vr + c), st.acc[i]);
             }
         }
         st.m = mnew;
@@ -176,11 +176,11 @@ __global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
         const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * P.S + q;
         if (!ring) {
             const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
-            T* O = static_cast<T*>(a.o) + b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2];
+            T* O = static_cast<T*>(a.o) + b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2];
 #pragma unroll
             for (int i = 0; i < kPer; ++i) {
                 const int c = lane + 32 * i;
-                if (c < P.d) stf(O + c, st.acc[i] * inv);
+                if (c < P.dv) stf(O + c, st.acc[i] * inv);
             }
             if (lane == 0) {
                 a.m[mi] = st.m;
@@ -193,11 +193,11 @@ __global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
             if (mn != -INFINITY) {
                 const float fa = mc == -INFINITY ? 0.f : expf(mc - mn);
                 const float fb = st.m == -INFINITY ? 0.f : expf(st.m - mn);
-                float* C = a.acc + ((static_cast<int64_t>(b) * P.S + q) * P.Hq + h) * P.d;
+                float* C = a.acc + ((static_cast<int64_t>(b) * P.S + q) * P.Hq + h) * P.dv;
 #pragma unroll
                 for (int i = 0; i < kPer; ++i) {
                     const int c = lane + 32 * i;
-                    if (c < P.d) C[c] = C[c] * fa + st.acc[i] * fb;
+                    if (c < P.dv) C[c] = C[c] * fa + st.acc[i] * fb;
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -226,10 +226,9 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
         const int q = blockIdx.x * kRows + r;
         if (q >= P.S) break;
         const int64_t qoff = b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2];
-        for (int c = lane; c < P.d; c += 32) {
-            sq[warp][c] = ldf(Q + qoff + c);
-            sdo[warp][c] = ldf(dO + qoff + c);
-        }
+        const int64_t ooff = b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2];
+        for (int c = lane; c < P.d; c += 32) sq[warp][c] = ldf(Q + qoff + c);
+        for (int c = lane; c < P.dv; c += 32) sdo[warp][c] = ldf(dO + ooff + c);
         __syncwarp();
         const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * a.Spad + q;
         const float lse = a.lse[mi], Dq = a.Dvec[mi];
@@ -249,10 +248,9 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
                     const T* vr = V + b * P.vs[0] + static_cast<int64_t>(k) * P.vs[1] + g * P.vs[2];
                     float dot = 0.f, dp = 0.f;
 #pragma unroll 8
-                    for (int c = 0; c < P.d; ++c) {
-                        dot = fmaf(sq[warp][c], ldf(kr + c), dot);
-                        dp = fmaf(sdo[warp][c], ldf(vr + c), dp);
-                    }
+                    for (int c = 0; c < P.d; ++c) dot = fmaf(sq[warp][c], ldf(kr + c), dot);
+#pragma unroll 8
+                    for (int c = 0; c < P.dv; ++c) dp = fmaf(sdo[warp][c], ldf(vr + c), dp);
                     const float z = dot * P.scale + bias_at(P, b, h, q, k);
                     dS = expf(z - lse) * (dp - Dq);
                 }
@@ -298,10 +296,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
         if (k >= P.S) break;
         const int64_t koff = b * P.ks[0] + static_cast<int64_t>(k) * P.ks[1] + g * P.ks[2];
         const int64_t voff = b * P.vs[0] + static_cast<int64_t>(k) * P.vs[1] + g * P.vs[2];
-        for (int c = lane; c < P.d; c += 32) {
-            sk[warp][c] = ldf(K + koff + c);
-            sv[warp][c] = ldf(V + voff + c);
-        }
+        for (int c = lane; c < P.d; c += 32) sk[warp][c] = ldf(K + koff + c);
+        for (int c = lane; c < P.dv; c += 32) sv[warp][c] = ldf(V + voff + c);
         __syncwarp();
         float dk[kPer], dv[kPer];
 #pragma unroll
@@ -319,12 +315,12 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
                     const float lse = a.lse[mi];
                     if (lse != INFINITY) {
                         const int64_t qoff = b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2];
+                        const int64_t ooff = b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2];
                         float dot = 0.f, dp = 0.f;
 #pragma unroll 8
-                        for (int c = 0; c < P.d; ++c) {
-                            dot = fmaf(ldf(Q + qoff + c), sk[warp][c], dot);
-                            dp = fmaf(ldf(dO + qoff + c), sv[warp][c], dp);
-                        }
+                        for (int c = 0; c < P.d; ++c) dot = fmaf(ldf(Q + qoff + c), sk[warp][c], dot);
+#pragma unroll 8
+                        for (int c = 0; c < P.dv; ++c) dp = fmaf(ldf(dO + ooff + c), sv[warp][c], dp);
                         const float z = dot * P.scale + bias_at(P, b, h, q, k);
                         p = expf(z - lse);
                         dS = p * (dp - a.Dvec[mi]);
@@ -338,13 +334,13 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
                     if (t >= nt) continue;
                     const int64_t qoff =
                         b * P.qs[0] + static_cast<int64_t>(q0 + t) * P.qs[1] + h * P.qs[2];
+                    const int64_t ooff =
+                        b * P.os[0] + static_cast<int64_t>(q0 + t) * P.os[1] + h * P.os[2];
 #pragma unroll
                     for (int i = 0; i < kPer; ++i) {
                         const int c = lane + 32 * i;
-                        if (c < P.d) {
-                            dk[i] = fmaf(st, ldf(Q + qoff + c), dk[i]);
-                            dv[i] = fmaf(pt, ldf(dO + qoff + c), dv[i]);
-                        }
+                        if (c < P.d) dk[i] = fmaf(st, ldf(Q + qoff + c), dk[i]);
+                        if (c < P.dv) dv[i] = fmaf(pt, ldf(dO + ooff + c), dv[i]);
                     }
                 }
             }
@@ -354,10 +350,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
 #pragma unroll
         for (int i = 0; i < kPer; ++i) {
             const int c = lane + 32 * i;
-            if (c < P.d) {
-                stf(dK + c, dk[i] * P.scale);
-                stf(dV + c, dv[i]);
-            }
+            if (c < P.d) stf(dK + c, dk[i] * P.scale);
+            if (c < P.dv) stf(dV + c, dv[i]);
         }
         __syncwarp();
     }

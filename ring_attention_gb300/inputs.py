@@ -49,7 +49,12 @@ class Workload:
     top_n: int = 0
     local_window: int = 0
     backward: bool = True
+    dv: int = 0                  # head dim of v and dO; 0 = d
     extra: dict = field(default_factory=dict, compare=False)
+
+    @property
+    def d_v(self) -> int:
+        return self.dv or self.d
 
 
 # The five workloads of the hot path, named by what they are.
@@ -65,7 +70,13 @@ RING_LONG = Workload("ring8_causal_padbias_B1_S131072_Hq32_Hkv8_d128", B=1, S=13
 BLOCK_SEL = Workload("blocksel_top8_B4_S8192_H8_d64", B=4, S=8192, Hq=8, Hkv=8, d=64,
                      causal=True, seed=4, sel_block=32, top_n=8, local_window=32, backward=False)
 
+# Beyond the five: separate value head dim (q, k with 128 channels, v and the output with
+# 64), the DeepSeek-style MLA shapes of the TransformerEngine page (section 4), causal.
+MLA_CAUSAL = Workload("mla_causal_B2_S4096_Hq128_Hkv8_dqk128_dv64", B=2, S=4096, Hq=128, Hkv=8, d=128,
+                      dv=64, causal=True, seed=2027)
+
 WORKLOADS = {w.name: w for w in (TINY_F32, GQA_CAUSAL, GQA_SWA, RING_LONG, BLOCK_SEL)}
+EXTRA_WORKLOADS = {w.name: w for w in (MLA_CAUSAL,)}
 
 
 def draw(shape_list, seed: int, dtype: str):
@@ -90,9 +101,9 @@ def make_inputs(w: Workload, *, S: int | None = None, B: int | None = None,
     S = w.S if S is None else S
     Hq = w.Hq if Hq is None else Hq
     Hkv = w.Hkv if Hkv is None else Hkv
-    shapes = [(B, S, Hq, w.d), (B, S, Hkv, w.d), (B, S, Hkv, w.d)]
+    shapes = [(B, S, Hq, w.d), (B, S, Hkv, w.d), (B, S, Hkv, w.d_v)]
     if w.backward:
-        shapes.append((B, S, Hq, w.d))
+        shapes.append((B, S, Hq, w.d_v))
     ts = draw(shapes, w.seed, w.dtype)
     q, k, v = ts[:3]
     dout = ts[3] if w.backward else None

@@ -25,7 +25,7 @@ def bpa():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(bpa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(bpa_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_entry_points():
@@ -142,4 +142,30 @@ def test_select_rejects_bad_arguments(bpa):
 def test_status_strings(bpa):
     L = bpa.lib()
     assert L.bpa_status_string(5) == b"BPA_ERR_TIMEOUT"
-    assert L.bpa_version() == 1
+    assert L.bpa_version() == 2
+
+
+def test_version_1_descriptor_is_accepted(bpa):
+    """A caller built against descriptor version 1 passes the shorter struct_size: the
+    value head dim defaults to d and the output strides to q's."""
+    L = bpa.lib()
+    D = _desc(bpa)
+    full = L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(D))
+    D.struct_size = bpa.bpa_attn_desc.dv.offset
+    assert L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(D)) == full
+    D.struct_size = bpa.bpa_attn_desc.dv.offset + 4
+    assert L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(D)) == 0
+
+
+def test_value_head_dim_checks_and_sizes(bpa):
+    L = bpa.lib()
+    D = _desc(bpa, ring_size=2)
+    base = L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D))
+    D.dv = D.d // 2   # separate value head dim: the forward ring carry is [B, S, Hq, dv]
+    half = L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D))
+    assert half == 256 + (base - 256) // 2
+    D.dv = 257
+    assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) == 0
+    assert b"value head dim" in L.bpa_last_error()
+    D.dv = -1
+    assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) == 0

@@ -226,3 +226,49 @@ def test_status_clean_after_normal_call(bpa):
     bpa.bpa_fwd(q, k, v, causal=True, workspace_buf=ws)
     torch.cuda.synchronize()
     bpa.bpa_check(ws)
+
+
+# ---- separate value head dim (q, k with d channels; v, o, dO with dv) ----------------------
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dims", [(128, 64), (64, 128), (96, 32)], ids=lambda d: f"d{d[0]}_dv{d[1]}")
+@pytest.mark.parametrize("mask", [dict(causal=True, window=(-1, -1)), dict(causal=False, window=(40, 9))],
+                         ids=_mask_id)
+def test_separate_value_head_dim(bpa, ora, dtype, dims, mask):
+    d, dv = dims
+    B, S, Hq, Hkv = 2, 150, 4, 2
+    q, k, v, do = draw([(B, S, Hq, d), (B, S, Hkv, d), (B, S, Hkv, dv), (B, S, Hq, dv)], 71 + d + dv, dtype)
+    tq, tk, tv = dev(q), dev(k), dev(v)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, **mask)
+    assert tuple(o.shape) == (B, S, Hq, dv)
+    dq, dk, dvv = bpa.bpa_bwd(tq, tk, tv, o, dev(do), m, l, **mask)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, **mask)
+    check_stats(m, l, rm, rl)
+    if dtype == "f32":
+        for got, ref in ((o, ro), (dq, rq), (dk, rk), (dvv, rv)):
+            assert max_abs(host(got), ref) <= FP32_MAX_ABS
+    else:
+        assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+        for got, ref in ((dq, rq), (dk, rk), (dvv, rv)):
+            assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2
+
+
+def test_output_strides_differ_from_query_strides(bpa, ora):
+    # o and dO as views into a wider [B, S, Hq, 2 dv] buffer: their strides are their own
+    B, S, Hq, Hkv, d, dv = 1, 130, 4, 2, 128, 64
+    q, k, v, do = draw([(B, S, Hq, d), (B, S, Hkv, d), (B, S, Hkv, dv), (B, S, Hq, dv)], 83, "bf16")
+    tq, tk, tv = dev(q), dev(k), dev(v)
+    obuf = torch.zeros((B, S, Hq, 2 * dv), dtype=torch.bfloat16, device="cuda")
+    o = obuf[..., dv:]
+    dobuf = torch.zeros((B, S, Hq, 2 * dv), dtype=torch.bfloat16, device="cuda")
+    dobuf[..., dv:] = dev(do)
+    tdo = dobuf[..., dv:]
+    _, m, l = bpa.bpa_fwd(tq, tk, tv, o=o, causal=True)
+    dq, dk, dvv = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, causal=True)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, causal=True)
+    assert float(obuf[..., :dv].abs().max()) == 0.0      # nothing written outside the view
+    assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+    check_stats(m, l, rm, rl)
+    for got, ref in ((dq, rq), (dk, rk), (dvv, rv)):
+        assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2

@@ -129,3 +129,19 @@ def test_block_selected_workload_full(bpa, ora):
                                    top_n=w.top_n, local_window=w.local_window)
     assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
     check_stats(m, l, rm, rl)
+
+
+def test_mla_workload_reduced(bpa, ora):
+    # the separate-value-head-dim workload (d_qk 128, d_v 64, causal) on a reduced
+    # sequence and head count with the same recipe and GQA ratio 16
+    w = W.MLA_CAUSAL
+    q, k, v, do, bias = W.make_inputs(w, B=1, S=1024, Hq=16, Hkv=1)
+    assert v.shape[-1] == 64 and do.shape[-1] == 64
+    from dataclasses import replace
+    o, m, l, (dq, dk, dv) = _run(bpa, replace(w, B=1, S=1024, Hq=16, Hkv=1), q, k, v, do, bias)
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, causal=True)
+    assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+    check_stats(m, l, rm, rl)
+    assert rel_l2(host(dq), rq) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dk), rk) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
