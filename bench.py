@@ -37,7 +37,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 def flops(w, entries):
-    return 4.0 * w.d * entries, 10.0 * w.d * entries
+    """Algorithmic FLOPs per allowed (query, key) entry: forward Q K^T (2 d) and P V (2 dv);
+    backward the recomputed Q K^T, dP = dO V^T, dV = P^T dO (2 dv each but the first, 2 d),
+    dK = dS^T Q and dQ = dS K (2 d each)."""
+    d, dv = w.d, w.d_v
+    return (2.0 * d + 2.0 * dv) * entries, (6.0 * d + 4.0 * dv) * entries
 
 
 def load_peaks():
@@ -147,7 +151,7 @@ def time_extra_workloads(bpa, dev, peak_tf):
     Inputs are drawn on the device from seeded generators (timing only; the
     parity tests use the numpy recipe)."""
     import torch
-    from ring_attention_gb300.inputs import BLOCK_SEL, GQA_SWA, RING_LONG, TINY_F32
+    from ring_attention_gb300.inputs import BLOCK_SEL, GQA_SWA, MLA_CAUSAL, RING_LONG, TINY_F32
 
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     out = {}
@@ -161,8 +165,8 @@ def time_extra_workloads(bpa, dev, peak_tf):
         dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
         q = rnd((w.B, w.S, w.Hq, w.d), dt, w.seed)
         k = rnd((w.B, w.S, w.Hkv, w.d), dt, w.seed + 1)
-        v = rnd((w.B, w.S, w.Hkv, w.d), dt, w.seed + 2)
-        do = rnd((w.B, w.S, w.Hq, w.d), dt, w.seed + 3)
+        v = rnd((w.B, w.S, w.Hkv, w.d_v), dt, w.seed + 2)
+        do = rnd((w.B, w.S, w.Hq, w.d_v), dt, w.seed + 3)
         bias = None
         if w.pad_tail:
             bias = torch.zeros((1, 1, 1, w.S), device=dev, dtype=torch.float32)
@@ -192,8 +196,9 @@ def time_extra_workloads(bpa, dev, peak_tf):
         f_fwd, f_bwd = flops(w, ent)
         mf, mb = statistics.mean(tf), statistics.mean(tb)
         el = 2 if dt == torch.bfloat16 else 4
-        fwd_bytes = el * w.B * w.S * w.d * (2 * w.Hq + 2 * w.Hkv)             # Q, K, V read, O written
-        bwd_bytes = el * w.B * w.S * w.d * (4 * w.Hq + 4 * w.Hkv)             # Q, K, V, O, dO read; dQ, dK, dV written
+        d, dv = w.d, w.d_v
+        fwd_bytes = el * w.B * w.S * ((d + dv) * w.Hq + (d + dv) * w.Hkv)    # Q, K, V read, O written
+        bwd_bytes = el * w.B * w.S * ((2 * d + 2 * dv) * w.Hq + (2 * d + 2 * dv) * w.Hkv)   # + dO, O read; dQ, dK, dV
         res = {"fwd_ms": mf, "bwd_ms": mb, "fwd_tflops": f_fwd / mf / 1e9, "bwd_tflops": f_bwd / mb / 1e9,
                "fwd_pct_peak": 100 * f_fwd / mf / 1e9 / peak_tf, "bwd_pct_peak": 100 * f_bwd / mb / 1e9 / peak_tf,
                "fwd_min_bytes_gbs": fwd_bytes / mf / 1e6, "bwd_min_bytes_gbs": bwd_bytes / mb / 1e6,
@@ -205,6 +210,7 @@ def time_extra_workloads(bpa, dev, peak_tf):
     out[GQA_SWA.name] = fwd_bwd(GQA_SWA, 20, 3)
     out[TINY_F32.name] = fwd_bwd(TINY_F32, 20, 3)
     out[RING_LONG.name] = fwd_bwd(RING_LONG, 2, 1)
+    out[MLA_CAUSAL.name] = fwd_bwd(MLA_CAUSAL, 10, 3)
 
     w = BLOCK_SEL
     q = rnd((w.B, w.S, w.Hq, w.d), torch.bfloat16, w.seed)

@@ -55,14 +55,21 @@ constexpr int kSoftmax = 256;    // threads of the two softmax warpgroups
 constexpr int SUBK = BK * 128;    // one 64-channel slab of the key tile
 constexpr int SUBQ = BQ * 128;    // one 64-channel slab of a query tile
 constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + BK * D * 2;
-constexpr int OFF_Q = OFF_V + BK * D * 2;
-constexpr int OFF_DO = OFF_Q + NS * BQ * D * 2;
-constexpr int OFF_DS = OFF_DO + NS * BQ * D * 2;    // dS^T [128 keys][64 q] bf16
-constexpr int OFF_ST = OFF_DS + BK * BQ * 2;        // per stage: lse[64], D[64] float
-constexpr int OFF_BAR = OFF_ST + NS * 512;
-constexpr int SMEM = OFF_BAR + 256 + 1024;
-static_assert(SMEM <= 232448, "shared memory");
+// Shared-memory layout for value head dim DV (128, or 64 with q, k of 128: separate
+// value head dims); V tiles and dO stages hold DV channels.
+template <int DV>
+struct BwdCfg {
+    static constexpr int OFF_V = OFF_K + BK * D * 2;
+    static constexpr int OFF_Q = OFF_V + BK * DV * 2;
+    static constexpr int OFF_DO = OFF_Q + NS * BQ * D * 2;
+    static constexpr int OFF_DS = OFF_DO + NS * BQ * DV * 2;   // dS^T [128 keys][64 q] bf16
+    static constexpr int OFF_ST = OFF_DS + BK * BQ * 2;        // per stage: lse[64], D[64] float
+    static constexpr int OFF_BAR = OFF_ST + NS * 512;
+    static constexpr int SMEM = OFF_BAR + 256 + 1024;
+    static constexpr int DO_BYTES = BQ * DV * 2;               // one dO stage
+    static constexpr uint32_t IDESC_V = idesc_bf16_f32(BK, DV, 0, 1);   // dV: A from TMEM, B MN-major
+    static_assert(SMEM <= 232448, "shared memory");
+};
 
 // barrier slots
 constexpr int B_KV = 0, B_QF = 1, B_QE = 1 + NS, B_S = 1 + 2 * NS, B_SF = 2 + 2 * NS, B_DP = 3 + 2 * NS,
@@ -71,7 +78,7 @@ constexpr int B_KV = 0, B_QF = 1, B_QE = 1 + NS, B_S = 1 + 2 * NS, B_SF = 2 + 2 
 static_assert(8 * NBAR + 8 <= 256, "barrier area");
 
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BK, BQ, 0, 0);     // S^T, dP^T: both K-major
-constexpr uint32_t IDESC_KV = idesc_bf16_f32(BK, D, 0, 1);     // dV, dK: A from TMEM, B MN-major
+constexpr uint32_t IDESC_KV = idesc_bf16_f32(BK, D, 0, 1);     // dK: A from TMEM, B MN-major
 constexpr uint32_t IDESC_Q = idesc_bf16_f32(D, BQ, 1, 1);      // dQ^T: both MN-major
 
 struct Work {
@@ -113,19 +120,21 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32
     mbar_wait(bar, parity, &never, status, 0xD1);
 }
 
+template <int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
              const BwdArgs a) {
+    using L = BwdCfg<DV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t sb = smem_u32(smem);
-    const uint32_t bar0 = sb + OFF_BAR;
+    const uint32_t bar0 = sb + L::OFF_BAR;
     auto BAR = [&](int i) { return bar0 + 8u * i; };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 8 * NBAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 8 * NBAR);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    const float* st_smem = reinterpret_cast<const float*>(smem + OFF_ST);
+    const float* st_smem = reinterpret_cast<const float*>(smem + L::OFF_ST);
 
     const Problem& P = a.P;
     const Work W = decode(a);
@@ -178,26 +187,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch(&tmK);
             tma_prefetch(&tmV);
             tma_prefetch(&tmDO);
-            mbar_expect_tx(BAR(B_KV), 2 * BK * D * 2);
-            for (int sub = 0; sub < 2; ++sub) {
+            mbar_expect_tx(BAR(B_KV), BK * (D + DV) * 2);
+            for (int sub = 0; sub < D / 64; ++sub)
                 tma_load_4d(sb + OFF_K + sub * SUBK, &tmK, BAR(B_KV), sub * 64, W.hkv, W.k0, W.b);
-                tma_load_4d(sb + OFF_V + sub * SUBK, &tmV, BAR(B_KV), sub * 64, W.hkv, W.k0, W.b);
-            }
+            for (int sub = 0; sub < DV / 64; ++sub)
+                tma_load_4d(sb + L::OFF_V + sub * SUBK, &tmV, BAR(B_KV), sub * 64, W.hkv, W.k0, W.b);
             int n_issued = 0;
             for (int it = 0; it < n_it; ++it) {
                 const int st = it % NS, use = it / NS;
                 if (use > 0 && !mbar_wait(BAR(B_QE + st), (use - 1) & 1, abort_flag, a.status, 0x40)) break;
                 const int h = iter_head(it), q0 = iter_q0(it);
-                mbar_expect_tx(BAR(B_QF + st), 2 * BQ * D * 2 + 512);
-                for (int sub = 0; sub < 2; ++sub) {
-                    tma_load_4d(sb + OFF_Q + st * BQ * D * 2 + sub * SUBQ, &tmQ, BAR(B_QF + st), sub * 64, h,
+                mbar_expect_tx(BAR(B_QF + st), BQ * D * 2 + L::DO_BYTES + 512);
+                for (int sub = 0; sub < D / 64; ++sub)
+                    tma_load_4d(sb + L::OFF_Q + st * BQ * D * 2 + sub * SUBQ, &tmQ, BAR(B_QF + st), sub * 64, h,
                                 q0, W.b);
-                    tma_load_4d(sb + OFF_DO + st * BQ * D * 2 + sub * SUBQ, &tmDO, BAR(B_QF + st), sub * 64,
+                for (int sub = 0; sub < DV / 64; ++sub)
+                    tma_load_4d(sb + L::OFF_DO + st * L::DO_BYTES + sub * SUBQ, &tmDO, BAR(B_QF + st), sub * 64,
                                 h, q0, W.b);
-                }
                 const int64_t row = (static_cast<int64_t>(W.b) * P.Hq + h) * a.Spad + q0;
-                bulk_load(sb + OFF_ST + st * 512, a.lse + row, 256, BAR(B_QF + st));
-                bulk_load(sb + OFF_ST + st * 512 + 256, a.Dvec + row, 256, BAR(B_QF + st));
+                bulk_load(sb + L::OFF_ST + st * 512, a.lse + row, 256, BAR(B_QF + st));
+                bulk_load(sb + L::OFF_ST + st * 512 + 256, a.Dvec + row, 256, BAR(B_QF + st));
                 n_issued = it + 1;
             }
             drain_wait(BAR(B_KV), 0, a.status);
@@ -211,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The whole warp runs the loop with warp-uniform operands; one elected lane issues.
         if (n_it > 0) {
             bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_KV), 0, abort_flag, a.status, 0x50));
-            const uint64_t kd0 = sdesc_sw128(sb + OFF_K, 16, 1024), vd0 = sdesc_sw128(sb + OFF_V, 16, 1024);
+            const uint64_t kd0 = sdesc_sw128(sb + OFF_K, 16, 1024), vd0 = sdesc_sw128(sb + L::OFF_V, 16, 1024);
             for (int it = 0; ok && it < n_it; ++it) {
                 const int st = it % NS, buf = it & 1;
                 if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_QF + st), (it / NS) & 1, abort_flag, a.status, 0x51))) break;
@@ -222,16 +231,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                   a.status, 0x55)))
                     break;
                 tc_fence_after();
-                const uint64_t qd = sdesc_sw128(sb + OFF_Q + st * BQ * D * 2, 16, 1024);
-                const uint64_t dod = sdesc_sw128(sb + OFF_DO + st * BQ * D * 2, 16, 1024);
+                const uint64_t qd = sdesc_sw128(sb + L::OFF_Q + st * BQ * D * 2, 16, 1024);
+                const uint64_t dod = sdesc_sw128(sb + L::OFF_DO + st * L::DO_BYTES, 16, 1024);
                 // S^T and dP^T are independent accumulations: interleaved, each waits less on
-                // its own previous step
+                // its own previous step (dP^T contracts over DV channels, S^T over D)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t offk = (kk >> 2) * SUBK + (kk & 3) * 32;
                     const uint32_t offq = (kk >> 2) * SUBQ + (kk & 3) * 32;
                     tc_mma_ss_w(tS, sdesc_advance(kd0, offk), sdesc_advance(qd, offq), IDESC_S, kk > 0);
-                    tc_mma_ss_w(tDP + buf * BQ, sdesc_advance(vd0, offk), sdesc_advance(dod, offq), IDESC_S, kk > 0);
+                    if (kk < DV / 16)
+                        tc_mma_ss_w(tDP + buf * BQ, sdesc_advance(vd0, offk), sdesc_advance(dod, offq), IDESC_S, kk > 0);
                 }
                 tc_commit_w(BAR(B_S));
                 tc_commit_w(BAR(B_DP + buf));
@@ -244,13 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer B: dV, dK, dQ^T
         if (n_it > 0) {
             const uint64_t kmn0 = sdesc_sw128(sb + OFF_K, SUBK, 1024);
-            const uint64_t dsmn = sdesc_sw128(sb + OFF_DS, 16, 1024);
+            const uint64_t dsmn = sdesc_sw128(sb + L::OFF_DS, 16, 1024);
             for (int p = 0; p < n_it; ++p) {
                 const int pst = p % NS, buf = p & 1;
                 if (!__all_sync(0xffffffffu, mbar_wait(BAR(B_DS), p & 1, abort_flag, a.status, 0x52))) break;
                 tc_fence_after();
-                const uint64_t qmn = sdesc_sw128(sb + OFF_Q + pst * BQ * D * 2, SUBQ, 1024);
-                const uint64_t domn = sdesc_sw128(sb + OFF_DO + pst * BQ * D * 2, SUBQ, 1024);
+                const uint64_t qmn = sdesc_sw128(sb + L::OFF_Q + pst * BQ * D * 2, SUBQ, 1024);
+                const uint64_t domn = sdesc_sw128(sb + L::OFF_DO + pst * L::DO_BYTES, SUBQ, 1024);
                 // bf16 pairs of query columns 16 kk .. 16 kk + 15: warpgroup kk / 2 wrote P^T at
                 // columns 32 (kk / 2) + 8 (kk % 2) of the dP^T buffer and dS^T 16 columns further
                 const uint32_t tPD = tDP + buf * BQ;
@@ -258,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < BQ / 16; ++kk) {
                     const uint32_t acc = (p > 0 || kk > 0) ? 1u : 0u;
                     const uint32_t tp = tPD + (kk >> 1) * 32 + (kk & 1) * 8;
-                    tc_mma_ts_w(tDV, tp, sdesc_advance(domn, kk * 2048), IDESC_KV, acc);
+                    tc_mma_ts_w(tDV, tp, sdesc_advance(domn, kk * 2048), L::IDESC_V, acc);
                     tc_mma_ts_w(tDK, tp + 16, sdesc_advance(qmn, kk * 2048), IDESC_KV, acc);
                 }
                 tc_commit_w(BAR(B_PRF + buf));   // the pairs have been read: issuer A may reuse the buffer
@@ -384,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_st16_nowait(tcol, ppk);
             tmem_st16_nowait(tcol + 16, dpk);
-            const uint32_t db = sb + OFF_DS;
+            const uint32_t db = sb + L::OFF_DS;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
                 st_shared_v4(db + sw128_offset(r, wg * 4 + cc), dpk[4 * cc], dpk[4 * cc + 1], dpk[4 * cc + 2],
@@ -414,11 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              : static_cast<__nv_bfloat16*>(a.dv) + W.b * P.vs[0] +
                                                    static_cast<int64_t>(kk) * P.vs[1] + W.hkv * P.vs[2];
                 float* carry_base = wg == 0 ? a.dk_acc : a.dv_acc;
+                const int ncol = wg == 0 ? D : DV;   // channels of dK / dV
                 float* carry = carry_base
-                                   ? carry_base + ((static_cast<int64_t>(W.b) * P.S + kk) * P.Hkv + W.hkv) * D
+                                   ? carry_base + ((static_cast<int64_t>(W.b) * P.S + kk) * P.Hkv + W.hkv) * ncol
                                    : nullptr;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < ncol / 32; ++c) {
                     uint32_t v[32];
                     if (n_it > 0) {
                         tmem_ld32(tacc + c * 32 + lane_base, v);
@@ -466,28 +477,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-}  // namespace
-
-bool bwd_tc_supported(const Problem& P) {
-    if (P.dtype != BPA_BF16 || P.d != D || P.dv != D || P.block_idx) return false;
-    if (P.ring_n > 1 && P.ring_blk % BK) return false;
-    return true;
-}
-
-cudaError_t launch_bwd_tc(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
+template <int DV>
+cudaError_t launch_dv(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
+    using L = BwdCfg<DV>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(k_bwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        e = cudaFuncSetAttribute(k_bwd_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
     const int nkt = (a.P.S + BK - 1) / BK;
     const int grid = nkt * a.P.Hkv * a.P.B;
-    k_bwd_tc<<<grid, kThreads, SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
+    k_bwd_tc<DV><<<grid, kThreads, L::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_tc_supported(const Problem& P) {
+    if (P.dtype != BPA_BF16 || P.d != D || (P.dv != D && P.dv != 64) || P.block_idx) return false;
+    if (P.ring_n > 1 && P.ring_blk % BK) return false;
+    return true;
+}
+
+cudaError_t launch_bwd_tc(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
+    return a.P.dv == 64 ? launch_dv<64>(a, maps, s) : launch_dv<128>(a, maps, s);
 }
 
 }  // namespace bpa

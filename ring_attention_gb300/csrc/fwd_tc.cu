@@ -7,7 +7,7 @@
 //     m' = max(m, rowmax S);  P = exp(S - m');  num = num * exp(m - m') + P V;
 //     den = den * exp(m - m') + rowsum P
 // Both query tiles share every K / V tile that is loaded.
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+d), O1 [384,384+d).
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+dv), O1 [384,384+dv).
 // P (bf16, two per 32-bit column) is written back over the first 64 columns
 // of its S tile and read from there by the P V product (A operand in TMEM).
 // Roles (320 threads):
@@ -47,7 +47,8 @@ constexpr float kTau = 8.f;   // lazy-rescale threshold, log2 units
 // columns, < 113 KB of shared memory) so that two run on an SM and one CTA's
 // loads and stores overlap the other's products (short key ranges, e.g. a
 // narrow sliding window).
-template <int D, int NQ>
+// D: head dim of q, k; DV: head dim of v and the output (DV == D, or D = 128 with DV = 64).
+template <int D, int DV, int NQ>
 struct FwdCfg {
     static constexpr int kThreads = NQ * 128 + 64;
     static constexpr int kTmemCols = NQ * 256;
@@ -55,14 +56,15 @@ struct FwdCfg {
     // K and V flow through separate rings: K tile j is needed one product
     // earlier than V tile j, so it gets more stages where space allows.
     static constexpr int NSK = NQ == 2 ? (D == 128 ? 3 : 4) : (D == 128 ? 1 : 2);   // K stages
-    static constexpr int NSV = NQ == 2 ? (D == 128 ? 2 : 4) : (D == 128 ? 1 : 2);   // V stages
+    static constexpr int NSV = NQ == 2 ? (DV == 128 ? 2 : (D == 128 ? 3 : 4)) : (DV == 128 ? 1 : 2);   // V stages
     static constexpr int Q_BYTES = BM * D * 2;     // one query tile
-    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int KV_BYTES = BN * D * 2;    // one K tile
+    static constexpr int V_BYTES = BN * DV * 2;    // one V tile
     static constexpr int SUB = 128 * 128;          // one 64-column slab of 128 rows
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
     static constexpr int OFF_V = OFF_K + NSK * KV_BYTES;
-    static constexpr int OFF_KB = OFF_V + NSV * KV_BYTES;   // per K stage: the tile's 128 key-bias values
+    static constexpr int OFF_KB = OFF_V + NSV * V_BYTES;    // per K stage: the tile's 128 key-bias values
     static constexpr int OFF_BAR = OFF_KB + NSK * BN * 4;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;   // + slack to align the base to 1024
     // barrier slots: Q full / empty; K full / empty, V full / empty; S, P, O full, O empty per
@@ -73,7 +75,7 @@ struct FwdCfg {
     static_assert(8 * NBAR + 16 <= 512, "barrier area");
     static_assert(SMEM <= 232448, "shared memory");
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0, 0);   // Q, K both K-major
-    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 0, 1);   // P (TMEM), V MN-major
+    static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DV, 0, 1);   // P (TMEM), V MN-major
     static_assert(NQ == 2 || 2 * SMEM <= 233472, "two single-tile CTAs must fit an SM");
 };
 
@@ -295,11 +297,11 @@ __device__ __forceinline__ float row_exp_1p(const RowCtx& R, float mref, uint32_
     return a + b;
 }
 
-template <int D, int NQ>
-__global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
+template <int D, int DV, int NQ>
+__global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
     k_fwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
-    using C = FwdCfg<D, NQ>;
+    using C = FwdCfg<D, DV, NQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -429,9 +431,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(BAR(C::B_VF + st), C::KV_BYTES);
-                    for (int sub = 0; sub < D / 64; ++sub)
-                        tma_load_4d(sb + C::OFF_V + st * C::KV_BYTES + sub * C::SUB, &tmV, BAR(C::B_VF + st), sub * 64,
+                    mbar_expect_tx(BAR(C::B_VF + st), C::V_BYTES);
+                    for (int sub = 0; sub < DV / 64; ++sub)
+                        tma_load_4d(sb + C::OFF_V + st * C::V_BYTES + sub * C::SUB, &tmV, BAR(C::B_VF + st), sub * 64,
                                     T.hkv, (T.kt0 + j) * BN, T.b);
                 }
                 if (!ok) break;
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                 };
                 auto issue_pv = [&](int i, int j, bool first) {
                     const int st = (gv + j) % C::NSV;
-                    const uint64_t vd = sdesc_sw128(sb + C::OFF_V + st * C::KV_BYTES, C::SUB, 1024);
+                    const uint64_t vd = sdesc_sw128(sb + C::OFF_V + st * C::V_BYTES, C::SUB, 1024);
                     const uint32_t t_p = tmem + i * BN, t_o = tmem + NQ * BN + i * 128;
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
@@ -657,7 +659,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                 // S(j) is complete, so every earlier P V has been added to O
                 const float f = o_resc ? fac : 1.f;
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = 0; cc < DV / 32; ++cc) {
                     uint32_t r[32];
                     tmem_ld32(tO + cc * 32, r);
 #pragma unroll
@@ -704,7 +706,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                     __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.os[0] +
                                        static_cast<int64_t>(qc) * P.os[1] + T.h * P.os[2];
     #pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                    for (int cc = 0; cc < DV / 32; ++cc) {
                         uint32_t r[32];
                         tmem_ld32(tO + cc * 32, r);
                         if (q < P.S) {
@@ -734,9 +736,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                     const float mn = fmaxf(mc, m_nat);
                     const float fa = mc == -INFINITY ? 0.f : ex2((mc - mn) * kLog2e);
                     const float fb = m_nat == -INFINITY ? 0.f : ex2((m_nat - mn) * kLog2e) * rel;
-                    float* Cr = a.acc + ((static_cast<int64_t>(T.b) * P.S + qc) * P.Hq + T.h) * D;
+                    float* Cr = a.acc + ((static_cast<int64_t>(T.b) * P.S + qc) * P.Hq + T.h) * DV;
     #pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                    for (int cc = 0; cc < DV / 32; ++cc) {
                         uint32_t r[32];
                         tmem_ld32(tO + cc * 32, r);
                         if (q < P.S && mn != -INFINITY) {
@@ -761,7 +763,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
                 // no key allowed for this tile: O = 0, m = -inf, l = 0
                 __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.os[0] +
                                    static_cast<int64_t>(q) * P.os[1] + T.h * P.os[2];
-                for (int cc = 0; cc < D; cc += 8) *reinterpret_cast<uint4*>(O + cc) = make_uint4(0, 0, 0, 0);
+                for (int cc = 0; cc < DV; cc += 8) *reinterpret_cast<uint4*>(O + cc) = make_uint4(0, 0, 0, 0);
                 a.m[mi] = -INFINITY;
                 a.l[mi] = 0.f;
             }
@@ -786,15 +788,15 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, NQ == 1 ? 2 : 1)
     }
 }
 
-template <int D, int NQ>
+template <int D, int DV, int NQ>
 cudaError_t launch(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
-    using C = FwdCfg<D, NQ>;
+    using C = FwdCfg<D, DV, NQ>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(k_fwd_tc<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        e = cudaFuncSetAttribute(k_fwd_tc<D, DV, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
@@ -809,7 +811,7 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
     const int nqp = (a.P.S + NQ * BM - 1) / (NQ * BM);
     const int64_t items = static_cast<int64_t>(nqp) * a.P.Hq * a.P.B;
     const int grid = static_cast<int>(std::min<int64_t>(items, static_cast<int64_t>(sms) * (NQ == 1 ? 2 : 1)));
-    k_fwd_tc<D, NQ><<<grid, C::kThreads, C::SMEM, s>>>(maps[0], maps[1], maps[2], a);
+    k_fwd_tc<D, DV, NQ><<<grid, C::kThreads, C::SMEM, s>>>(maps[0], maps[1], maps[2], a);
     return cudaGetLastError();
 }
 
@@ -823,7 +825,8 @@ int key_tiles_per_query_tile(const Problem& P) {
 }  // namespace
 
 bool fwd_tc_supported(const Problem& P) {
-    if (P.dtype != BPA_BF16 || (P.d != 64 && P.d != 128) || P.dv != P.d || P.block_idx) return false;
+    if (P.dtype != BPA_BF16 || (P.d != 64 && P.d != 128) || P.block_idx) return false;
+    if (P.dv != P.d && !(P.d == 128 && P.dv == 64)) return false;
     if (P.ring_n > 1 && P.ring_blk % BM) return false;
     return true;
 }
@@ -832,8 +835,9 @@ cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap* maps, cudaStream_
     const Problem& P = a.P;
     // short key ranges: single-tile CTAs, two per SM; a ring block must hold whole CTAs
     const bool single = key_tiles_per_query_tile(P) <= 4 || P.S <= BM || (P.ring_n > 1 && P.ring_blk % (2 * BM));
-    if (P.d == 128) return single ? launch<128, 1>(a, maps, s) : launch<128, 2>(a, maps, s);
-    return single ? launch<64, 1>(a, maps, s) : launch<64, 2>(a, maps, s);
+    if (P.d == 128 && P.dv == 64) return single ? launch<128, 64, 1>(a, maps, s) : launch<128, 64, 2>(a, maps, s);
+    if (P.d == 128) return single ? launch<128, 128, 1>(a, maps, s) : launch<128, 128, 2>(a, maps, s);
+    return single ? launch<64, 64, 1>(a, maps, s) : launch<64, 64, 2>(a, maps, s);
 }
 
 }  // namespace bpa

@@ -145,3 +145,31 @@ def test_mla_workload_reduced(bpa, ora):
     assert rel_l2(host(dq), rq) <= BF16_GRAD_REL_L2
     assert rel_l2(host(dk), rk) <= BF16_GRAD_REL_L2
     assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
+
+
+@pytest.mark.slow
+def test_mla_workload_full_size_sampled(bpa, ora):
+    # full size (B 2, S 4096, Hq 128, Hkv 8, d_qk 128, d_v 64, causal): sampled query rows
+    # (O, m, l, dQ) and sampled keys (dK, dV) against the oracle
+    w = W.MLA_CAUSAL
+    q, k, v, do, bias = W.make_inputs(w)
+    o, m, l, (dq, dk, dv) = _run(bpa, w, q, k, v, do, bias)
+    assert tuple(o.shape) == (w.B, w.S, w.Hq, 64) and tuple(dv.shape) == (w.B, w.S, w.Hkv, 64)
+    rng = np.random.default_rng(2027)
+    qs = sorted({0, 1, 127, 128, 129, w.S - 1} | set(rng.integers(0, w.S, 60).tolist()))
+    rows = [(int(rng.integers(0, w.B)), int(rng.integers(0, w.Hq)), qq) for qq in qs]
+    ro, rm, rl, rdq = ora.rows(q, k, v, do, rows, causal=True)
+    ho, hdq = o.cpu(), dq.cpu()
+    go = np.stack([ho[b, s, h].float().numpy() for b, h, s in rows])
+    gdq = np.stack([hdq[b, s, h].float().numpy() for b, h, s in rows])
+    assert max_abs(go, ro) <= BF16_O_MAX_ABS
+    gm = np.array([m[b, h, s].item() for b, h, s in rows])
+    gl = np.array([l[b, h, s].item() for b, h, s in rows])
+    assert np.max(np.abs(gm - rm) / (1 + np.abs(rm))) <= 1e-3
+    assert np.max(np.abs(gl - rl) / np.abs(rl)) <= 1e-3
+    assert rel_l2(gdq, rdq) <= BF16_GRAD_REL_L2
+    keys = sorted({0, 1, 127, 128, w.S - 1} | set(rng.integers(0, w.S, 20).tolist()))
+    b, g = 1, 5
+    rdk, rdv = ora.keys(q, k, v, do, b, g, keys, causal=True)
+    assert rel_l2(dk[b, keys, g].float().cpu().numpy(), rdk) <= BF16_GRAD_REL_L2
+    assert rel_l2(dv[b, keys, g].float().cpu().numpy(), rdv) <= BF16_GRAD_REL_L2
