@@ -328,6 +328,41 @@ def test_gradients_match_finite_differences(ora, cfg):
         assert err < 1e-6, f"d{name}: relative error {err}"
 
 
+def test_block_selected_gradients_match_finite_differences(ora):
+    """Backward of block-selected attention (AnnAttention, faiss_block_attention, trained
+    through): the selection is discrete and held fixed, so the gradients are those of
+    attention under the union mask.  Checked against central differences of <dO, O>
+    with O from the brute-force loop above, not from the oracle's forward."""
+    B, S, Hq, Hkv, d, dv, bs, n, W = 1, 16, 2, 1, 3, 2, 4, 2, 3
+    q, k, v, do = (rnd((B, S, Hq, d), 151), rnd((B, S, Hkv, d), 152), rnd((B, S, Hkv, dv), 153),
+                   rnd((B, S, Hq, dv), 154))
+    # per query block: earlier blocks, -1 padding, and the block just before the query's
+    # (which overlaps the local window: union, counted once)
+    idx = np.array([[[[-1, -1], [0, -1], [0, 1], [2, 0]],
+                     [[-1, -1], [-1, -1], [1, -1], [1, 2]]]], dtype=np.int32)
+    kw = dict(causal=True, block_idx=idx, sel_block=bs, local_window=W, scale=0.7)
+    dq, dk, dvv, *_ = ora.attention_bwd(q, k, v, do, top_n=n, **kw)
+    h = 1e-6
+
+    def loss(qq, kk, vv):
+        return float((brute_force(qq, kk, vv, **kw)[0] * do).sum())
+
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dvv)):
+        fd = np.zeros_like(x)
+        for ix in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[ix] += h
+            xm[ix] -= h
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            fd[ix] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        err = np.abs(fd - g).max() / max(np.abs(g).max(), 1e-30)
+        assert err < 1e-6, f"d{name}: relative error {err}"
+    # keys of block 3 are selected by no query and lie in no local window but their own
+    # block's: their gradients come from block 3's queries alone
+    assert np.abs(dk[0, 12:]).max() > 0
+
+
 # --------------------------------------------------------------------------
 # sampled rows / keys agree with the full evaluation
 # --------------------------------------------------------------------------
