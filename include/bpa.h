@@ -94,7 +94,7 @@ typedef struct bpa_attn_desc {
     int32_t ring_step_begin;   /* first ring step of this call, 0 <= begin < end */
     int32_t ring_step_end;     /* one past the last step; 0 selects ring_size */
     const int32_t* block_idx;  /* block-selected mode: [B, Hq, S/sel_block, top_n] from */
-    int32_t sel_block;         /*   bpa_select_blocks (-1 entries are ignored); forward only */
+    int32_t sel_block;         /*   bpa_select_blocks (-1 entries are ignored) */
     int32_t top_n;
     int32_t local_window;      /* keys q - local_window + 1 .. q are always allowed */
     /* Fields below were added in descriptor version 2 (bpa_version() >= 2).  A caller
@@ -111,8 +111,9 @@ typedef struct bpa_attn_desc {
  * Forward: a status header, plus, when ring_size > 1, the float32 running
  * numerator [B, S, Hq, dv].  Backward: the header, D = rowsum(dO * O) and
  * the log-sum-exp [B, Hq, S'] (S' = S rounded up to 64), the float32 dQ
- * accumulator [B, Hq, S', d], plus, when ring_size > 1, float32 dK and dV
- * carries [B, S, Hkv, d] and [B, S, Hkv, dv]. */
+ * accumulator [B, Hq, S', d], plus, when ring_size > 1 or in block-selected
+ * mode, float32 dK and dV carries / accumulators [B, S, Hkv, d] and
+ * [B, S, Hkv, dv]. */
 size_t bpa_workspace_size(int32_t op, const bpa_attn_desc* desc);
 
 /* Forward pass.
@@ -144,7 +145,10 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l,
  * one call (ring_step_begin / ring_step_end must select the whole sweep).
  * dq, dk, dv have the dtype of the inputs and the strides of q, k, v; o and
  * dout are [B, S, Hq, dv] with o_strides.
- * Block-selected mode is not supported (BPA_ERR_UNSUPPORTED). */
+ * Block-selected mode (ring_size 1) is supported: the selection is held
+ * fixed ("AnnAttention", faiss_block_attention.py, which trains through the
+ * gathered attention; no gradient reaches the indices), so the gradients are
+ * those of attention under the union mask of the forward pass. */
 bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout,
                    const float* m, const float* l, void* dq, void* dk, void* dv,
                    void* workspace, size_t workspace_bytes, void* stream);

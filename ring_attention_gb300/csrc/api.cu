@@ -157,8 +157,10 @@ BwdLayout bwd_layout(const Problem& P) {
     const size_t nk = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.d;
     const size_t nv = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.dv;
     L.dk = L.dq + round256(nq);
-    L.dv = L.dk + (P.ring_n > 1 ? round256(nk) : 0);
-    L.total = L.dv + (P.ring_n > 1 ? round256(nv) : 0);
+    // float32 dK / dV: the ring's travelling carries, or the block-selected backward's accumulators
+    const bool kv_acc = P.ring_n > 1 || P.block_idx;
+    L.dv = L.dk + (kv_acc ? round256(nk) : 0);
+    L.total = L.dv + (kv_acc ? round256(nv) : 0);
     return L;
 }
 
@@ -331,7 +333,6 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
     if (st != BPA_OK) return st;
     if (!o || !dout || !m || !l || !dq || !dk || !dv)
         return fail(BPA_ERR_INVALID_ARG, "o, dout, m, l, dq, dk or dv is NULL");
-    if (P.block_idx) return fail(BPA_ERR_UNSUPPORTED, "backward of block-selected attention");
     const int n = P.ring_n;
     const int begin = desc->ring_step_begin, end = desc->ring_step_end ? desc->ring_step_end : n;
     if (begin != 0 || end != n)
@@ -360,8 +361,26 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
     a.Spad = L.Spad;
     a.status = reinterpret_cast<uint32_t*>(ws);
 
-    bool tc = bwd_tc_supported(P) && tma_layout_ok(P) && aligned16(o) && aligned16(dout) && aligned16(dq) &&
-              aligned16(dk) && aligned16(dv);
+    if (P.block_idx && gather_supported(P) && aligned16(dout) && aligned16(dq) && aligned16(dk) && aligned16(dv)) {
+        // gathered backward: dQ written per query block, dK / dV reduced into float32 accumulators
+        a.dk_acc = reinterpret_cast<float*>(ws + L.dk);
+        a.dv_acc = reinterpret_cast<float*>(ws + L.dv);
+        if ((e = launch_bwd_pre(a, s)) != cudaSuccess) return cuda_fail(e, "backward pre-pass");
+        marks.mark(1, s);
+        const size_t nk = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.d;
+        const size_t nv = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.dv;
+        if ((e = cudaMemsetAsync(a.dk_acc, 0, nk, s)) != cudaSuccess ||
+            (e = cudaMemsetAsync(a.dv_acc, 0, nv, s)) != cudaSuccess)
+            return cuda_fail(e, "clearing the dK / dV accumulators");
+        if ((e = launch_gather_bwd(a, s)) != cudaSuccess) return cuda_fail(e, "block-selected backward launch");
+        marks.mark(2, s);
+        e = launch_cast_dkdv(a, s);
+        marks.mark(3, s);
+        return e == cudaSuccess ? BPA_OK : cuda_fail(e, "dK / dV cast");
+    }
+    // other block-selected problems run on the CUDA-core kernels, which visit only the selected blocks
+    bool tc = !P.block_idx && bwd_tc_supported(P) && tma_layout_ok(P) && aligned16(o) && aligned16(dout) &&
+              aligned16(dq) && aligned16(dk) && aligned16(dv);
     CUtensorMap maps[4];
     if (tc) {
         tc = make_map(&maps[0], P.q, P.d, P.Hq, P.S, P.B, P.qs, 64) &&

@@ -310,6 +310,21 @@ cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;   // the tensor-core backward always meets the vector conditions
 }
 
+cudaError_t launch_cast_dkdv(const BwdArgs& a, cudaStream_t s) {
+    const Problem& P = a.P;
+    const int64_t nk = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.d;
+    const int64_t nv = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.dv;
+    const bool vec_ok = P.dtype == BPA_BF16 && P.d % 8 == 0 && P.dv % 8 == 0 &&
+                        ((reinterpret_cast<uintptr_t>(a.dk) | reinterpret_cast<uintptr_t>(a.dv)) & 15u) == 0 &&
+                        ((P.ks[0] | P.ks[1] | P.ks[2] | P.vs[0] | P.vs[1] | P.vs[2]) & 7) == 0;
+    if (!vec_ok) return cudaErrorInvalidValue;
+    k_cast_out_bf16v<<<grid_for(nk / 8, 256), 256, 0, s>>>(a.dk_acc, static_cast<__nv_bfloat16*>(a.dk), P.B, P.S,
+                                                           P.Hkv, P.d, P.ks[0], P.ks[1], P.ks[2]);
+    k_cast_out_bf16v<<<grid_for(nv / 8, 256), 256, 0, s>>>(a.dv_acc, static_cast<__nv_bfloat16*>(a.dv), P.B, P.S,
+                                                           P.Hkv, P.dv, P.vs[0], P.vs[1], P.vs[2]);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {
     k_wait_selftest<<<1, 32, 0, s>>>(status, limit_ns);
     return cudaGetLastError();

@@ -52,7 +52,7 @@ struct BwdArgs {
     float* lse;         // [B, Hq, Spad] m + log(l) (natural log); +inf on padding / empty rows
     int Spad;           // S rounded up to 64
     float* dq_acc;      // [B, Hq, Spad / 4, d, 4] float32 (four consecutive queries of a channel together)
-    float* dk_acc;      // ring carries [B, S, Hkv, d] float32, or nullptr
+    float* dk_acc;      // ring carries / block-selected accumulators [B, S, Hkv, d] float32, or nullptr
     float* dv_acc;
     int ring_idx;
     uint32_t* status;
@@ -76,6 +76,8 @@ cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s);
 cudaError_t launch_bwd_tc(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s);
 cudaError_t launch_gather_fwd(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_gather_bwd(const BwdArgs& a, cudaStream_t s);   // needs dk_acc / dv_acc cleared
+cudaError_t launch_cast_dkdv(const BwdArgs& a, cudaStream_t s);    // dk_acc / dv_acc -> dk / dv (bf16)
 cudaError_t launch_ring_init(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_ring_finalize(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t s);

@@ -128,6 +128,10 @@ BPA_DEV void bulk_reduce_add_f32(float* dst, uint32_t src, uint32_t bytes) {
                  : "memory");
 }
 // dst[0..3] += (x, y, z, w) in global memory (16-byte aligned), no return value.
+BPA_DEV void red_add_v2(float* dst, float x, float y) {
+    asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(reinterpret_cast<uint64_t>(dst)), "f"(x), "f"(y)
+                 : "memory");
+}
 BPA_DEV void red_add_v4(float* dst, float x, float y, float z, float w) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(reinterpret_cast<uint64_t>(dst)), "f"(x),
                  "f"(y), "f"(z), "f"(w)
@@ -366,6 +370,10 @@ BPA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uin
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+BPA_DEV void st_shared_u32(uint32_t addr, uint32_t a) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
 }
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a

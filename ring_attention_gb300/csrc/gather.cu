@@ -59,6 +59,41 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// mma.sync m16n8k16 fragment layouts (g = lane / 4, t = lane % 4):
+//   A 16x16 row-major:  a0 (row g, k 2t..2t+1), a1 (row g+8, k 2t..), a2 (row g, k 2t+8..), a3 (row g+8, k 2t+8..)
+//   B 16x8:             b0 (k 2t..2t+1, col g), b1 (k 2t+8..2t+9, col g)
+//   C 16x8 float:       c0, c1 (row g, cols 2t, 2t+1), c2, c3 (row g+8, cols 2t, 2t+1)
+// ldmatrix gives lane i row i/4, elements 2(i%4), 2(i%4)+1 of each 8x8 matrix (.trans: the
+// transpose), so row-major tiles load as A or K-major B fragments and column-major ones
+// with .trans.
+
+// The distinct key blocks query block i visits, ascending: the blocks its local window
+// touches and its selected blocks (entries outside [0, i] are ignored).  Run by one lane.
+__device__ int visit_list(const Problem& P, int64_t unit, int i, int* list) {
+    int n = 0;
+    const int32_t* sel = P.block_idx + unit * P.top_n;
+    const int wfirst = max(0, (BS * i - (P.local_window - 1))) / BS;
+    auto add = [&](int kb) {
+        if (kb < 0 || kb > i) return;
+        for (int x = 0; x < n; ++x)
+            if (list[x] == kb) return;
+        if (n < kMaxList) list[n++] = kb;
+    };
+    if (P.local_window > 0)
+        for (int kb = wfirst; kb <= i; ++kb) add(kb);
+    for (int x = 0; x < P.top_n; ++x) add(sel[x]);
+    for (int x = 1; x < n; ++x) {   // ascending
+        const int key = list[x];
+        int y = x - 1;
+        while (y >= 0 && list[y] > key) {
+            list[y + 1] = list[y];
+            --y;
+        }
+        list[y + 1] = key;
+    }
+    return n;
+}
+
 __global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
     const Problem& P = a.P;
     __shared__ WarpSmem sm[kWarps];
@@ -76,30 +111,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
     const uint32_t sk = smem_u32(S.k), sv = smem_u32(S.v);
 
     // ---- key blocks to visit: selected blocks and the blocks the local window touches
-    if (lane == 0) {
-        int n = 0;
-        const int32_t* sel = P.block_idx + (static_cast<int64_t>(unit)) * P.top_n;
-        const int wfirst = max(0, (BS * i - (P.local_window - 1))) / BS;
-        auto add = [&](int kb) {
-            if (kb < 0 || kb > i) return;
-            for (int x = 0; x < n; ++x)
-                if (S.list[x] == kb) return;
-            if (n < kMaxList) S.list[n++] = kb;
-        };
-        if (P.local_window > 0)
-            for (int kb = wfirst; kb <= i; ++kb) add(kb);
-        for (int x = 0; x < P.top_n; ++x) add(sel[x]);
-        for (int x = 1; x < n; ++x) {   // ascending
-            const int key = S.list[x];
-            int y = x - 1;
-            while (y >= 0 && S.list[y] > key) {
-                S.list[y + 1] = S.list[y];
-                --y;
-            }
-            S.list[y + 1] = key;
-        }
-        S.n = n;
-    }
+    if (lane == 0) S.n = visit_list(P, unit, i, S.list);
     __syncwarp();
     const int nlist = S.n;
 
@@ -273,6 +285,268 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
         }
 }
 
+
+// ---- backward -------------------------------------------------------------------------
+// Same unit of work and visiting order as the forward.  Per key block kb of the list:
+//   S = Q K^T, P = exp(s S - LSE) under the forward's mask, dP = dO V^T, dS = P (dP - D),
+//   dQ += dS K                       (registers; written once, scaled, at the end),
+//   dV[kb] += P^T dO, dK[kb] += s dS^T Q   (float32 accumulators, vector reductions: a key
+//                                          block is shared by every query block that
+//                                          selected it and by its local windows).
+// "AnnAttention", faiss_block_attention.py trains through the gathered attention with the
+// selection held fixed; the gradients are those of "bpt.py", _blockwise_attention_bwd
+// restricted to the visited blocks.
+constexpr int kWarpsB = 2;   // query blocks per CTA (static shared memory < 48 KB)
+
+struct __align__(128) WarpSmemB {
+    __nv_bfloat16 k[BS * D];      // [key][ch], 128-byte rows, swz()
+    __nv_bfloat16 v[BS * D];
+    __nv_bfloat16 q[BS * D];      // [query][ch] of the warp's query block
+    __nv_bfloat16 dout[BS * D];
+    __nv_bfloat16 p[BS * BS];     // P and dS of the current key block: [query][key], 64-byte rows, swz32()
+    __nv_bfloat16 ds[BS * BS];
+    int list[kMaxList];
+    int n;
+};
+
+__device__ __forceinline__ uint32_t swz32(int row, int chunk) {   // byte offset in a [32][64 B] tile
+    return static_cast<uint32_t>(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
+// Copies 32 rows x 64 bf16 channels (row stride rs elements) into a swizzled tile.
+__device__ __forceinline__ void stage_rows(uint32_t dst, const __nv_bfloat16* src, int64_t rs, int lane) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int idx = u * 32 + lane, row = idx >> 3, chunk = idx & 7;
+        const uint4 x = *reinterpret_cast<const uint4*>(src + row * rs + chunk * 8);
+        st_shared_v4(dst + swz(row, chunk), x.x, x.y, x.z, x.w);
+    }
+}
+
+// acc (32 rows x 64 channels, C fragments) = X^T Y, X a swizzled [query][row] 32 x 32 tile,
+// Y a swizzled [query][ch] 32 x 64 tile: rows of the result are X's columns (keys).
+__device__ __forceinline__ void tn_product(float (&acc)[2][8][4], uint32_t x, uint32_t y, int lane) {
+    const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {   // 16 queries per k step
+        uint32_t xa[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            // A = X^T (keys x queries) from [query][key] storage by .trans:
+            // matrix mi holds keys mt*16 + (mi & 1) * 8 + 0..7, queries kk*16 + (mi >> 1) * 8 + 0..7
+            const int row = kk * 16 + (mi >> 1) * 8 + rr, chunk = mt * 2 + (mi & 1);
+            ldsm_x4_t(x + swz32(row, chunk), xa[mt][0], xa[mt][1], xa[mt][2], xa[mt][3]);
+        }
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+            // B = Y (queries x channels) from [query][ch] storage by .trans, two channel n-tiles
+            const int row = kk * 16 + (mi & 1) * 8 + rr, chunk = np * 2 + (mi >> 1);
+            uint32_t b00, b01, b10, b11;
+            ldsm_x4_t(y + swz(row, chunk), b00, b01, b10, b11);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                mma16816(acc[mt][np * 2 + 0], xa[mt], b00, b01);
+                mma16816(acc[mt][np * 2 + 1], xa[mt], b10, b11);
+            }
+        }
+    }
+}
+
+// S (32 x 32, C fragments) = A B^T with A a swizzled [row][ch] 32 x 64 tile (queries) and B
+// one of the same shape (keys): A fragments by ldmatrix, B fragments straight from B's rows.
+__device__ __forceinline__ void nt_product(float (&s)[2][4][4], uint32_t a, uint32_t b, int lane) {
+    const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) s[mt][nt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+        uint32_t fa[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            // matrix mi: rows mt*16 + (mi & 1) * 8 + 0..7, channels ks*16 + (mi >> 1) * 8 + 0..7
+            const int row = mt * 16 + (mi & 1) * 8 + rr, chunk = ks * 2 + (mi >> 1);
+            ldsm_x4(a + swz(row, chunk), fa[mt][0], fa[mt][1], fa[mt][2], fa[mt][3]);
+        }
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+            const int row = np * 16 + (mi >> 1) * 8 + rr, chunk = ks * 2 + (mi & 1);
+            uint32_t b00, b01, b10, b11;
+            ldsm_x4(b + swz(row, chunk), b00, b01, b10, b11);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                mma16816(s[mt][np * 2 + 0], fa[mt], b00, b01);
+                mma16816(s[mt][np * 2 + 1], fa[mt], b10, b11);
+            }
+        }
+    }
+}
+
+// Writes a 32 x 32 C-fragment tile as bf16 into a swizzled [query][key] tile.
+__device__ __forceinline__ void store_tile32(uint32_t dst, const float (&s)[2][4][4], int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int row = mt * 16 + g + hh * 8;
+                st_shared_u32(dst + swz32(row, nt) + 4 * t, pack_bf16(s[mt][nt][hh * 2], s[mt][nt][hh * 2 + 1]));
+            }
+}
+
+// Adds a 32 x 64 C-fragment tile (times mul) to rows key0.. of a float32 [B, S, Hkv, 64] accumulator.
+__device__ __forceinline__ void reduce_rows(float* acc_row0, int64_t row_stride, const float (&x)[2][8][4], float mul,
+                                            int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float* row = acc_row0 + (mt * 16 + g + hh * 8) * row_stride + 2 * t;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) red_add_v2(row + nt * 8, x[mt][nt][hh * 2] * mul, x[mt][nt][hh * 2 + 1] * mul);
+        }
+}
+
+__global__ void __launch_bounds__(kWarpsB * 32) k_gather_bwd(const BwdArgs a) {
+    const Problem& P = a.P;
+    __shared__ WarpSmemB sm[kWarpsB];
+    static_assert(sizeof(WarpSmemB) % 128 == 0, "per-warp tiles must stay 16-byte aligned");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3, mi = lane >> 3, rr = lane & 7;
+    const int nblk = P.S / BS;
+    const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarpsB + warp;   // (b, h, i)
+    if (unit >= static_cast<int64_t>(P.B) * P.Hq * nblk) return;
+    const int i = static_cast<int>(unit % nblk);
+    const int h = static_cast<int>((unit / nblk) % P.Hq);
+    const int b = static_cast<int>(unit / (static_cast<int64_t>(nblk) * P.Hq));
+    const int hkv = h / P.G;
+    WarpSmemB& W = sm[warp];
+    const uint32_t sk = smem_u32(W.k), sv = smem_u32(W.v), sq = smem_u32(W.q), sdo = smem_u32(W.dout),
+                   sp = smem_u32(W.p), sds = smem_u32(W.ds);
+
+    if (lane == 0) W.n = visit_list(P, unit, i, W.list);
+    const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(P.q) + b * P.qs[0] + h * P.qs[2];
+    const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(a.dout) + b * P.os[0] + h * P.os[2];
+    stage_rows(sq, Q + static_cast<int64_t>(BS) * i * P.qs[1], P.qs[1], lane);
+    stage_rows(sdo, dO + static_cast<int64_t>(BS) * i * P.os[1], P.os[1], lane);
+    __syncwarp();
+    const int nlist = W.n;
+
+    // per-row statistics: rows mt*16 + g + hh*8 of the block
+    float lse2[2][2], Drow[2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int64_t r = (static_cast<int64_t>(b) * P.Hq + h) * a.Spad + BS * i + mt * 16 + g + hh * 8;
+            lse2[mt][hh] = a.lse[r] * kLog2e;   // +inf on rows with no allowed key: P = 0
+            Drow[mt][hh] = a.Dvec[r];
+        }
+    const float sl2 = P.scale * kLog2e;
+    float dq[2][8][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dq[mt][nt][e] = 0.f;
+
+    const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(P.k) + b * P.ks[0] + hkv * P.ks[2];
+    const __nv_bfloat16* V = static_cast<const __nv_bfloat16*>(P.v) + b * P.vs[0] + hkv * P.vs[2];
+    const int64_t acc_rs = static_cast<int64_t>(P.Hkv) * D;   // float32 accumulators [B, S, Hkv, 64]
+    float* dKacc = a.dk_acc + (static_cast<int64_t>(b) * P.S * P.Hkv + hkv) * D;
+    float* dVacc = a.dv_acc + (static_cast<int64_t>(b) * P.S * P.Hkv + hkv) * D;
+    const int32_t* selrow = P.block_idx + unit * P.top_n;
+
+    for (int x = 0; x < nlist; ++x) {
+        const int kb = W.list[x];
+        bool selected = false;
+        for (int y = 0; y < P.top_n; ++y) selected |= selrow[y] == kb;
+        __syncwarp();   // the previous block's reads of K, V and the P / dS tiles are done
+        stage_rows(sk, K + static_cast<int64_t>(BS) * kb * P.ks[1], P.ks[1], lane);
+        stage_rows(sv, V + static_cast<int64_t>(BS) * kb * P.vs[1], P.vs[1], lane);
+        __syncwarp();
+
+        float s[2][4][4], dp[2][4][4];
+        nt_product(s, sq, sk, lane);     // Q K^T
+        nt_product(dp, sdo, sv, lane);   // dO V^T
+        // P and dS under the forward's mask
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int q = BS * i + mt * 16 + g + hh * 8;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int k = BS * kb + nt * 8 + 2 * t + e;
+                        const bool ok = k <= q && (selected || k > q - P.local_window) &&
+                                        (!P.causal || k <= q) && (P.wl < 0 || k >= q - P.wl) &&
+                                        (P.wr < 0 || k <= q + P.wr);
+                        const float p = ok ? ex2(s[mt][nt][hh * 2 + e] * sl2 - lse2[mt][hh]) : 0.f;
+                        s[mt][nt][hh * 2 + e] = p;
+                        dp[mt][nt][hh * 2 + e] = p * (dp[mt][nt][hh * 2 + e] - Drow[mt][hh]);
+                    }
+            }
+        store_tile32(sp, s, lane);
+        store_tile32(sds, dp, lane);
+        __syncwarp();
+        // dQ += dS K: dS fragments from its [query][key] tile, K^T fragments by ldmatrix.trans
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            uint32_t da[2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const int row = mt * 16 + (mi & 1) * 8 + rr, chunk = kk * 2 + (mi >> 1);
+                ldsm_x4(sds + swz32(row, chunk), da[mt][0], da[mt][1], da[mt][2], da[mt][3]);
+            }
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                const int row = kk * 16 + (mi & 1) * 8 + rr, chunk = np * 2 + (mi >> 1);
+                uint32_t b00, b01, b10, b11;
+                ldsm_x4_t(sk + swz(row, chunk), b00, b01, b10, b11);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    mma16816(dq[mt][np * 2 + 0], da[mt], b00, b01);
+                    mma16816(dq[mt][np * 2 + 1], da[mt], b10, b11);
+                }
+            }
+        }
+        float acc[2][8][4];
+        // dV[kb] += P^T dO
+        tn_product(acc, sp, sdo, lane);
+        reduce_rows(dVacc + static_cast<int64_t>(BS) * kb * acc_rs, acc_rs, acc, 1.f, lane);
+        // dK[kb] += scale dS^T Q
+        tn_product(acc, sds, sq, lane);
+        reduce_rows(dKacc + static_cast<int64_t>(BS) * kb * acc_rs, acc_rs, acc, P.scale, lane);
+    }
+
+    // ---- dQ = scale * sum dS K, written once
+    __nv_bfloat16* dQ = static_cast<__nv_bfloat16*>(a.dq) + b * P.qs[0] + h * P.qs[2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            __nv_bfloat16* row = dQ + static_cast<int64_t>(BS * i + mt * 16 + g + hh * 8) * P.qs[1];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+                *reinterpret_cast<uint32_t*>(row + nt * 8 + 2 * t) =
+                    pack_bf16(dq[mt][nt][hh * 2 + 0] * P.scale, dq[mt][nt][hh * 2 + 1] * P.scale);
+        }
+}
 }  // namespace
 
 bool gather_supported(const Problem& P) {
@@ -286,6 +560,12 @@ bool gather_supported(const Problem& P) {
          P.os[2]) & 7)
         return false;
     return true;
+}
+
+cudaError_t launch_gather_bwd(const BwdArgs& a, cudaStream_t s) {
+    const int64_t units = static_cast<int64_t>(a.P.B) * a.P.Hq * (a.P.S / BS);
+    k_gather_bwd<<<static_cast<unsigned>((units + kWarpsB - 1) / kWarpsB), kWarpsB * 32, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gather_fwd(const FwdArgs& a, cudaStream_t s) {

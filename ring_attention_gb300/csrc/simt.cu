@@ -210,6 +210,43 @@ __global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
     }
 }
 
+// dQ contribution of the keys [klo, khi] to one query row (lane owns dims lane + 32 i):
+//   acc += sum_k P (dP - D) K_k   (the scale is applied by the caller)
+template <typename T>
+__device__ void dq_keys(const Problem& P, int b, int h, int g, int q, int klo, int khi, const float* sq,
+                        const float* sdo, float lse, float Dq, float* acc) {
+    const int lane = threadIdx.x & 31;
+    const T* K = static_cast<const T*>(P.k);
+    const T* V = static_cast<const T*>(P.v);
+    for (int k0 = klo; k0 <= khi; k0 += 32) {
+        const int k = k0 + lane;
+        float dS = 0.f;
+        if (k <= khi && allowed(P, b, h, q, k)) {
+            const T* kr = K + b * P.ks[0] + static_cast<int64_t>(k) * P.ks[1] + g * P.ks[2];
+            const T* vr = V + b * P.vs[0] + static_cast<int64_t>(k) * P.vs[1] + g * P.vs[2];
+            float dot = 0.f, dp = 0.f;
+#pragma unroll 8
+            for (int c = 0; c < P.d; ++c) dot = fmaf(sq[c], ldf(kr + c), dot);
+#pragma unroll 8
+            for (int c = 0; c < P.dv; ++c) dp = fmaf(sdo[c], ldf(vr + c), dp);
+            const float z = dot * P.scale + bias_at(P, b, h, q, k);
+            dS = expf(z - lse) * (dp - Dq);
+        }
+        const int nt = min(32, khi - k0 + 1);
+#pragma unroll 8
+        for (int t = 0; t < 32; ++t) {
+            const float st = __shfl_sync(0xffffffffu, dS, t);
+            if (t >= nt) continue;
+            const T* kr = K + b * P.ks[0] + static_cast<int64_t>(k0 + t) * P.ks[1] + g * P.ks[2];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int c = lane + 32 * i;
+                if (c < P.d) acc[i] = fmaf(st, ldf(kr + c), acc[i]);
+            }
+        }
+    }
+}
+
 // dQ of one query row per warp:  dQ = scale * sum_k P (dP - D) K_k
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
@@ -219,8 +256,6 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
     __shared__ float sq[kWarps][kMaxD];
     __shared__ float sdo[kWarps][kMaxD];
     const T* Q = static_cast<const T*>(P.q);
-    const T* K = static_cast<const T*>(P.k);
-    const T* V = static_cast<const T*>(P.v);
     const T* dO = static_cast<const T*>(a.dout);
     for (int r = warp; r < kRows; r += kWarps) {
         const int q = blockIdx.x * kRows + r;
@@ -239,32 +274,17 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
         if (P.causal) hi = min(hi, q);
         if (P.wr >= 0) hi = min(hi, q + P.wr);
         if (P.wl >= 0) lo = max(lo, q - P.wl);
-        if (lse != INFINITY) {
-            for (int k0 = lo; k0 <= hi; k0 += 32) {
-                const int k = k0 + lane;
-                float dS = 0.f;
-                if (k <= hi && allowed(P, b, h, q, k)) {
-                    const T* kr = K + b * P.ks[0] + static_cast<int64_t>(k) * P.ks[1] + g * P.ks[2];
-                    const T* vr = V + b * P.vs[0] + static_cast<int64_t>(k) * P.vs[1] + g * P.vs[2];
-                    float dot = 0.f, dp = 0.f;
-#pragma unroll 8
-                    for (int c = 0; c < P.d; ++c) dot = fmaf(sq[warp][c], ldf(kr + c), dot);
-#pragma unroll 8
-                    for (int c = 0; c < P.dv; ++c) dp = fmaf(sdo[warp][c], ldf(vr + c), dp);
-                    const float z = dot * P.scale + bias_at(P, b, h, q, k);
-                    dS = expf(z - lse) * (dp - Dq);
-                }
-                const int nt = min(32, hi - k0 + 1);
-#pragma unroll 8
-                for (int t = 0; t < 32; ++t) {
-                    const float st = __shfl_sync(0xffffffffu, dS, t);
-                    if (t >= nt) continue;
-                    const T* kr = K + b * P.ks[0] + static_cast<int64_t>(k0 + t) * P.ks[1] + g * P.ks[2];
-#pragma unroll
-                    for (int i = 0; i < kPer; ++i) {
-                        const int c = lane + 32 * i;
-                        if (c < P.d) acc[i] = fmaf(st, ldf(kr + c), acc[i]);
-                    }
+        if (lse != INFINITY && lo <= hi) {
+            if (!P.block_idx) {
+                dq_keys<T>(P, b, h, g, q, lo, hi, sq[warp], sdo[warp], lse, Dq, acc);
+            } else {
+                // the key blocks the forward visited: the local window's and the selected ones
+                for (int kb = lo / P.sel_block; kb <= hi / P.sel_block; ++kb) {
+                    const int k0 = max(lo, kb * P.sel_block);
+                    const int k1 = min(hi, kb * P.sel_block + P.sel_block - 1);
+                    const bool local = k1 > q - P.local_window && k0 <= q;
+                    if (!local && !selected(P, b, h, q, kb)) continue;
+                    dq_keys<T>(P, b, h, g, q, k0, k1, sq[warp], sdo[warp], lse, Dq, acc);
                 }
             }
         }
@@ -278,8 +298,58 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
     }
 }
 
+// dK, dV contributions of the queries [qlo, qhi] of q head h to one key row:
+//   dk += sum_q dS Q_q,   dv += sum_q P dO_q   (the scale on dk is applied by the caller)
+template <typename T>
+__device__ void dkdv_queries(const BwdArgs& a, int b, int h, int k, int qlo, int qhi, const float* sk,
+                             const float* sv, float* dk, float* dv) {
+    const Problem& P = a.P;
+    const int lane = threadIdx.x & 31;
+    const T* Q = static_cast<const T*>(P.q);
+    const T* dO = static_cast<const T*>(a.dout);
+    for (int q0 = qlo; q0 <= qhi; q0 += 32) {
+        const int q = q0 + lane;
+        float p = 0.f, dS = 0.f;
+        if (q <= qhi && allowed(P, b, h, q, k)) {
+            const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * a.Spad + q;
+            const float lse = a.lse[mi];
+            if (lse != INFINITY) {
+                const int64_t qoff = b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2];
+                const int64_t ooff = b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2];
+                float dot = 0.f, dp = 0.f;
+#pragma unroll 8
+                for (int c = 0; c < P.d; ++c) dot = fmaf(ldf(Q + qoff + c), sk[c], dot);
+#pragma unroll 8
+                for (int c = 0; c < P.dv; ++c) dp = fmaf(ldf(dO + ooff + c), sv[c], dp);
+                const float z = dot * P.scale + bias_at(P, b, h, q, k);
+                p = expf(z - lse);
+                dS = p * (dp - a.Dvec[mi]);
+            }
+        }
+        const int nt = min(32, qhi - q0 + 1);
+#pragma unroll 8
+        for (int t = 0; t < 32; ++t) {
+            const float pt = __shfl_sync(0xffffffffu, p, t);
+            const float st = __shfl_sync(0xffffffffu, dS, t);
+            if (t >= nt) continue;
+            const int64_t qoff = b * P.qs[0] + static_cast<int64_t>(q0 + t) * P.qs[1] + h * P.qs[2];
+            const int64_t ooff = b * P.os[0] + static_cast<int64_t>(q0 + t) * P.os[1] + h * P.os[2];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int c = lane + 32 * i;
+                if (c < P.d) dk[i] = fmaf(st, ldf(Q + qoff + c), dk[i]);
+                if (c < P.dv) dv[i] = fmaf(pt, ldf(dO + ooff + c), dv[i]);
+            }
+        }
+    }
+}
+
 // dK, dV of one key row per warp, summed over the q heads of its group:
 //   dK = scale * sum_q dS Q_q,   dV = sum_q P dO_q
+// In block-selected mode (AnnAttention, faiss_block_attention) a key is seen by the
+// queries whose local window holds it and by every query of the query blocks that
+// selected its block; the warp finds those query blocks 32 at a time with a ballot
+// (selection is per query block) and visits only them.
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) {
     const Problem& P = a.P;
@@ -287,10 +357,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ float sk[kWarps][kMaxD];
     __shared__ float sv[kWarps][kMaxD];
-    const T* Q = static_cast<const T*>(P.q);
     const T* K = static_cast<const T*>(P.k);
     const T* V = static_cast<const T*>(P.v);
-    const T* dO = static_cast<const T*>(a.dout);
     for (int r = warp; r < kRows; r += kWarps) {
         const int k = blockIdx.x * kRows + r;
         if (k >= P.S) break;
@@ -306,42 +374,26 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
         if (P.causal) lo = max(lo, k);
         if (P.wr >= 0) lo = max(lo, k - P.wr);
         if (P.wl >= 0) hi = min(hi, k + P.wl);
-        for (int h = g * P.G; h < (g + 1) * P.G; ++h) {
-            for (int q0 = lo; q0 <= hi; q0 += 32) {
-                const int q = q0 + lane;
-                float p = 0.f, dS = 0.f;
-                if (q <= hi && allowed(P, b, h, q, k)) {
-                    const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * a.Spad + q;
-                    const float lse = a.lse[mi];
-                    if (lse != INFINITY) {
-                        const int64_t qoff = b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] + h * P.qs[2];
-                        const int64_t ooff = b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2];
-                        float dot = 0.f, dp = 0.f;
-#pragma unroll 8
-                        for (int c = 0; c < P.d; ++c) dot = fmaf(ldf(Q + qoff + c), sk[warp][c], dot);
-#pragma unroll 8
-                        for (int c = 0; c < P.dv; ++c) dp = fmaf(ldf(dO + ooff + c), sv[warp][c], dp);
-                        const float z = dot * P.scale + bias_at(P, b, h, q, k);
-                        p = expf(z - lse);
-                        dS = p * (dp - a.Dvec[mi]);
-                    }
+        for (int h = g * P.G; h < (g + 1) * P.G && lo <= hi; ++h) {
+            if (!P.block_idx) {
+                dkdv_queries<T>(a, b, h, k, lo, hi, sk[warp], sv[warp], dk, dv);
+                continue;
+            }
+            const int sb = P.sel_block, kb = k / sb;
+            const int llo = max(lo, k), lhi = min(hi, k + P.local_window - 1);   // local-window queries
+            for (int qb0 = lo / sb; qb0 <= hi / sb; qb0 += 32) {
+                const int qb = qb0 + lane;
+                bool visit = false;
+                if (qb <= hi / sb) {
+                    const int q0 = qb * sb, q1 = q0 + sb - 1;
+                    visit = (q0 <= lhi && q1 >= llo) || selected(P, b, h, q0, kb);
                 }
-                const int nt = min(32, hi - q0 + 1);
-#pragma unroll 8
-                for (int t = 0; t < 32; ++t) {
-                    const float pt = __shfl_sync(0xffffffffu, p, t);
-                    const float st = __shfl_sync(0xffffffffu, dS, t);
-                    if (t >= nt) continue;
-                    const int64_t qoff =
-                        b * P.qs[0] + static_cast<int64_t>(q0 + t) * P.qs[1] + h * P.qs[2];
-                    const int64_t ooff =
-                        b * P.os[0] + static_cast<int64_t>(q0 + t) * P.os[1] + h * P.os[2];
-#pragma unroll
-                    for (int i = 0; i < kPer; ++i) {
-                        const int c = lane + 32 * i;
-                        if (c < P.d) dk[i] = fmaf(st, ldf(Q + qoff + c), dk[i]);
-                        if (c < P.dv) dv[i] = fmaf(pt, ldf(dO + ooff + c), dv[i]);
-                    }
+                unsigned todo = __ballot_sync(0xffffffffu, visit);
+                while (todo) {
+                    const int qv = qb0 + __ffs(todo) - 1;
+                    todo &= todo - 1;
+                    dkdv_queries<T>(a, b, h, k, max(lo, qv * sb), min(hi, qv * sb + sb - 1), sk[warp], sv[warp],
+                                    dk, dv);
                 }
             }
         }

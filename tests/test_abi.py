@@ -123,8 +123,8 @@ def test_backward_rejects_bad_arguments(bpa):
     p = 0x80000
     st = L.bpa_bwd(ctypes.byref(D), p, p, p, p, p, p, p, p, 1 << 30, None)
     assert st == bpa.BPA_ERR_INVALID_ARG
-    D = _desc(bpa, block_idx=0x1000, sel_block=32, top_n=8, local_window=32)
-    assert L.bpa_bwd(ctypes.byref(D), p, p, p, p, p, p, p, p, 1 << 30, None) == bpa.BPA_ERR_UNSUPPORTED
+    D = _desc(bpa, block_idx=0x1000, sel_block=32, top_n=8, local_window=32, ring_size=2)
+    assert L.bpa_bwd(ctypes.byref(D), p, p, p, p, p, p, p, p, 1 << 30, None) == bpa.BPA_ERR_INVALID_ARG
     D = _desc(bpa)
     assert L.bpa_bwd(ctypes.byref(D), p, 0, p, p, p, p, p, p, 1 << 30, None) == bpa.BPA_ERR_INVALID_ARG
 

@@ -207,6 +207,88 @@ def test_block_selected_attention(bpa, ora):
     check_stats(m, l, om, ol)
 
 
+def _planted_selection(B, H, S, bs, n, seed):
+    """Valid block indices without running a selection: per query block up to n distinct
+    strictly earlier blocks, ascending, padded with -1 (the layout bpa_select_blocks writes)."""
+    rng = np.random.default_rng(seed)
+    idx = np.full((B, H, S // bs, n), -1, dtype=np.int32)
+    for b in range(B):
+        for h in range(H):
+            for i in range(S // bs):
+                pick = np.sort(rng.permutation(i)[:rng.integers(0, n + 1)])
+                idx[b, h, i, :len(pick)] = pick
+    return idx
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_block_selected_backward(bpa, ora, dtype):
+    # gradients through the gathered attention with the selection held fixed
+    B, S, H, d, bs, n = 2, 512, 2, 64, 32, 4
+    q, k, v, do = draw([(B, S, H, d)] * 4, 62, dtype)
+    tq, tk, tv = dev(q), dev(k), dev(v)
+    idx = bpa.bpa_select_blocks(tq, tk, block_size=bs, top_n=n)
+    kw = dict(causal=True, sel_block=bs, top_n=n, local_window=32)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, block_idx=idx, **kw)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, dev(do), m, l, block_idx=idx, **kw)
+    torch.cuda.synchronize()
+    ridx = ora.select_blocks(q, k, block_size=bs, top_n=n)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, block_idx=ridx, **kw)
+    check_stats(m, l, rm, rl)
+    if dtype == "f32":
+        for got, ref in ((o, ro), (dq, rq), (dk, rk), (dv, rv)):
+            assert max_abs(host(got), ref) <= FP32_MAX_ABS
+    else:
+        for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+            assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2
+
+
+@pytest.mark.parametrize("geom", [(336, 16, 3, 20), (320, 32, 8, 0), (320, 64, 2, 100)],
+                         ids=lambda g: "S%d_bs%d_n%d_w%d" % g)
+def test_block_selected_backward_planted(bpa, ora, geom):
+    # GQA, a per-key bias, a separate value head dim, a sequence that ends inside a
+    # chunk of 32 rows (S = 336), local windows narrower and wider than a block (and
+    # none), and query blocks that select nothing
+    S, bs, n, lw = geom
+    B, Hq, Hkv, d, dv = 1, 4, 2, 64, 32
+    q, k, v, do = draw([(B, S, Hq, d), (B, S, Hkv, d), (B, S, Hkv, dv), (B, S, Hq, dv)], 63 + bs, "bf16")
+    bias = _bias("keys", B, Hq, S, 7)
+    idx = _planted_selection(B, Hq, S, bs, n, 64 + bs)
+    kw = dict(causal=True, sel_block=bs, top_n=n, local_window=lw)
+    tq, tk, tv, tb, ti = dev(q), dev(k), dev(v), dev(bias), torch.from_numpy(idx).cuda()
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, bias=tb, block_idx=ti, **kw)
+    dq, dk, dvv = bpa.bpa_bwd(tq, tk, tv, o, dev(do), m, l, bias=tb, block_idx=ti, **kw)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, bias=bias, block_idx=idx, **kw)
+    assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+    check_stats(m, l, rm, rl)
+    for got, ref in ((dq, rq), (dk, rk), (dvv, rv)):
+        assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2
+
+
+@pytest.mark.parametrize("lw", [0, 20, 64])
+def test_block_selected_backward_gathered(bpa, ora, lw):
+    # the shapes the gathered kernels take (bf16, d = d_v = 64, 32-row blocks, no bias):
+    # GQA, planted selections with -1 padding and blocks shared by many query blocks,
+    # local windows of none, part of a block and two blocks
+    B, S, Hq, Hkv, d, bs, n = 2, 384, 4, 2, 64, 32, 5
+    q, k, v, do = draw([(B, S, Hq, d), (B, S, Hkv, d), (B, S, Hkv, d), (B, S, Hq, d)], 65 + lw, "bf16")
+    idx = _planted_selection(B, Hq, S, bs, n, 66 + lw)
+    kw = dict(causal=True, sel_block=bs, top_n=n, local_window=lw)
+    tq, tk, tv, ti = dev(q), dev(k), dev(v), torch.from_numpy(idx).cuda()
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, block_idx=ti, **kw)
+    dq, dk, dvv = bpa.bpa_bwd(tq, tk, tv, o, dev(do), m, l, block_idx=ti, **kw)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, block_idx=idx, **kw)
+    assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+    check_stats(m, l, rm, rl)
+    for got, ref in ((dq, rq), (dk, rk), (dvv, rv)):
+        assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2
+    # rows with no allowed key (first query block without a local window) have zero dQ
+    if lw == 0:
+        assert float(dq[:, :bs].abs().max()) == 0.0
+
+
 def test_bounded_wait_reports_timeout(bpa):
     ws = bpa.workspace(256, "cuda")
     bpa.bpa_debug_wait_timeout(ws, 200_000_000)   # 0.2 s
