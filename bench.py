@@ -151,7 +151,7 @@ def time_extra_workloads(bpa, dev, peak_tf):
     Inputs are drawn on the device from seeded generators (timing only; the
     parity tests use the numpy recipe)."""
     import torch
-    from ring_attention_gb300.inputs import BLOCK_SEL, GQA_SWA, MLA_CAUSAL, RING_LONG, TINY_F32
+    from ring_attention_gb300.inputs import BLOCK_SEL, BLOCK_SEL_JOINT, GQA_SWA, MLA_CAUSAL, RING_LONG, TINY_F32
 
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     out = {}
@@ -212,41 +212,44 @@ def time_extra_workloads(bpa, dev, peak_tf):
     out[RING_LONG.name] = fwd_bwd(RING_LONG, 2, 1)
     out[MLA_CAUSAL.name] = fwd_bwd(MLA_CAUSAL, 10, 3)
 
-    w = BLOCK_SEL
-    q = rnd((w.B, w.S, w.Hq, w.d), torch.bfloat16, w.seed)
-    k = rnd((w.B, w.S, w.Hkv, w.d), torch.bfloat16, w.seed + 1)
-    v = rnd((w.B, w.S, w.Hkv, w.d), torch.bfloat16, w.seed + 2)
-    idx = bpa.bpa_select_blocks(q, k, block_size=w.sel_block, top_n=w.top_n)
-    kw = dict(causal=True, block_idx=idx, sel_block=w.sel_block, top_n=w.top_n, local_window=w.local_window)
-    do = rnd((w.B, w.S, w.Hq, w.d), torch.bfloat16, w.seed + 3)
-    o, m, l = bpa.bpa_fwd(q, k, v, **kw)
-    wsb = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_BWD, bpa.make_desc(q, k, v, **kw)), dev)
-    dq, dk, dv = bpa.bpa_bwd(q, k, v, o, do, m, l, workspace_buf=wsb, **kw)
-    ts, ta, tb = [], [], []
-    for it in range(23):
-        a, b, c, e = E(), E(), E(), E()
-        a.record()
-        bpa.bpa_select_blocks(q, k, block_size=w.sel_block, top_n=w.top_n, out=idx)
-        b.record()
-        bpa.bpa_fwd(q, k, v, o=o, m=m, l=l, **kw)
-        c.record()
-        bpa.bpa_bwd(q, k, v, o, do, m, l, dq=dq, dk=dk, dv=dv, workspace_buf=wsb, **kw)
-        e.record()
-        torch.cuda.synchronize()
-        if it >= 3:
-            ts.append(a.elapsed_time(b))
-            ta.append(b.elapsed_time(c))
-            tb.append(c.elapsed_time(e))
-    # algorithmic bytes: Q, K, V read once and O written once (the gathered re-reads come from L2);
-    # backward: Q, K, V, O, dO read, dQ, dK, dV written
-    qkvo = 2 * w.B * w.S * w.d * (2 * w.Hq + 2 * w.Hkv)
-    bwd_bytes = 2 * w.B * w.S * w.d * (4 * w.Hq + 4 * w.Hkv)
-    nb = (idx >= 0).sum().item()
-    out[w.name] = {"select_ms": statistics.mean(ts), "attention_ms": statistics.mean(ta),
-                   "attention_min_bytes_gbs": qkvo / statistics.mean(ta) / 1e6,
-                   "backward_ms": statistics.mean(tb),
-                   "backward_min_bytes_gbs": bwd_bytes / statistics.mean(tb) / 1e6,
-                   "selected_blocks": int(nb), "steps": 20}
+    def block_selected(w):
+        q = rnd((w.B, w.S, w.Hq, w.d), torch.bfloat16, w.seed)
+        k = rnd((w.B, w.S, w.Hkv, w.d), torch.bfloat16, w.seed + 1)
+        v = rnd((w.B, w.S, w.Hkv, w.d), torch.bfloat16, w.seed + 2)
+        idx = bpa.bpa_select_blocks(q, k, block_size=w.sel_block, top_n=w.top_n)
+        kw = dict(causal=True, block_idx=idx, sel_block=w.sel_block, top_n=w.top_n, local_window=w.local_window)
+        do = rnd((w.B, w.S, w.Hq, w.d), torch.bfloat16, w.seed + 3)
+        o, m, l = bpa.bpa_fwd(q, k, v, **kw)
+        wsb = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_BWD, bpa.make_desc(q, k, v, **kw)), dev)
+        dq, dk, dv = bpa.bpa_bwd(q, k, v, o, do, m, l, workspace_buf=wsb, **kw)
+        ts, ta, tb = [], [], []
+        for it in range(23):
+            a, b, c, e = E(), E(), E(), E()
+            a.record()
+            bpa.bpa_select_blocks(q, k, block_size=w.sel_block, top_n=w.top_n, out=idx)
+            b.record()
+            bpa.bpa_fwd(q, k, v, o=o, m=m, l=l, **kw)
+            c.record()
+            bpa.bpa_bwd(q, k, v, o, do, m, l, dq=dq, dk=dk, dv=dv, workspace_buf=wsb, **kw)
+            e.record()
+            torch.cuda.synchronize()
+            if it >= 3:
+                ts.append(a.elapsed_time(b))
+                ta.append(b.elapsed_time(c))
+                tb.append(c.elapsed_time(e))
+        # algorithmic bytes: Q, K, V read once and O written once (the gathered re-reads come from L2);
+        # backward: Q, K, V, O, dO read, dQ, dK, dV written
+        qkvo = 2 * w.B * w.S * w.d * (2 * w.Hq + 2 * w.Hkv)
+        bwd_bytes = 2 * w.B * w.S * w.d * (4 * w.Hq + 4 * w.Hkv)
+        nb = (idx >= 0).sum().item()
+        return {"select_ms": statistics.mean(ts), "attention_ms": statistics.mean(ta),
+                "attention_min_bytes_gbs": qkvo / statistics.mean(ta) / 1e6,
+                "backward_ms": statistics.mean(tb),
+                "backward_min_bytes_gbs": bwd_bytes / statistics.mean(tb) / 1e6,
+                "selected_blocks": int(nb), "steps": 20}
+
+    out[BLOCK_SEL.name] = block_selected(BLOCK_SEL)
+    out[BLOCK_SEL_JOINT.name] = block_selected(BLOCK_SEL_JOINT)
     return out
 
 

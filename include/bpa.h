@@ -75,7 +75,7 @@ typedef enum { BPA_OP_FWD = 0, BPA_OP_BWD = 1 } bpa_op;
 typedef struct bpa_attn_desc {
     uint32_t struct_size;      /* = sizeof(bpa_attn_desc) */
     int32_t dtype;             /* bpa_dtype of q, k, v, o, dout, dq, dk, dv */
-    int32_t B, S, Hq, Hkv, d;  /* Sq = Sk = S; Hq % Hkv == 0; 1 <= d <= 256 (head dim of q, k) */
+    int32_t B, S, Hq, Hkv, d;  /* Sq = Sk = S; Hq % Hkv == 0; 1 <= d <= 512 (head dim of q, k) */
     const void* q;             /* [B, S, Hq, d] */
     const void* k;             /* [B, S, Hkv, d] */
     const void* v;             /* [B, S, Hkv, dv] */
@@ -102,7 +102,7 @@ typedef struct bpa_attn_desc {
      * o_strides = q_strides.  Separate value head dims follow "JAX: Single-GPU Attention
      * with TransformerEngine", section 4 (DeepSeek-style MLA head dimensions: q, k with
      * head dim d, v and the output with head dim dv). */
-    int32_t dv;                /* head dim of v, o, dout and the dv gradient; 0 selects d; <= 256 */
+    int32_t dv;                /* head dim of v, o, dout and the dv gradient; 0 selects d; <= 512 */
     int64_t o_strides[3];      /* (b, s, h) strides of o and dout; all 0 selects q_strides */
 } bpa_attn_desc;
 
@@ -168,7 +168,7 @@ size_t bpa_select_workspace_size(int32_t B, int32_t S, int32_t H, int32_t d, int
  * with -1, to block_idx_out int32 [B, H, S/block_size, top_n].  Sums and
  * not means are compared; they rank identically.
  * q and k are [B, S, H, d] (dtype bpa_dtype) with (b, s, h) strides.
- * S % block_size == 0, 1 <= top_n <= 64, d <= 256. */
+ * S % block_size == 0, 1 <= top_n <= 64, d <= 512. */
 bpa_status bpa_select_blocks(const void* q, const void* k, int32_t dtype, int32_t B,
                              int32_t S, int32_t H, int32_t d, const int64_t q_strides[3],
                              const int64_t k_strides[3], int32_t block_size, int32_t top_n,

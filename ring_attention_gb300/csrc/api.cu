@@ -69,10 +69,10 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
         return fail(BPA_ERR_INVALID_ARG, "B, S, Hq, Hkv, d must be >= 1");
     if (d->Hq % d->Hkv)
         return fail(BPA_ERR_INVALID_ARG, "Hq (%d) must be a multiple of Hkv (%d)", d->Hq, d->Hkv);
-    if (d->d > 256) return fail(BPA_ERR_UNSUPPORTED, "head dim %d > 256", d->d);
+    if (d->d > 512) return fail(BPA_ERR_UNSUPPORTED, "head dim %d > 512", d->d);
     const int dv = v2 && d->dv ? d->dv : d->d;
     if (dv < 1) return fail(BPA_ERR_INVALID_ARG, "dv must be >= 1 (or 0 for d)");
-    if (dv > 256) return fail(BPA_ERR_UNSUPPORTED, "value head dim %d > 256", dv);
+    if (dv > 512) return fail(BPA_ERR_UNSUPPORTED, "value head dim %d > 512", dv);
     const bool own_os = v2 && (d->o_strides[0] | d->o_strides[1] | d->o_strides[2]) != 0;
     if (need_qkv && (!d->q || !d->k || !d->v)) return fail(BPA_ERR_INVALID_ARG, "q, k or v is NULL");
     if (d->window_left < -1 || d->window_right < -1)
@@ -434,7 +434,7 @@ bpa_status bpa_select_blocks(const void* q, const void* k, int32_t dtype, int32_
         return fail(BPA_ERR_INVALID_ARG, "q, k, strides or block_idx_out is NULL");
     if (dtype != BPA_BF16 && dtype != BPA_FP32) return fail(BPA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
     if (B < 1 || S < 1 || H < 1 || d < 1) return fail(BPA_ERR_INVALID_ARG, "B, S, H, d must be >= 1");
-    if (d > 256) return fail(BPA_ERR_UNSUPPORTED, "head dim %d > 256", d);
+    if (d > 512) return fail(BPA_ERR_UNSUPPORTED, "head dim %d > 512", d);
     if (block_size < 1 || S % block_size)
         return fail(BPA_ERR_INVALID_ARG, "block_size (%d) must divide S (%d)", block_size, S);
     if (top_n < 1 || top_n > 64) return fail(BPA_ERR_INVALID_ARG, "top_n must be in [1, 64]");

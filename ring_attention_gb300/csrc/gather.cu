@@ -1,4 +1,5 @@
-// gather.cu - block-selected attention forward over gathered key blocks (bf16, d = 64, 32-key blocks).
+// gather.cu - block-selected attention over gathered key blocks, forward and backward
+// (bf16, head dim d = 64 NW with NW in {1, 2, 4, 8}, 32-row blocks).
 //
 // For query q in block i the allowed keys are the local window q-W+1..q
 // united with the key blocks selected for block i ("AnnAttention",
@@ -8,11 +9,16 @@
 // visit (the selected ones and those the local window touches), then folds
 // them one at a time into a running (max, numerator, denominator) carry in
 // registers ("bpt.py", _blockwise_attention_fwd / scan_kv_block).
-// The products are small (32 x 32 x 64 per block), gathered from scattered
-// blocks, so they run on mma.sync m16n8k16 from registers: Q stays in A
-// fragments, K and V blocks are staged in XOR-swizzled shared memory and
-// read with ldmatrix.  The kernel is bound by L2 / HBM traffic of the
+// The products are small (32 x 32 x 64 per block and warp), gathered from
+// scattered blocks, so they run on mma.sync m16n8k16 from registers: Q stays
+// in A fragments, K and V blocks are staged in XOR-swizzled shared memory and
+// read with ldmatrix.  The kernels are bound by L2 / HBM traffic of the
 // gathered blocks, not by the tensor cores.
+// Head dims above 64 (the joint view of "AnnAttention", which flattens the heads
+// into one embedding of H d channels) split the channels over NW warps per query
+// block: each warp keeps its 64-channel slice of Q, K, V, O (and of dO, dQ, dK, dV),
+// and only the 32 x 32 partial sums of S (and dP) are exchanged through shared
+// memory, added in a fixed order so that every warp holds the same bits.
 #include <math.h>
 
 #include "bpa_internal.h"
@@ -22,8 +28,7 @@ namespace bpa {
 namespace {
 
 constexpr int BS = 32;        // block size (query rows and keys)
-constexpr int D = 64;         // head dim
-constexpr int kWarps = 4;     // query blocks per CTA
+constexpr int D = 64;         // channels per warp (one slice of the head dim)
 constexpr int kMaxList = 24;  // key blocks per query block (top_n + window blocks)
 
 // 128-byte aligned so that every warp's tiles start on a 16-byte boundary
@@ -57,6 +62,50 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// CTA geometry for NW warps per query block.  Shared memory (dynamic): the warps' own
+// tiles, then one float exchange buffer [NW][32 fragments][32 lanes] per query block
+// (two in the backward, for S and dP) when NW > 1.
+template <int NW>
+struct Geom {
+    static constexpr int QB_F = NW >= 4 ? 1 : 4 / NW;   // query blocks per CTA, forward
+    static constexpr int QB_B = NW >= 2 ? 1 : 2;        // backward
+    static constexpr int XCH = NW > 1 ? NW * 32 * 32 : 0;   // floats of one exchange buffer
+};
+
+// Barrier over the NW warps of one query block (named barrier slot + 1; 0 is __syncthreads).
+template <int NW>
+__device__ __forceinline__ void group_sync(int slot) {
+    if (NW == 1)
+        __syncwarp();
+    else
+        asm volatile("bar.sync %0, %1;" ::"r"(slot + 1), "r"(NW * 32) : "memory");
+}
+
+__device__ __forceinline__ void put_partial(float* xch_w, const float (&x)[2][4][4], int lane) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) xch_w[((mt * 4 + nt) * 4 + e) * 32 + lane] = x[mt][nt][e];
+}
+
+template <int NW>
+__device__ __forceinline__ void sum_partials(float (&x)[2][4][4], const float* xch, int lane) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = ((mt * 4 + nt) * 4 + e) * 32 + lane;
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < NW; ++w) v += xch[w * 1024 + j];
+                x[mt][nt][e] = v;
+            }
 }
 
 // mma.sync m16n8k16 fragment layouts (g = lane / 4, t = lane % 4):
@@ -94,20 +143,24 @@ __device__ int visit_list(const Problem& P, int64_t unit, int i, int* list) {
     return n;
 }
 
-__global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
+template <int NW>
+__global__ void __launch_bounds__(Geom<NW>::QB_F * NW * 32) k_gather_fwd(const FwdArgs a) {
+    using G = Geom<NW>;
     const Problem& P = a.P;
-    __shared__ WarpSmem sm[kWarps];
+    extern __shared__ __align__(128) uint8_t gsm[];
     static_assert(sizeof(WarpSmem) % 128 == 0, "per-warp tiles must stay 16-byte aligned");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot = warp / NW, c0 = D * (warp % NW);   // query block of the CTA, channel slice
     const int g = lane >> 2, t = lane & 3;
     const int nblk = P.S / BS;
-    const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarps + warp;   // (b, h, i)
-    if (unit >= static_cast<int64_t>(P.B) * P.Hq * nblk) return;
+    const int64_t unit = static_cast<int64_t>(blockIdx.x) * G::QB_F + slot;   // (b, h, i)
+    if (unit >= static_cast<int64_t>(P.B) * P.Hq * nblk) return;   // the whole query block's warps
     const int i = static_cast<int>(unit % nblk);
     const int h = static_cast<int>((unit / nblk) % P.Hq);
     const int b = static_cast<int>(unit / (static_cast<int64_t>(nblk) * P.Hq));
     const int hkv = h / P.G;
-    WarpSmem& S = sm[warp];
+    WarpSmem& S = reinterpret_cast<WarpSmem*>(gsm)[warp];
+    float* xch = reinterpret_cast<float*>(gsm + sizeof(WarpSmem) * G::QB_F * NW) + slot * G::XCH;
     const uint32_t sk = smem_u32(S.k), sv = smem_u32(S.v);
 
     // ---- key blocks to visit: selected blocks and the blocks the local window touches
@@ -116,19 +169,19 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
     const int nlist = S.n;
 
     // ---- Q fragments (A operand): rows mt*16 + {g, g+8}, channels ks*16 + {2t, 2t+1, 2t+8, 2t+9}
-    const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(P.q) + b * P.qs[0] + h * P.qs[2];
+    const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(P.q) + b * P.qs[0] + h * P.qs[2] + c0;
     uint32_t qa[2][4][4];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
-            const int r0 = BS * i + mt * 16 + g, c0 = ks * 16 + 2 * t;
+            const int r0 = BS * i + mt * 16 + g, cc = ks * 16 + 2 * t;
             const __nv_bfloat16* p0 = Q + static_cast<int64_t>(r0) * P.qs[1];
             const __nv_bfloat16* p1 = Q + static_cast<int64_t>(r0 + 8) * P.qs[1];
-            qa[mt][ks][0] = *reinterpret_cast<const uint32_t*>(p0 + c0);
-            qa[mt][ks][1] = *reinterpret_cast<const uint32_t*>(p1 + c0);
-            qa[mt][ks][2] = *reinterpret_cast<const uint32_t*>(p0 + c0 + 8);
-            qa[mt][ks][3] = *reinterpret_cast<const uint32_t*>(p1 + c0 + 8);
+            qa[mt][ks][0] = *reinterpret_cast<const uint32_t*>(p0 + cc);
+            qa[mt][ks][1] = *reinterpret_cast<const uint32_t*>(p1 + cc);
+            qa[mt][ks][2] = *reinterpret_cast<const uint32_t*>(p0 + cc + 8);
+            qa[mt][ks][3] = *reinterpret_cast<const uint32_t*>(p1 + cc + 8);
         }
 
     const float sl2 = P.scale * kLog2e;
@@ -148,8 +201,8 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
             lrow[mt][hh] = 0.f;
         }
 
-    const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(P.k) + b * P.ks[0] + hkv * P.ks[2];
-    const __nv_bfloat16* V = static_cast<const __nv_bfloat16*>(P.v) + b * P.vs[0] + hkv * P.vs[2];
+    const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(P.k) + b * P.ks[0] + hkv * P.ks[2] + c0;
+    const __nv_bfloat16* V = static_cast<const __nv_bfloat16*>(P.v) + b * P.vs[0] + hkv * P.vs[2] + c0;
     const int32_t* selrow = P.block_idx + static_cast<int64_t>(unit) * P.top_n;
 
     for (int x = 0; x < nlist; ++x) {
@@ -192,6 +245,12 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
                     mma16816(s[mt][np * 2 + 1], qa[mt][ks], b10, b11);
                 }
             }
+        }
+        if (NW > 1) {   // S over all channels: add the slices' partial sums
+            put_partial(xch + (warp % NW) * 1024, s, lane);
+            group_sync<NW>(slot);
+            sum_partials<NW>(s, xch, lane);
+            group_sync<NW>(slot);
         }
         // ---- scale, mask, online softmax
 #pragma unroll
@@ -265,7 +324,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
     }
 
     // ---- epilogue: O = num / den, m, l
-    __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + b * P.os[0] + h * P.os[2];
+    __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + b * P.os[0] + h * P.os[2] + c0;
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -277,7 +336,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
             for (int nt = 0; nt < 8; ++nt)
                 *reinterpret_cast<uint32_t*>(orow + nt * 8 + 2 * t) =
                     pack_bf16(o[mt][nt][hh * 2 + 0] * inv, o[mt][nt][hh * 2 + 1] * inv);
-            if (t == 0) {
+            if (t == 0 && c0 == 0) {
                 const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * P.S + q;
                 a.m[mi] = mrow[mt][hh] == -INFINITY ? -INFINITY : mrow[mt][hh] * kLn2;
                 a.l[mi] = lrow[mt][hh];
@@ -296,8 +355,6 @@ __global__ void __launch_bounds__(kWarps * 32) k_gather_fwd(const FwdArgs a) {
 // "AnnAttention", faiss_block_attention.py trains through the gathered attention with the
 // selection held fixed; the gradients are those of "bpt.py", _blockwise_attention_bwd
 // restricted to the visited blocks.
-constexpr int kWarpsB = 2;   // query blocks per CTA (static shared memory < 48 KB)
-
 struct __align__(128) WarpSmemB {
     __nv_bfloat16 k[BS * D];      // [key][ch], 128-byte rows, swz()
     __nv_bfloat16 v[BS * D];
@@ -419,26 +476,30 @@ __device__ __forceinline__ void reduce_rows(float* acc_row0, int64_t row_stride,
         }
 }
 
-__global__ void __launch_bounds__(kWarpsB * 32) k_gather_bwd(const BwdArgs a) {
+template <int NW>
+__global__ void __launch_bounds__(Geom<NW>::QB_B * NW * 32) k_gather_bwd(const BwdArgs a) {
+    using G = Geom<NW>;
     const Problem& P = a.P;
-    __shared__ WarpSmemB sm[kWarpsB];
+    extern __shared__ __align__(128) uint8_t gsm[];
     static_assert(sizeof(WarpSmemB) % 128 == 0, "per-warp tiles must stay 16-byte aligned");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot = warp / NW, c0 = D * (warp % NW);   // query block of the CTA, channel slice
     const int g = lane >> 2, t = lane & 3, mi = lane >> 3, rr = lane & 7;
     const int nblk = P.S / BS;
-    const int64_t unit = static_cast<int64_t>(blockIdx.x) * kWarpsB + warp;   // (b, h, i)
-    if (unit >= static_cast<int64_t>(P.B) * P.Hq * nblk) return;
+    const int64_t unit = static_cast<int64_t>(blockIdx.x) * G::QB_B + slot;   // (b, h, i)
+    if (unit >= static_cast<int64_t>(P.B) * P.Hq * nblk) return;   // the whole query block's warps
     const int i = static_cast<int>(unit % nblk);
     const int h = static_cast<int>((unit / nblk) % P.Hq);
     const int b = static_cast<int>(unit / (static_cast<int64_t>(nblk) * P.Hq));
     const int hkv = h / P.G;
-    WarpSmemB& W = sm[warp];
+    WarpSmemB& W = reinterpret_cast<WarpSmemB*>(gsm)[warp];
+    float* xch = reinterpret_cast<float*>(gsm + sizeof(WarpSmemB) * G::QB_B * NW) + slot * 2 * G::XCH;
     const uint32_t sk = smem_u32(W.k), sv = smem_u32(W.v), sq = smem_u32(W.q), sdo = smem_u32(W.dout),
                    sp = smem_u32(W.p), sds = smem_u32(W.ds);
 
     if (lane == 0) W.n = visit_list(P, unit, i, W.list);
-    const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(P.q) + b * P.qs[0] + h * P.qs[2];
-    const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(a.dout) + b * P.os[0] + h * P.os[2];
+    const __nv_bfloat16* Q = static_cast<const __nv_bfloat16*>(P.q) + b * P.qs[0] + h * P.qs[2] + c0;
+    const __nv_bfloat16* dO = static_cast<const __nv_bfloat16*>(a.dout) + b * P.os[0] + h * P.os[2] + c0;
     stage_rows(sq, Q + static_cast<int64_t>(BS) * i * P.qs[1], P.qs[1], lane);
     stage_rows(sdo, dO + static_cast<int64_t>(BS) * i * P.os[1], P.os[1], lane);
     __syncwarp();
@@ -463,11 +524,11 @@ __global__ void __launch_bounds__(kWarpsB * 32) k_gather_bwd(const BwdArgs a) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) dq[mt][nt][e] = 0.f;
 
-    const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(P.k) + b * P.ks[0] + hkv * P.ks[2];
-    const __nv_bfloat16* V = static_cast<const __nv_bfloat16*>(P.v) + b * P.vs[0] + hkv * P.vs[2];
-    const int64_t acc_rs = static_cast<int64_t>(P.Hkv) * D;   // float32 accumulators [B, S, Hkv, 64]
-    float* dKacc = a.dk_acc + (static_cast<int64_t>(b) * P.S * P.Hkv + hkv) * D;
-    float* dVacc = a.dv_acc + (static_cast<int64_t>(b) * P.S * P.Hkv + hkv) * D;
+    const __nv_bfloat16* K = static_cast<const __nv_bfloat16*>(P.k) + b * P.ks[0] + hkv * P.ks[2] + c0;
+    const __nv_bfloat16* V = static_cast<const __nv_bfloat16*>(P.v) + b * P.vs[0] + hkv * P.vs[2] + c0;
+    const int64_t acc_rs = static_cast<int64_t>(P.Hkv) * D * NW;   // float32 accumulators [B, S, Hkv, d]
+    float* dKacc = a.dk_acc + (static_cast<int64_t>(b) * P.S * P.Hkv + hkv) * (D * NW) + c0;
+    float* dVacc = a.dv_acc + (static_cast<int64_t>(b) * P.S * P.Hkv + hkv) * (D * NW) + c0;
     const int32_t* selrow = P.block_idx + unit * P.top_n;
 
     for (int x = 0; x < nlist; ++x) {
@@ -482,6 +543,14 @@ __global__ void __launch_bounds__(kWarpsB * 32) k_gather_bwd(const BwdArgs a) {
         float s[2][4][4], dp[2][4][4];
         nt_product(s, sq, sk, lane);     // Q K^T
         nt_product(dp, sdo, sv, lane);   // dO V^T
+        if (NW > 1) {   // over all channels: add the slices' partial sums
+            put_partial(xch + (warp % NW) * 1024, s, lane);
+            put_partial(xch + G::XCH + (warp % NW) * 1024, dp, lane);
+            group_sync<NW>(slot);
+            sum_partials<NW>(s, xch, lane);
+            sum_partials<NW>(dp, xch + G::XCH, lane);
+            group_sync<NW>(slot);
+        }
         // P and dS under the forward's mask
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
@@ -535,7 +604,7 @@ __global__ void __launch_bounds__(kWarpsB * 32) k_gather_bwd(const BwdArgs a) {
     }
 
     // ---- dQ = scale * sum dS K, written once
-    __nv_bfloat16* dQ = static_cast<__nv_bfloat16*>(a.dq) + b * P.qs[0] + h * P.qs[2];
+    __nv_bfloat16* dQ = static_cast<__nv_bfloat16*>(a.dq) + b * P.qs[0] + h * P.qs[2] + c0;
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -550,7 +619,8 @@ __global__ void __launch_bounds__(kWarpsB * 32) k_gather_bwd(const BwdArgs a) {
 }  // namespace
 
 bool gather_supported(const Problem& P) {
-    if (P.dtype != BPA_BF16 || P.d != D || P.dv != D || !P.block_idx || P.sel_block != BS) return false;
+    if (P.dtype != BPA_BF16 || P.d != P.dv || !P.block_idx || P.sel_block != BS) return false;
+    if (P.d != 64 && P.d != 128 && P.d != 256 && P.d != 512) return false;
     if (P.top_n + 3 > kMaxList || P.local_window > 2 * BS) return false;
     if (P.ring_n != 1 || P.bias) return false;
     // 16-byte rows for the staged copies, 4-byte fragment loads
@@ -562,16 +632,52 @@ bool gather_supported(const Problem& P) {
     return true;
 }
 
-cudaError_t launch_gather_bwd(const BwdArgs& a, cudaStream_t s) {
+namespace {
+
+template <int NW>
+cudaError_t gather_fwd_nw(const FwdArgs& a, cudaStream_t s) {
+    using G = Geom<NW>;
     const int64_t units = static_cast<int64_t>(a.P.B) * a.P.Hq * (a.P.S / BS);
-    k_gather_bwd<<<static_cast<unsigned>((units + kWarpsB - 1) / kWarpsB), kWarpsB * 32, 0, s>>>(a);
+    const size_t smem = sizeof(WarpSmem) * G::QB_F * NW + sizeof(float) * G::XCH * G::QB_F;
+    cudaError_t e = cudaFuncSetAttribute(k_gather_fwd<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    k_gather_fwd<NW><<<static_cast<unsigned>((units + G::QB_F - 1) / G::QB_F), G::QB_F * NW * 32, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather_fwd(const FwdArgs& a, cudaStream_t s) {
+template <int NW>
+cudaError_t gather_bwd_nw(const BwdArgs& a, cudaStream_t s) {
+    using G = Geom<NW>;
     const int64_t units = static_cast<int64_t>(a.P.B) * a.P.Hq * (a.P.S / BS);
-    k_gather_fwd<<<static_cast<unsigned>((units + kWarps - 1) / kWarps), kWarps * 32, 0, s>>>(a);
+    const size_t smem = sizeof(WarpSmemB) * G::QB_B * NW + sizeof(float) * 2 * G::XCH * G::QB_B;
+    cudaError_t e = cudaFuncSetAttribute(k_gather_bwd<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    k_gather_bwd<NW><<<static_cast<unsigned>((units + G::QB_B - 1) / G::QB_B), G::QB_B * NW * 32, smem, s>>>(a);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gather_fwd(const FwdArgs& a, cudaStream_t s) {
+    switch (a.P.d) {
+        case 64: return gather_fwd_nw<1>(a, s);
+        case 128: return gather_fwd_nw<2>(a, s);
+        case 256: return gather_fwd_nw<4>(a, s);
+        case 512: return gather_fwd_nw<8>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gather_bwd(const BwdArgs& a, cudaStream_t s) {
+    switch (a.P.d) {
+        case 64: return gather_bwd_nw<1>(a, s);
+        case 128: return gather_bwd_nw<2>(a, s);
+        case 256: return gather_bwd_nw<4>(a, s);
+        case 512: return gather_bwd_nw<8>(a, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace bpa

@@ -15,10 +15,10 @@
 namespace bpa {
 namespace {
 
-constexpr int kMaxD = 256;
+constexpr int kMaxD = 512;
 constexpr int kRows = 16;   // rows per CTA
 constexpr int kWarps = 4;   // warps per CTA
-constexpr int kPer = kMaxD / 32;
+// KP: channels per lane (lane owns dims lane + 32 i, i < KP): 8 up to 256 channels, 16 above
 
 template <typename T>
 __device__ __forceinline__ float ldf(const T* p);
@@ -88,14 +88,15 @@ __device__ __forceinline__ float bias_at(const Problem& P, int b, int h, int q, 
 }
 
 // Forward state of one query row, spread over the warp (lane owns dims lane + 32 i).
+template <int KP>
 struct RowState {
     float m, l;
-    float acc[kPer];
+    float acc[KP];
 };
 
-template <typename T>
+template <typename T, int KP>
 __device__ void fold_keys(const Problem& P, int b, int h, int g, int q, int klo, int khi,
-                          const float* sq, RowState& st) {
+                          const float* sq, RowState<KP>& st) {
     const int lane = threadIdx.x & 31;
     const T* K = static_cast<const T*>(P.k);
     const T* V = static_cast<const T*>(P.v);
@@ -117,7 +118,7 @@ __device__ void fold_keys(const Problem& P, int b, int h, int g, int q, int klo,
         const float p = ok ? expf(s - mnew) : 0.f;
         st.l = st.l * corr + warp_sum(p);
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) st.acc[i] *= corr;
+        for (int i = 0; i < KP; ++i) st.acc[i] *= corr;
         const int nt = min(32, khi - k0 + 1);   // keys of this chunk inside the range
 #pragma unroll 8
         for (int t = 0; t < 32; ++t) {
@@ -125,7 +126,7 @@ __device__ void fold_keys(const Problem& P, int b, int h, int g, int q, int klo,
             if (t >= nt) continue;
             const T* vr = V + b * P.vs[0] + static_cast<int64_t>(k0 + t) * P.vs[1] + g * P.vs[2];
 #pragma unroll
-            for (int i = 0; i < kPer; ++i) {
+            for (int i = 0; i < KP; ++i) {
                 const int c = lane + 32 * i;
                 if (c < P.dv) st.acc[i] = fmaf(pt, ldf(vr + c), st.acc[i]);
             }
@@ -134,7 +135,7 @@ __device__ void fold_keys(const Problem& P, int b, int h, int g, int q, int klo,
     }
 }
 
-template <typename T>
+template <typename T, int KP>
 __global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
     const Problem& P = a.P;
     const int b = blockIdx.z, h = blockIdx.y, g = h / P.G;
@@ -153,14 +154,14 @@ __global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
         if (P.causal) hi = min(hi, q);
         if (P.wr >= 0) hi = min(hi, q + P.wr);
         if (P.wl >= 0) lo = max(lo, q - P.wl);
-        RowState st;
+        RowState<KP> st;
         st.m = -INFINITY;
         st.l = 0.f;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) st.acc[i] = 0.f;
+        for (int i = 0; i < KP; ++i) st.acc[i] = 0.f;
         if (lo <= hi) {
             if (!P.block_idx) {
-                fold_keys<T>(P, b, h, g, q, lo, hi, sq[warp], st);
+                fold_keys<T, KP>(P, b, h, g, q, lo, hi, sq[warp], st);
             } else {
                 // visit each key block once: selected blocks and the blocks of
                 // the local window, in ascending order (a set union)
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
                     const int k1 = min(hi, kb * P.sel_block + P.sel_block - 1);
                     const bool local = k1 > q - P.local_window && k0 <= q;
                     if (!local && !selected(P, b, h, q, kb)) continue;
-                    fold_keys<T>(P, b, h, g, q, k0, k1, sq[warp], st);
+                    fold_keys<T, KP>(P, b, h, g, q, k0, k1, sq[warp], st);
                 }
             }
         }
@@ -178,7 +179,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
             const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
             T* O = static_cast<T*>(a.o) + b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2];
 #pragma unroll
-            for (int i = 0; i < kPer; ++i) {
+            for (int i = 0; i < KP; ++i) {
                 const int c = lane + 32 * i;
                 if (c < P.dv) stf(O + c, st.acc[i] * inv);
             }
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
                 const float fb = st.m == -INFINITY ? 0.f : expf(st.m - mn);
                 float* C = a.acc + ((static_cast<int64_t>(b) * P.S + q) * P.Hq + h) * P.dv;
 #pragma unroll
-                for (int i = 0; i < kPer; ++i) {
+                for (int i = 0; i < KP; ++i) {
                     const int c = lane + 32 * i;
                     if (c < P.dv) C[c] = C[c] * fa + st.acc[i] * fb;
                 }
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
 
 // dQ contribution of the keys [klo, khi] to one query row (lane owns dims lane + 32 i):
 //   acc += sum_k P (dP - D) K_k   (the scale is applied by the caller)
-template <typename T>
+template <typename T, int KP>
 __device__ void dq_keys(const Problem& P, int b, int h, int g, int q, int klo, int khi, const float* sq,
                         const float* sdo, float lse, float Dq, float* acc) {
     const int lane = threadIdx.x & 31;
@@ -239,7 +240,7 @@ __device__ void dq_keys(const Problem& P, int b, int h, int g, int q, int klo, i
             if (t >= nt) continue;
             const T* kr = K + b * P.ks[0] + static_cast<int64_t>(k0 + t) * P.ks[1] + g * P.ks[2];
 #pragma unroll
-            for (int i = 0; i < kPer; ++i) {
+            for (int i = 0; i < KP; ++i) {
                 const int c = lane + 32 * i;
                 if (c < P.d) acc[i] = fmaf(st, ldf(kr + c), acc[i]);
             }
@@ -248,7 +249,7 @@ __device__ void dq_keys(const Problem& P, int b, int h, int g, int q, int klo, i
 }
 
 // dQ of one query row per warp:  dQ = scale * sum_k P (dP - D) K_k
-template <typename T>
+template <typename T, int KP>
 __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
     const Problem& P = a.P;
     const int b = blockIdx.z, h = blockIdx.y, g = h / P.G;
@@ -267,16 +268,16 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
         __syncwarp();
         const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * a.Spad + q;
         const float lse = a.lse[mi], Dq = a.Dvec[mi];
-        float acc[kPer];
+        float acc[KP];
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+        for (int i = 0; i < KP; ++i) acc[i] = 0.f;
         int lo = 0, hi = P.S - 1;
         if (P.causal) hi = min(hi, q);
         if (P.wr >= 0) hi = min(hi, q + P.wr);
         if (P.wl >= 0) lo = max(lo, q - P.wl);
         if (lse != INFINITY && lo <= hi) {
             if (!P.block_idx) {
-                dq_keys<T>(P, b, h, g, q, lo, hi, sq[warp], sdo[warp], lse, Dq, acc);
+                dq_keys<T, KP>(P, b, h, g, q, lo, hi, sq[warp], sdo[warp], lse, Dq, acc);
             } else {
                 // the key blocks the forward visited: the local window's and the selected ones
                 for (int kb = lo / P.sel_block; kb <= hi / P.sel_block; ++kb) {
@@ -284,13 +285,13 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
                     const int k1 = min(hi, kb * P.sel_block + P.sel_block - 1);
                     const bool local = k1 > q - P.local_window && k0 <= q;
                     if (!local && !selected(P, b, h, q, kb)) continue;
-                    dq_keys<T>(P, b, h, g, q, k0, k1, sq[warp], sdo[warp], lse, Dq, acc);
+                    dq_keys<T, KP>(P, b, h, g, q, k0, k1, sq[warp], sdo[warp], lse, Dq, acc);
                 }
             }
         }
         T* dQ = static_cast<T*>(a.dq) + qoff;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
+        for (int i = 0; i < KP; ++i) {
             const int c = lane + 32 * i;
             if (c < P.d) stf(dQ + c, acc[i] * P.scale);
         }
@@ -300,7 +301,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
 
 // dK, dV contributions of the queries [qlo, qhi] of q head h to one key row:
 //   dk += sum_q dS Q_q,   dv += sum_q P dO_q   (the scale on dk is applied by the caller)
-template <typename T>
+template <typename T, int KP>
 __device__ void dkdv_queries(const BwdArgs& a, int b, int h, int k, int qlo, int qhi, const float* sk,
                              const float* sv, float* dk, float* dv) {
     const Problem& P = a.P;
@@ -335,7 +336,7 @@ __device__ void dkdv_queries(const BwdArgs& a, int b, int h, int k, int qlo, int
             const int64_t qoff = b * P.qs[0] + static_cast<int64_t>(q0 + t) * P.qs[1] + h * P.qs[2];
             const int64_t ooff = b * P.os[0] + static_cast<int64_t>(q0 + t) * P.os[1] + h * P.os[2];
 #pragma unroll
-            for (int i = 0; i < kPer; ++i) {
+            for (int i = 0; i < KP; ++i) {
                 const int c = lane + 32 * i;
                 if (c < P.d) dk[i] = fmaf(st, ldf(Q + qoff + c), dk[i]);
                 if (c < P.dv) dv[i] = fmaf(pt, ldf(dO + ooff + c), dv[i]);
@@ -350,7 +351,7 @@ __device__ void dkdv_queries(const BwdArgs& a, int b, int h, int k, int qlo, int
 // queries whose local window holds it and by every query of the query blocks that
 // selected its block; the warp finds those query blocks 32 at a time with a ballot
 // (selection is per query block) and visits only them.
-template <typename T>
+template <typename T, int KP>
 __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) {
     const Problem& P = a.P;
     const int b = blockIdx.z, g = blockIdx.y;
@@ -367,16 +368,16 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
         for (int c = lane; c < P.d; c += 32) sk[warp][c] = ldf(K + koff + c);
         for (int c = lane; c < P.dv; c += 32) sv[warp][c] = ldf(V + voff + c);
         __syncwarp();
-        float dk[kPer], dv[kPer];
+        float dk[KP], dv[KP];
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) dk[i] = dv[i] = 0.f;
+        for (int i = 0; i < KP; ++i) dk[i] = dv[i] = 0.f;
         int lo = 0, hi = P.S - 1;  // queries that may see key k
         if (P.causal) lo = max(lo, k);
         if (P.wr >= 0) lo = max(lo, k - P.wr);
         if (P.wl >= 0) hi = min(hi, k + P.wl);
         for (int h = g * P.G; h < (g + 1) * P.G && lo <= hi; ++h) {
             if (!P.block_idx) {
-                dkdv_queries<T>(a, b, h, k, lo, hi, sk[warp], sv[warp], dk, dv);
+                dkdv_queries<T, KP>(a, b, h, k, lo, hi, sk[warp], sv[warp], dk, dv);
                 continue;
             }
             const int sb = P.sel_block, kb = k / sb;
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
                 while (todo) {
                     const int qv = qb0 + __ffs(todo) - 1;
                     todo &= todo - 1;
-                    dkdv_queries<T>(a, b, h, k, max(lo, qv * sb), min(hi, qv * sb + sb - 1), sk[warp], sv[warp],
+                    dkdv_queries<T, KP>(a, b, h, k, max(lo, qv * sb), min(hi, qv * sb + sb - 1), sk[warp], sv[warp],
                                     dk, dv);
                 }
             }
@@ -400,7 +401,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
         T* dK = static_cast<T*>(a.dk) + koff;
         T* dV = static_cast<T*>(a.dv) + voff;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
+        for (int i = 0; i < KP; ++i) {
             const int c = lane + 32 * i;
             if (c < P.d) stf(dK + c, dk[i] * P.scale);
             if (c < P.dv) stf(dV + c, dv[i]);
@@ -411,28 +412,42 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
 
 }  // namespace
 
-cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s) {
+namespace {
+
+template <int KP>
+cudaError_t fwd_simt_kp(const FwdArgs& a, cudaStream_t s) {
     const Problem& P = a.P;
     dim3 grid((P.S + kRows - 1) / kRows, P.Hq, P.B);
     if (P.dtype == BPA_FP32)
-        k_fwd_simt<float><<<grid, kWarps * 32, 0, s>>>(a);
+        k_fwd_simt<float, KP><<<grid, kWarps * 32, 0, s>>>(a);
     else
-        k_fwd_simt<__nv_bfloat16><<<grid, kWarps * 32, 0, s>>>(a);
+        k_fwd_simt<__nv_bfloat16, KP><<<grid, kWarps * 32, 0, s>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s) {
+template <int KP>
+cudaError_t bwd_simt_kp(const BwdArgs& a, cudaStream_t s) {
     const Problem& P = a.P;
     dim3 gq((P.S + kRows - 1) / kRows, P.Hq, P.B);
     dim3 gk((P.S + kRows - 1) / kRows, P.Hkv, P.B);
     if (P.dtype == BPA_FP32) {
-        k_bwd_dq_simt<float><<<gq, kWarps * 32, 0, s>>>(a);
-        k_bwd_dkdv_simt<float><<<gk, kWarps * 32, 0, s>>>(a);
+        k_bwd_dq_simt<float, KP><<<gq, kWarps * 32, 0, s>>>(a);
+        k_bwd_dkdv_simt<float, KP><<<gk, kWarps * 32, 0, s>>>(a);
     } else {
-        k_bwd_dq_simt<__nv_bfloat16><<<gq, kWarps * 32, 0, s>>>(a);
-        k_bwd_dkdv_simt<__nv_bfloat16><<<gk, kWarps * 32, 0, s>>>(a);
+        k_bwd_dq_simt<__nv_bfloat16, KP><<<gq, kWarps * 32, 0, s>>>(a);
+        k_bwd_dkdv_simt<__nv_bfloat16, KP><<<gk, kWarps * 32, 0, s>>>(a);
     }
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s) {
+    return (a.P.d > 256 || a.P.dv > 256) ? fwd_simt_kp<16>(a, s) : fwd_simt_kp<8>(a, s);
+}
+
+cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s) {
+    return (a.P.d > 256 || a.P.dv > 256) ? bwd_simt_kp<16>(a, s) : bwd_simt_kp<8>(a, s);
 }
 
 }  // namespace bpa

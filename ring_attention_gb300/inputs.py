@@ -75,8 +75,14 @@ BLOCK_SEL = Workload("blocksel_top8_B4_S8192_H8_d64", B=4, S=8192, Hq=8, Hkv=8, 
 MLA_CAUSAL = Workload("mla_causal_B2_S4096_Hq128_Hkv8_dqk128_dv64", B=2, S=4096, Hq=128, Hkv=8, d=128,
                       dv=64, causal=True, seed=2027)
 
+# The joint view of the block-selected workload ("AnnAttention", faiss_block_attention
+# flattens the heads into one embedding): the same numbers as BLOCK_SEL (one generator,
+# the same seed and C order) read as one head of 8 x 64 = 512 channels, with backward.
+BLOCK_SEL_JOINT = Workload("blocksel_joint_top8_B4_S8192_H1_d512", B=4, S=8192, Hq=1, Hkv=1, d=512,
+                           causal=True, seed=4, sel_block=32, top_n=8, local_window=32)
+
 WORKLOADS = {w.name: w for w in (TINY_F32, GQA_CAUSAL, GQA_SWA, RING_LONG, BLOCK_SEL)}
-EXTRA_WORKLOADS = {w.name: w for w in (MLA_CAUSAL,)}
+EXTRA_WORKLOADS = {w.name: w for w in (MLA_CAUSAL, BLOCK_SEL_JOINT)}
 
 
 def draw(shape_list, seed: int, dtype: str):

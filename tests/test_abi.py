@@ -80,7 +80,7 @@ def _desc(bpa, **over):
     (dict(struct_size=8), 1),
     (dict(dtype=7), 1),
     (dict(Hq=6, Hkv=4), 1),
-    (dict(d=512), 2),
+    (dict(d=513), 2),
     (dict(S=0), 1),
     (dict(q=0), 1),
     (dict(window_left=-2), 1),
@@ -164,7 +164,7 @@ def test_value_head_dim_checks_and_sizes(bpa):
     D.dv = D.d // 2   # separate value head dim: the forward ring carry is [B, S, Hq, dv]
     half = L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D))
     assert half == 256 + (base - 256) // 2
-    D.dv = 257
+    D.dv = 513
     assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) == 0
     assert b"value head dim" in L.bpa_last_error()
     D.dv = -1

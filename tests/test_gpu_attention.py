@@ -289,6 +289,60 @@ def test_block_selected_backward_gathered(bpa, ora, lw):
         assert float(dq[:, :bs].abs().max()) == 0.0
 
 
+@pytest.mark.parametrize("d", [128, 256, 512])
+def test_block_selected_wide_heads(bpa, ora, d):
+    # the joint view: the channels of all heads read as fewer, wider heads (512 = H d),
+    # selection on the wide block sums, forward and backward on the channel-split gather
+    B, S, C = 1, 512, 512
+    H, bs, n = C // d, 32, 6
+    q, k, v, do = (x.reshape(B, S, H, d) for x in draw([(B, S, 8, 64)] * 4, 67, "bf16"))
+    tq, tk, tv = dev(q), dev(k), dev(v)
+    idx = bpa.bpa_select_blocks(tq, tk, block_size=bs, top_n=n)
+    kw = dict(causal=True, sel_block=bs, top_n=n, local_window=32)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, block_idx=idx, **kw)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, dev(do), m, l, block_idx=idx, **kw)
+    torch.cuda.synchronize()
+    ridx = ora.select_blocks(q, k, block_size=bs, top_n=n)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, block_idx=ridx, **kw)
+    assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+    check_stats(m, l, rm, rl)
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2
+
+
+def test_block_selected_wide_heads_gqa_planted(bpa, ora):
+    # channel-split gather with GQA (4 q heads on 2 kv heads of 128 channels), planted
+    # selections and a local window of part of a block
+    B, S, Hq, Hkv, d, bs, n, lw = 2, 256, 4, 2, 128, 32, 4, 20
+    q, k, v, do = draw([(B, S, Hq, d), (B, S, Hkv, d), (B, S, Hkv, d), (B, S, Hq, d)], 68, "bf16")
+    idx = _planted_selection(B, Hq, S, bs, n, 69)
+    kw = dict(causal=True, sel_block=bs, top_n=n, local_window=lw)
+    tq, tk, tv, ti = dev(q), dev(k), dev(v), torch.from_numpy(idx).cuda()
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, block_idx=ti, **kw)
+    dq, dk, dvv = bpa.bpa_bwd(tq, tk, tv, o, dev(do), m, l, block_idx=ti, **kw)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, block_idx=idx, **kw)
+    assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+    check_stats(m, l, rm, rl)
+    for got, ref in ((dq, rq), (dk, rk), (dvv, rv)):
+        assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2
+
+
+def test_fp32_head_dim_512(bpa, ora):
+    # the CUDA-core kernels with 16 channels per lane
+    B, S, Hq, Hkv, d = 1, 70, 2, 1, 512
+    q, k, v, do = draw([(B, S, Hq, d), (B, S, Hkv, d), (B, S, Hkv, d), (B, S, Hq, d)], 70, "f32")
+    tq, tk, tv = dev(q), dev(k), dev(v)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, causal=True)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, dev(do), m, l, causal=True)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, causal=True)
+    check_stats(m, l, rm, rl)
+    for got, ref in ((o, ro), (dq, rq), (dk, rk), (dv, rv)):
+        assert max_abs(host(got), ref) <= FP32_MAX_ABS
+
+
 def test_bounded_wait_reports_timeout(bpa):
     ws = bpa.workspace(256, "cuda")
     bpa.bpa_debug_wait_timeout(ws, 200_000_000)   # 0.2 s

@@ -153,6 +153,27 @@ def test_block_selected_workload_backward_reduced(bpa, ora):
     assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
 
 
+def test_block_selected_joint_workload_reduced(bpa, ora):
+    # the joint view (one head of 512 channels) of the block-selected workload's numbers
+    # at S = 2048: selection on the 512-channel block sums, forward and backward
+    w = W.BLOCK_SEL_JOINT
+    q, k, v, do, _ = W.make_inputs(w, B=1, S=2048)
+    tq, tk, tv = dev(q), dev(k), dev(v)
+    idx = bpa.bpa_select_blocks(tq, tk, block_size=w.sel_block, top_n=w.top_n)
+    kw = dict(causal=True, sel_block=w.sel_block, top_n=w.top_n, local_window=w.local_window)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, block_idx=idx, **kw)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, dev(do), m, l, block_idx=idx, **kw)
+    torch.cuda.synchronize()
+    ridx = ora.select_blocks(q, k, block_size=w.sel_block, top_n=w.top_n)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ridx)
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, block_idx=ridx, **kw)
+    assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+    check_stats(m, l, rm, rl)
+    assert rel_l2(host(dq), rq) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dk), rk) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
+
+
 def test_mla_workload_reduced(bpa, ora):
     # the separate-value-head-dim workload (d_qk 128, d_v 64, causal) on a reduced
     # sequence and head count with the same recipe and GQA ratio 16
