@@ -38,7 +38,14 @@
  *     product over strictly earlier blocks; the sums (not means) rank the
  *     same; ties go to the lower block; fewer than top_n candidates pad
  *     with -1; the local window (keys q-W+1..q) and the selected blocks
- *     combine as a set union.
+ *     combine as a set union;
+ *   - variable lengths ([te] section 1, SequenceDescriptor.from_seqlens):
+ *     batch b holds Lq = seqlens_q[b] queries and Lk = seqlens_kv[b] keys
+ *     (NULL: S; seqlens_kv NULL: the query lengths); later positions are
+ *     padding, take part in nothing and get O = 0, m = -inf, l = 0 and zero
+ *     gradients; the causal / window rule compares k with q + off, off = 0
+ *     (top-left) or Lk - Lq (bottom-right: the queries are the last Lq
+ *     positions of the key sequence).
  */
 #include <math.h>
 #include <stdint.h>
@@ -59,6 +66,9 @@ typedef struct {
     int64_t bias_strides[4];        /* b, h, q, k in elements; 0 broadcasts */
     const int32_t* block_idx;       /* NULL or [B][Hq][S/sel_block][top_n] */
     int32_t sel_block, top_n, local_window;
+    const int32_t* seqlens_q;       /* NULL or [B]: valid queries per batch entry */
+    const int32_t* seqlens_kv;      /* NULL or [B]: valid keys (NULL: seqlens_q) */
+    int32_t bottom_right;           /* 1: causal / window diagonal at k = q + Lk - Lq */
 } ora_desc;
 
 /* ---- element access: inputs are widened exactly to double ------------- */
@@ -98,21 +108,37 @@ static double* widen_kv(const ora_desc* D, const void* src, int w) {
 
 /* ---- the mask ([te] _make_causal_swa_mask; [bpt] causal; [ann]) -------- */
 
+/* Valid query / key counts of batch entry b and the offset of the causal /
+ * window diagonal. */
+static void lengths(const ora_desc* D, int b, int* lq, int* lk, int* off) {
+    int nq = D->seqlens_q ? D->seqlens_q[b] : D->S;
+    int nk = D->seqlens_kv ? D->seqlens_kv[b] : nq;
+    *lq = nq;
+    *lk = nk;
+    *off = D->bottom_right ? nk - nq : 0;
+}
+
 /* Keys that can be allowed for query q lie in [lo, hi]; used only to skip
- * keys that the causal / window rule excludes anyway. */
-static void key_range(const ora_desc* D, int q, int* lo, int* hi) {
-    int a = 0, z = D->S - 1;
-    if (D->causal && q < z) z = q;
-    if (D->window_right >= 0 && q + D->window_right < z) z = q + D->window_right;
-    if (D->window_left >= 0 && q - D->window_left > a) a = q - D->window_left;
+ * keys that the length / causal / window rule excludes anyway. */
+static void key_range(const ora_desc* D, int b, int q, int* lo, int* hi) {
+    int lq, lk, off;
+    lengths(D, b, &lq, &lk, &off);
+    int a = 0, z = lk - 1, c = q + off;
+    if (q >= lq) z = -1;
+    if (D->causal && c < z) z = c;
+    if (D->window_right >= 0 && c + D->window_right < z) z = c + D->window_right;
+    if (D->window_left >= 0 && c - D->window_left > a) a = c - D->window_left;
     *lo = a;
     *hi = z;
 }
 
 static int allowed(const ora_desc* D, int b, int h, int q, int k) {
-    if (D->causal && k > q) return 0;
-    if (D->window_left >= 0 && k < q - D->window_left) return 0;
-    if (D->window_right >= 0 && k > q + D->window_right) return 0;
+    int lq, lk, off;
+    lengths(D, b, &lq, &lk, &off);
+    if (q >= lq || k >= lk) return 0;
+    if (D->causal && k > q + off) return 0;
+    if (D->window_left >= 0 && k < q + off - D->window_left) return 0;
+    if (D->window_right >= 0 && k > q + off + D->window_right) return 0;
     if (D->block_idx) {
         int in_local = (k <= q) && (k >= q - (D->local_window - 1));
         int in_sel = 0;
@@ -152,7 +178,7 @@ static int row_forward(const ora_desc* D, const double* qrow, const double* Kh,
                        const double* Vh, int b, int h, int q, double* z, double* o,
                        double* m_out, double* l_out) {
     int lo, hi;
-    key_range(D, q, &lo, &hi);
+    key_range(D, b, q, &lo, &hi);
     double m = -INFINITY;
     for (int k = lo; k <= hi; ++k) {
         if (allowed(D, b, h, q, k)) {
@@ -276,7 +302,7 @@ int ora_bwd(const ora_desc* D, const void* q, const void* k, const void* v,
                         double Dq = dot(dorow, orow, D->dv);
                         double* dqrow = dq + (((int64_t)b * D->S + s) * D->Hq + h) * D->d;
                         int lo, hi;
-                        key_range(D, s, &lo, &hi);
+                        key_range(D, b, s, &lo, &hi);
                         for (int kk = lo; kk <= hi; ++kk) {
                             if (z[kk] == -INFINITY) continue;
                             double P = exp(z[kk] - m) / l;
@@ -455,7 +481,7 @@ int ora_rows(const ora_desc* D, const void* q, const void* k, const void* v,
                 load_row(dorow, dout, D->in_dtype, D->B, D->S, D->Hq, D->dv, b, s, h);
                 double Dq = dot(dorow, orow, D->dv);
                 int lo, hi;
-                key_range(D, s, &lo, &hi);
+                key_range(D, b, s, &lo, &hi);
                 for (int kk = lo; kk <= hi; ++kk) {
                     if (z[kk] == -INFINITY) continue;
                     double P = exp(z[kk] - m[r]) / l[r];
@@ -490,8 +516,8 @@ int ora_keys(const ora_desc* D, const void* q, const void* k, const void* v,
     for (int t = 0; t < nkeys; ++t)
         if (keys[t] < kmin) kmin = keys[t];
     /* rows that may see a sampled key: all rows when there is no causal
-     * rule, rows q >= kmin otherwise */
-    int q0 = D->causal ? kmin : 0;
+     * rule or the diagonal is shifted, rows q >= kmin otherwise */
+    int q0 = (D->causal && !D->bottom_right) ? kmin : 0;
     int nq = S - q0;
     int64_t nr = (int64_t)G * nq;
     double* M = (double*)malloc((size_t)nr * sizeof(double));

@@ -47,6 +47,8 @@ class _Desc(ctypes.Structure):
         ("bias", ctypes.c_void_p), ("bias_strides", ctypes.c_int64 * 4),
         ("block_idx", ctypes.c_void_p), ("sel_block", ctypes.c_int32),
         ("top_n", ctypes.c_int32), ("local_window", ctypes.c_int32),
+        ("seqlens_q", ctypes.c_void_p), ("seqlens_kv", ctypes.c_void_p),
+        ("bottom_right", ctypes.c_int32),
     ]
 
 
@@ -99,7 +101,7 @@ def _ptr(a):
 
 
 def _desc(q, k, v, *, causal, window, scale, bias, block_idx, sel_block, top_n,
-          local_window, in_dtype):
+          local_window, in_dtype, seqlens_q=None, seqlens_kv=None, bottom_right=False):
     B, S, Hq, d = q.shape
     Hkv, dv = k.shape[2], v.shape[3]
     if k.shape != (B, S, Hkv, d) or v.shape != (B, S, Hkv, dv):
@@ -136,6 +138,14 @@ def _desc(q, k, v, *, causal, window, scale, bias, block_idx, sel_block, top_n,
         keep.append(bi)
         D.block_idx = bi.ctypes.data
         D.sel_block, D.top_n, D.local_window = sel_block, top_n, local_window
+    for name, lens in (("seqlens_q", seqlens_q), ("seqlens_kv", seqlens_kv)):
+        if lens is not None:
+            ln = np.ascontiguousarray(lens, dtype=np.int32)
+            if ln.shape != (B,) or ln.min() < 0 or ln.max() > S:
+                raise ValueError(f"{name} must be [B] with values in [0, S]")
+            keep.append(ln)
+            setattr(D, name, ln.ctypes.data)
+    D.bottom_right = int(bool(bottom_right))
     return D, keep
 
 
@@ -145,12 +155,14 @@ def _check(rc, what):
 
 
 def attention_fwd(q, k, v, *, causal=False, window=None, scale=None, bias=None,
-                  block_idx=None, sel_block=32, top_n=8, local_window=32):
+                  block_idx=None, sel_block=32, top_n=8, local_window=32, seqlens_q=None,
+                  seqlens_kv=None, bottom_right=False):
     """One-shot masked softmax attention.  Returns (o, m, l) in float64."""
     (q, dt), (k, _), (v, _) = _in(q), _in(k), _in(v)
     D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
                     block_idx=block_idx, sel_block=sel_block, top_n=top_n,
-                    local_window=local_window, in_dtype=dt)
+                    local_window=local_window, in_dtype=dt, seqlens_q=seqlens_q,
+                    seqlens_kv=seqlens_kv, bottom_right=bottom_right)
     B, S, Hq, _ = q.shape
     o = np.zeros((B, S, Hq, v.shape[3]))
     m = np.zeros((B, Hq, S))
@@ -161,12 +173,14 @@ def attention_fwd(q, k, v, *, causal=False, window=None, scale=None, bias=None,
 
 
 def attention_bwd(q, k, v, dout, *, causal=False, window=None, scale=None, bias=None,
-                  block_idx=None, sel_block=32, top_n=8, local_window=32):
+                  block_idx=None, sel_block=32, top_n=8, local_window=32, seqlens_q=None,
+                  seqlens_kv=None, bottom_right=False):
     """Analytic gradients.  Returns (dq, dk, dv, o, m, l) in float64."""
     (q, dt), (k, _), (v, _), (dout, _) = _in(q), _in(k), _in(v), _in(dout)
     D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
                     block_idx=block_idx, sel_block=sel_block, top_n=top_n,
-                    local_window=local_window, in_dtype=dt)
+                    local_window=local_window, in_dtype=dt, seqlens_q=seqlens_q,
+                    seqlens_kv=seqlens_kv, bottom_right=bottom_right)
     B, S, Hq, d = q.shape
     Hkv, dv_ = k.shape[2], v.shape[3]
     dq = np.zeros((B, S, Hq, d))
@@ -196,13 +210,15 @@ def blockwise_fwd(q, k, v, *, query_chunk, key_chunk, ring_size=1, causal=False,
     return o, m, l
 
 
-def rows(q, k, v, dout, row_list, *, causal=False, window=None, scale=None, bias=None):
+def rows(q, k, v, dout, row_list, *, causal=False, window=None, scale=None, bias=None,
+         seqlens_q=None, seqlens_kv=None, bottom_right=False):
     """O, m, l and dQ of the sampled (b, h, q) rows.  dout may be None (no dQ)."""
     (q, dt), (k, _), (v, _) = _in(q), _in(k), _in(v)
     if dout is not None:
         dout, _ = _in(dout)
     D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
-                    block_idx=None, sel_block=32, top_n=8, local_window=32, in_dtype=dt)
+                    block_idx=None, sel_block=32, top_n=8, local_window=32, in_dtype=dt,
+                    seqlens_q=seqlens_q, seqlens_kv=seqlens_kv, bottom_right=bottom_right)
     rl = np.ascontiguousarray(np.asarray(row_list, dtype=np.int32).reshape(-1, 3))
     n = rl.shape[0]
     o = np.zeros((n, v.shape[3]))
@@ -215,11 +231,12 @@ def rows(q, k, v, dout, row_list, *, causal=False, window=None, scale=None, bias
 
 
 def keys(q, k, v, dout, b, g, key_list, *, causal=False, window=None, scale=None,
-         bias=None):
+         bias=None, seqlens_q=None, seqlens_kv=None, bottom_right=False):
     """dK and dV of the sampled keys of kv head g at batch b."""
     (q, dt), (k, _), (v, _), (dout, _) = _in(q), _in(k), _in(v), _in(dout)
     D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
-                    block_idx=None, sel_block=32, top_n=8, local_window=32, in_dtype=dt)
+                    block_idx=None, sel_block=32, top_n=8, local_window=32, in_dtype=dt,
+                    seqlens_q=seqlens_q, seqlens_kv=seqlens_kv, bottom_right=bottom_right)
     kl = np.ascontiguousarray(np.asarray(key_list, dtype=np.int32).reshape(-1))
     n = kl.shape[0]
     dk = np.zeros((n, q.shape[3]))

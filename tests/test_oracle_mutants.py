@@ -20,9 +20,11 @@ MUTANTS = [
     ("bias_dropped", "+ bias_at(D, b, h, q, k);", ";"),
     ("ds_sign", "double dS = P * (dP - Dq);", "double dS = P * (dP + Dq);"),
     ("gqa_head_map", "int g = h / G;", "int g = h % D->Hkv;"),
-    ("window_left_off_by_one", "k < q - D->window_left) return 0;", "k <= q - D->window_left) return 0;"),
-    ("window_right_range", "z = q + D->window_right;", "z = q + D->window_right - 1;"),
-    ("causal_excludes_diagonal", "if (D->causal && k > q) return 0;", "if (D->causal && k >= q) return 0;"),
+    ("window_left_off_by_one", "k < q + off - D->window_left) return 0;", "k <= q + off - D->window_left) return 0;"),
+    ("window_right_range", "z = c + D->window_right;", "z = c + D->window_right - 1;"),
+    ("causal_excludes_diagonal", "if (D->causal && k > q + off) return 0;", "if (D->causal && k >= q + off) return 0;"),
+    ("varlen_keys_not_cut", "if (q >= lq || k >= lk) return 0;", "if (q >= lq) return 0;"),
+    ("bottom_right_offset_sign", "*off = D->bottom_right ? nk - nq : 0;", "*off = D->bottom_right ? nq - nk : 0;"),
     ("dk_transposed_operand", "dkr[c] = dkr[c] + D->scale * dS * qrow[c];",
      "dkr[c] = dkr[c] + D->scale * dS * kr[c];", 1),
     ("dq_scale_dropped", "dqrow[c] = dqrow[c] + D->scale * dS * kr[c];", "dqrow[c] = dqrow[c] + dS * kr[c];"),
@@ -59,6 +61,9 @@ def battery(ora):
     yield lambda: pins.test_select_ties_keep_lower_block(ora)
     yield lambda: pins.test_select_fewer_candidates_than_top_n(ora)
     yield lambda: pins.test_block_selected_attention_matches_brute_force(ora)
+    for case in pins.VARLEN_CASES:
+        yield lambda case=case: pins.test_varlen_matches_rebuilt_problems(ora, case, dict(causal=True, window=(3, 0)))
+    yield lambda: pins.test_varlen_padding_is_inert(ora)
 
 
 def _build_mutant(tmp_path, name, text):

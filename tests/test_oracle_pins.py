@@ -364,6 +364,128 @@ def test_block_selected_gradients_match_finite_differences(ora):
 
 
 # --------------------------------------------------------------------------
+# variable lengths (TransformerEngine page, section 1: SequenceDescriptor)
+# --------------------------------------------------------------------------
+def varlen_via_brute(q, k, v, lq, lk, bottom_right, causal, window, scale):
+    """Each batch entry rebuilt as an ordinary problem on one position axis: key j at
+    position j + shift, query i at i + off + shift (off = Lk - Lq when the queries are the
+    last Lq positions of the key sequence, else 0); positions that hold no key get a
+    -1e300 bias so they carry no weight.  Rows whose best score is that bias have no real
+    key (O = 0, m = -inf, l = 0).  Returns (o, m, l) in the padded layout."""
+    B, S, Hq, d = q.shape
+    Hkv, dv = k.shape[2], v.shape[3]
+    o = np.zeros((B, S, Hq, dv))
+    m = np.full((B, Hq, S), -np.inf)
+    l = np.zeros((B, Hq, S))
+    for b in range(B):
+        nq, nk = int(lq[b]), int(lk[b])
+        if nq == 0:
+            continue
+        off = nk - nq if bottom_right else 0
+        shift = max(0, -off)
+        n = max(nk, nq + off) + shift
+        qe = np.zeros((1, n, Hq, d))
+        ke = np.zeros((1, n, Hkv, d))
+        ve = np.zeros((1, n, Hkv, dv))
+        qe[0, off + shift:off + shift + nq] = q[b, :nq]
+        ke[0, shift:shift + nk] = k[b, :nk]
+        ve[0, shift:shift + nk] = v[b, :nk]
+        bias = np.full((1, 1, 1, n), -1e300)
+        bias[..., shift:shift + nk] = 0.0
+        eo, em, el = brute_force(qe, ke, ve, causal=causal, window=window, scale=scale, bias=bias)
+        rows = slice(off + shift, off + shift + nq)
+        real = em[0, :, rows] > -1e200            # [Hq, nq]
+        o[b, :nq] = np.where(real.T[..., None], eo[0, rows], 0.0)
+        m[b, :, :nq] = np.where(real, em[0, :, rows], -np.inf)
+        l[b, :, :nq] = np.where(real, el[0, :, rows], 0.0)
+    return o, m, l
+
+
+VARLEN_CASES = [   # (query lengths, key lengths or None (the query lengths), bottom-right)
+    ([12, 7, 5, 0], None, False),
+    ([12, 7, 5, 3], [12, 9, 3, 6], False),
+    ([12, 4, 5, 1], [12, 9, 11, 6], True),
+    ([9, 12, 2, 7], [5, 6, 12, 0], True),
+]
+
+
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=["same", "topleft", "bottomright", "bottomright_short_keys"])
+@pytest.mark.parametrize("mask", [dict(causal=True, window=(-1, -1)), dict(causal=False, window=(-1, -1)),
+                                  dict(causal=True, window=(3, 0)), dict(causal=False, window=(2, 1))],
+                         ids=["causal", "full", "swa3", "win2_1"])
+def test_varlen_matches_rebuilt_problems(ora, case, mask):
+    lq, lk, br = case
+    B, S, Hq, Hkv, d, dv = 4, 12, 4, 2, 3, 2
+    q, k, v = rnd((B, S, Hq, d), 161), rnd((B, S, Hkv, d), 162), rnd((B, S, Hkv, dv), 163)
+    kw = dict(scale=0.7, **mask)
+    o, m, l = ora.attention_fwd(q, k, v, seqlens_q=lq, seqlens_kv=lk, bottom_right=br, **kw)
+    bo, bm, bl = varlen_via_brute(q, k, v, lq, lq if lk is None else lk, br, **kw)
+    np.testing.assert_allclose(o, bo, rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(np.isfinite(m), np.isfinite(bm))
+    fin = np.isfinite(bm)
+    np.testing.assert_allclose(m[fin], bm[fin], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l, bl, rtol=1e-12, atol=1e-13)
+
+
+def test_varlen_padding_is_inert(ora):
+    # padded positions take part in nothing: changing them changes no output, their own
+    # outputs and gradients are exactly zero
+    B, S, Hq, Hkv, d = 3, 10, 2, 1, 4
+    lq, lk = [10, 6, 3], [10, 8, 2]
+    q, k, v, do = (rnd((B, S, Hq, d), 171), rnd((B, S, Hkv, d), 172), rnd((B, S, Hkv, d), 173),
+                   rnd((B, S, Hq, d), 174))
+    kw = dict(causal=True, seqlens_q=lq, seqlens_kv=lk, bottom_right=True)
+    r1 = ora.attention_bwd(q, k, v, do, **kw)
+    q2, k2, v2, do2 = q.copy(), k.copy(), v.copy(), do.copy()
+    for b in range(B):
+        q2[b, lq[b]:] = 50.0
+        do2[b, lq[b]:] = -7.0
+        k2[b, lk[b]:] = 30.0
+        v2[b, lk[b]:] = 1e6
+    r2 = ora.attention_bwd(q2, k2, v2, do2, **kw)
+    for x, y in zip(r1, r2):
+        np.testing.assert_array_equal(x, y)
+    dq, dk, dvv, o, m, l = r1
+    for b in range(B):
+        assert not dq[b, lq[b]:].any() and not o[b, lq[b]:].any()
+        assert np.all(np.isneginf(m[b, :, lq[b]:])) and not l[b, :, lq[b]:].any()
+        assert not dk[b, lk[b]:].any() and not dvv[b, lk[b]:].any()
+    # the sampled-key evaluation agrees, padded keys included (no causal rule, so that
+    # nothing but the length keeps them out)
+    kw = dict(causal=False, seqlens_q=lq, seqlens_kv=lk)
+    dq, dk, dvv, *_ = ora.attention_bwd(q, k, v, do, **kw)
+    sk, sv = ora.keys(q, k, v, do, 1, 0, [0, 5, 7, 8, 9], **kw)
+    np.testing.assert_allclose(sk, dk[1, [0, 5, 7, 8, 9], 0], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(sv, dvv[1, [0, 5, 7, 8, 9], 0], rtol=1e-12, atol=1e-14)
+    assert not sk[3:].any() and not sv[3:].any() and sk[:3].any()
+
+
+def test_varlen_gradients_match_finite_differences(ora):
+    B, S, Hq, Hkv, d, dv = 2, 6, 2, 1, 2, 2
+    lq, lk = [6, 3], [4, 5]
+    q, k, v, do = (rnd((B, S, Hq, d), 181), rnd((B, S, Hkv, d), 182), rnd((B, S, Hkv, dv), 183),
+                   rnd((B, S, Hq, dv), 184))
+    kw = dict(causal=True, window=(2, 0), scale=0.9)
+    dq, dk, dvv, *_ = ora.attention_bwd(q, k, v, do, seqlens_q=lq, seqlens_kv=lk, bottom_right=True, **kw)
+    h = 1e-6
+
+    def loss(qq, kk, vv):
+        return float((varlen_via_brute(qq, kk, vv, lq, lk, True, **kw)[0] * do).sum())
+
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dvv)):
+        fd = np.zeros_like(x)
+        for ix in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[ix] += h
+            xm[ix] -= h
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            fd[ix] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        err = np.abs(fd - g).max() / max(np.abs(g).max(), 1e-30)
+        assert err < 1e-6, f"d{name}: relative error {err}"
+
+
+# --------------------------------------------------------------------------
 # sampled rows / keys agree with the full evaluation
 # --------------------------------------------------------------------------
 def test_sampled_rows_and_keys_match_full(ora):
