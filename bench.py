@@ -151,7 +151,8 @@ def time_extra_workloads(bpa, dev, peak_tf):
     Inputs are drawn on the device from seeded generators (timing only; the
     parity tests use the numpy recipe)."""
     import torch
-    from ring_attention_gb300.inputs import BLOCK_SEL, BLOCK_SEL_JOINT, GQA_SWA, MLA_CAUSAL, RING_LONG, TINY_F32
+    from ring_attention_gb300.inputs import (BLOCK_SEL, BLOCK_SEL_JOINT, GQA_SWA, MLA_CAUSAL, RING_LONG, TINY_F32,
+                                             VARLEN_CAUSAL)
 
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     out = {}
@@ -173,6 +174,13 @@ def time_extra_workloads(bpa, dev, peak_tf):
             bias[..., w.S - w.pad_tail:] = -1e9
         kw = dict(causal=w.causal, window=w.window, bias=bias, query_chunk=w.query_chunk, key_chunk=w.key_chunk,
                   ring_size=w.ring_size)
+        tok_q = tok_k = w.B * w.S
+        if w.seqlens_q:
+            lens_q = list(w.seqlens_q)
+            lens_k = list(w.seqlens_kv) if w.seqlens_kv else lens_q
+            kw.update(seqlens_q=torch.tensor(lens_q, dtype=torch.int32, device=dev),
+                      seqlens_kv=torch.tensor(lens_k, dtype=torch.int32, device=dev), bottom_right=w.bottom_right)
+            tok_q, tok_k = sum(lens_q), sum(lens_k)
         D = bpa.make_desc(q, k, v, **kw)
         wsf = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_FWD, D), dev)
         wsb = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_BWD, D), dev)
@@ -197,8 +205,9 @@ def time_extra_workloads(bpa, dev, peak_tf):
         mf, mb = statistics.mean(tf), statistics.mean(tb)
         el = 2 if dt == torch.bfloat16 else 4
         d, dv = w.d, w.d_v
-        fwd_bytes = el * w.B * w.S * ((d + dv) * w.Hq + (d + dv) * w.Hkv)    # Q, K, V read, O written
-        bwd_bytes = el * w.B * w.S * ((2 * d + 2 * dv) * w.Hq + (2 * d + 2 * dv) * w.Hkv)   # + dO, O read; dQ, dK, dV
+        # valid tokens only: Q, K, V read, O written; backward + dO, O read, dQ, dK, dV written
+        fwd_bytes = el * (tok_q * (d + dv) * w.Hq + tok_k * (d + dv) * w.Hkv)
+        bwd_bytes = el * (tok_q * (2 * d + 2 * dv) * w.Hq + tok_k * (2 * d + 2 * dv) * w.Hkv)
         res = {"fwd_ms": mf, "bwd_ms": mb, "fwd_tflops": f_fwd / mf / 1e9, "bwd_tflops": f_bwd / mb / 1e9,
                "fwd_pct_peak": 100 * f_fwd / mf / 1e9 / peak_tf, "bwd_pct_peak": 100 * f_bwd / mb / 1e9 / peak_tf,
                "fwd_min_bytes_gbs": fwd_bytes / mf / 1e6, "bwd_min_bytes_gbs": bwd_bytes / mb / 1e6,
@@ -211,6 +220,7 @@ def time_extra_workloads(bpa, dev, peak_tf):
     out[TINY_F32.name] = fwd_bwd(TINY_F32, 20, 3)
     out[RING_LONG.name] = fwd_bwd(RING_LONG, 2, 1)
     out[MLA_CAUSAL.name] = fwd_bwd(MLA_CAUSAL, 10, 3)
+    out[VARLEN_CAUSAL.name] = fwd_bwd(VARLEN_CAUSAL, 10, 3)
 
     def block_selected(w):
         q = rnd((w.B, w.S, w.Hq, w.d), torch.bfloat16, w.seed)

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define BPA_VERSION 2
+#define BPA_VERSION 3
 
 typedef enum {
     BPA_OK = 0,
@@ -104,6 +104,21 @@ typedef struct bpa_attn_desc {
      * head dim d, v and the output with head dim dv). */
     int32_t dv;                /* head dim of v, o, dout and the dv gradient; 0 selects d; <= 512 */
     int64_t o_strides[3];      /* (b, s, h) strides of o and dout; all 0 selects q_strides */
+    /* Fields below were added in descriptor version 3 (bpa_version() >= 3); a version-2
+     * caller (struct_size = offsetof(bpa_attn_desc, seqlens_q)) gets full-length sequences.
+     * Variable lengths follow the sequence descriptor of "JAX: Single-GPU Attention with
+     * TransformerEngine", section 1 (SequenceDescriptor.from_seqlens): batch entry b holds
+     * Lq = seqlens_q[b] queries and Lk = seqlens_kv[b] keys at positions 0..L-1 of the
+     * padded [B, S, H, d] tensors.  Later positions are padding: they attend to nothing
+     * and nothing attends to them; their rows of o, dq get 0, of m -inf, of l 0, and
+     * their rows of dk, dv get 0.  Padding must hold finite numbers (it is read by the
+     * tiled loads and weighted by exactly 0).  Values are clamped to [0, S].  Needs
+     * ring_size 1 and no block selection. */
+    const int32_t* seqlens_q;  /* device int32 [B] or NULL (every entry S) */
+    const int32_t* seqlens_kv; /* device int32 [B] or NULL (the query lengths) */
+    int32_t bottom_right;      /* 0: causal / window diagonal at k = q (top-left, both
+                                * sequences start together); 1: at k = q + Lk - Lq (the
+                                * queries are the last Lq positions of the key sequence) */
 } bpa_attn_desc;
 
 /* Bytes of workspace bpa_fwd (op = BPA_OP_FWD) or bpa_bwd (op = BPA_OP_BWD)

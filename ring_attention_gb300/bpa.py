@@ -44,6 +44,8 @@ class bpa_attn_desc(ctypes.Structure):
         ("block_idx", ctypes.c_void_p), ("sel_block", ctypes.c_int32),
         ("top_n", ctypes.c_int32), ("local_window", ctypes.c_int32),
         ("dv", ctypes.c_int32), ("o_strides", ctypes.c_int64 * 3),
+        ("seqlens_q", ctypes.c_void_p), ("seqlens_kv", ctypes.c_void_p),
+        ("bottom_right", ctypes.c_int32),
     ]
 
 
@@ -117,7 +119,7 @@ def _stream_ptr(stream) -> int:
 
 def make_desc(q, k, v, *, o=None, causal=False, window=(-1, -1), scale=None, bias=None, query_chunk=0,
               key_chunk=0, ring_size=1, ring_steps=None, block_idx=None, sel_block=0, top_n=0,
-              local_window=0) -> bpa_attn_desc:
+              local_window=0, seqlens_q=None, seqlens_kv=None, bottom_right=False) -> bpa_attn_desc:
     """Fill a bpa_attn_desc from torch tensors (no data is touched).  The value head dim
     is v's last dim; o (the output, or dout, which shares its strides) sets o_strides."""
     B, S, Hq, d = q.shape
@@ -153,6 +155,12 @@ def make_desc(q, k, v, *, o=None, causal=False, window=(-1, -1), scale=None, bia
             raise ValueError("block_idx must be a contiguous int32 tensor")
         D.block_idx = block_idx.data_ptr()
         D.sel_block, D.top_n, D.local_window = int(sel_block), int(top_n), int(local_window)
+    for name, lens in (("seqlens_q", seqlens_q), ("seqlens_kv", seqlens_kv)):
+        if lens is not None:
+            if lens.dtype != torch.int32 or lens.shape != (B,) or not lens.is_contiguous() or lens.device != q.device:
+                raise ValueError(f"{name} must be a contiguous int32 [B] tensor on q's device")
+            setattr(D, name, lens.data_ptr())
+    D.bottom_right = int(bool(bottom_right))
     return D
 
 

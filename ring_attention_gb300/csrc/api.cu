@@ -58,11 +58,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // ---- descriptor validation ---------------------------------------------------
 bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     if (!d) return fail(BPA_ERR_INVALID_ARG, "desc is NULL");
-    const size_t v1_size = offsetof(bpa_attn_desc, dv);   // descriptor version 1: no dv, o_strides
-    if (d->struct_size != sizeof(bpa_attn_desc) && d->struct_size != v1_size)
-        return fail(BPA_ERR_INVALID_ARG, "desc->struct_size is %u, expected %zu (or %zu)", d->struct_size,
-                    sizeof(bpa_attn_desc), v1_size);
-    const bool v2 = d->struct_size == sizeof(bpa_attn_desc);
+    const size_t v1_size = offsetof(bpa_attn_desc, dv);          // version 1: no dv, o_strides
+    const size_t v2_size = offsetof(bpa_attn_desc, seqlens_q);   // version 2: no sequence lengths
+    if (d->struct_size != sizeof(bpa_attn_desc) && d->struct_size != v1_size && d->struct_size != v2_size)
+        return fail(BPA_ERR_INVALID_ARG, "desc->struct_size is %u, expected %zu (or %zu, %zu)", d->struct_size,
+                    sizeof(bpa_attn_desc), v2_size, v1_size);
+    const bool v2 = d->struct_size >= v2_size;
+    const bool v3 = d->struct_size == sizeof(bpa_attn_desc);
+    const bool varlen = v3 && (d->seqlens_q || d->seqlens_kv);
     if (d->dtype != BPA_BF16 && d->dtype != BPA_FP32)
         return fail(BPA_ERR_INVALID_ARG, "unknown dtype %d", d->dtype);
     if (d->B < 1 || d->S < 1 || d->Hq < 1 || d->Hkv < 1 || d->d < 1)
@@ -97,6 +100,8 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
         if (d->local_window < 0) return fail(BPA_ERR_INVALID_ARG, "local_window must be >= 0");
         if (n != 1) return fail(BPA_ERR_INVALID_ARG, "block-selected mode needs ring_size 1");
     }
+    if (varlen && (n != 1 || d->block_idx))
+        return fail(BPA_ERR_INVALID_ARG, "sequence lengths need ring_size 1 and no block selection");
     P.B = d->B;
     P.S = d->S;
     P.Hq = d->Hq;
@@ -123,6 +128,9 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     P.ring_n = n;
     P.ring_blk = blk;
     P.block_idx = d->block_idx;
+    P.seqlens_q = varlen ? d->seqlens_q : nullptr;
+    P.seqlens_kv = varlen ? d->seqlens_kv : nullptr;
+    P.bottom_right = v3 && d->bottom_right ? 1 : 0;
     P.sel_block = d->block_idx ? d->sel_block : 0;
     P.top_n = d->block_idx ? d->top_n : 0;
     P.local_window = d->block_idx ? d->local_window : 0;

@@ -26,7 +26,26 @@ struct Problem {
     int ring_n, ring_blk;      // ring_blk = S / ring_n
     const int32_t* block_idx;
     int sel_block, top_n, local_window;
+    const int32_t* seqlens_q;  // device [B] or nullptr: valid queries per batch entry
+    const int32_t* seqlens_kv; // device [B] or nullptr (then the query lengths)
+    int bottom_right;          // diagonal at k = q + Lk - Lq instead of k = q
 };
+
+// Valid query / key counts of one batch entry and the offset of the causal / window
+// diagonal (k is compared with q + off).
+struct Lens {
+    int lq, lk, off;
+};
+
+#ifdef __CUDACC__
+__device__ __forceinline__ Lens lens_of(const Problem& P, int b) {
+    Lens L;
+    L.lq = P.seqlens_q ? min(max(__ldg(P.seqlens_q + b), 0), P.S) : P.S;
+    L.lk = P.seqlens_kv ? min(max(__ldg(P.seqlens_kv + b), 0), P.S) : L.lq;
+    L.off = P.bottom_right ? L.lk - L.lq : 0;
+    return L;
+}
+#endif
 
 struct FwdArgs {
     Problem P;

@@ -85,6 +85,7 @@ struct Work {
     int b, hkv, k0;
     int q_lo, q_hi;      // query rows that may see this key tile (ring block included)
     int qt_lo, n_qt, n_it;
+    int lk, off;         // valid keys of the batch entry, offset of the causal / window diagonal
 };
 
 __device__ __forceinline__ Work decode(const BwdArgs& a) {
@@ -96,17 +97,20 @@ __device__ __forceinline__ Work decode(const BwdArgs& a) {
     w.hkv = r % P.Hkv;
     const int kt = r / P.Hkv;    // lowest key tiles (most causal work) first
     w.k0 = kt * BK;
-    const int k_last = min(w.k0 + BK - 1, P.S - 1);
-    int lo = 0, hi = P.S - 1;
+    const Lens len = lens_of(P, w.b);   // full lengths unless the problem has sequence lengths
+    w.lk = len.lk;
+    w.off = len.off;
+    const int k_last = min(w.k0 + BK - 1, len.lk - 1);
+    int lo = 0, hi = w.k0 < len.lk ? len.lq - 1 : -1;
     if (a.dk_acc) {   // ring step: the query block that meets this key block now
         const int j = w.k0 / P.ring_blk;
         const int iq = (j + a.ring_idx) % P.ring_n;
         lo = iq * P.ring_blk;
         hi = lo + P.ring_blk - 1;
     }
-    if (P.causal) lo = max(lo, w.k0);
-    if (P.wr >= 0) lo = max(lo, w.k0 - P.wr);
-    if (P.wl >= 0) hi = min(hi, k_last + P.wl);
+    if (P.causal) lo = max(lo, w.k0 - w.off);
+    if (P.wr >= 0) lo = max(lo, w.k0 - w.off - P.wr);
+    if (P.wl >= 0) hi = min(hi, k_last - w.off + P.wl);
     w.q_lo = lo;
     w.q_hi = hi;
     w.qt_lo = lo / BQ;
@@ -293,10 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const int k = W.k0 + r;
         int qmin = W.q_lo, qmax = min(W.q_hi, P.S - 1);
-        if (P.causal) qmin = max(qmin, k);
-        if (P.wr >= 0) qmin = max(qmin, k - P.wr);
-        if (P.wl >= 0) qmax = min(qmax, k + P.wl);
-        if (k >= P.S) qmax = -1;
+        if (P.causal) qmin = max(qmin, k - W.off);
+        if (P.wr >= 0) qmin = max(qmin, k - W.off - P.wr);
+        if (P.wl >= 0) qmax = min(qmax, k - W.off + P.wl);
+        if (k >= W.lk) qmax = -1;
         const float sl2 = P.scale * kLog2e;
         bool aborted = false;
 

@@ -85,6 +85,7 @@ struct Tile {
     int kt0;                 // first key tile visited by the CTA
     int n;                   // key tiles visited by the CTA
     int lo[2], hi[2];        // per query tile: visited step range [lo, hi] (empty if lo > hi)
+    int lq, off;             // valid query rows of the batch entry, offset of the causal / window diagonal
 };
 
 // Work item `item` (heaviest causal query pairs first) -> its query tiles and key range.
@@ -102,8 +103,11 @@ __device__ __forceinline__ Tile decode_tile(const FwdArgs& a, int item) {
     const int qp = nqp - 1 - r / P.B;   // heaviest (causal) query pairs first
     t.h = t.hkv * P.G + gi;
     t.q0 = qp * NQ * BM;
+    const Lens len = lens_of(P, t.b);   // full lengths unless the problem has sequence lengths
+    t.lq = len.lq;
+    t.off = len.off;
     t.rlo = 0;
-    t.rhi = P.S - 1;
+    t.rhi = len.lk - 1;
     if (a.acc) {
         const int i = t.q0 / P.ring_blk;
         const int j = ((i - a.ring_idx) % P.ring_n + P.ring_n) % P.ring_n;
@@ -114,12 +118,12 @@ __device__ __forceinline__ Tile decode_tile(const FwdArgs& a, int item) {
     int ulo = 1 << 30, uhi = -1;
 #pragma unroll
     for (int i = 0; i < NQ; ++i) {
-        const int qa = t.q0 + i * BM, qb = min(qa + BM - 1, P.S - 1);
+        const int qa = t.q0 + i * BM, qb = min(qa + BM - 1, t.lq - 1);
         int lo = t.rlo, hi = t.rhi;
-        if (qa >= P.S) hi = -1;
-        if (P.causal) hi = min(hi, qb);
-        if (P.wr >= 0) hi = min(hi, qb + P.wr);
-        if (P.wl >= 0) lo = max(lo, qa - P.wl);
+        if (qa >= t.lq) hi = -1;
+        if (P.causal) hi = min(hi, qb + t.off);
+        if (P.wr >= 0) hi = min(hi, qb + t.off + P.wr);
+        if (P.wl >= 0) lo = max(lo, qa + t.off - P.wl);
         if (lo <= hi) {
             ktlo[i] = lo / BN;
             kthi[i] = hi / BN;
@@ -582,10 +586,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
             const Tile T = decode_tile<NQ>(a, item);
             const int q = T.q0 + qt * BM + t;
             int kmin = T.rlo, kmax = min(T.rhi, P.S - 1);
-            if (P.causal) kmax = min(kmax, q);
-            if (P.wr >= 0) kmax = min(kmax, q + P.wr);
-            if (P.wl >= 0) kmin = max(kmin, q - P.wl);
-            if (q >= P.S) kmax = -1;              // padding row: nothing allowed
+            if (P.causal) kmax = min(kmax, q + T.off);
+            if (P.wr >= 0) kmax = min(kmax, q + T.off + P.wr);
+            if (P.wl >= 0) kmin = max(kmin, q + T.off - P.wl);
+            if (q >= T.lq) kmax = -1;             // padding row: nothing allowed
             const float* bias_row =
                 P.bias ? P.bias + T.b * P.bs[0] + T.h * P.bs[1] + static_cast<int64_t>(min(q, P.S - 1)) * P.bs[2]
                        : nullptr;

@@ -72,14 +72,29 @@ __device__ __forceinline__ bool selected(const Problem& P, int b, int h, int q, 
 }
 
 __device__ __forceinline__ bool allowed(const Problem& P, int b, int h, int q, int k) {
-    if (P.causal && k > q) return false;
-    if (P.wl >= 0 && k < q - P.wl) return false;
-    if (P.wr >= 0 && k > q + P.wr) return false;
+    const Lens L = lens_of(P, b);
+    if (q >= L.lq || k >= L.lk) return false;   // padding
+    const int c = q + L.off;                    // the diagonal key of row q
+    if (P.causal && k > c) return false;
+    if (P.wl >= 0 && k < c - P.wl) return false;
+    if (P.wr >= 0 && k > c + P.wr) return false;
     if (P.block_idx) {
         bool local = k <= q && k > q - P.local_window;
         if (!local && !selected(P, b, h, q, k / P.sel_block)) return false;
     }
     return true;
+}
+
+// Narrows [lo, hi] to the keys that can be allowed for query q of batch entry b
+// (lengths, causal / window diagonal).
+__device__ __forceinline__ void key_span(const Problem& P, int b, int q, int& lo, int& hi) {
+    const Lens L = lens_of(P, b);
+    const int c = q + L.off;
+    hi = min(hi, L.lk - 1);
+    if (q >= L.lq) hi = -1;
+    if (P.causal) hi = min(hi, c);
+    if (P.wr >= 0) hi = min(hi, c + P.wr);
+    if (P.wl >= 0) lo = max(lo, c - P.wl);
 }
 
 __device__ __forceinline__ float bias_at(const Problem& P, int b, int h, int q, int k) {
@@ -151,9 +166,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
         __syncwarp();
         int lo, hi;
         ring_range(P, ring, a.ring_idx, q, lo, hi);
-        if (P.causal) hi = min(hi, q);
-        if (P.wr >= 0) hi = min(hi, q + P.wr);
-        if (P.wl >= 0) lo = max(lo, q - P.wl);
+        key_span(P, b, q, lo, hi);
         RowState<KP> st;
         st.m = -INFINITY;
         st.l = 0.f;
@@ -272,9 +285,7 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dq_simt(const BwdArgs a) {
 #pragma unroll
         for (int i = 0; i < KP; ++i) acc[i] = 0.f;
         int lo = 0, hi = P.S - 1;
-        if (P.causal) hi = min(hi, q);
-        if (P.wr >= 0) hi = min(hi, q + P.wr);
-        if (P.wl >= 0) lo = max(lo, q - P.wl);
+        key_span(P, b, q, lo, hi);
         if (lse != INFINITY && lo <= hi) {
             if (!P.block_idx) {
                 dq_keys<T, KP>(P, b, h, g, q, lo, hi, sq[warp], sdo[warp], lse, Dq, acc);
@@ -372,9 +383,13 @@ __global__ void __launch_bounds__(kWarps * 32) k_bwd_dkdv_simt(const BwdArgs a) 
 #pragma unroll
         for (int i = 0; i < KP; ++i) dk[i] = dv[i] = 0.f;
         int lo = 0, hi = P.S - 1;  // queries that may see key k
-        if (P.causal) lo = max(lo, k);
-        if (P.wr >= 0) lo = max(lo, k - P.wr);
-        if (P.wl >= 0) hi = min(hi, k + P.wl);
+        {
+            const Lens L = lens_of(P, b);
+            hi = k < L.lk ? L.lq - 1 : -1;
+            if (P.causal) lo = max(lo, k - L.off);
+            if (P.wr >= 0) lo = max(lo, k - L.off - P.wr);
+            if (P.wl >= 0) hi = min(hi, k - L.off + P.wl);
+        }
         for (int h = g * P.G; h < (g + 1) * P.G && lo <= hi; ++h) {
             if (!P.block_idx) {
                 dkdv_queries<T, KP>(a, b, h, k, lo, hi, sk[warp], sv[warp], dk, dv);

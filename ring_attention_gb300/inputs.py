@@ -50,6 +50,9 @@ class Workload:
     local_window: int = 0
     backward: bool = True
     dv: int = 0                  # head dim of v and dO; 0 = d
+    seqlens_q: tuple = ()        # per batch entry: valid queries (empty: all S)
+    seqlens_kv: tuple = ()       # valid keys (empty: the query lengths)
+    bottom_right: bool = False   # causal / window diagonal at k = q + Lk - Lq
     extra: dict = field(default_factory=dict, compare=False)
 
     @property
@@ -81,8 +84,15 @@ MLA_CAUSAL = Workload("mla_causal_B2_S4096_Hq128_Hkv8_dqk128_dv64", B=2, S=4096,
 BLOCK_SEL_JOINT = Workload("blocksel_joint_top8_B4_S8192_H1_d512", B=4, S=8192, Hq=1, Hkv=1, d=512,
                            causal=True, seed=4, sel_block=32, top_n=8, local_window=32)
 
+# Variable-length (padded) batch of the GQA causal shape: eight sequences of mixed
+# lengths in [B, 4096, H, d] tensors (the TransformerEngine page's sequence descriptor
+# with padding), lengths chosen to straddle tile boundaries.
+VARLEN_CAUSAL = Workload("varlen_gqa_causal_B8_S4096_Hq32_Hkv8_d128", B=8, S=4096, Hq=32, Hkv=8, d=128,
+                         causal=True, seed=2028,
+                         seqlens_q=(4096, 3511, 2987, 2048, 1536, 1023, 700, 129))
+
 WORKLOADS = {w.name: w for w in (TINY_F32, GQA_CAUSAL, GQA_SWA, RING_LONG, BLOCK_SEL)}
-EXTRA_WORKLOADS = {w.name: w for w in (MLA_CAUSAL, BLOCK_SEL_JOINT)}
+EXTRA_WORKLOADS = {w.name: w for w in (MLA_CAUSAL, BLOCK_SEL_JOINT, VARLEN_CAUSAL)}
 
 
 def draw(shape_list, seed: int, dtype: str):
@@ -122,19 +132,25 @@ def make_inputs(w: Workload, *, S: int | None = None, B: int | None = None,
 
 
 def unmasked_entries(w: Workload, S: int | None = None) -> int:
-    """Number of (query, key) pairs the causal / window mask allows, times B*Hq.
+    """Number of (query, key) pairs the lengths and the causal / window mask allow,
+    summed over the batch, times Hq.
 
     Counts positions only (a key with a -1e9 padding bias still counts)."""
     S = w.S if S is None else S
-    qpos = np.arange(S, dtype=np.int64)
-    lo = np.zeros(S, dtype=np.int64)
-    hi = np.full(S, S - 1, dtype=np.int64)
-    if w.causal:
-        hi = np.minimum(hi, qpos)
-    wl, wr = w.window
-    if wr >= 0:
-        hi = np.minimum(hi, qpos + wr)
-    if wl >= 0:
-        lo = np.maximum(lo, qpos - wl)
-    per_head = int(np.maximum(hi - lo + 1, 0).sum())
-    return per_head * w.B * w.Hq
+    total = 0
+    for b in range(w.B):
+        lq = w.seqlens_q[b] if w.seqlens_q else S
+        lk = w.seqlens_kv[b] if w.seqlens_kv else lq
+        off = lk - lq if w.bottom_right else 0
+        c = np.arange(lq, dtype=np.int64) + off
+        lo = np.zeros(lq, dtype=np.int64)
+        hi = np.full(lq, lk - 1, dtype=np.int64)
+        if w.causal:
+            hi = np.minimum(hi, c)
+        wl, wr = w.window
+        if wr >= 0:
+            hi = np.minimum(hi, c + wr)
+        if wl >= 0:
+            lo = np.maximum(lo, c - wl)
+        total += int(np.maximum(hi - lo + 1, 0).sum())
+    return total * w.Hq

@@ -142,7 +142,7 @@ def test_select_rejects_bad_arguments(bpa):
 def test_status_strings(bpa):
     L = bpa.lib()
     assert L.bpa_status_string(5) == b"BPA_ERR_TIMEOUT"
-    assert L.bpa_version() == 2
+    assert L.bpa_version() == 3
 
 
 def test_version_1_descriptor_is_accepted(bpa):
@@ -155,6 +155,26 @@ def test_version_1_descriptor_is_accepted(bpa):
     assert L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(D)) == full
     D.struct_size = bpa.bpa_attn_desc.dv.offset + 4
     assert L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(D)) == 0
+    # version 2: no sequence lengths; the fields past the shorter struct are not read
+    D = _desc(bpa, seqlens_q=0x1000, ring_size=2)
+    D.struct_size = bpa.bpa_attn_desc.seqlens_q.offset
+    assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) > 0
+
+
+def test_sequence_lengths_checks(bpa):
+    L = bpa.lib()
+    p = 0x80000
+    for over in (dict(ring_size=2), dict(block_idx=0x1000, sel_block=32, top_n=8, local_window=32)):
+        for field in ("seqlens_q", "seqlens_kv"):
+            D = _desc(bpa, **{field: 0x2000}, **over)
+            assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) == 0
+            assert b"sequence lengths" in L.bpa_last_error()
+            assert L.bpa_fwd(ctypes.byref(D), p, p, p, p, 1 << 30, None) == bpa.BPA_ERR_INVALID_ARG
+    # lengths with the full-sequence layout need no more workspace
+    D0 = _desc(bpa)
+    D1 = _desc(bpa, seqlens_q=0x2000, seqlens_kv=0x3000, bottom_right=1)
+    assert L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(D1)) == L.bpa_workspace_size(
+        bpa.BPA_OP_BWD, ctypes.byref(D0))
 
 
 def test_value_head_dim_checks_and_sizes(bpa):

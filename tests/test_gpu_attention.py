@@ -343,6 +343,48 @@ def test_fp32_head_dim_512(bpa, ora):
         assert max_abs(host(got), ref) <= FP32_MAX_ABS
 
 
+VARLEN = [   # (query lengths, key lengths or None, bottom-right)
+    ([300, 129, 1, 0], None, False),
+    ([300, 77, 256, 5], [300, 200, 129, 0], False),
+    ([64, 129, 300, 2], [300, 131, 257, 300], True),
+    ([300, 200, 17, 128], [150, 128, 3, 300], True),
+]
+
+
+@pytest.mark.parametrize("case", VARLEN, ids=["same", "topleft", "bottomright", "bottomright_short_keys"])
+@pytest.mark.parametrize("mask", [MASKS[0], MASKS[1], MASKS[2], MASKS[3]], ids=_mask_id)
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("f32", 64)], ids=["bf16_d128", "bf16_d64", "f32"])
+def test_variable_lengths(bpa, ora, case, mask, dtype, d):
+    # padded batches: per-entry query / key lengths crossing tile boundaries, empty
+    # entries, both diagonal alignments; the padding holds random finite numbers
+    lq, lk, br = case
+    B, S, Hq, Hkv = 4, 300, 4, 2
+    q, k, v, do = draw([(B, S, Hq, d), (B, S, Hkv, d), (B, S, Hkv, d), (B, S, Hq, d)], 81 + d, dtype)
+    tlq = torch.tensor(lq, dtype=torch.int32, device="cuda")
+    tlk = None if lk is None else torch.tensor(lk, dtype=torch.int32, device="cuda")
+    kw = dict(seqlens_q=tlq, seqlens_kv=tlk, bottom_right=br, **mask)
+    tq, tk, tv = dev(q), dev(k), dev(v)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, **kw)
+    dq, dk, dvv = bpa.bpa_bwd(tq, tk, tv, o, dev(do), m, l, **kw)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, seqlens_q=lq, seqlens_kv=lk, bottom_right=br, **mask)
+    check_stats(m, l, rm, rl)
+    if dtype == "f32":
+        for got, ref in ((o, ro), (dq, rq), (dk, rk), (dvv, rv)):
+            assert max_abs(host(got), ref) <= FP32_MAX_ABS
+    else:
+        assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+        for got, ref in ((dq, rq), (dk, rk), (dvv, rv)):
+            assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2
+    # padding rows are exactly zero
+    lkk = lq if lk is None else lk
+    for b in range(B):
+        assert float(o[b, lq[b]:].abs().max() if lq[b] < S else 0) == 0.0
+        assert float(dq[b, lq[b]:].abs().max() if lq[b] < S else 0) == 0.0
+        assert float(dk[b, lkk[b]:].abs().max() if lkk[b] < S else 0) == 0.0
+        assert float(dvv[b, lkk[b]:].abs().max() if lkk[b] < S else 0) == 0.0
+
+
 def test_bounded_wait_reports_timeout(bpa):
     ws = bpa.workspace(256, "cuda")
     bpa.bpa_debug_wait_timeout(ws, 200_000_000)   # 0.2 s

@@ -174,6 +174,24 @@ def test_block_selected_joint_workload_reduced(bpa, ora):
     assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
 
 
+def test_varlen_workload_reduced(bpa, ora):
+    # the variable-length workload's recipe and lengths with fewer heads (GQA ratio 4)
+    w = W.VARLEN_CAUSAL
+    q, k, v, do, _ = W.make_inputs(w, Hq=8, Hkv=2)
+    lq = list(w.seqlens_q)
+    tl = torch.tensor(lq, dtype=torch.int32, device="cuda")
+    tq, tk, tv = dev(q), dev(k), dev(v)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, causal=True, seqlens_q=tl)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, dev(do), m, l, causal=True, seqlens_q=tl)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, causal=True, seqlens_q=lq)
+    assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+    check_stats(m, l, rm, rl)
+    assert rel_l2(host(dq), rq) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dk), rk) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
+
+
 def test_mla_workload_reduced(bpa, ora):
     # the separate-value-head-dim workload (d_qk 128, d_v 64, causal) on a reduced
     # sequence and head count with the same recipe and GQA ratio 16

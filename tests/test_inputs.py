@@ -1,0 +1,34 @@
+"""Host-side helpers of the seeded inputs: the entry count the throughput figures
+divide by agrees with the oracle's own mask (with q = k = 0 every allowed key has
+weight 1, so the row sums l count the allowed keys)."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+from ring_attention_gb300 import inputs as W
+
+
+@pytest.mark.parametrize("w", [
+    W.Workload("t_causal", B=2, S=40, Hq=2, Hkv=1, d=4, causal=True),
+    W.Workload("t_swa", B=1, S=40, Hq=3, Hkv=1, d=4, causal=True, window=(5, 0)),
+    W.Workload("t_win", B=1, S=40, Hq=1, Hkv=1, d=4, window=(3, 7)),
+    W.Workload("t_varlen", B=3, S=40, Hq=2, Hkv=2, d=4, causal=True, seqlens_q=(40, 17, 0)),
+    W.Workload("t_varlen_br", B=3, S=40, Hq=2, Hkv=1, d=4, causal=True, window=(6, 0),
+               seqlens_q=(9, 40, 3), seqlens_kv=(30, 12, 0), bottom_right=True),
+], ids=lambda w: w.name)
+def test_unmasked_entries_counts_allowed_pairs(ora, w):
+    z = np.zeros((w.B, w.S, w.Hq, w.d))
+    zk = np.zeros((w.B, w.S, w.Hkv, w.d))
+    _, _, l = ora.attention_fwd(z, zk, zk, causal=w.causal, window=w.window,
+                                seqlens_q=list(w.seqlens_q) or None,
+                                seqlens_kv=list(w.seqlens_kv) or None, bottom_right=w.bottom_right)
+    assert W.unmasked_entries(w) == int(round(l.sum()))
+
+
+def test_named_workload_counts():
+    assert W.unmasked_entries(W.GQA_CAUSAL) == 2 * 32 * 4096 * 4097 // 2
+    full = replace(W.VARLEN_CAUSAL, seqlens_q=())
+    assert W.unmasked_entries(W.VARLEN_CAUSAL) < W.unmasked_entries(full)
+    lens = W.VARLEN_CAUSAL.seqlens_q
+    assert W.unmasked_entries(W.VARLEN_CAUSAL) == 32 * sum(n * (n + 1) // 2 for n in lens)
