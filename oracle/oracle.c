@@ -45,7 +45,14 @@
  *     padding, take part in nothing and get O = 0, m = -inf, l = 0 and zero
  *     gradients; the causal / window rule compares k with q + off, off = 0
  *     (top-left) or Lk - Lq (bottom-right: the queries are the last Lq
- *     positions of the key sequence).
+ *     positions of the key sequence);
+ *   - sink attention ([te] "Other attention knobs", softmax_type off_by_one
+ *     or learnable; the page names it without a formula): every valid row's
+ *     softmax denominator gains exp(sink[h]), an extra logit with no value
+ *     vector (off_by_one: sink = 0):  P = exp(z) / (exp(sink) + sum exp(z));
+ *     m and l include it (m = max(max z, sink)), so a row with no allowed key
+ *     has O = 0, m = sink, l = 1; the sink's gradient is
+ *     dsink[h] = -sum over rows of P_sink * <dO, O>.
  */
 #include <math.h>
 #include <stdint.h>
@@ -69,6 +76,8 @@ typedef struct {
     const int32_t* seqlens_q;       /* NULL or [B]: valid queries per batch entry */
     const int32_t* seqlens_kv;      /* NULL or [B]: valid keys (NULL: seqlens_q) */
     int32_t bottom_right;           /* 1: causal / window diagonal at k = q + Lk - Lq */
+    const double* sink;             /* NULL or [Hq]: extra softmax logit per q head */
+    double* dsink;                  /* NULL or [Hq]: gradient of sink (written by ora_bwd) */
 } ora_desc;
 
 /* ---- element access: inputs are widened exactly to double ------------- */
@@ -180,21 +189,28 @@ static int row_forward(const ora_desc* D, const double* qrow, const double* Kh,
     int lo, hi;
     key_range(D, b, q, &lo, &hi);
     double m = -INFINITY;
+    int any = 0;
     for (int k = lo; k <= hi; ++k) {
         if (allowed(D, b, h, q, k)) {
             z[k] = score(D, qrow, Kh, b, h, q, k);
             if (z[k] > m) m = z[k];
+            any = 1;
         } else {
             z[k] = -INFINITY;
         }
     }
+    int lq, lk, off;
+    lengths(D, b, &lq, &lk, &off);
+    const int with_sink = D->sink != NULL && q < lq;   /* padding rows take part in nothing */
+    const double sk = with_sink ? D->sink[h] : -INFINITY;
+    if (sk > m) m = sk;
     for (int c = 0; c < D->dv; ++c) o[c] = 0.0;
     if (m == -INFINITY) {
         *m_out = -INFINITY;
         *l_out = 0.0;
         return 0;
     }
-    double l = 0.0;
+    double l = with_sink ? exp(sk - m) : 0.0;
     for (int k = lo; k <= hi; ++k)
         if (z[k] != -INFINITY) l = l + exp(z[k] - m);
     for (int k = lo; k <= hi; ++k) {
@@ -205,7 +221,7 @@ static int row_forward(const ora_desc* D, const double* qrow, const double* Kh,
     }
     *m_out = m;
     *l_out = l;
-    return 1;
+    return any;
 }
 
 static const double* head(const double* X, const ora_desc* D, int b, int g, int w) {
@@ -270,6 +286,9 @@ int ora_bwd(const ora_desc* D, const void* q, const void* k, const void* v,
     memset(dq, 0, sizeof(double) * (size_t)D->B * D->S * D->Hq * D->d);
     memset(dk, 0, sizeof(double) * (size_t)D->B * D->S * D->Hkv * D->d);
     memset(dv, 0, sizeof(double) * (size_t)D->B * D->S * D->Hkv * D->dv);
+    /* per (b, h) partial sums of the sink gradient, added in a fixed order at the end */
+    double* ds_part = D->dsink ? (double*)calloc((size_t)D->B * D->Hq, sizeof(double)) : NULL;
+    if (D->dsink && !ds_part) { free(Kw); free(Vw); return 1; }
 #pragma omp parallel
     {
         double* z = (double*)malloc((size_t)D->S * sizeof(double));
@@ -300,6 +319,7 @@ int ora_bwd(const ora_desc* D, const void* q, const void* k, const void* v,
                         if (l_out) l_out[ml] = l;
                         if (!any) continue;
                         double Dq = dot(dorow, orow, D->dv);
+                        if (ds_part) ds_part[b * D->Hq + h] -= exp(D->sink[h] - m) / l * Dq;
                         double* dqrow = dq + (((int64_t)b * D->S + s) * D->Hq + h) * D->d;
                         int lo, hi;
                         key_range(D, b, s, &lo, &hi);
@@ -326,6 +346,14 @@ int ora_bwd(const ora_desc* D, const void* q, const void* k, const void* v,
         free(qrow);
         free(dorow);
         free(orow);
+    }
+    if (ds_part) {
+        for (int h = 0; h < D->Hq; ++h) {
+            double acc = 0.0;
+            for (int b = 0; b < D->B; ++b) acc = acc + ds_part[b * D->Hq + h];
+            D->dsink[h] = acc;
+        }
+        free(ds_part);
     }
     free(Kw);
     free(Vw);

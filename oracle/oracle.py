@@ -49,6 +49,7 @@ class _Desc(ctypes.Structure):
         ("top_n", ctypes.c_int32), ("local_window", ctypes.c_int32),
         ("seqlens_q", ctypes.c_void_p), ("seqlens_kv", ctypes.c_void_p),
         ("bottom_right", ctypes.c_int32),
+        ("sink", ctypes.c_void_p), ("dsink", ctypes.c_void_p),
     ]
 
 
@@ -101,7 +102,7 @@ def _ptr(a):
 
 
 def _desc(q, k, v, *, causal, window, scale, bias, block_idx, sel_block, top_n,
-          local_window, in_dtype, seqlens_q=None, seqlens_kv=None, bottom_right=False):
+          local_window, in_dtype, seqlens_q=None, seqlens_kv=None, bottom_right=False, sink=None):
     B, S, Hq, d = q.shape
     Hkv, dv = k.shape[2], v.shape[3]
     if k.shape != (B, S, Hkv, d) or v.shape != (B, S, Hkv, dv):
@@ -146,6 +147,12 @@ def _desc(q, k, v, *, causal, window, scale, bias, block_idx, sel_block, top_n,
             keep.append(ln)
             setattr(D, name, ln.ctypes.data)
     D.bottom_right = int(bool(bottom_right))
+    if sink is not None:
+        sk = np.ascontiguousarray(sink, dtype=np.float64)
+        if sk.shape != (Hq,):
+            raise ValueError("sink must be [Hq]")
+        keep.append(sk)
+        D.sink = sk.ctypes.data
     return D, keep
 
 
@@ -156,13 +163,13 @@ def _check(rc, what):
 
 def attention_fwd(q, k, v, *, causal=False, window=None, scale=None, bias=None,
                   block_idx=None, sel_block=32, top_n=8, local_window=32, seqlens_q=None,
-                  seqlens_kv=None, bottom_right=False):
+                  seqlens_kv=None, bottom_right=False, sink=None):
     """One-shot masked softmax attention.  Returns (o, m, l) in float64."""
     (q, dt), (k, _), (v, _) = _in(q), _in(k), _in(v)
     D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
                     block_idx=block_idx, sel_block=sel_block, top_n=top_n,
                     local_window=local_window, in_dtype=dt, seqlens_q=seqlens_q,
-                    seqlens_kv=seqlens_kv, bottom_right=bottom_right)
+                    seqlens_kv=seqlens_kv, bottom_right=bottom_right, sink=sink)
     B, S, Hq, _ = q.shape
     o = np.zeros((B, S, Hq, v.shape[3]))
     m = np.zeros((B, Hq, S))
@@ -174,13 +181,20 @@ def attention_fwd(q, k, v, *, causal=False, window=None, scale=None, bias=None,
 
 def attention_bwd(q, k, v, dout, *, causal=False, window=None, scale=None, bias=None,
                   block_idx=None, sel_block=32, top_n=8, local_window=32, seqlens_q=None,
-                  seqlens_kv=None, bottom_right=False):
-    """Analytic gradients.  Returns (dq, dk, dv, o, m, l) in float64."""
+                  seqlens_kv=None, bottom_right=False, sink=None, want_dsink=False):
+    """Analytic gradients.  Returns (dq, dk, dv, o, m, l) in float64, plus dsink [Hq]
+    when want_dsink (a sink must be given)."""
     (q, dt), (k, _), (v, _), (dout, _) = _in(q), _in(k), _in(v), _in(dout)
     D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
                     block_idx=block_idx, sel_block=sel_block, top_n=top_n,
                     local_window=local_window, in_dtype=dt, seqlens_q=seqlens_q,
-                    seqlens_kv=seqlens_kv, bottom_right=bottom_right)
+                    seqlens_kv=seqlens_kv, bottom_right=bottom_right, sink=sink)
+    dsink = None
+    if want_dsink:
+        if sink is None:
+            raise ValueError("want_dsink needs a sink")
+        dsink = np.zeros(q.shape[2])
+        D.dsink = dsink.ctypes.data
     B, S, Hq, d = q.shape
     Hkv, dv_ = k.shape[2], v.shape[3]
     dq = np.zeros((B, S, Hq, d))
@@ -191,6 +205,8 @@ def attention_bwd(q, k, v, dout, *, causal=False, window=None, scale=None, bias=
     l = np.zeros((B, Hq, S))
     _check(_load().ora_bwd(ctypes.byref(D), _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq),
                            _ptr(dk), _ptr(dv), _ptr(o), _ptr(m), _ptr(l)), "bwd")
+    if want_dsink:
+        return dq, dk, dv, o, m, l, dsink
     return dq, dk, dv, o, m, l
 
 

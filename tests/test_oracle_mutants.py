@@ -25,6 +25,9 @@ MUTANTS = [
     ("causal_excludes_diagonal", "if (D->causal && k > q + off) return 0;", "if (D->causal && k >= q + off) return 0;"),
     ("varlen_keys_not_cut", "if (q >= lq || k >= lk) return 0;", "if (q >= lq) return 0;"),
     ("bottom_right_offset_sign", "*off = D->bottom_right ? nk - nq : 0;", "*off = D->bottom_right ? nq - nk : 0;"),
+    ("sink_left_out_of_denominator", "double l = with_sink ? exp(sk - m) : 0.0;", "double l = 0.0;"),
+    ("sink_left_out_of_max", "if (sk > m) m = sk;", "if (sk > m && any) m = sk;"),
+    ("sink_gradient_sign", "ds_part[b * D->Hq + h] -= exp(", "ds_part[b * D->Hq + h] += exp("),
     ("dk_transposed_operand", "dkr[c] = dkr[c] + D->scale * dS * qrow[c];",
      "dkr[c] = dkr[c] + D->scale * dS * kr[c];", 1),
     ("dq_scale_dropped", "dqrow[c] = dqrow[c] + D->scale * dS * kr[c];", "dqrow[c] = dqrow[c] + dS * kr[c];"),
@@ -64,6 +67,9 @@ def battery(ora):
     for case in pins.VARLEN_CASES:
         yield lambda case=case: pins.test_varlen_matches_rebuilt_problems(ora, case, dict(causal=True, window=(3, 0)))
     yield lambda: pins.test_varlen_padding_is_inert(ora)
+    yield lambda: pins.test_sink_equals_extra_key(ora, True, "learnable")
+    yield lambda: pins.test_sink_rows_without_keys_and_padding(ora)
+    yield lambda: pins.test_sink_gradients_match_finite_differences(ora)
 
 
 def _build_mutant(tmp_path, name, text):

@@ -486,6 +486,79 @@ def test_varlen_gradients_match_finite_differences(ora):
 
 
 # --------------------------------------------------------------------------
+# sink attention (TransformerEngine page, "Other attention knobs": softmax_type
+# off_by_one / learnable): an extra logit per head with no value vector
+# --------------------------------------------------------------------------
+def sink_via_brute(q, k, v, sink, causal, scale):
+    """The sink as one more key: position 0 of a one-longer sequence holds a zero key
+    whose per-head bias is the sink logit and a zero value; query i sits at position
+    i + 1, so under the causal rule it still sees the sink and its own keys 0..i."""
+    B, S, Hq, d = q.shape
+    Hkv, dv = k.shape[2], v.shape[3]
+    qe = np.concatenate([np.zeros((B, 1, Hq, d)), q], axis=1)
+    ke = np.concatenate([np.zeros((B, 1, Hkv, d)), k], axis=1)
+    ve = np.concatenate([np.zeros((B, 1, Hkv, dv)), v], axis=1)
+    bias = np.zeros((1, Hq, 1, S + 1))
+    bias[0, :, 0, 0] = sink
+    o, m, l = brute_force(qe, ke, ve, causal=causal, scale=scale, bias=bias)
+    return o[:, 1:], m[:, :, 1:], l[:, :, 1:]
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+@pytest.mark.parametrize("kind", ["off_by_one", "learnable"])
+def test_sink_equals_extra_key(ora, causal, kind):
+    B, S, Hq, Hkv, d, dv = 2, 9, 4, 2, 3, 2
+    q, k, v = rnd((B, S, Hq, d), 191), rnd((B, S, Hkv, d), 192), rnd((B, S, Hkv, dv), 193)
+    sink = np.zeros(Hq) if kind == "off_by_one" else np.array([0.7, -2.0, 3.5, -0.1])
+    o, m, l = ora.attention_fwd(q, k, v, causal=causal, scale=0.8, sink=sink)
+    bo, bm, bl = sink_via_brute(q, k, v, sink, causal, 0.8)
+    np.testing.assert_allclose(o, bo, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(m, bm, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l, bl, rtol=1e-12, atol=1e-13)
+
+
+def test_sink_rows_without_keys_and_padding(ora):
+    # a row with no allowed key keeps only the sink: O = 0, m = sink, l = 1; padding rows
+    # of a shorter sequence take part in nothing (m = -inf, l = 0)
+    B, S, H, d = 2, 8, 2, 4
+    q, k, v = rnd((B, S, H, d), 194), rnd((B, S, H, d), 195), rnd((B, S, H, d), 196)
+    idx = np.full((B, H, S // 4, 2), -1, dtype=np.int32)
+    sink = np.array([0.25, -1.5])
+    o, m, l = ora.attention_fwd(q, k, v, causal=True, block_idx=idx, sel_block=4, top_n=2,
+                                local_window=0, sink=sink)
+    assert not o.any() and np.array_equal(l, np.ones_like(l))
+    np.testing.assert_array_equal(m, np.broadcast_to(sink[None, :, None], m.shape))
+    o, m, l = ora.attention_fwd(q, k, v, causal=True, seqlens_q=[8, 5], sink=sink)
+    assert np.all(np.isneginf(m[1, :, 5:])) and not l[1, :, 5:].any() and not o[1, 5:].any()
+    assert np.all(np.isfinite(m[:, :, :5]))
+
+
+def test_sink_gradients_match_finite_differences(ora):
+    B, S, Hq, Hkv, d, dv = 1, 6, 2, 1, 3, 2
+    q, k, v, do = (rnd((B, S, Hq, d), 197), rnd((B, S, Hkv, d), 198), rnd((B, S, Hkv, dv), 199),
+                   rnd((B, S, Hq, dv), 200))
+    sink = np.array([0.4, -0.9])
+    dq, dk, dvv, o, m, l, dsink = ora.attention_bwd(q, k, v, do, causal=True, scale=0.6, sink=sink,
+                                                    want_dsink=True)
+    h = 1e-6
+
+    def loss(qq, kk, vv, ss):
+        return float((sink_via_brute(qq, kk, vv, ss, True, 0.6)[0] * do).sum())
+
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dvv), ("sink", sink, dsink)):
+        fd = np.zeros_like(x)
+        for ix in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[ix] += h
+            xm[ix] -= h
+            ap = {"q": (xp, k, v, sink), "k": (q, xp, v, sink), "v": (q, k, xp, sink), "sink": (q, k, v, xp)}[name]
+            am = {"q": (xm, k, v, sink), "k": (q, xm, v, sink), "v": (q, k, xm, sink), "sink": (q, k, v, xm)}[name]
+            fd[ix] = (loss(*ap) - loss(*am)) / (2 * h)
+        err = np.abs(fd - g).max() / max(np.abs(g).max(), 1e-30)
+        assert err < 1e-6, f"d{name}: relative error {err}"
+
+
+# --------------------------------------------------------------------------
 # sampled rows / keys agree with the full evaluation
 # --------------------------------------------------------------------------
 def test_sampled_rows_and_keys_match_full(ora):
