@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define BPA_VERSION 3
+#define BPA_VERSION 4
 
 typedef enum {
     BPA_OK = 0,
@@ -119,6 +119,16 @@ typedef struct bpa_attn_desc {
     int32_t bottom_right;      /* 0: causal / window diagonal at k = q (top-left, both
                                 * sequences start together); 1: at k = q + Lk - Lq (the
                                 * queries are the last Lq positions of the key sequence) */
+    /* Fields below were added in descriptor version 4 (bpa_version() >= 4); a version-3
+     * caller (struct_size = offsetof(bpa_attn_desc, sink)) gets plain softmax.  Sink
+     * attention: "JAX: Single-GPU Attention with TransformerEngine", Other attention knobs
+     * (softmax_type "off_by_one" or "learnable"), read as one extra logit per q head with
+     * no value vector in every valid row's softmax:  P = exp(z) / (exp(sink[h]) + sum exp(z))
+     * (off_by_one: sink = 0).  m and l include it (m = max(max z, sink)); a row with no
+     * allowed key gets O = 0, m = sink, l = 1.  Needs ring_size 1. */
+    const float* sink;         /* device float32 [Hq] or NULL (plain softmax) */
+    float* dsink;              /* device float32 [Hq] or NULL: bpa_bwd writes
+                                * dsink[h] = -sum over valid rows of P_sink <dO, O> */
 } bpa_attn_desc;
 
 /* Bytes of workspace bpa_fwd (op = BPA_OP_FWD) or bpa_bwd (op = BPA_OP_BWD)

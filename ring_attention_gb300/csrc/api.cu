@@ -60,11 +60,14 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     if (!d) return fail(BPA_ERR_INVALID_ARG, "desc is NULL");
     const size_t v1_size = offsetof(bpa_attn_desc, dv);          // version 1: no dv, o_strides
     const size_t v2_size = offsetof(bpa_attn_desc, seqlens_q);   // version 2: no sequence lengths
-    if (d->struct_size != sizeof(bpa_attn_desc) && d->struct_size != v1_size && d->struct_size != v2_size)
-        return fail(BPA_ERR_INVALID_ARG, "desc->struct_size is %u, expected %zu (or %zu, %zu)", d->struct_size,
-                    sizeof(bpa_attn_desc), v2_size, v1_size);
+    const size_t v3_size = offsetof(bpa_attn_desc, sink);        // version 3: no sink
+    if (d->struct_size != sizeof(bpa_attn_desc) && d->struct_size != v1_size && d->struct_size != v2_size &&
+        d->struct_size != v3_size)
+        return fail(BPA_ERR_INVALID_ARG, "desc->struct_size is %u, expected %zu (or %zu, %zu, %zu)", d->struct_size,
+                    sizeof(bpa_attn_desc), v3_size, v2_size, v1_size);
     const bool v2 = d->struct_size >= v2_size;
-    const bool v3 = d->struct_size == sizeof(bpa_attn_desc);
+    const bool v3 = d->struct_size >= v3_size;
+    const bool v4 = d->struct_size == sizeof(bpa_attn_desc);
     const bool varlen = v3 && (d->seqlens_q || d->seqlens_kv);
     if (d->dtype != BPA_BF16 && d->dtype != BPA_FP32)
         return fail(BPA_ERR_INVALID_ARG, "unknown dtype %d", d->dtype);
@@ -102,6 +105,8 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     }
     if (varlen && (n != 1 || d->block_idx))
         return fail(BPA_ERR_INVALID_ARG, "sequence lengths need ring_size 1 and no block selection");
+    if (v4 && d->sink && n != 1) return fail(BPA_ERR_INVALID_ARG, "sink attention needs ring_size 1");
+    if (v4 && d->dsink && !d->sink) return fail(BPA_ERR_INVALID_ARG, "dsink needs a sink");
     P.B = d->B;
     P.S = d->S;
     P.Hq = d->Hq;
@@ -131,6 +136,8 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     P.seqlens_q = varlen ? d->seqlens_q : nullptr;
     P.seqlens_kv = varlen ? d->seqlens_kv : nullptr;
     P.bottom_right = v3 && d->bottom_right ? 1 : 0;
+    P.sink = v4 ? d->sink : nullptr;
+    P.dsink = v4 ? d->dsink : nullptr;
     P.sel_block = d->block_idx ? d->sel_block : 0;
     P.top_n = d->block_idx ? d->top_n : 0;
     P.local_window = d->block_idx ? d->local_window : 0;
@@ -313,6 +320,7 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
     }
     if (n == 1) {
         e = tc ? launch_fwd_tc(a, maps, s) : launch_fwd_simt(a, s);
+        if (e == cudaSuccess && P.sink && (P.seqlens_q || P.seqlens_kv)) e = launch_pad_stats(a, s);
         marks.mark(1, s);
         marks.mark(2, s);
         return e == cudaSuccess ? BPA_OK : cuda_fail(e, "forward launch");
@@ -373,7 +381,8 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
         // gathered backward: dQ written per query block, dK / dV reduced into float32 accumulators
         a.dk_acc = reinterpret_cast<float*>(ws + L.dk);
         a.dv_acc = reinterpret_cast<float*>(ws + L.dv);
-        if ((e = launch_bwd_pre(a, s)) != cudaSuccess) return cuda_fail(e, "backward pre-pass");
+        if ((e = launch_bwd_pre(a, s)) != cudaSuccess || (P.dsink && (e = launch_sink_grad(a, s)) != cudaSuccess))
+            return cuda_fail(e, "backward pre-pass");
         marks.mark(1, s);
         const size_t nk = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.d;
         const size_t nv = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.dv;
@@ -397,7 +406,8 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
              make_map(&maps[3], dout, P.dv, P.Hq, P.S, P.B, P.os, 64);
     }
     if (!tc) {
-        if ((e = launch_bwd_pre(a, s)) != cudaSuccess) return cuda_fail(e, "backward pre-pass");
+        if ((e = launch_bwd_pre(a, s)) != cudaSuccess || (P.dsink && (e = launch_sink_grad(a, s)) != cudaSuccess))
+            return cuda_fail(e, "backward pre-pass");
         marks.mark(1, s);
         e = launch_bwd_simt(a, s);
         marks.mark(2, s);
@@ -405,7 +415,8 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
         return e == cudaSuccess ? BPA_OK : cuda_fail(e, "backward launch");
     }
     a.dq_acc = reinterpret_cast<float*>(ws + L.dq);
-    if ((e = launch_bwd_pre(a, s)) != cudaSuccess) return cuda_fail(e, "backward pre-pass");
+    if ((e = launch_bwd_pre(a, s)) != cudaSuccess || (P.dsink && (e = launch_sink_grad(a, s)) != cudaSuccess))
+            return cuda_fail(e, "backward pre-pass");
     marks.mark(1, s);
     if (n == 1) {
         if ((e = launch_bwd_tc(a, maps, s)) != cudaSuccess) return cuda_fail(e, "backward launch");

@@ -325,6 +325,57 @@ cudaError_t launch_cast_dkdv(const BwdArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Gradient of the sink logits: dsink[h] = -sum over (b, row) of P_sink <dO, O> with
+// P_sink = exp(sink[h] - LSE); padding rows (LSE = +inf) add nothing.  One CTA per q head,
+// rows in a fixed order and a fixed reduction tree: the result does not depend on timing.
+__global__ void __launch_bounds__(256) k_sink_grad(const BwdArgs a) {
+    const Problem& P = a.P;
+    const int h = blockIdx.x;
+    const float sk = P.sink[h];
+    float acc = 0.f;
+    for (int b = 0; b < P.B; ++b) {
+        const int64_t base = (static_cast<int64_t>(b) * P.Hq + h) * a.Spad;
+        for (int r = threadIdx.x; r < a.Spad; r += blockDim.x) {
+            const float lse = a.lse[base + r];
+            if (lse != INFINITY) acc -= expf(sk - lse) * a.Dvec[base + r];
+        }
+    }
+    __shared__ float red[256];
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) P.dsink[h] = red[0];
+}
+
+// m = -inf, l = 0 on the padding rows (q >= Lq) of a variable-length problem.
+__global__ void k_pad_stats(const FwdArgs a) {
+    const Problem& P = a.P;
+    const int64_t rows = static_cast<int64_t>(P.B) * P.Hq * P.S;
+    for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < rows;
+         r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int q = static_cast<int>(r % P.S);
+        const int b = static_cast<int>(r / (static_cast<int64_t>(P.S) * P.Hq));
+        if (q >= lens_of(P, b).lq) {
+            a.m[r] = -INFINITY;
+            a.l[r] = 0.f;
+        }
+    }
+}
+
+cudaError_t launch_pad_stats(const FwdArgs& a, cudaStream_t s) {
+    const int64_t rows = static_cast<int64_t>(a.P.B) * a.P.Hq * a.P.S;
+    k_pad_stats<<<grid_for(rows, 256), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sink_grad(const BwdArgs& a, cudaStream_t s) {
+    k_sink_grad<<<a.P.Hq, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {
     k_wait_selftest<<<1, 32, 0, s>>>(status, limit_ns);
     return cudaGetLastError();

@@ -29,6 +29,8 @@ struct Problem {
     const int32_t* seqlens_q;  // device [B] or nullptr: valid queries per batch entry
     const int32_t* seqlens_kv; // device [B] or nullptr (then the query lengths)
     int bottom_right;          // diagonal at k = q + Lk - Lq instead of k = q
+    const float* sink;         // device [Hq] sink logits (natural log units) or nullptr
+    float* dsink;              // device [Hq] sink gradient (backward output) or nullptr
 };
 
 // Valid query / key counts of one batch entry and the offset of the causal / window
@@ -101,6 +103,8 @@ cudaError_t launch_ring_init(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_ring_finalize(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_sink_grad(const BwdArgs& a, cudaStream_t s);   // after the pre-pass (LSE, D)
+cudaError_t launch_pad_stats(const FwdArgs& a, cudaStream_t s);   // m, l of padding rows
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 

@@ -144,6 +144,17 @@ __device__ __forceinline__ Tile decode_tile(const FwdArgs& a, int item) {
     return t;
 }
 
+// Sink attention: the sink logit sk (natural log units) joins a row's softmax max and
+// denominator but brings no value vector.  From the row's sum lsum relative to m_used and
+// its true max m_true (log2 units) returns (denominator relative to m_used, final max,
+// final sum relative to the final max).  Out of line: it runs once per row and item.
+__device__ __noinline__ float3 with_sink(float sk, float lsum, float m_used, float m_true) {
+    const float s2 = sk * kLog2e;
+    const float m_fin = fmaxf(m_true, s2);
+    return make_float3(lsum + ex2(s2 - m_used), m_fin,
+                       (m_true == -INFINITY ? 0.f : lsum * ex2(m_used - m_fin)) + ex2(s2 - m_fin));
+}
+
 // bounded wait that ignores the abort flag: used to drain in-flight work
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
     int never = 0;
@@ -699,14 +710,26 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
             const int qc = min(q, P.S - 1);
             const int64_t mi = (static_cast<int64_t>(T.b) * P.Hq + T.h) * P.S + qc;
             const bool has_work = jlo <= jhi;
+            // with a sink every row takes it here; padding rows of variable-length problems get
+            // their m, l reset by a pass after the kernel (their O is 0 either way), which keeps
+            // the row length out of the live registers
+            const bool sink_row = P.sink != nullptr;
             if (!aborted && has_work) {
                 tc_fence_after();
                 // statistics relative to the true row max
                 const float rel = m_true == -INFINITY ? 0.f : ex2(m_used - m_true);
-                const float l_true = lsum * rel;
-                const float m_nat = m_true * kLn2;
+                float l_true = lsum * rel;
+                float m_fin = m_true;
+                float den = lsum;   // softmax denominator relative to m_used
+                if (sink_row) {
+                    const float3 r = with_sink(__ldg(P.sink + T.h), lsum, m_used, m_true);
+                    den = r.x;
+                    m_fin = r.y;
+                    l_true = r.z;
+                }
+                const float m_nat = m_fin * kLn2;
                 if (!a.acc) {
-                    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+                    const float inv = den > 0.f ? 1.f / den : 0.f;
                     __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.os[0] +
                                        static_cast<int64_t>(qc) * P.os[1] + T.h * P.os[2];
     #pragma unroll 1
@@ -764,12 +787,12 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
                     }
                 }
             } else if (!aborted && !has_work && !a.acc && q < P.S) {
-                // no key allowed for this tile: O = 0, m = -inf, l = 0
+                // no key allowed for this tile: O = 0, m = -inf, l = 0 (with a sink: m = sink, l = 1)
                 __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.os[0] +
                                    static_cast<int64_t>(q) * P.os[1] + T.h * P.os[2];
                 for (int cc = 0; cc < DV; cc += 8) *reinterpret_cast<uint4*>(O + cc) = make_uint4(0, 0, 0, 0);
-                a.m[mi] = -INFINITY;
-                a.l[mi] = 0.f;
+                a.m[mi] = sink_row ? __ldg(P.sink + T.h) : -INFINITY;   // only the sink: m = sink, l = 1
+                a.l[mi] = sink_row ? 1.f : 0.f;
             }
 
             if (T.n > 0) {

@@ -330,7 +330,14 @@ __global__ void __launch_bounds__(Geom<NW>::QB_F * NW * 32) k_gather_fwd(const F
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int q = BS * i + mt * 16 + g + hh * 8;
-            const float inv = lrow[mt][hh] > 0.f ? 1.f / lrow[mt][hh] : 0.f;
+            float scale_o = 1.f;
+            if (P.sink) {   // sink logit: joins the max and the denominator, contributes no value
+                const float s2 = __ldg(P.sink + h) * kLog2e, mn = fmaxf(mrow[mt][hh], s2);
+                scale_o = mrow[mt][hh] == -INFINITY ? 0.f : ex2(mrow[mt][hh] - mn);
+                lrow[mt][hh] = lrow[mt][hh] * scale_o + ex2(s2 - mn);
+                mrow[mt][hh] = mn;
+            }
+            const float inv = lrow[mt][hh] > 0.f ? scale_o / lrow[mt][hh] : 0.f;
             __nv_bfloat16* orow = O + static_cast<int64_t>(q) * P.os[1];
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)

@@ -188,6 +188,16 @@ __global__ void __launch_bounds__(kWarps * 32) k_fwd_simt(const FwdArgs a) {
             }
         }
         const int64_t mi = (static_cast<int64_t>(b) * P.Hq + h) * P.S + q;
+        if (!ring && P.sink && q < lens_of(P, b).lq) {
+            // sink logit: joins the max and the denominator, contributes no value
+            const float sk = __ldg(P.sink + h);
+            const float mn = fmaxf(st.m, sk);
+            const float f = st.m == -INFINITY ? 0.f : expf(st.m - mn);
+#pragma unroll
+            for (int i = 0; i < KP; ++i) st.acc[i] *= f;
+            st.l = st.l * f + expf(sk - mn);
+            st.m = mn;
+        }
         if (!ring) {
             const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
             T* O = static_cast<T*>(a.o) + b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2];

@@ -142,7 +142,7 @@ def test_select_rejects_bad_arguments(bpa):
 def test_status_strings(bpa):
     L = bpa.lib()
     assert L.bpa_status_string(5) == b"BPA_ERR_TIMEOUT"
-    assert L.bpa_version() == 3
+    assert L.bpa_version() == 4
 
 
 def test_version_1_descriptor_is_accepted(bpa):
@@ -158,6 +158,23 @@ def test_version_1_descriptor_is_accepted(bpa):
     # version 2: no sequence lengths; the fields past the shorter struct are not read
     D = _desc(bpa, seqlens_q=0x1000, ring_size=2)
     D.struct_size = bpa.bpa_attn_desc.seqlens_q.offset
+    assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) > 0
+
+
+def test_sink_checks(bpa):
+    L = bpa.lib()
+    D = _desc(bpa, sink=0x2000, ring_size=2)
+    assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) == 0
+    assert b"sink" in L.bpa_last_error()
+    D = _desc(bpa, dsink=0x2000)
+    assert L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(D)) == 0
+    assert b"dsink needs a sink" in L.bpa_last_error()
+    D = _desc(bpa, sink=0x2000, dsink=0x3000)
+    assert L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(D)) == L.bpa_workspace_size(
+        bpa.BPA_OP_BWD, ctypes.byref(_desc(bpa)))
+    # version 3: the sink fields past the shorter struct are not read
+    D = _desc(bpa, sink=0x2000, ring_size=2)
+    D.struct_size = bpa.bpa_attn_desc.sink.offset
     assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) > 0
 
 

@@ -385,6 +385,46 @@ def test_variable_lengths(bpa, ora, case, mask, dtype, d):
         assert float(dvv[b, lkk[b]:].abs().max() if lkk[b] < S else 0) == 0.0
 
 
+@pytest.mark.parametrize("path", ["tc_d128", "tc_d64_swa", "f32", "gather", "varlen"])
+def test_sink_attention(bpa, ora, path):
+    # sink logits per q head (a "learnable" set, one of them 0 as in off_by_one) on the
+    # tensor-core, CUDA-core and gathered forwards, and the sink gradient
+    B, S, Hq, Hkv = 2, 300, 4, 2
+    d = 128 if path == "tc_d128" else 64
+    dtype = "f32" if path == "f32" else "bf16"
+    q, k, v, do = draw([(B, S, Hq, d), (B, S, Hkv, d), (B, S, Hkv, d), (B, S, Hq, d)], 90 + d, dtype)
+    sink = np.array([0.0, 1.5, -2.0, 4.0])
+    kw, okw = dict(causal=True), dict(causal=True)
+    if path == "tc_d64_swa":
+        kw["window"] = okw["window"] = (40, 0)
+    if path == "gather":   # block-selected, d = 64: rows of the first block see no key
+        q, k, v, do = (np.ascontiguousarray(x[:, :288]) for x in (q, k, v, do))
+        idx = _planted_selection(B, Hq, 288, 32, 3, 92)
+        kw.update(block_idx=torch.from_numpy(idx).cuda(), sel_block=32, top_n=3, local_window=0)
+        okw.update(block_idx=idx, sel_block=32, top_n=3, local_window=0)
+    if path == "varlen":
+        lens = [300, 131]
+        kw["seqlens_q"] = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        okw["seqlens_q"] = lens
+    tsink = torch.tensor(sink, dtype=torch.float32, device="cuda")
+    tds = torch.zeros(Hq, dtype=torch.float32, device="cuda")
+    tq, tk, tv = dev(q), dev(k), dev(v)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, sink=tsink, **kw)
+    dq, dk, dvv = bpa.bpa_bwd(tq, tk, tv, o, dev(do), m, l, sink=tsink, dsink=tds, **kw)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl, rds = ora.attention_bwd(q, k, v, do, sink=sink, want_dsink=True, **okw)
+    check_stats(m, l, rm, rl)
+    if dtype == "f32":
+        for got, ref in ((o, ro), (dq, rq), (dk, rk), (dvv, rv)):
+            assert max_abs(host(got), ref) <= FP32_MAX_ABS
+        assert rel_l2(host(tds), rds) <= 1e-5
+    else:
+        assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+        for got, ref in ((dq, rq), (dk, rk), (dvv, rv)):
+            assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2
+        assert rel_l2(host(tds), rds) <= BF16_GRAD_REL_L2
+
+
 def test_bounded_wait_reports_timeout(bpa):
     ws = bpa.workspace(256, "cuda")
     bpa.bpa_debug_wait_timeout(ws, 200_000_000)   # 0.2 s
