@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define BPA_VERSION 4
+#define BPA_VERSION 5
 
 typedef enum {
     BPA_OK = 0,
@@ -129,6 +129,15 @@ typedef struct bpa_attn_desc {
     const float* sink;         /* device float32 [Hq] or NULL (plain softmax) */
     float* dsink;              /* device float32 [Hq] or NULL: bpa_bwd writes
                                 * dsink[h] = -sum over valid rows of P_sink <dO, O> */
+    /* Field added in descriptor version 5 (bpa_version() >= 5); a version-4 caller
+     * (struct_size = offsetof(bpa_attn_desc, deterministic)) gets 0.  The determinism knob
+     * of "JAX: Single-GPU Attention with TransformerEngine", Other attention knobs
+     * (NVTE_ALLOW_NONDETERMINISTIC_ALGO=0): with 1, bpa_bwd gives bit-identical dq, dk, dv
+     * on every call: each key tile's dQ contribution goes to its own float32 slice of the
+     * workspace (no atomic adds) and the slices are added in ascending key order.  The
+     * workspace then holds one dQ slice per 128-key tile (bpa_workspace_size grows by about
+     * that factor).  Needs ring_size 1. */
+    int32_t deterministic;
 } bpa_attn_desc;
 
 /* Bytes of workspace bpa_fwd (op = BPA_OP_FWD) or bpa_bwd (op = BPA_OP_BWD)

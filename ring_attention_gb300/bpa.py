@@ -47,6 +47,7 @@ class bpa_attn_desc(ctypes.Structure):
         ("seqlens_q", ctypes.c_void_p), ("seqlens_kv", ctypes.c_void_p),
         ("bottom_right", ctypes.c_int32),
         ("sink", ctypes.c_void_p), ("dsink", ctypes.c_void_p),
+        ("deterministic", ctypes.c_int32),
     ]
 
 
@@ -121,7 +122,7 @@ def _stream_ptr(stream) -> int:
 def make_desc(q, k, v, *, o=None, causal=False, window=(-1, -1), scale=None, bias=None, query_chunk=0,
               key_chunk=0, ring_size=1, ring_steps=None, block_idx=None, sel_block=0, top_n=0,
               local_window=0, seqlens_q=None, seqlens_kv=None, bottom_right=False, sink=None,
-              dsink=None) -> bpa_attn_desc:
+              dsink=None, deterministic=False) -> bpa_attn_desc:
     """Fill a bpa_attn_desc from torch tensors (no data is touched).  The value head dim
     is v's last dim; o (the output, or dout, which shares its strides) sets o_strides."""
     B, S, Hq, d = q.shape
@@ -168,6 +169,7 @@ def make_desc(q, k, v, *, o=None, causal=False, window=(-1, -1), scale=None, bia
             if t.dtype != torch.float32 or t.shape != (Hq,) or not t.is_contiguous() or t.device != q.device:
                 raise ValueError(f"{name} must be a contiguous float32 [Hq] tensor on q's device")
             setattr(D, name, t.data_ptr())
+    D.deterministic = int(bool(deterministic))
     return D
 
 

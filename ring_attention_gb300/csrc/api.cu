@@ -61,13 +61,15 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     const size_t v1_size = offsetof(bpa_attn_desc, dv);          // version 1: no dv, o_strides
     const size_t v2_size = offsetof(bpa_attn_desc, seqlens_q);   // version 2: no sequence lengths
     const size_t v3_size = offsetof(bpa_attn_desc, sink);        // version 3: no sink
+    const size_t v4_size = offsetof(bpa_attn_desc, deterministic);   // version 4: no determinism knob
     if (d->struct_size != sizeof(bpa_attn_desc) && d->struct_size != v1_size && d->struct_size != v2_size &&
-        d->struct_size != v3_size)
-        return fail(BPA_ERR_INVALID_ARG, "desc->struct_size is %u, expected %zu (or %zu, %zu, %zu)", d->struct_size,
-                    sizeof(bpa_attn_desc), v3_size, v2_size, v1_size);
+        d->struct_size != v3_size && d->struct_size != v4_size)
+        return fail(BPA_ERR_INVALID_ARG, "desc->struct_size is %u, expected %zu (or %zu, %zu, %zu, %zu)",
+                    d->struct_size, sizeof(bpa_attn_desc), v4_size, v3_size, v2_size, v1_size);
     const bool v2 = d->struct_size >= v2_size;
     const bool v3 = d->struct_size >= v3_size;
-    const bool v4 = d->struct_size == sizeof(bpa_attn_desc);
+    const bool v4 = d->struct_size >= v4_size;
+    const bool v5 = d->struct_size == sizeof(bpa_attn_desc);
     const bool varlen = v3 && (d->seqlens_q || d->seqlens_kv);
     if (d->dtype != BPA_BF16 && d->dtype != BPA_FP32)
         return fail(BPA_ERR_INVALID_ARG, "unknown dtype %d", d->dtype);
@@ -107,6 +109,7 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
         return fail(BPA_ERR_INVALID_ARG, "sequence lengths need ring_size 1 and no block selection");
     if (v4 && d->sink && n != 1) return fail(BPA_ERR_INVALID_ARG, "sink attention needs ring_size 1");
     if (v4 && d->dsink && !d->sink) return fail(BPA_ERR_INVALID_ARG, "dsink needs a sink");
+    if (v5 && d->deterministic && n != 1) return fail(BPA_ERR_INVALID_ARG, "deterministic mode needs ring_size 1");
     P.B = d->B;
     P.S = d->S;
     P.Hq = d->Hq;
@@ -138,6 +141,7 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     P.bottom_right = v3 && d->bottom_right ? 1 : 0;
     P.sink = v4 ? d->sink : nullptr;
     P.dsink = v4 ? d->dsink : nullptr;
+    P.det = v5 && d->deterministic ? 1 : 0;
     P.sel_block = d->block_idx ? d->sel_block : 0;
     P.top_n = d->block_idx ? d->top_n : 0;
     P.local_window = d->block_idx ? d->local_window : 0;
@@ -167,8 +171,10 @@ BwdLayout bwd_layout(const Problem& P) {
     L.D = kHeader;
     L.lse = L.D + round256(rows * sizeof(float));
     L.dq = L.lse + round256(rows * sizeof(float));
-    // dQ accumulator [B, Hq, Spad / 4, d, 4]: four consecutive queries of one channel side by side
-    const size_t nq = sizeof(float) * P.B * static_cast<size_t>(L.Spad) * P.Hq * P.d;
+    // dQ accumulator [B, Hq, Spad / 4, d, 4]: four consecutive queries of one channel side by side;
+    // deterministic mode: one per 128-key tile
+    const size_t nkt = P.det ? (P.S + 127) / 128 : 1;
+    const size_t nq = sizeof(float) * P.B * static_cast<size_t>(L.Spad) * P.Hq * P.d * nkt;
     const size_t nk = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.d;
     const size_t nv = sizeof(float) * P.B * static_cast<size_t>(P.S) * P.Hkv * P.dv;
     L.dk = L.dq + round256(nq);
@@ -377,7 +383,7 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
     a.Spad = L.Spad;
     a.status = reinterpret_cast<uint32_t*>(ws);
 
-    if (P.block_idx && gather_supported(P) && aligned16(dout) && aligned16(dq) && aligned16(dk) && aligned16(dv)) {
+    if (P.block_idx && !P.det && gather_supported(P) && aligned16(dout) && aligned16(dq) && aligned16(dk) && aligned16(dv)) {
         // gathered backward: dQ written per query block, dK / dV reduced into float32 accumulators
         a.dk_acc = reinterpret_cast<float*>(ws + L.dk);
         a.dv_acc = reinterpret_cast<float*>(ws + L.dv);
@@ -434,7 +440,7 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
         }
     }
     marks.mark(2, s);
-    e = launch_bwd_post(a, s);
+    e = P.det ? launch_dq_reduce(a, s) : launch_bwd_post(a, s);
     marks.mark(3, s);
     return e == cudaSuccess ? BPA_OK : cuda_fail(e, "backward post-pass");
 }

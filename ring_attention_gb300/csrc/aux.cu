@@ -271,7 +271,7 @@ cudaError_t launch_ring_finalize(const FwdArgs& a, cudaStream_t s) {
 cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t s) {
     const Problem& P = a.P;
     const int64_t rows = static_cast<int64_t>(P.B) * P.Hq * a.Spad;
-    const int zero = a.dq_acc != nullptr;
+    const int zero = a.dq_acc != nullptr && !P.det;   // deterministic slices are written, not added to
     const int tpr = P.dv / 8;
     const bool vec_ok = ((reinterpret_cast<uintptr_t>(a.o) | reinterpret_cast<uintptr_t>(a.dout)) & 15u) == 0 &&
                         ((P.os[0] | P.os[1] | P.os[2]) & 7) == 0;

@@ -31,6 +31,7 @@ struct Problem {
     int bottom_right;          // diagonal at k = q + Lk - Lq instead of k = q
     const float* sink;         // device [Hq] sink logits (natural log units) or nullptr
     float* dsink;              // device [Hq] sink gradient (backward output) or nullptr
+    int det;                   // deterministic backward (no atomic adds anywhere)
 };
 
 // Valid query / key counts of one batch entry and the offset of the causal / window
@@ -72,7 +73,8 @@ struct BwdArgs {
     float* Dvec;        // [B, Hq, Spad] rowsum(dO * O); padding rows hold 0
     float* lse;         // [B, Hq, Spad] m + log(l) (natural log); +inf on padding / empty rows
     int Spad;           // S rounded up to 64
-    float* dq_acc;      // [B, Hq, Spad / 4, d, 4] float32 (four consecutive queries of a channel together)
+    float* dq_acc;      // [B, Hq, Spad / 4, d, 4] float32 (four consecutive queries of a channel together);
+                        // deterministic mode: one such slice per 128-key tile, [nkt][B, Hq, Spad / 4, d, 4]
     float* dk_acc;      // ring carries / block-selected accumulators [B, S, Hkv, d] float32, or nullptr
     float* dv_acc;
     int ring_idx;
@@ -105,6 +107,7 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_post(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_sink_grad(const BwdArgs& a, cudaStream_t s);   // after the pre-pass (LSE, D)
 cudaError_t launch_pad_stats(const FwdArgs& a, cudaStream_t s);   // m, l of padding rows
+cudaError_t launch_dq_reduce(const BwdArgs& a, cudaStream_t s);   // deterministic mode: slices -> dq
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
 

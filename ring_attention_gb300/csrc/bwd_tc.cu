@@ -39,6 +39,8 @@
 //              running the loop with warp-uniform operands, one elected lane issuing.
 #include <math.h>
 
+#include <algorithm>
+
 #include "bpa_internal.h"
 #include "common.cuh"
 
@@ -88,14 +90,12 @@ struct Work {
     int lk, off;         // valid keys of the batch entry, offset of the causal / window diagonal
 };
 
-__device__ __forceinline__ Work decode(const BwdArgs& a) {
+// The work of key tile kt of (batch b, kv head hkv): the query rows that may see it.
+__device__ __forceinline__ Work decode_tile_of(const BwdArgs& a, int b, int hkv, int kt) {
     const Problem& P = a.P;
-    int r = blockIdx.x;
     Work w;
-    w.b = r % P.B;
-    r /= P.B;
-    w.hkv = r % P.Hkv;
-    const int kt = r / P.Hkv;    // lowest key tiles (most causal work) first
+    w.b = b;
+    w.hkv = hkv;
     w.k0 = kt * BK;
     const Lens len = lens_of(P, w.b);   // full lengths unless the problem has sequence lengths
     w.lk = len.lk;
@@ -119,12 +119,18 @@ __device__ __forceinline__ Work decode(const BwdArgs& a) {
     return w;
 }
 
+__device__ __forceinline__ Work decode(const BwdArgs& a) {
+    const Problem& P = a.P;
+    const int r = blockIdx.x;   // lowest key tiles (most causal work) first
+    return decode_tile_of(a, r % P.B, (r / P.B) % P.Hkv, r / (P.B * P.Hkv));
+}
+
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
     int never = 0;
     mbar_wait(bar, parity, &never, status, 0xD1);
 }
 
-template <int DV>
+template <int DV, bool DET>
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -316,6 +322,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(BAR(B_DQE));
             float* dst = a.dq_acc + (static_cast<int64_t>(W.b) * P.Hq + iter_head(t)) * a.Spad * D +
                          (static_cast<int64_t>((iter_q0(t) + cq) >> 2) * D + r) * 4;
+            if (DET) {   // this key tile's own slice: written once, added in key order later
+                dst += static_cast<int64_t>(W.k0 / BK) * P.B * P.Hq * a.Spad * D;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4*>(dst + j * (4 * D)) =
+                        make_float4(__uint_as_float(v[4 * j]) * P.scale, __uint_as_float(v[4 * j + 1]) * P.scale,
+                                    __uint_as_float(v[4 * j + 2]) * P.scale, __uint_as_float(v[4 * j + 3]) * P.scale);
+                return true;
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j)
                 red_add_v4(dst + j * (4 * D), __uint_as_float(v[4 * j]) * P.scale,
@@ -484,22 +499,88 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int DV>
 cudaError_t launch_dv(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
     using L = BwdCfg<DV>;
-    static bool configured[64] = {};
+    // the deterministic variant is a separate instantiation: the default kernel's code is
+    // left exactly as it is without the knob
+    static bool configured[2][64] = {};
+    const int det = a.P.det ? 1 : 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[dev]) {
-        e = cudaFuncSetAttribute(k_bwd_tc<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (dev < 0 || dev >= 64 || !configured[det][dev]) {
+        e = det ? cudaFuncSetAttribute(k_bwd_tc<DV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM)
+                : cudaFuncSetAttribute(k_bwd_tc<DV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[dev] = true;
+        if (dev >= 0 && dev < 64) configured[det][dev] = true;
     }
     const int nkt = (a.P.S + BK - 1) / BK;
     const int grid = nkt * a.P.Hkv * a.P.B;
-    k_bwd_tc<DV><<<grid, kThreads, L::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
+    if (det)
+        k_bwd_tc<DV, true><<<grid, kThreads, L::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
+    else
+        k_bwd_tc<DV, false><<<grid, kThreads, L::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
     return cudaGetLastError();
 }
 
+// Deterministic mode: dQ = the sum of the key tiles' slices, in ascending key-tile order,
+// cast to bf16.  One warp per (batch, q head, four query rows); a key tile's slice is read
+// only if that tile's CTA visited the rows' 64-row query tile (the decoder above decides,
+// as it did for the CTA), so unwritten slice rows are never read.
+__global__ void k_dq_reduce(const BwdArgs a) {
+    const Problem& P = a.P;
+    const int lane = threadIdx.x & 31, even = (lane & 1) == 0;
+    const int n4 = (P.S + 3) / 4, nkt = (P.S + BK - 1) / BK;
+    const int64_t slice = static_cast<int64_t>(P.B) * P.Hq * a.Spad * D;
+    const int64_t groups = static_cast<int64_t>(P.B) * P.Hq * n4;
+    const int64_t wstride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t gi = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); gi < groups;
+         gi += wstride) {
+        const int q4 = static_cast<int>(gi % n4);
+        const int h = static_cast<int>((gi / n4) % P.Hq);
+        const int b = static_cast<int>(gi / (static_cast<int64_t>(n4) * P.Hq));
+        const int qt = q4 * 4 / BQ;
+        const int64_t off = ((static_cast<int64_t>(b) * P.Hq + h) * (a.Spad / 4) + q4) * D * 4;
+        float4 acc[D / 32];
+#pragma unroll
+        for (int g = 0; g < D / 32; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int kt = 0; kt < nkt; ++kt) {
+            const Work w = decode_tile_of(a, b, h / P.G, kt);
+            if (qt < w.qt_lo || qt >= w.qt_lo + w.n_qt) continue;
+            const float4* in = reinterpret_cast<const float4*>(a.dq_acc + kt * slice + off);
+#pragma unroll
+            for (int g = 0; g < D / 32; ++g) {
+                const float4 x = in[g * 32 + lane];
+                acc[g].x += x.x;
+                acc[g].y += x.y;
+                acc[g].z += x.z;
+                acc[g].w += x.w;
+            }
+        }
+        // lane = channel c0 + lane; its float4 holds queries 4 q4 .. 4 q4 + 3: even lanes write
+        // rows 4 q4, 4 q4 + 1 and odd lanes rows 4 q4 + 2, + 3 as channel pairs
+        const int qa = q4 * 4 + (even ? 0 : 2);
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.dq) + b * P.qs[0] + h * P.qs[2];
+#pragma unroll
+        for (int g = 0; g < D / 32; ++g) {
+            const float4 x = acc[g];
+            const float y0 = __shfl_xor_sync(0xffffffffu, even ? x.z : x.x, 1);
+            const float y1 = __shfl_xor_sync(0xffffffffu, even ? x.w : x.y, 1);
+            const int c = g * 32 + lane - (even ? 0 : 1);
+            const uint32_t w0 = even ? pack_bf16(x.x, y0) : pack_bf16(y0, x.z);
+            const uint32_t w1 = even ? pack_bf16(x.y, y1) : pack_bf16(y1, x.w);
+            if (qa < P.S) *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(qa) * P.qs[1] + c) = w0;
+            if (qa + 1 < P.S) *reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(qa + 1) * P.qs[1] + c) = w1;
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_dq_reduce(const BwdArgs& a, cudaStream_t s) {
+    const int64_t warps = static_cast<int64_t>(a.P.B) * a.P.Hq * ((a.P.S + 3) / 4);
+    const int64_t blocks = std::min<int64_t>((warps + 7) / 8, 1 << 20);
+    k_dq_reduce<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
 
 bool bwd_tc_supported(const Problem& P) {
     if (P.dtype != BPA_BF16 || P.d != D || (P.dv != D && P.dv != 64) || P.block_idx) return false;

@@ -142,7 +142,7 @@ def test_select_rejects_bad_arguments(bpa):
 def test_status_strings(bpa):
     L = bpa.lib()
     assert L.bpa_status_string(5) == b"BPA_ERR_TIMEOUT"
-    assert L.bpa_version() == 4
+    assert L.bpa_version() == 5
 
 
 def test_version_1_descriptor_is_accepted(bpa):
@@ -159,6 +159,21 @@ def test_version_1_descriptor_is_accepted(bpa):
     D = _desc(bpa, seqlens_q=0x1000, ring_size=2)
     D.struct_size = bpa.bpa_attn_desc.seqlens_q.offset
     assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) > 0
+
+
+def test_deterministic_checks_and_workspace(bpa):
+    L = bpa.lib()
+    D = _desc(bpa, deterministic=1, ring_size=2)
+    assert L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(D)) == 0
+    assert b"deterministic" in L.bpa_last_error()
+    # one dQ slice per 128-key tile: S = 256 -> two slices of 4 * B * Hq * S' * d bytes
+    base = L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(_desc(bpa)))
+    det = L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(_desc(bpa, deterministic=1)))
+    assert det - base == 4 * 2 * 8 * 256 * 128
+    # version 4: the flag past the shorter struct is not read
+    D = _desc(bpa, deterministic=1, ring_size=2)
+    D.struct_size = bpa.bpa_attn_desc.deterministic.offset
+    assert L.bpa_workspace_size(bpa.BPA_OP_BWD, ctypes.byref(D)) > 0
 
 
 def test_sink_checks(bpa):

@@ -425,6 +425,40 @@ def test_sink_attention(bpa, ora, path):
         assert rel_l2(host(tds), rds) <= BF16_GRAD_REL_L2
 
 
+@pytest.mark.parametrize("case", ["causal", "swa_gqa4", "varlen", "f32", "block_selected"])
+def test_deterministic_backward(bpa, ora, case):
+    # the determinism knob: two backward calls give bit-identical gradients, and they match
+    # the oracle like the default mode
+    B, S, Hq, Hkv, d = 2, 300, 8, 2, 128
+    dtype, kw, okw = "bf16", dict(causal=True), dict(causal=True)
+    if case == "swa_gqa4":
+        kw["window"] = okw["window"] = (70, 0)
+    if case == "f32":
+        dtype, d = "f32", 64
+    if case == "block_selected":
+        S, Hkv, d = 256, 8, 64
+        idx = _planted_selection(B, Hq, S, 32, 3, 93)
+        kw.update(block_idx=torch.from_numpy(idx).cuda(), sel_block=32, top_n=3, local_window=32)
+        okw.update(block_idx=idx, sel_block=32, top_n=3, local_window=32)
+    if case == "varlen":
+        kw["seqlens_q"] = torch.tensor([300, 170], dtype=torch.int32, device="cuda")
+        okw["seqlens_q"] = [300, 170]
+    q, k, v, do = draw([(B, S, Hq, d), (B, S, Hkv, d), (B, S, Hkv, d), (B, S, Hq, d)], 94 + d, dtype)
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, **kw)
+    g1 = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, deterministic=True, **kw)
+    g2 = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, deterministic=True, **kw)
+    torch.cuda.synchronize()
+    for x, y in zip(g1, g2):
+        assert torch.equal(x, y)
+    rq, rk, rv, *_ = ora.attention_bwd(q, k, v, do, **okw)
+    for got, ref in zip(g1, (rq, rk, rv)):
+        if dtype == "f32":
+            assert max_abs(host(got), ref) <= FP32_MAX_ABS
+        else:
+            assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2
+
+
 def test_bounded_wait_reports_timeout(bpa):
     ws = bpa.workspace(256, "cuda")
     bpa.bpa_debug_wait_timeout(ws, 200_000_000)   # 0.2 s
