@@ -162,7 +162,7 @@ def time_extra_workloads(bpa, dev, peak_tf):
         g.manual_seed(seed)
         return torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(dtype)
 
-    def fwd_bwd(w, steps, warmup):
+    def fwd_bwd(w, steps, warmup, deterministic=False):
         dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
         q = rnd((w.B, w.S, w.Hq, w.d), dt, w.seed)
         k = rnd((w.B, w.S, w.Hkv, w.d), dt, w.seed + 1)
@@ -173,7 +173,7 @@ def time_extra_workloads(bpa, dev, peak_tf):
             bias = torch.zeros((1, 1, 1, w.S), device=dev, dtype=torch.float32)
             bias[..., w.S - w.pad_tail:] = -1e9
         kw = dict(causal=w.causal, window=w.window, bias=bias, query_chunk=w.query_chunk, key_chunk=w.key_chunk,
-                  ring_size=w.ring_size)
+                  ring_size=w.ring_size, deterministic=deterministic)
         tok_q = tok_k = w.B * w.S
         if w.seqlens_q:
             lens_q = list(w.seqlens_q)
@@ -221,6 +221,8 @@ def time_extra_workloads(bpa, dev, peak_tf):
     out[RING_LONG.name] = fwd_bwd(RING_LONG, 2, 1)
     out[MLA_CAUSAL.name] = fwd_bwd(MLA_CAUSAL, 10, 3)
     out[VARLEN_CAUSAL.name] = fwd_bwd(VARLEN_CAUSAL, 10, 3)
+    # the headline workload with the determinism knob (per-key-tile dQ slices, ordered sum)
+    out[GQA_CAUSAL.name + "_deterministic"] = fwd_bwd(GQA_CAUSAL, 10, 3, deterministic=True)
 
     def block_selected(w):
         q = rnd((w.B, w.S, w.Hq, w.d), torch.bfloat16, w.seed)

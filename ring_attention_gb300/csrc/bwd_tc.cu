@@ -121,8 +121,12 @@ __device__ __forceinline__ Work decode_tile_of(const BwdArgs& a, int b, int hkv,
 
 __device__ __forceinline__ Work decode(const BwdArgs& a) {
     const Problem& P = a.P;
-    const int r = blockIdx.x;   // lowest key tiles (most causal work) first
-    return decode_tile_of(a, r % P.B, (r / P.B) % P.Hkv, r / (P.B * P.Hkv));
+    int r = blockIdx.x;
+    const int b = r % P.B;
+    r /= P.B;
+    const int hkv = r % P.Hkv;
+    const int kt = r / P.Hkv;    // lowest key tiles (most causal work) first
+    return decode_tile_of(a, b, hkv, kt);
 }
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
