@@ -3,8 +3,9 @@
 
 One step = bpa_fwd + bpa_bwd over one batch of the GQA causal workload
 (B=2, S=4096, Hq=32, Hkv=8, d=128, bf16, seed 1), inputs resident in HBM.
-FLOPs count only allowed (query, key) entries: 4*d per entry forward
-(Q K^T and P V), 10*d backward (the five contractions, recompute included).
+FLOPs count only allowed (query, key) entries: 2*(d + dv) per entry forward
+(Q K^T and P V), 6*d + 4*dv backward (the five contractions, recompute included);
+4*d and 10*d for this workload (dv = d).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -42,6 +43,24 @@ def flops(w, entries):
     dK = dS^T Q and dQ = dS K (2 d each)."""
     d, dv = w.d, w.d_v
     return (2.0 * d + 2.0 * dv) * entries, (6.0 * d + 4.0 * dv) * entries
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest x over the ranks of the initialised process group (x itself on one
+    process): every rank's timed region is measured, the slowest one counts."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput of weak-scaled replicas: the units all ranks processed over
+    the slowest rank's time."""
+    return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
 
 
 def load_peaks():
@@ -398,15 +417,11 @@ def main():
     bwd_main_ms = [e[1].elapsed_time(e[2]) for e in evb]
     bwd_pre_ms = [e[0].elapsed_time(e[1]) for e in evb]
     bwd_post_ms = [e[2].elapsed_time(e[3]) for e in evb]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
 
     entries = unmasked_entries(w)
     f_fwd, f_bwd = flops(w, entries)
-    value = (f_fwd + f_bwd) * K * world / (total_ms * 1e-3) / 1e12
+    value = aggregate_tflops(f_fwd + f_bwd, K, world, total_ms)
     ms_per_step = total_ms / K
     peaks, peaks_kind = load_peaks()
     peak_tf = float(peaks["bf16_tflops"])
@@ -442,12 +457,8 @@ def main():
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = (f_fwd + f_bwd) * args.e2e_steps * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    e2e_val = aggregate_tflops(f_fwd + f_bwd, args.e2e_steps, world, e2e_ms)
 
     extra = None
     if rank == 0 and not args.no_extra:
