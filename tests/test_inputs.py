@@ -1,6 +1,8 @@
 """Host-side helpers of the seeded inputs: the entry count the throughput figures
 divide by agrees with the oracle's own mask (with q = k = 0 every allowed key has
 weight 1, so the row sums l count the allowed keys)."""
+import json
+import os
 from dataclasses import replace
 
 import numpy as np
@@ -32,3 +34,16 @@ def test_named_workload_counts():
     assert W.unmasked_entries(W.VARLEN_CAUSAL) < W.unmasked_entries(full)
     lens = W.VARLEN_CAUSAL.seqlens_q
     assert W.unmasked_entries(W.VARLEN_CAUSAL) == 32 * sum(n * (n + 1) // 2 for n in lens)
+
+
+def test_mla_workload_matches_the_printed_shapes():
+    # the page prints the MLA run's output and gradient shapes; the workload that stands in
+    # for it must produce exactly those (o: [B, S, Hq, dv]; dq, dk, dv: q's, k's, v's shapes)
+    with open(os.path.join(os.path.dirname(__file__), "golden", "mla_shapes.json")) as f:
+        g = json.load(f)
+    w = W.MLA_CAUSAL
+    assert (w.d, w.d_v, w.seed) == (g["qk_head_dim"], g["v_head_dim"], g["seed"])
+    assert [w.B, w.S, w.Hq, w.d_v] == g["output_shape"]
+    assert [[w.B, w.S, w.Hq, w.d], [w.B, w.S, w.Hkv, w.d], [w.B, w.S, w.Hkv, w.d_v]] == g["grad_shapes"]
+    q, k, v, do, _ = W.make_inputs(w, S=8)
+    assert q.shape[-1] == 128 and k.shape[-1] == 128 and v.shape[-1] == 64 and do.shape[-1] == 64
