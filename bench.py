@@ -165,6 +165,41 @@ def cpu_oracle_sample(w, budget_s: float):
     return tf, dt, desc, oracle.num_threads(), S
 
 
+def oracle_baselines(budget_s: float = 15.0):
+    """The float64 oracle timed on the host cores beside the GPU path (a reported baseline,
+    not a target): full runs of the tiny fp32, sliding-window and block-selected workloads;
+    the long ring workload on a reduced S of the same recipe, its full-run time extrapolated
+    by the ratio of unmasked entries and labelled as such.  (The headline workload's sample
+    is the line's cpu_baseline.)"""
+    from oracle import oracle
+    from ring_attention_gb300.inputs import BLOCK_SEL, GQA_SWA, RING_LONG, TINY_F32
+    oracle.build()
+    out = {"cores": oracle.num_threads(), "kind": "oracle"}
+    for w in (TINY_F32, GQA_SWA):
+        q, k, v, do, bias = make_inputs(w)
+        t0 = time.perf_counter()
+        oracle.attention_bwd(q, k, v, do, causal=w.causal, window=w.window, bias=bias)
+        dt = time.perf_counter() - t0
+        f = sum(flops(w, unmasked_entries(w)))
+        out[w.name] = {"run": "full", "fwd_bwd_s": dt, "tflops": f / dt / 1e12}
+    w = BLOCK_SEL
+    q, k, v, _, _ = make_inputs(w)
+    t0 = time.perf_counter()
+    idx = oracle.select_blocks(q, k, block_size=w.sel_block, top_n=w.top_n)
+    t1 = time.perf_counter()
+    oracle.attention_fwd(q, k, v, causal=True, block_idx=idx, sel_block=w.sel_block, top_n=w.top_n,
+                         local_window=w.local_window)
+    t2 = time.perf_counter()
+    out[w.name] = {"run": "full", "select_s": t1 - t0, "fwd_s": t2 - t1}
+    w = RING_LONG
+    tf, dt, _, _, S = cpu_oracle_sample(w, budget_s)
+    part = unmasked_entries(w, S) // w.B
+    out[w.name] = {"run": f"B=1, S={S} of the same recipe; full run extrapolated by unmasked entries",
+                   "fwd_bwd_s": dt, "tflops": tf,
+                   "extrapolated_full_fwd_bwd_s": dt * unmasked_entries(w) / part}
+    return out
+
+
 def time_extra_workloads(bpa, dev, peak_tf):
     """Secondary workloads (not the headline): device-timed per-call times.
     Inputs are drawn on the device from seeded generators (timing only; the
@@ -465,9 +500,12 @@ def main():
         extra = time_extra_workloads(bpa, dev, peak_tf)
 
     cpu = None
+    oracle_others = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, desc, cores, _ = cpu_oracle_sample(w, 20.0)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+        if not args.no_extra:
+            oracle_others = oracle_baselines()
 
     if rank == 0:
         line = {
@@ -495,6 +533,7 @@ def main():
             "clocks": clocks.summary(),
             "wall_s_timed_region": wall,
             "extra": extra,
+            "oracle_baselines": oracle_others,
         }
         print(json.dumps(line))
     if world > 1:
