@@ -72,12 +72,22 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+def code_digest(path: str) -> str:
+    """sha256[:16] of a C / CUDA source with its comments and white space removed: edits to
+    comments alone keep the digest, any change to the code changes it."""
+    import re
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()[:16]
+
+
 def kernel_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of the kernel (else None)."""
+    on the current code of the kernel (else None)."""
     src = {"k_bwd_tc": "bwd_tc.cu", "k_fwd_tc": "fwd_tc.cu"}[kernel]
     path = os.path.join(ROOT, "ring_attention_gb300", "csrc", src)
-    digest = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    digest = code_digest(path)
     table = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(table):
         return None

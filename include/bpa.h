@@ -75,7 +75,9 @@ typedef enum { BPA_OP_FWD = 0, BPA_OP_BWD = 1 } bpa_op;
 typedef struct bpa_attn_desc {
     uint32_t struct_size;      /* = sizeof(bpa_attn_desc) */
     int32_t dtype;             /* bpa_dtype of q, k, v, o, dout, dq, dk, dv */
-    int32_t B, S, Hq, Hkv, d;  /* Sq = Sk = S; Hq % Hkv == 0; 1 <= d <= 512 (head dim of q, k) */
+    int32_t B, S, Hq, Hkv, d;  /* q, k, v share the padded length S (shorter sequences: the
+                                * version-3 lengths below); Hq % Hkv == 0; 1 <= d <= 512 (head
+                                * dim of q, k) */
     const void* q;             /* [B, S, Hq, d] */
     const void* k;             /* [B, S, Hkv, d] */
     const void* v;             /* [B, S, Hkv, dv] */

@@ -1,9 +1,11 @@
-// fwd_tc.cu - blockwise attention forward on the 5th-generation tensor cores (bf16, d = 64 / 128).
+// fwd_tc.cu - blockwise attention forward on the 5th-generation tensor cores (bf16; (d, dv) =
+// (64, 64), (128, 128) or (128, 64)).
 //
-// One CTA owns two consecutive 128-row query tiles of one (batch, q head)
-// and walks the 128-key tiles their masks allow, folding each into a running
-// (max, numerator, denominator) carry per query row ("bpt.py",
-// _blockwise_attention_fwd / scan_kv_block):
+// Persistent: one CTA per SM (two for the one-tile variant) takes work items from a
+// counter, heaviest first; an item is two consecutive 128-row query tiles of one
+// (batch, q head).  For each item the CTA walks the 128-key tiles the masks (and the
+// batch entry's sequence lengths) allow, folding each into a running (max, numerator,
+// denominator) carry per query row ("bpt.py", _blockwise_attention_fwd / scan_kv_block):
 //     m' = max(m, rowmax S);  P = exp(S - m');  num = num * exp(m - m') + P V;
 //     den = den * exp(m - m') + rowsum P
 // Both query tiles share every K / V tile that is loaded.
@@ -26,6 +28,8 @@
 // numerator and denominator share the reference.
 // Fully masked tiles are never visited (key ranges are cut by position); only
 // tiles that straddle a mask edge apply the elementwise mask.
+// The epilogue divides by the denominator (plus the sink term with sink attention) and
+// stores O, m, l.
 // Every wait is bounded (common.cuh); on a timeout the CTA drains its in-flight
 // copies and MMAs, frees TMEM and returns.
 #include <math.h>

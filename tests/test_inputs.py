@@ -47,3 +47,18 @@ def test_mla_workload_matches_the_printed_shapes():
     assert [[w.B, w.S, w.Hq, w.d], [w.B, w.S, w.Hkv, w.d], [w.B, w.S, w.Hkv, w.d_v]] == g["grad_shapes"]
     q, k, v, do, _ = W.make_inputs(w, S=8)
     assert q.shape[-1] == 128 and k.shape[-1] == 128 and v.shape[-1] == 64 and do.shape[-1] == 64
+
+
+def test_code_digest_ignores_comments_only(tmp_path):
+    # the traffic figures stay tied to the kernel's code: comment edits keep the digest,
+    # any change of code changes it
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    a = tmp_path / "a.cu"
+    a.write_text("// head\nint f(int x) { /* twice */ return 2 * x; }\n")
+    b = tmp_path / "b.cu"
+    b.write_text("// another head\n\nint f(int x) {\n    return 2 * x;   // doubled\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f(int x) { return 3 * x; }\n")
+    assert bench.code_digest(str(a)) == bench.code_digest(str(b)) != bench.code_digest(str(c))
