@@ -52,7 +52,17 @@
  *     vector (off_by_one: sink = 0):  P = exp(z) / (exp(sink) + sum exp(z));
  *     m and l include it (m = max(max z, sink)), so a row with no allowed key
  *     has O = 0, m = sink, l = 1; the sink's gradient is
- *     dsink[h] = -sum over rows of P_sink * <dO, O>.
+ *     dsink[h] = -sum over rows of P_sink * <dO, O>;
+ *   - attention dropout ([bpt] _blockwise_attention_fwd / _bwd and the
+ *     blockwise attention helper: a Bernoulli(p) mask over (batch, head, q, k)
+ *     whose dropped entries get the dtype minimum added to the score, i.e.
+ *     they leave the softmax, which renormalises over the kept keys; no
+ *     1/(1-p) factor): the JAX generator is not available, so the mask comes
+ *     from the counter-based generator Philox4x32-10 (Salmon, Moraes, Dror,
+ *     Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011) with the
+ *     64-bit seed as key and the position as counter, {k / 4, q, h, b}; word
+ *     k % 4 of the output is the entry's 32-bit draw, and the entry is
+ *     dropped when the draw is below the threshold p * 2^32.
  */
 #include <math.h>
 #include <stdint.h>
@@ -78,6 +88,8 @@ typedef struct {
     int32_t bottom_right;           /* 1: causal / window diagonal at k = q + Lk - Lq */
     const double* sink;             /* NULL or [Hq]: extra softmax logit per q head */
     double* dsink;                  /* NULL or [Hq]: gradient of sink (written by ora_bwd) */
+    uint32_t drop_threshold;        /* 0: no dropout; else drop entries whose draw < this */
+    uint32_t drop_seed_lo, drop_seed_hi;
 } ora_desc;
 
 /* ---- element access: inputs are widened exactly to double ------------- */
@@ -115,6 +127,41 @@ static double* widen_kv(const ora_desc* D, const void* src, int w) {
     return out;
 }
 
+/* ---- Philox4x32-10 (the SC 2011 paper's definition) --------------------
+ * One round maps the counter (c0, c1, c2, c3) with key (k0, k1) to
+ *   (hi(B c2) ^ c1 ^ k0, lo(B c2), hi(A c0) ^ c3 ^ k1, lo(A c0))
+ * with A = 0xD2511F53, B = 0xCD9E8D57 (hi / lo: the halves of the 64-bit
+ * product); between rounds the key grows by the Weyl increments
+ * (0x9E3779B9, 0xBB67AE85).  Ten rounds. */
+static void philox4x32_10(const uint32_t ctr[4], uint32_t k0, uint32_t k1, uint32_t out[4]) {
+    uint32_t c[4] = {ctr[0], ctr[1], ctr[2], ctr[3]};
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t pa = (uint64_t)0xD2511F53u * c[0];
+        const uint64_t pb = (uint64_t)0xCD9E8D57u * c[2];
+        const uint32_t n0 = (uint32_t)(pb >> 32) ^ c[1] ^ k0;
+        const uint32_t n1 = (uint32_t)pb;
+        const uint32_t n2 = (uint32_t)(pa >> 32) ^ c[3] ^ k1;
+        const uint32_t n3 = (uint32_t)pa;
+        c[0] = n0;
+        c[1] = n1;
+        c[2] = n2;
+        c[3] = n3;
+    }
+    for (int i = 0; i < 4; ++i) out[i] = c[i];
+}
+
+/* The 32-bit draw of score entry (b, h, q, k): counter {k / 4, q, h, b}, word k % 4. */
+static uint32_t drop_draw(const ora_desc* D, int b, int h, int q, int k) {
+    const uint32_t ctr[4] = {(uint32_t)k >> 2, (uint32_t)q, (uint32_t)h, (uint32_t)b};
+    uint32_t out[4];
+    philox4x32_10(ctr, D->drop_seed_lo, D->drop_seed_hi, out);
+    return out[k & 3];
+}
+
 /* ---- the mask ([te] _make_causal_swa_mask; [bpt] causal; [ann]) -------- */
 
 /* Valid query / key counts of batch entry b and the offset of the causal /
@@ -148,6 +195,7 @@ static int allowed(const ora_desc* D, int b, int h, int q, int k) {
     if (D->causal && k > q + off) return 0;
     if (D->window_left >= 0 && k < q + off - D->window_left) return 0;
     if (D->window_right >= 0 && k > q + off + D->window_right) return 0;
+    if (D->drop_threshold && drop_draw(D, b, h, q, k) < D->drop_threshold) return 0;   /* dropped */
     if (D->block_idx) {
         int in_local = (k <= q) && (k >= q - (D->local_window - 1));
         int in_sel = 0;
@@ -683,6 +731,22 @@ int ora_select(const void* q, const void* k, int32_t in_dtype, int32_t B, int32_
         free(pick);
     }
     return fail;
+}
+
+/* The dropout decisions of one (b, h) block: keep[q * S + k] = 1 unless the
+ * entry's draw falls below the threshold (positions only; other masks are not
+ * applied).  For the pins. */
+int ora_dropout_keep(const ora_desc* D, int32_t b, int32_t h, uint8_t* keep) {
+    for (int q = 0; q < D->S; ++q)
+        for (int k = 0; k < D->S; ++k)
+            keep[(int64_t)q * D->S + k] = !(D->drop_threshold && drop_draw(D, b, h, q, k) < D->drop_threshold);
+    return 0;
+}
+
+/* Philox4x32-10 itself, for the pins. */
+int ora_philox4x32_10(const uint32_t* ctr, uint32_t k0, uint32_t k1, uint32_t* out) {
+    philox4x32_10(ctr, k0, k1, out);
+    return 0;
 }
 
 int ora_num_threads(void) {

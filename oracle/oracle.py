@@ -50,6 +50,8 @@ class _Desc(ctypes.Structure):
         ("seqlens_q", ctypes.c_void_p), ("seqlens_kv", ctypes.c_void_p),
         ("bottom_right", ctypes.c_int32),
         ("sink", ctypes.c_void_p), ("dsink", ctypes.c_void_p),
+        ("drop_threshold", ctypes.c_uint32), ("drop_seed_lo", ctypes.c_uint32),
+        ("drop_seed_hi", ctypes.c_uint32),
     ]
 
 
@@ -67,8 +69,10 @@ def _bind(lib):
     lib.ora_rows.argtypes = [dp, P, P, P, P, i32, P, P, P, P, P]
     lib.ora_keys.argtypes = [dp, P, P, P, P, i32, i32, i32, P, P, P]
     lib.ora_select.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32, P]
+    lib.ora_dropout_keep.argtypes = [dp, i32, i32, P]
+    lib.ora_philox4x32_10.argtypes = [P, ctypes.c_uint32, ctypes.c_uint32, P]
     for f in ("ora_fwd", "ora_bwd", "ora_blockwise_fwd", "ora_rows", "ora_keys",
-              "ora_select", "ora_num_threads"):
+              "ora_select", "ora_num_threads", "ora_dropout_keep", "ora_philox4x32_10"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -102,7 +106,8 @@ def _ptr(a):
 
 
 def _desc(q, k, v, *, causal, window, scale, bias, block_idx, sel_block, top_n,
-          local_window, in_dtype, seqlens_q=None, seqlens_kv=None, bottom_right=False, sink=None):
+          local_window, in_dtype, seqlens_q=None, seqlens_kv=None, bottom_right=False, sink=None,
+          dropout_p=0.0, dropout_seed=0):
     B, S, Hq, d = q.shape
     Hkv, dv = k.shape[2], v.shape[3]
     if k.shape != (B, S, Hkv, d) or v.shape != (B, S, Hkv, dv):
@@ -153,7 +158,21 @@ def _desc(q, k, v, *, causal, window, scale, bias, block_idx, sel_block, top_n,
             raise ValueError("sink must be [Hq]")
         keep.append(sk)
         D.sink = sk.ctypes.data
+    _set_dropout(D, dropout_p, dropout_seed)
     return D, keep
+
+
+def dropout_threshold(p: float) -> int:
+    """Entries whose 32-bit draw is below this are dropped: round(p * 2^32)."""
+    if not 0.0 <= p < 1.0:
+        raise ValueError("dropout probability must be in [0, 1)")
+    return min(int(round(p * 2.0 ** 32)), 2 ** 32 - 1)
+
+
+def _set_dropout(D, p, seed):
+    D.drop_threshold = dropout_threshold(p)
+    seed = int(seed) & (2 ** 64 - 1)
+    D.drop_seed_lo, D.drop_seed_hi = seed & 0xFFFFFFFF, seed >> 32
 
 
 def _check(rc, what):
@@ -163,13 +182,14 @@ def _check(rc, what):
 
 def attention_fwd(q, k, v, *, causal=False, window=None, scale=None, bias=None,
                   block_idx=None, sel_block=32, top_n=8, local_window=32, seqlens_q=None,
-                  seqlens_kv=None, bottom_right=False, sink=None):
+                  seqlens_kv=None, bottom_right=False, sink=None, dropout_p=0.0, dropout_seed=0):
     """One-shot masked softmax attention.  Returns (o, m, l) in float64."""
     (q, dt), (k, _), (v, _) = _in(q), _in(k), _in(v)
     D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
                     block_idx=block_idx, sel_block=sel_block, top_n=top_n,
                     local_window=local_window, in_dtype=dt, seqlens_q=seqlens_q,
-                    seqlens_kv=seqlens_kv, bottom_right=bottom_right, sink=sink)
+                    seqlens_kv=seqlens_kv, bottom_right=bottom_right, sink=sink,
+                    dropout_p=dropout_p, dropout_seed=dropout_seed)
     B, S, Hq, _ = q.shape
     o = np.zeros((B, S, Hq, v.shape[3]))
     m = np.zeros((B, Hq, S))
@@ -181,14 +201,16 @@ def attention_fwd(q, k, v, *, causal=False, window=None, scale=None, bias=None,
 
 def attention_bwd(q, k, v, dout, *, causal=False, window=None, scale=None, bias=None,
                   block_idx=None, sel_block=32, top_n=8, local_window=32, seqlens_q=None,
-                  seqlens_kv=None, bottom_right=False, sink=None, want_dsink=False):
+                  seqlens_kv=None, bottom_right=False, sink=None, want_dsink=False, dropout_p=0.0,
+                  dropout_seed=0):
     """Analytic gradients.  Returns (dq, dk, dv, o, m, l) in float64, plus dsink [Hq]
     when want_dsink (a sink must be given)."""
     (q, dt), (k, _), (v, _), (dout, _) = _in(q), _in(k), _in(v), _in(dout)
     D, keep = _desc(q, k, v, causal=causal, window=window, scale=scale, bias=bias,
                     block_idx=block_idx, sel_block=sel_block, top_n=top_n,
                     local_window=local_window, in_dtype=dt, seqlens_q=seqlens_q,
-                    seqlens_kv=seqlens_kv, bottom_right=bottom_right, sink=sink)
+                    seqlens_kv=seqlens_kv, bottom_right=bottom_right, sink=sink,
+                    dropout_p=dropout_p, dropout_seed=dropout_seed)
     dsink = None
     if want_dsink:
         if sink is None:
@@ -273,4 +295,22 @@ def select_blocks(q, k, *, block_size=32, top_n=8):
     out = np.zeros((B, H, S // block_size, top_n), dtype=np.int32)
     _check(_load().ora_select(_ptr(q), _ptr(k), dt, B, S, H, d, block_size, top_n, _ptr(out)),
            "select")
+    return out
+
+
+def dropout_keep(S, b, h, *, dropout_p, dropout_seed):
+    """The dropout decisions of batch entry b, q head h: uint8 [S, S], 1 = kept."""
+    D = _Desc()
+    D.S = S
+    _set_dropout(D, dropout_p, dropout_seed)
+    keep = np.zeros((S, S), dtype=np.uint8)
+    _check(_load().ora_dropout_keep(ctypes.byref(D), int(b), int(h), _ptr(keep)), "dropout_keep")
+    return keep
+
+
+def philox4x32_10(counter, key):
+    """The oracle's Philox4x32-10: four uint32 counter words, two key words -> four words."""
+    c = np.ascontiguousarray(counter, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    _check(_load().ora_philox4x32_10(_ptr(c), int(key[0]), int(key[1]), _ptr(out)), "philox")
     return out

@@ -28,6 +28,11 @@ MUTANTS = [
     ("sink_left_out_of_denominator", "double l = with_sink ? exp(sk - m) : 0.0;", "double l = 0.0;"),
     ("sink_left_out_of_max", "if (sk > m) m = sk;", "if (sk > m && any) m = sk;"),
     ("sink_gradient_sign", "ds_part[b * D->Hq + h] -= exp(", "ds_part[b * D->Hq + h] += exp("),
+    ("dropout_one_word_per_call", "return out[k & 3];", "return out[0];"),
+    ("dropout_counter_without_head", "(uint32_t)q, (uint32_t)h, (uint32_t)b};", "(uint32_t)q, 0u, (uint32_t)b};"),
+    ("dropout_keeps_the_dropped", "drop_draw(D, b, h, q, k) < D->drop_threshold) return 0;",
+     "drop_draw(D, b, h, q, k) >= D->drop_threshold) return 0;"),
+    ("dropout_not_applied", "if (D->drop_threshold && drop_draw(D, b, h, q, k) < D->drop_threshold) return 0;", ";"),
     ("dk_transposed_operand", "dkr[c] = dkr[c] + D->scale * dS * qrow[c];",
      "dkr[c] = dkr[c] + D->scale * dS * kr[c];", 1),
     ("dq_scale_dropped", "dqrow[c] = dqrow[c] + D->scale * dS * kr[c];", "dqrow[c] = dqrow[c] + dS * kr[c];"),
@@ -70,6 +75,8 @@ def battery(ora):
     yield lambda: pins.test_sink_equals_extra_key(ora, True, "learnable")
     yield lambda: pins.test_sink_rows_without_keys_and_padding(ora)
     yield lambda: pins.test_sink_gradients_match_finite_differences(ora)
+    yield lambda: pins.test_dropout_draws_are_bernoulli(ora, 0.1)
+    yield lambda: pins.test_dropout_is_the_fixed_mask(ora, True)
 
 
 def _build_mutant(tmp_path, name, text):

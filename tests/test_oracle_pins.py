@@ -559,6 +559,100 @@ def test_sink_gradients_match_finite_differences(ora):
 
 
 # --------------------------------------------------------------------------
+# attention dropout (bpt.py: a Bernoulli(p) mask over (batch, head, q, k); the dropped
+# entries leave the softmax) with the draws of a counter-based generator
+# --------------------------------------------------------------------------
+def brute_masked(q, k, v, keep, causal, scale):
+    """Brute force with the dropped entries given a -1e300 bias; rows whose best score is
+    that bias keep no real key (O = 0, m = -inf, l = 0).  keep: [B, Hq, S, S]."""
+    bias = np.where(keep.astype(bool), 0.0, -1e300)
+    o, m, l = brute_force(q, k, v, causal=causal, scale=scale, bias=bias)
+    real = m > -1e200
+    o = np.where(np.transpose(real, (0, 2, 1))[..., None], o, 0.0)
+    return o, np.where(real, m, -np.inf), np.where(real, l, 0.0)
+
+
+def _keep_all(B, Hq, S, p, seed, ora):
+    return np.stack([np.stack([ora.dropout_keep(S, b, h, dropout_p=p, dropout_seed=seed) for h in range(Hq)])
+                     for b in range(B)])
+
+
+@pytest.mark.parametrize("p", [0.1, 0.5])
+def test_dropout_draws_are_bernoulli(ora, p):
+    S, n = 512, 512 * 512
+    masks = [ora.dropout_keep(S, b, h, dropout_p=p, dropout_seed=1234) for b, h in ((0, 0), (0, 1), (3, 0))]
+    for keep in masks:
+        drop = 1.0 - keep.astype(np.float64)
+        sigma = (p * (1 - p) / n) ** 0.5
+        assert abs(drop.mean() - p) < 5 * sigma
+        # no correlation between neighbouring keys (in and across the groups of four that
+        # share one generator call), neighbouring rows
+        for a, b in ((drop[:, :-1], drop[:, 1:]), (drop[:, :-4], drop[:, 4:]), (drop[:-1], drop[1:])):
+            c = np.corrcoef(a.ravel(), b.ravel())[0, 1]
+            assert abs(c) < 5 / a.size ** 0.5
+    # heads and batch entries draw different masks; the seed decides, repeatably
+    assert (masks[0] != masks[1]).mean() > 0.5 * 2 * p * (1 - p)
+    assert (masks[0] != masks[2]).mean() > 0.5 * 2 * p * (1 - p)
+    assert np.array_equal(masks[0], ora.dropout_keep(S, 0, 0, dropout_p=p, dropout_seed=1234))
+    assert not np.array_equal(masks[0], ora.dropout_keep(S, 0, 0, dropout_p=p, dropout_seed=1235))
+    assert ora.dropout_keep(64, 0, 0, dropout_p=0.0, dropout_seed=7).all()
+
+
+def test_philox_is_a_bijection_of_the_counter(ora):
+    # distinct counters give distinct outputs for one key (each round permutes the counter
+    # space), and changing the key changes every word
+    rng = np.random.default_rng(208)
+    ctrs = {tuple(int(x) for x in c) for c in rng.integers(0, 2 ** 32, (4096, 4), dtype=np.uint64)}
+    ctrs |= {(i, 0, 0, 0) for i in range(256)} | {(0, 0, i, 0) for i in range(256)}
+    outs = {tuple(ora.philox4x32_10(c, (17, 29)).tolist()) for c in ctrs}
+    assert len(outs) == len(ctrs)
+    a = ora.philox4x32_10([1, 2, 3, 4], (17, 29))
+    b = ora.philox4x32_10([1, 2, 3, 4], (18, 29))
+    assert np.all(a != b)
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "full"])
+def test_dropout_is_the_fixed_mask(ora, causal):
+    B, S, Hq, Hkv, d, dv = 2, 24, 4, 2, 3, 2
+    q, k, v = rnd((B, S, Hq, d), 201), rnd((B, S, Hkv, d), 202), rnd((B, S, Hkv, dv), 203)
+    p, seed = 0.4, 99
+    o, m, l = ora.attention_fwd(q, k, v, causal=causal, scale=0.7, dropout_p=p, dropout_seed=seed)
+    bo, bm, bl = brute_masked(q, k, v, _keep_all(B, Hq, S, p, seed, ora), causal, 0.7)
+    np.testing.assert_allclose(o, bo, rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(np.isfinite(m), np.isfinite(bm))
+    np.testing.assert_allclose(l, bl, rtol=1e-12, atol=1e-13)
+    # p = 0 is plain attention
+    o0, _, _ = ora.attention_fwd(q, k, v, causal=causal, scale=0.7, dropout_p=0.0, dropout_seed=seed)
+    po, _, _ = ora.attention_fwd(q, k, v, causal=causal, scale=0.7)
+    np.testing.assert_array_equal(o0, po)
+
+
+def test_dropout_gradients_match_finite_differences(ora):
+    B, S, Hq, Hkv, d, dv = 1, 8, 2, 1, 2, 2
+    q, k, v, do = (rnd((B, S, Hq, d), 204), rnd((B, S, Hkv, d), 205), rnd((B, S, Hkv, dv), 206),
+                   rnd((B, S, Hq, dv), 207))
+    p, seed = 0.3, 5
+    dq, dk, dvv, *_ = ora.attention_bwd(q, k, v, do, causal=True, scale=0.9, dropout_p=p, dropout_seed=seed)
+    keep = _keep_all(B, Hq, S, p, seed, ora)
+    h = 1e-6
+
+    def loss(qq, kk, vv):
+        return float((brute_masked(qq, kk, vv, keep, True, 0.9)[0] * do).sum())
+
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dvv)):
+        fd = np.zeros_like(x)
+        for ix in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[ix] += h
+            xm[ix] -= h
+            ap = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            am = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            fd[ix] = (loss(*ap) - loss(*am)) / (2 * h)
+        err = np.abs(fd - g).max() / max(np.abs(g).max(), 1e-30)
+        assert err < 1e-6, f"d{name}: relative error {err}"
+
+
+# --------------------------------------------------------------------------
 # sampled rows / keys agree with the full evaluation
 # --------------------------------------------------------------------------
 def test_sampled_rows_and_keys_match_full(ora):
