@@ -506,7 +506,7 @@ def main():
     e2e_val = aggregate_tflops(f_fwd + f_bwd, args.e2e_steps, world, e2e_ms)
 
     extra = None
-    if rank == 0 and not args.no_extra:
+    if rank == 0 and world == 1 and not args.no_extra:   # at N > 1 the other GPUs would idle meanwhile
         extra = time_extra_workloads(bpa, dev, peak_tf)
 
     cpu = None
