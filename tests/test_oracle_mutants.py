@@ -33,6 +33,12 @@ MUTANTS = [
     ("dropout_keeps_the_dropped", "drop_draw(D, b, h, q, k) < D->drop_threshold) return 0;",
      "drop_draw(D, b, h, q, k) >= D->drop_threshold) return 0;"),
     ("dropout_not_applied", "if (D->drop_threshold && drop_draw(D, b, h, q, k) < D->drop_threshold) return 0;", ";"),
+    # slips inside the generator keep it a bijection with good statistics; only its
+    # published known answers catch them
+    ("philox_round_constant", "(uint64_t)0xD2511F53u * c[0]", "(uint64_t)0xD2511F55u * c[0]"),
+    ("philox_weyl_increment", "k1 += 0xBB67AE85u;", "k1 += 0xBB67AE87u;"),
+    ("philox_hi_lo_swapped", "const uint32_t n1 = (uint32_t)pb;", "const uint32_t n1 = (uint32_t)(pb >> 32) ^ 1u;"),
+    ("philox_nine_rounds", "for (int r = 0; r < 10; ++r) {", "for (int r = 0; r < 9; ++r) {"),
     ("dk_transposed_operand", "dkr[c] = dkr[c] + D->scale * dS * qrow[c];",
      "dkr[c] = dkr[c] + D->scale * dS * kr[c];", 1),
     ("dq_scale_dropped", "dqrow[c] = dqrow[c] + D->scale * dS * kr[c];", "dqrow[c] = dqrow[c] + dS * kr[c];"),
@@ -75,6 +81,7 @@ def battery(ora):
     yield lambda: pins.test_sink_equals_extra_key(ora, True, "learnable")
     yield lambda: pins.test_sink_rows_without_keys_and_padding(ora)
     yield lambda: pins.test_sink_gradients_match_finite_differences(ora)
+    yield lambda: pins.test_philox_known_answers(ora)
     yield lambda: pins.test_dropout_draws_are_bernoulli(ora, 0.1)
     yield lambda: pins.test_dropout_is_the_fixed_mask(ora, True)
 

@@ -598,6 +598,19 @@ def test_dropout_draws_are_bernoulli(ora, p):
     assert ora.dropout_keep(64, 0, 0, dropout_p=0.0, dropout_seed=7).all()
 
 
+def test_philox_known_answers(ora):
+    # the generator's published known-answer vectors (SC 2011 paper's Random123
+    # distribution): a wrong round constant, Weyl increment or word order fails these even
+    # though the map would stay a bijection with good statistics
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.json")) as f:
+        kat = json.load(f)
+    for vec in kat["vectors"]:
+        ctr = [int(x, 16) for x in vec["counter"]]
+        key = tuple(int(x, 16) for x in vec["key"])
+        got = [int(x) for x in ora.philox4x32_10(ctr, key)]
+        assert got == [int(x, 16) for x in vec["expected"]], vec
+
+
 def test_philox_is_a_bijection_of_the_counter(ora):
     # distinct counters give distinct outputs for one key (each round permutes the counter
     # space), and changing the key changes every word
