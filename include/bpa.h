@@ -33,8 +33,11 @@
  *     elements and every base pointer 16-byte aligned.
  *   - m and l are float32 [B, Hq, S], contiguous, natural-log units of z.
  *   - All pointers are device pointers owned by the caller.  The library
- *     allocates no device memory and keeps no per-call state; scratch
- *     lives in the caller's workspace (size from bpa_workspace_size).
+ *     allocates no device memory at run time and keeps no per-call state;
+ *     scratch lives in the caller's workspace (size from bpa_workspace_size).
+ *     The one exception is static: every GPU that loads the library holds a
+ *     fixed 16 MiB __device__ array until the process exits, the scratch of
+ *     bpa_select_blocks_noalloc (unused by every other entry point).
  *   - Calls are asynchronous on the given stream (a cudaStream_t passed as
  *     void*; NULL is the legacy default stream).  Argument errors are
  *     returned before anything is launched.  Launch failures return
@@ -204,7 +207,9 @@ size_t bpa_select_workspace_size(int32_t B, int32_t S, int32_t H, int32_t d, int
  * with -1, to block_idx_out int32 [B, H, S/block_size, top_n].  Sums and
  * not means are compared; they rank identically.
  * q and k are [B, S, H, d] (dtype bpa_dtype) with (b, s, h) strides.
- * S % block_size == 0, 1 <= top_n <= 64, d <= 512. */
+ * S % block_size == 0, S / block_size <= 4096, 1 <= top_n <= 64, d <= 512.
+ * A NaN score (from non-finite inputs; the page does not rank one) ranks
+ * below every number, NaN scores in block order. */
 bpa_status bpa_select_blocks(const void* q, const void* k, int32_t dtype, int32_t B,
                              int32_t S, int32_t H, int32_t d, const int64_t q_strides[3],
                              const int64_t k_strides[3], int32_t block_size, int32_t top_n,
@@ -227,13 +232,18 @@ bpa_status bpa_select_blocks(const void* q, const void* k, int32_t dtype, int32_
  *     before anything is launched; use bpa_select_blocks for them.
  *   - The first call on each device looks up the buffer's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on that device.
+ *     before any stream capture on that device.  The address is kept for the
+ *     life of the process and does not survive cudaDeviceReset: do not call
+ *     this entry point after resetting the device.
  *   - All calls share the one buffer, which keeps the last call's contents:
  *     each call clears the status word and overwrites every block sum it
  *     reads.  Calls whose kernels overlap on the GPU (different streams, or
  *     host threads without ordering between them) race on the buffer:
  *     order them on one stream.
- *   - Errors come back through the returned code and bpa_last_error(). */
+ *   - Argument errors are reported exactly as bpa_select_blocks reports
+ *     them, before the size limit is checked.  Errors come back through the
+ *     returned code and bpa_last_error(); the selection kernels write no
+ *     device-side status, so there is nothing for bpa_check to read here. */
 size_t bpa_select_noalloc_max_bytes(void);
 bpa_status bpa_select_blocks_noalloc(const void* q, const void* k, int32_t dtype, int32_t B,
                                      int32_t S, int32_t H, int32_t d,

@@ -215,6 +215,13 @@ static double bias_at(const ora_desc* D, int b, int h, int q, int k) {
     return D->bias[b * st[0] + h * st[1] + q * st[2] + k * st[3]];
 }
 
+/* Selection order: a larger score first.  A NaN score (only non-finite inputs give one;
+ * the pages do not say how to rank it) ranks below every number. */
+static int ranks_above(double a, double b) {
+    if (isnan(b)) return !isnan(a);
+    return a > b;
+}
+
 static double dot(const double* a, const double* b, int n) {
     double acc = 0.0;
     for (int c = 0; c < n; ++c) acc = acc + a[c] * b[c];
@@ -714,7 +721,7 @@ int ora_select(const void* q, const void* k, int32_t in_dtype, int32_t B, int32_
                         int best = -1;
                         for (int j = 0; j < i; ++j) {
                             if (pick[j]) continue;
-                            if (best < 0 || sc[j] > sc[best]) best = j;
+                            if (best < 0 || ranks_above(sc[j], sc[best])) best = j;
                         }
                         pick[best] = 1;
                     }

@@ -246,6 +246,25 @@ cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 }  // namespace
 
 namespace bpa {
+
+bpa_status check_select_args(const void* q, const void* k, int32_t dtype, int32_t B, int32_t S, int32_t H,
+                             int32_t d, const int64_t q_strides[3], const int64_t k_strides[3],
+                             int32_t block_size, int32_t top_n, const int32_t* block_idx_out) {
+    if (!q || !k || !q_strides || !k_strides || !block_idx_out)
+        return fail(BPA_ERR_INVALID_ARG, "q, k, strides or block_idx_out is NULL");
+    if (dtype != BPA_BF16 && dtype != BPA_FP32) return fail(BPA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (B < 1 || S < 1 || H < 1 || d < 1) return fail(BPA_ERR_INVALID_ARG, "B, S, H, d must be >= 1");
+    if (d > 512) return fail(BPA_ERR_UNSUPPORTED, "head dim %d > 512", d);
+    if (block_size < 1 || S % block_size)
+        return fail(BPA_ERR_INVALID_ARG, "block_size (%d) must divide S (%d)", block_size, S);
+    if (S / block_size > kSelectMaxBlocks)
+        return fail(BPA_ERR_UNSUPPORTED, "%d blocks per sequence, more than %d", S / block_size, kSelectMaxBlocks);
+    if (top_n < 1 || top_n > 64) return fail(BPA_ERR_INVALID_ARG, "top_n must be in [1, 64]");
+    for (int i = 0; i < 3; ++i)
+        if (q_strides[i] < 0 || k_strides[i] < 0) return fail(BPA_ERR_INVALID_ARG, "strides must be >= 0");
+    return BPA_OK;
+}
+
 // Lets other translation units of the library report an error through bpa_last_error.
 void set_last_error(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
 }  // namespace bpa
@@ -455,18 +474,11 @@ bpa_status bpa_select_blocks(const void* q, const void* k, int32_t dtype, int32_
                              int32_t d, const int64_t q_strides[3], const int64_t k_strides[3],
                              int32_t block_size, int32_t top_n, int32_t* block_idx_out, void* workspace,
                              size_t workspace_bytes, void* stream) {
-    if (!q || !k || !q_strides || !k_strides || !block_idx_out)
-        return fail(BPA_ERR_INVALID_ARG, "q, k, strides or block_idx_out is NULL");
-    if (dtype != BPA_BF16 && dtype != BPA_FP32) return fail(BPA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
-    if (B < 1 || S < 1 || H < 1 || d < 1) return fail(BPA_ERR_INVALID_ARG, "B, S, H, d must be >= 1");
-    if (d > 512) return fail(BPA_ERR_UNSUPPORTED, "head dim %d > 512", d);
-    if (block_size < 1 || S % block_size)
-        return fail(BPA_ERR_INVALID_ARG, "block_size (%d) must divide S (%d)", block_size, S);
-    if (top_n < 1 || top_n > 64) return fail(BPA_ERR_INVALID_ARG, "top_n must be in [1, 64]");
-    for (int i = 0; i < 3; ++i)
-        if (q_strides[i] < 0 || k_strides[i] < 0) return fail(BPA_ERR_INVALID_ARG, "strides must be >= 0");
+    bpa_status st = bpa::check_select_args(q, k, dtype, B, S, H, d, q_strides, k_strides, block_size, top_n,
+                                           block_idx_out);
+    if (st != BPA_OK) return st;
     const size_t need = bpa_select_workspace_size(B, S, H, d, block_size);
-    bpa_status st = check_ws(workspace, workspace_bytes, need);
+    st = check_ws(workspace, workspace_bytes, need);
     if (st != BPA_OK) return st;
     cudaStream_t s = as_stream(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -113,6 +113,14 @@ cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream
 
 void set_last_error(const char* msg);
 
+// Most blocks per sequence the selection takes (its per-warp score list lives in shared memory).
+constexpr int kSelectMaxBlocks = 4096;
+
+// The argument checks of bpa_select_blocks other than the workspace's (sets the last error).
+bpa_status check_select_args(const void* q, const void* k, int32_t dtype, int32_t B, int32_t S, int32_t H,
+                             int32_t d, const int64_t q_strides[3], const int64_t k_strides[3],
+                             int32_t block_size, int32_t top_n, const int32_t* block_idx_out);
+
 bool fwd_tc_supported(const Problem& P);
 bool bwd_tc_supported(const Problem& P);
 bool gather_supported(const Problem& P);

@@ -25,7 +25,10 @@ constexpr size_t kScratchBytes = static_cast<size_t>(16) << 20;
 
 static __device__ __align__(256) unsigned char g_select_scratch[kScratchBytes];
 
-// Device address of g_select_scratch, looked up once per device.
+// Device address of g_select_scratch, looked up once per device and kept for
+// the life of the process: it does not survive cudaDeviceReset (or any other
+// teardown of the device's primary context), after which this entry point must
+// not be called again in the same process.
 std::mutex g_mu;
 void* g_addr[64] = {};
 
@@ -57,12 +60,11 @@ bpa_status bpa_select_blocks_noalloc(const void* q, const void* k, int32_t dtype
                                      int32_t H, int32_t d, const int64_t q_strides[3],
                                      const int64_t k_strides[3], int32_t block_size, int32_t top_n,
                                      int32_t* block_idx_out, void* stream) {
+    // the argument errors first, the same as bpa_select_blocks reports them
+    const bpa_status st = bpa::check_select_args(q, k, dtype, B, S, H, d, q_strides, k_strides, block_size,
+                                                 top_n, block_idx_out);
+    if (st != BPA_OK) return st;
     const size_t need = bpa_select_workspace_size(B, S, H, d, block_size);
-    if (need == 0) {
-        // invalid sizes: let the regular entry point report exactly what is wrong
-        return bpa_select_blocks(q, k, dtype, B, S, H, d, q_strides, k_strides, block_size, top_n,
-                                 block_idx_out, nullptr, 0, stream);
-    }
     if (need > kScratchBytes) {
         char msg[256];
         snprintf(msg, sizeof msg,

@@ -42,15 +42,20 @@ __global__ void k_block_sums(const SelectArgs a) {
     }
 }
 
+// Ranking: a larger score first, the lower block on equal scores; a NaN score
+// (non-finite inputs) ranks below every number, NaNs in block order.
 __device__ __forceinline__ bool better(double sa, int ja, double sb, int jb) {
+    const bool na = sa != sa, nb = sb != sb;
+    if (na != nb) return nb;
+    if (na) return ja < jb;
     return sa > sb || (sa == sb && ja < jb);
 }
 
 constexpr int kSelWarps = 4;
 
 // one warp per (b, h, query block i); the scores of the i earlier blocks live
-// in shared memory (kSelWarps * nblk doubles).  Scores of finite inputs are
-// finite, so a taken entry is marked with NaN.
+// in shared memory (kSelWarps * nblk doubles), followed by one "taken" byte
+// per block and warp.
 __global__ void __launch_bounds__(kSelWarps * 32) k_select(const SelectArgs a) {
     extern __shared__ double sc_all[];
     const int nblk = a.S / a.block;
@@ -60,12 +65,15 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_select(const SelectArgs a) {
     const int i = static_cast<int>(unit % nblk);
     const int64_t bh = unit / nblk;
     double* sc = sc_all + static_cast<int64_t>(warp) * nblk;
+    unsigned char* taken = reinterpret_cast<unsigned char*>(sc_all + static_cast<int64_t>(kSelWarps) * nblk) +
+                           static_cast<int64_t>(warp) * nblk;
     const double* qs = a.qsum + (bh * nblk + i) * a.d;
     for (int j = lane; j < i; j += 32) {
         const double* ks = a.ksum + (bh * nblk + j) * a.d;
         double acc = 0.0;
         for (int c = 0; c < a.d; ++c) acc = __dadd_rn(acc, __dmul_rn(qs[c], ks[c]));
         sc[j] = acc;
+        taken[j] = 0;
     }
     __syncwarp();
     const int take = i < a.top_n ? i : a.top_n;
@@ -74,8 +82,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_select(const SelectArgs a) {
         double bs = 0.0;
         int bj = -1;
         for (int j = lane; j < i; j += 32) {
+            if (taken[j]) continue;
             const double s = sc[j];
-            if (s != s) continue;   // taken
             if (bj < 0 || better(s, j, bs, bj)) {
                 bs = s;
                 bj = j;
@@ -93,7 +101,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_select(const SelectArgs a) {
         if (t < 32 && lane == t) pick0 = bj;
         if (t >= 32 && lane == t - 32) pick1 = bj;
         __syncwarp();
-        if (lane == 0) sc[bj] = __longlong_as_double(0x7ff8000000000000ll);
+        // t < take <= i leaves an untaken candidate, so bj >= 0 here
+        if (lane == 0 && bj >= 0) taken[bj] = 1;
         __syncwarp();
     }
     int picks[64];
@@ -131,7 +140,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t units = static_cast<int64_t>(a.B) * a.H * nblk;
-    const size_t smem = sizeof(double) * kSelWarps * static_cast<size_t>(nblk);
+    const size_t smem = (sizeof(double) + 1) * kSelWarps * static_cast<size_t>(nblk);
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;

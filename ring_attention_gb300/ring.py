@@ -31,26 +31,29 @@ class RingTimeout(RuntimeError):
 def exchange(tensors: Sequence[torch.Tensor], *, group=None,
              timeout: datetime.timedelta = datetime.timedelta(seconds=30)) -> list:
     """One hop: send every tensor to rank i + 1, receive the same shapes from rank i - 1.
-    Message t of a hop carries tag t, so the tensors cannot be confused."""
+    Message t of a hop carries tag t, so the tensors cannot be confused.
+
+    The hop's sends and receives are posted together as one batch
+    (``batch_isend_irecv``): with NCCL that is one group of point-to-point operations, so
+    no rank's send waits behind a receive its peer queued after its own send (two ranks,
+    where the next and the previous rank are the same peer, would otherwise deadlock).
+    A timeout only ends the host's wait; with NCCL the queued transfer may still be pending
+    on the device, so a rank that sees RingTimeout must not launch further work on that
+    process group."""
     n = dist.get_world_size(group)
     i = dist.get_rank(group)
     dst, src = (i + 1) % n, (i - 1) % n
     if n == 1:
         return list(tensors)
     out = [torch.empty_like(t) for t in tensors]
-    sends = [dist.isend(t.contiguous(), dst, group=group, tag=tag) for tag, t in enumerate(tensors)]
-    recvs = [dist.irecv(r, src, group=group, tag=tag) for tag, r in enumerate(out)]
-    for w in recvs:
+    ops = [dist.P2POp(dist.isend, t.contiguous(), dst, group=group, tag=tag) for tag, t in enumerate(tensors)]
+    ops += [dist.P2POp(dist.irecv, r, src, group=group, tag=tag) for tag, r in enumerate(out)]
+    for w in dist.batch_isend_irecv(ops):
         try:
             w.wait(timeout)
         except RuntimeError as e:
-            raise RingTimeout(f"rank {i}: no block from rank {src} within {timeout.total_seconds():g} s") from e
-    for w in sends:
-        try:
-            w.wait(timeout)
-        except RuntimeError as e:
-            raise RingTimeout(f"rank {i}: rank {dst} did not take its block within "
-                              f"{timeout.total_seconds():g} s") from e
+            raise RingTimeout(f"rank {i}: the hop (block to rank {dst}, block from rank {src}) did not "
+                              f"complete within {timeout.total_seconds():g} s") from e
     return out
 
 

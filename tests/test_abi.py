@@ -137,6 +137,23 @@ def test_select_rejects_bad_arguments(bpa):
     assert L.bpa_select_blocks(p, p, 0, 4, 8192, 8, 64, st, st, 32, 0, p, p, 1 << 30, None) == 1
     assert L.bpa_select_blocks(p, p, 0, 4, 8192, 8, 64, st, st, 32, 8, p, p, 16, None) == 3
     assert L.bpa_select_workspace_size(4, 8192, 8, 64, 32) == 256 + 2 * 4 * 8 * 256 * 64 * 8
+    # more blocks per sequence than the selection kernel holds
+    assert L.bpa_select_blocks(p, p, 0, 1, 4097 * 8, 1, 8, st, st, 8, 4, p, p, 1 << 40, None) == 2
+
+
+def test_select_noalloc_reports_argument_errors_first(bpa):
+    # a problem beyond the built-in scratch with a bad argument reports the argument,
+    # exactly like the workspace entry point, not the scratch limit
+    L = bpa.lib()
+    st = (ctypes.c_int64 * 3)(65536 * 8 * 512, 8 * 512, 512)
+    p = 0x80000
+    big = (4, 65536, 8, 512, 32)      # far more than 16 MiB of block sums
+    assert L.bpa_select_workspace_size(*big) > L.bpa_select_noalloc_max_bytes()
+    assert L.bpa_select_blocks_noalloc(p, p, 0, *big[:4], st, st, 32, 100, p, None) == bpa.BPA_ERR_INVALID_ARG
+    assert b"top_n" in L.bpa_last_error()
+    assert L.bpa_select_blocks_noalloc(p, p, 0, *big[:4], st, st, 32, 8, 0, None) == bpa.BPA_ERR_INVALID_ARG
+    assert L.bpa_select_blocks_noalloc(p, p, 0, *big[:4], st, st, 32, 8, p, None) == bpa.BPA_ERR_UNSUPPORTED
+    assert b"scratch" in L.bpa_last_error()
 
 
 def test_status_strings(bpa):

@@ -107,6 +107,52 @@ def test_backward_bf16(bpa, ora, shape, mask):
     assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
 
 
+def _general_bias(kind, B, Hq, S, seed):
+    # bpt.py's bias takes each dim as 1 (broadcast) or full: a bias that depends on the
+    # query position ([B, Hq, S, S] or a per-row [B, 1, S, 1]) reaches the backward
+    # kernels' query-dependent branch
+    rng = np.random.default_rng(seed)
+    shape = {"full": (B, Hq, S, S), "rows": (B, 1, S, 1)}[kind]
+    return rng.standard_normal(shape).astype(np.float32)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("mask", [MASKS[0], MASKS[3]], ids=_mask_id)
+@pytest.mark.parametrize("bias_kind", ["full", "rows"])
+def test_backward_general_bias_bf16(bpa, ora, d, mask, bias_kind):
+    B, S, Hq, Hkv = 2, 300, 4, 2
+    q, k, v, do = _inputs((B, S, Hq, Hkv, d), 51 + d)
+    bias = _general_bias(bias_kind, B, Hq, S, 52)
+    tq, tk, tv, tdo, tb = dev(q), dev(k), dev(v), dev(do), dev(bias)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, bias=tb, **mask)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, bias=tb, **mask)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, bias=bias, **mask)
+    assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+    check_stats(m, l, rm, rl)
+    assert rel_l2(host(dq), rq) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dk), rk) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
+
+
+@pytest.mark.parametrize("mask", [MASKS[0], MASKS[3]], ids=_mask_id)
+@pytest.mark.parametrize("bias_kind", ["full", "rows"])
+def test_backward_general_bias_fp32(bpa, ora, mask, bias_kind):
+    B, S, Hq, Hkv, d = 2, 300, 4, 2, 64
+    q, k, v, do = _inputs((B, S, Hq, Hkv, d), 53, dtype="f32")
+    bias = _general_bias(bias_kind, B, Hq, S, 54)
+    tq, tk, tv, tdo, tb = dev(q), dev(k), dev(v), dev(do), dev(bias)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, bias=tb, **mask)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, bias=tb, **mask)
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, bias=bias, **mask)
+    assert max_abs(host(o), ro) <= FP32_MAX_ABS
+    assert max_abs(host(dq), rq) <= FP32_MAX_ABS
+    assert max_abs(host(dk), rk) <= FP32_MAX_ABS
+    assert max_abs(host(dv), rv) <= FP32_MAX_ABS
+    check_stats(m, l, rm, rl)
+
+
 @pytest.mark.parametrize("mask", [MASKS[0], MASKS[3], MASKS[4]], ids=_mask_id)
 def test_fp32_forward_backward(bpa, ora, mask):
     shape = (2, 150, 4, 2, 64)
@@ -174,6 +220,19 @@ def test_ring_backward(bpa, ora, ring):
 def test_select_blocks_bit_exact(bpa, ora, dims):
     B, S, H, d, bs, n = dims
     q, k = draw([(B, S, H, d), (B, S, H, d)], 51 + S, "bf16")
+    idx = bpa.bpa_select_blocks(dev(q), dev(k), block_size=bs, top_n=n)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), ora.select_blocks(q, k, block_size=bs, top_n=n))
+
+
+def test_select_blocks_nan_scores(bpa, ora):
+    # a NaN in a key block (every score against it NaN) and one in a query block (all its
+    # scores NaN): NaN ranks below every number, and no kernel access leaves its buffers
+    B, S, H, d, bs, n = 1, 512, 2, 16, 16, 4
+    q, k = draw([(B, S, H, d), (B, S, H, d)], 57, "f32")
+    k[0, 3 * bs + 2, 0, 5] = np.nan
+    q[0, 9 * bs, 1, 1] = np.nan
+    q[0, 0, 0, 0] = np.nan       # block 0 of warp 0 (no candidates: all -1)
     idx = bpa.bpa_select_blocks(dev(q), dev(k), block_size=bs, top_n=n)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(idx.cpu().numpy(), ora.select_blocks(q, k, block_size=bs, top_n=n))

@@ -38,6 +38,8 @@ MUTANTS = [
     ("philox_round_constant", "(uint64_t)0xD2511F53u * c[0]", "(uint64_t)0xD2511F55u * c[0]"),
     ("philox_weyl_increment", "k1 += 0xBB67AE85u;", "k1 += 0xBB67AE87u;"),
     ("philox_hi_lo_swapped", "const uint32_t n1 = (uint32_t)pb;", "const uint32_t n1 = (uint32_t)(pb >> 32) ^ 1u;"),
+    ("select_nan_order_of_visit", "if (best < 0 || ranks_above(sc[j], sc[best])) best = j;",
+     "if (best < 0 || sc[j] > sc[best]) best = j;"),
     ("philox_nine_rounds", "for (int r = 0; r < 10; ++r) {", "for (int r = 0; r < 9; ++r) {"),
     ("dk_transposed_operand", "dkr[c] = dkr[c] + D->scale * dS * qrow[c];",
      "dkr[c] = dkr[c] + D->scale * dS * kr[c];", 1),
@@ -49,8 +51,7 @@ MUTANTS = [
     # the visiting order of the ring changes rounding only, so the planted
     # slip is a ring that revisits its own KV block instead of rotating
     ("ring_does_not_rotate", "int j = ((i - idx) % n + n) % n;", "int j = i;"),
-    ("select_ties_upper", "if (best < 0 || sc[j] > sc[best]) best = j;",
-     "if (best < 0 || sc[j] >= sc[best]) best = j;"),
+    ("select_ties_upper", "    return a > b;\n}", "    return a >= b;\n}"),
     ("local_window_wide", "(k >= q - (D->local_window - 1))", "(k >= q - D->local_window)"),
     ("union_drops_selected", "if (sel[t] >= 0 && k / D->sel_block == sel[t]) in_sel = 1;",
      "if (sel[t] >= 0 && k / D->sel_block == sel[t] + 1) in_sel = 1;"),
@@ -74,6 +75,7 @@ def battery(ora):
     yield lambda: pins.test_select_planted_ranking(ora)
     yield lambda: pins.test_select_ties_keep_lower_block(ora)
     yield lambda: pins.test_select_fewer_candidates_than_top_n(ora)
+    yield lambda: pins.test_select_nan_scores_rank_last(ora)
     yield lambda: pins.test_block_selected_attention_matches_brute_force(ora)
     for case in pins.VARLEN_CASES:
         yield lambda case=case: pins.test_varlen_matches_rebuilt_problems(ora, case, dict(causal=True, window=(3, 0)))

@@ -711,8 +711,9 @@ def brute_select(q, k, block_size, top_n):
                     s = 0.0
                     for c in range(d):
                         s += qs[i][c] * ks[j][c]
-                    scored.append((-s, j))
-                best = sorted(j for _, j in sorted(scored)[:top_n])
+                    # a NaN score ranks below every number, NaNs in block order
+                    scored.append((1, 0.0, j) if s != s else (0, -s, j))
+                best = sorted(e[-1] for e in sorted(scored)[:top_n])
                 out[b, h, i, :len(best)] = best
     return out
 
@@ -768,6 +769,19 @@ def test_select_fewer_candidates_than_top_n(ora):
     got = ora.select_blocks(q, k, block_size=4, top_n=8)[0, 0]
     for i in range(6):
         assert list(got[i]) == list(range(i)) + [-1] * (8 - i)
+
+
+def test_select_nan_scores_rank_last(ora):
+    # a NaN in one key block makes every score against that block NaN, a NaN in one query
+    # block every score of that block: those rank below every number, in block order
+    B, S, H, d, bs, n = 1, 48, 2, 4, 4, 3
+    q, k = rnd((B, S, H, d), 133), rnd((B, S, H, d), 134)
+    k[0, 2 * bs + 1, 0, 2] = np.nan     # key block 2 of head 0
+    q[0, 7 * bs, 1, 0] = np.nan         # query block 7 of head 1
+    got = ora.select_blocks(q, k, block_size=bs, top_n=n)
+    np.testing.assert_array_equal(got, brute_select(q, k, bs, n))
+    assert 2 not in got[0, 0, 3 + n:].ravel()     # blocks with n finite candidates skip it
+    assert list(got[0, 1, 7]) == [0, 1, 2]        # all NaN: the lowest blocks
 
 
 def test_block_selected_attention_matches_brute_force(ora):
