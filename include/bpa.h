@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define BPA_VERSION 5
+#define BPA_VERSION 6
 
 typedef enum {
     BPA_OK = 0,
@@ -143,6 +143,22 @@ typedef struct bpa_attn_desc {
      * workspace then holds one dQ slice per 128-key tile (bpa_workspace_size grows by about
      * that factor).  Needs ring_size 1. */
     int32_t deterministic;
+    /* Fields below were added in descriptor version 6 (bpa_version() >= 6); a version-5
+     * caller (struct_size = offsetof(bpa_attn_desc, dropout_threshold)) gets no dropout.
+     * Attention dropout as "bpt.py" applies it (_blockwise_attention_fwd / _bwd with
+     * attn_pdrop, _chunk_attention_bias): each score entry (b, h, q, k) is dropped with
+     * probability p, and a dropped entry leaves the softmax (the dtype minimum is added to
+     * its score), so the row renormalises over the kept keys; no 1/(1-p) factor.  m and l
+     * cover the kept keys only.  The decision is an integer comparison, identical on every
+     * path and in both passes: the 32-bit draw of entry (b, h, q, k) is word k % 4 of
+     * Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC 2011) with key (seed low 32 bits, seed
+     * high 32 bits) and counter (k / 4, q, h, b), at the entry's positions in the padded
+     * [B, S, ...] tensors, and the entry is dropped when the draw is below
+     * dropout_threshold = round(p * 2^32) (capped at 2^32 - 1).  bpa_bwd must be given the
+     * threshold and seed of the forward call. */
+    uint32_t dropout_threshold;   /* 0: no dropout */
+    uint32_t dropout_reserved;    /* must be 0 */
+    uint64_t dropout_seed;
 } bpa_attn_desc;
 
 /* Bytes of workspace bpa_fwd (op = BPA_OP_FWD) or bpa_bwd (op = BPA_OP_BWD)

@@ -48,6 +48,8 @@ class bpa_attn_desc(ctypes.Structure):
         ("bottom_right", ctypes.c_int32),
         ("sink", ctypes.c_void_p), ("dsink", ctypes.c_void_p),
         ("deterministic", ctypes.c_int32),
+        ("dropout_threshold", ctypes.c_uint32), ("dropout_reserved", ctypes.c_uint32),
+        ("dropout_seed", ctypes.c_uint64),
     ]
 
 
@@ -122,7 +124,7 @@ def _stream_ptr(stream) -> int:
 def make_desc(q, k, v, *, o=None, causal=False, window=(-1, -1), scale=None, bias=None, query_chunk=0,
               key_chunk=0, ring_size=1, ring_steps=None, block_idx=None, sel_block=0, top_n=0,
               local_window=0, seqlens_q=None, seqlens_kv=None, bottom_right=False, sink=None,
-              dsink=None, deterministic=False) -> bpa_attn_desc:
+              dsink=None, deterministic=False, dropout_p=0.0, dropout_seed=0) -> bpa_attn_desc:
     """Fill a bpa_attn_desc from torch tensors (no data is touched).  The value head dim
     is v's last dim; o (the output, or dout, which shares its strides) sets o_strides."""
     B, S, Hq, d = q.shape
@@ -170,7 +172,18 @@ def make_desc(q, k, v, *, o=None, causal=False, window=(-1, -1), scale=None, bia
                 raise ValueError(f"{name} must be a contiguous float32 [Hq] tensor on q's device")
             setattr(D, name, t.data_ptr())
     D.deterministic = int(bool(deterministic))
+    D.dropout_threshold = dropout_threshold(dropout_p)
+    D.dropout_seed = int(dropout_seed) & (2 ** 64 - 1)
     return D
+
+
+def dropout_threshold(p: float) -> int:
+    """The descriptor's dropout threshold for drop probability p: round(p * 2^32), at most
+    2^32 - 1 (entries whose 32-bit draw is below it are dropped)."""
+    p = float(p)
+    if not 0.0 <= p < 1.0:
+        raise ValueError("dropout_p must be in [0, 1)")
+    return min(int(round(p * 4294967296.0)), 4294967295)
 
 
 def bpa_workspace_size(op: int, desc: bpa_attn_desc) -> int:

@@ -62,14 +62,16 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     const size_t v2_size = offsetof(bpa_attn_desc, seqlens_q);   // version 2: no sequence lengths
     const size_t v3_size = offsetof(bpa_attn_desc, sink);        // version 3: no sink
     const size_t v4_size = offsetof(bpa_attn_desc, deterministic);   // version 4: no determinism knob
+    const size_t v5_size = offsetof(bpa_attn_desc, dropout_threshold);   // version 5: no dropout
     if (d->struct_size != sizeof(bpa_attn_desc) && d->struct_size != v1_size && d->struct_size != v2_size &&
-        d->struct_size != v3_size && d->struct_size != v4_size)
-        return fail(BPA_ERR_INVALID_ARG, "desc->struct_size is %u, expected %zu (or %zu, %zu, %zu, %zu)",
-                    d->struct_size, sizeof(bpa_attn_desc), v4_size, v3_size, v2_size, v1_size);
+        d->struct_size != v3_size && d->struct_size != v4_size && d->struct_size != v5_size)
+        return fail(BPA_ERR_INVALID_ARG, "desc->struct_size is %u, expected %zu (or %zu, %zu, %zu, %zu, %zu)",
+                    d->struct_size, sizeof(bpa_attn_desc), v5_size, v4_size, v3_size, v2_size, v1_size);
     const bool v2 = d->struct_size >= v2_size;
     const bool v3 = d->struct_size >= v3_size;
     const bool v4 = d->struct_size >= v4_size;
-    const bool v5 = d->struct_size == sizeof(bpa_attn_desc);
+    const bool v5 = d->struct_size >= v5_size;
+    const bool v6 = d->struct_size == sizeof(bpa_attn_desc);
     const bool varlen = v3 && (d->seqlens_q || d->seqlens_kv);
     if (d->dtype != BPA_BF16 && d->dtype != BPA_FP32)
         return fail(BPA_ERR_INVALID_ARG, "unknown dtype %d", d->dtype);
@@ -110,6 +112,7 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     if (v4 && d->sink && n != 1) return fail(BPA_ERR_INVALID_ARG, "sink attention needs ring_size 1");
     if (v4 && d->dsink && !d->sink) return fail(BPA_ERR_INVALID_ARG, "dsink needs a sink");
     if (v5 && d->deterministic && n != 1) return fail(BPA_ERR_INVALID_ARG, "deterministic mode needs ring_size 1");
+    if (v6 && d->dropout_reserved) return fail(BPA_ERR_INVALID_ARG, "dropout_reserved must be 0");
     P.B = d->B;
     P.S = d->S;
     P.Hq = d->Hq;
@@ -142,6 +145,9 @@ bpa_status make_problem(const bpa_attn_desc* d, Problem& P, bool need_qkv) {
     P.sink = v4 ? d->sink : nullptr;
     P.dsink = v4 ? d->dsink : nullptr;
     P.det = v5 && d->deterministic ? 1 : 0;
+    P.drop_thr = v6 ? d->dropout_threshold : 0u;
+    P.drop_k0 = v6 ? static_cast<uint32_t>(d->dropout_seed) : 0u;
+    P.drop_k1 = v6 ? static_cast<uint32_t>(d->dropout_seed >> 32) : 0u;
     P.sel_block = d->block_idx ? d->sel_block : 0;
     P.top_n = d->block_idx ? d->top_n : 0;
     P.local_window = d->block_idx ? d->local_window : 0;

@@ -32,6 +32,8 @@ struct Problem {
     const float* sink;         // device [Hq] sink logits (natural log units) or nullptr
     float* dsink;              // device [Hq] sink gradient (backward output) or nullptr
     int det;                   // deterministic backward (no atomic adds anywhere)
+    uint32_t drop_thr;         // attention dropout: entries whose draw is below this are dropped (0: none)
+    uint32_t drop_k0, drop_k1; // Philox4x32-10 key: the 64-bit seed's low and high words
 };
 
 // Valid query / key counts of one batch entry and the offset of the causal / window

@@ -134,7 +134,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32
     mbar_wait(bar, parity, &never, status, 0xD1);
 }
 
-template <int DV, bool DET>
+// DET: deterministic dQ slices; DROP: attention dropout.  Each is a separate instantiation,
+// so that the default kernel's code stays as it is without the knobs.
+template <int DV, bool DET, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -391,6 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (q < qmin || q > qmax) p[c] = 0.f;
                 }
             }
+            if constexpr (DROP) {   // dropped entries leave the softmax: P = 0, hence dS = 0
+                const uint32_t keep = dropout_keep_q32(P.drop_thr, P.drop_k0, P.drop_k1, W.b, h, q0, k, lane);
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    if (!((keep >> c) & 1u)) p[c] = 0.f;
+            }
             // the dS^T buffer is free once the dQ product of the previous tile has read it
             if (it > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(B_PF), (it - 1) & 1, abort_flag, a.status, 0x61))) {
                 aborted = true;
@@ -503,25 +511,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int DV>
 cudaError_t launch_dv(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
     using L = BwdCfg<DV>;
-    // the deterministic variant is a separate instantiation: the default kernel's code is
-    // left exactly as it is without the knob
-    static bool configured[2][64] = {};
-    const int det = a.P.det ? 1 : 0;
+    // the deterministic and dropout variants are separate instantiations: the default
+    // kernel's code is left exactly as it is without the knobs
+    static bool configured[4][64] = {};
+    const int var = (a.P.det ? 1 : 0) | (a.P.drop_thr ? 2 : 0);
+    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, BwdArgs) =
+        var == 0 ? k_bwd_tc<DV, false, false>
+                 : (var == 1 ? k_bwd_tc<DV, true, false> : (var == 2 ? k_bwd_tc<DV, false, true> : k_bwd_tc<DV, true, true>));
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !configured[det][dev]) {
-        e = det ? cudaFuncSetAttribute(k_bwd_tc<DV, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM)
-                : cudaFuncSetAttribute(k_bwd_tc<DV, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+    if (dev < 0 || dev >= 64 || !configured[var][dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[det][dev] = true;
+        if (dev >= 0 && dev < 64) configured[var][dev] = true;
     }
     const int nkt = (a.P.S + BK - 1) / BK;
     const int grid = nkt * a.P.Hkv * a.P.B;
-    if (det)
-        k_bwd_tc<DV, true><<<grid, kThreads, L::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
-    else
-        k_bwd_tc<DV, false><<<grid, kThreads, L::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
+    kern<<<grid, kThreads, L::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
     return cudaGetLastError();
 }
 

@@ -415,4 +415,78 @@ BPA_DEV float fmax3(float a, float b, float c) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// ---- attention dropout's generator --------------------------------------------
+// Philox4x32-10 as defined by Salmon, Moraes, Dror and Shaw ("Parallel random numbers: as
+// easy as 1, 2, 3", SC 2011): ten rounds, each multiplying counter words 0 and 2 by the
+// round multipliers 0xD2511F53 and 0xCD9E8D57 and mixing the high halves of the 64-bit
+// products with the other two words and the round key; the key (k0, k1) advances by the
+// Weyl constants 0x9E3779B9 and 0xBB67AE85 between rounds.
+BPA_DEV uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = static_cast<uint64_t>(c.x) * 0xD2511F53u;
+        const uint64_t p1 = static_cast<uint64_t>(c.z) * 0xCD9E8D57u;
+        c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
+                       static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// The draws of score entries (b, h, q, 4 kg .. 4 kg + 3): one generator call with counter
+// (kg, q, h, b) keyed by the dropout seed; word i belongs to key 4 kg + i.
+BPA_DEV uint4 dropout_draws(uint32_t k0, uint32_t k1, int b, int h, int q, int kg) {
+    return philox4x32_10(make_uint4(static_cast<uint32_t>(kg), static_cast<uint32_t>(q), static_cast<uint32_t>(h),
+                                    static_cast<uint32_t>(b)),
+                         k0, k1);
+}
+
+// Whether score entry (b, h, q, k) is kept (its draw is not below the threshold).
+BPA_DEV bool dropout_keep(uint32_t thr, uint32_t k0, uint32_t k1, int b, int h, int q, int k) {
+    const uint4 w = dropout_draws(k0, k1, b, h, q, k >> 2);
+    const int i = k & 3;
+    const uint32_t x = i == 0 ? w.x : (i == 1 ? w.y : (i == 2 ? w.z : w.w));
+    return x >= thr;
+}
+
+// Keep bits of 32 consecutive keys k0 .. k0 + 31 (k0 a multiple of 4) for one row: bit j
+// is key k0 + j.  Out of line: a tile's softmax calls it a few times per row.
+static __device__ __noinline__ uint32_t dropout_keep32(uint32_t thr, uint32_t s0, uint32_t s1, int b, int h, int q, int k0) {
+    uint32_t bits = 0;
+#pragma unroll 2
+    for (int g = 0; g < 8; ++g) {
+        const uint4 x = dropout_draws(s0, s1, b, h, q, (k0 >> 2) + g);
+        bits |= ((x.x >= thr ? 1u : 0u) | (x.y >= thr ? 2u : 0u) | (x.z >= thr ? 4u : 0u) | (x.w >= thr ? 8u : 0u))
+                << (4 * g);
+    }
+    return bits;
+}
+
+// Keep bits of one key k for 32 consecutive queries q0 .. q0 + 31 (bit c: query q0 + c),
+// for a warp whose lanes hold consecutive keys (k % 4 == lane % 4).  The four keys of a
+// generator call sit in the four lanes of a quad: lane r computes the draws of queries
+// q0 + 4i + r and the quad exchanges words, so each call serves four entries.
+// Every lane of the warp must call it.
+static __device__ __noinline__ uint32_t dropout_keep_q32(uint32_t thr, uint32_t s0, uint32_t s1, int b, int h, int q0,
+                                                  int k, int lane) {
+    const int r = lane & 3, base = lane & ~3;
+    uint32_t bits = 0;
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+        const uint4 w = dropout_draws(s0, s1, b, h, q0 + 4 * i + r, k >> 2);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            // lane r reads from quad lane (r + t) % 4 the word of its own key r, which that
+            // lane (s) sends as its word (s - t) % 4
+            const int widx = (r - t) & 3;
+            const uint32_t send = widx == 0 ? w.x : (widx == 1 ? w.y : (widx == 2 ? w.z : w.w));
+            const int src = (r + t) & 3;
+            const uint32_t got = __shfl_sync(0xffffffffu, send, base | src);
+            bits |= (got >= thr ? 1u : 0u) << (4 * i + src);
+        }
+    }
+    return bits;
+}
+
 }  // namespace bpa

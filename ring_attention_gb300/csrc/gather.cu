@@ -143,7 +143,8 @@ __device__ int visit_list(const Problem& P, int64_t unit, int i, int* list) {
     return n;
 }
 
-template <int NW>
+// DROP: the attention-dropout instantiation (dropped entries leave the softmax)
+template <int NW, bool DROP>
 __global__ void __launch_bounds__(Geom<NW>::QB_F * NW * 32) k_gather_fwd(const FwdArgs a) {
     using G = Geom<NW>;
     const Problem& P = a.P;
@@ -260,18 +261,25 @@ __global__ void __launch_bounds__(Geom<NW>::QB_F * NW * 32) k_gather_fwd(const F
                 const int q = BS * i + mt * 16 + g + hh * 8;
                 float mx = -INFINITY;
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
+                for (int nt = 0; nt < 4; ++nt) {
+                    uint32_t dw[2] = {0u, 0u};   // draws of keys (e = 0, 1), dropout only
+                    if constexpr (DROP) {
+                        const uint4 w = dropout_draws(P.drop_k0, P.drop_k1, b, h, q, (BS * kb + nt * 8 + 2 * t) >> 2);
+                        dw[0] = (t & 1) ? w.z : w.x;
+                        dw[1] = (t & 1) ? w.w : w.y;
+                    }
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int k = BS * kb + nt * 8 + 2 * t + e;
                         const bool ok = k <= q && (selected || k > q - P.local_window) &&
                                         (!P.causal || k <= q) && (P.wl < 0 || k >= q - P.wl) &&
-                                        (P.wr < 0 || k <= q + P.wr);
+                                        (P.wr < 0 || k <= q + P.wr) && (!DROP || dw[e] >= P.drop_thr);
                         float v = s[mt][nt][hh * 2 + e] * sl2;
                         v = ok ? v : -INFINITY;
                         s[mt][nt][hh * 2 + e] = v;
                         mx = fmaxf(mx, v);
                     }
+                }
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
                 const float mnew = fmaxf(mrow[mt][hh], mx);
@@ -483,7 +491,7 @@ __device__ __forceinline__ void reduce_rows(float* acc_row0, int64_t row_stride,
         }
 }
 
-template <int NW>
+template <int NW, bool DROP>
 __global__ void __launch_bounds__(Geom<NW>::QB_B * NW * 32) k_gather_bwd(const BwdArgs a) {
     using G = Geom<NW>;
     const Problem& P = a.P;
@@ -565,17 +573,24 @@ __global__ void __launch_bounds__(Geom<NW>::QB_B * NW * 32) k_gather_bwd(const B
             for (int hh = 0; hh < 2; ++hh) {
                 const int q = BS * i + mt * 16 + g + hh * 8;
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt)
+                for (int nt = 0; nt < 4; ++nt) {
+                    uint32_t dw[2] = {0u, 0u};   // draws of keys (e = 0, 1), dropout only
+                    if constexpr (DROP) {
+                        const uint4 w = dropout_draws(P.drop_k0, P.drop_k1, b, h, q, (BS * kb + nt * 8 + 2 * t) >> 2);
+                        dw[0] = (t & 1) ? w.z : w.x;
+                        dw[1] = (t & 1) ? w.w : w.y;
+                    }
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int k = BS * kb + nt * 8 + 2 * t + e;
                         const bool ok = k <= q && (selected || k > q - P.local_window) &&
                                         (!P.causal || k <= q) && (P.wl < 0 || k >= q - P.wl) &&
-                                        (P.wr < 0 || k <= q + P.wr);
+                                        (P.wr < 0 || k <= q + P.wr) && (!DROP || dw[e] >= P.drop_thr);
                         const float p = ok ? ex2(s[mt][nt][hh * 2 + e] * sl2 - lse2[mt][hh]) : 0.f;
                         s[mt][nt][hh * 2 + e] = p;
                         dp[mt][nt][hh * 2 + e] = p * (dp[mt][nt][hh * 2 + e] - Drow[mt][hh]);
                     }
+                }
             }
         store_tile32(sp, s, lane);
         store_tile32(sds, dp, lane);
@@ -646,10 +661,10 @@ cudaError_t gather_fwd_nw(const FwdArgs& a, cudaStream_t s) {
     using G = Geom<NW>;
     const int64_t units = static_cast<int64_t>(a.P.B) * a.P.Hq * (a.P.S / BS);
     const size_t smem = sizeof(WarpSmem) * G::QB_F * NW + sizeof(float) * G::XCH * G::QB_F;
-    cudaError_t e = cudaFuncSetAttribute(k_gather_fwd<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    void (*kern)(const FwdArgs) = a.P.drop_thr ? k_gather_fwd<NW, true> : k_gather_fwd<NW, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    k_gather_fwd<NW><<<static_cast<unsigned>((units + G::QB_F - 1) / G::QB_F), G::QB_F * NW * 32, smem, s>>>(a);
+    kern<<<static_cast<unsigned>((units + G::QB_F - 1) / G::QB_F), G::QB_F * NW * 32, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -658,10 +673,10 @@ cudaError_t gather_bwd_nw(const BwdArgs& a, cudaStream_t s) {
     using G = Geom<NW>;
     const int64_t units = static_cast<int64_t>(a.P.B) * a.P.Hq * (a.P.S / BS);
     const size_t smem = sizeof(WarpSmemB) * G::QB_B * NW + sizeof(float) * 2 * G::XCH * G::QB_B;
-    cudaError_t e = cudaFuncSetAttribute(k_gather_bwd<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    void (*kern)(const BwdArgs) = a.P.drop_thr ? k_gather_bwd<NW, true> : k_gather_bwd<NW, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    k_gather_bwd<NW><<<static_cast<unsigned>((units + G::QB_B - 1) / G::QB_B), G::QB_B * NW * 32, smem, s>>>(a);
+    kern<<<static_cast<unsigned>((units + G::QB_B - 1) / G::QB_B), G::QB_B * NW * 32, smem, s>>>(a);
     return cudaGetLastError();
 }
 

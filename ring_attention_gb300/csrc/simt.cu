@@ -82,6 +82,8 @@ __device__ __forceinline__ bool allowed(const Problem& P, int b, int h, int q, i
         bool local = k <= q && k > q - P.local_window;
         if (!local && !selected(P, b, h, q, k / P.sel_block)) return false;
     }
+    // attention dropout: a dropped entry leaves the softmax like a masked one
+    if (P.drop_thr && !dropout_keep(P.drop_thr, P.drop_k0, P.drop_k1, b, h, q, k)) return false;
     return true;
 }
 

@@ -159,7 +159,7 @@ def test_select_noalloc_reports_argument_errors_first(bpa):
 def test_status_strings(bpa):
     L = bpa.lib()
     assert L.bpa_status_string(5) == b"BPA_ERR_TIMEOUT"
-    assert L.bpa_version() == 5
+    assert L.bpa_version() == 6
 
 
 def test_version_1_descriptor_is_accepted(bpa):
@@ -238,3 +238,16 @@ def test_value_head_dim_checks_and_sizes(bpa):
     assert b"value head dim" in L.bpa_last_error()
     D.dv = -1
     assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) == 0
+
+
+def test_dropout_fields(bpa):
+    L = bpa.lib()
+    D = _desc(bpa, dropout_threshold=1 << 30, dropout_seed=2 ** 63 + 5)
+    assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) > 0
+    D = _desc(bpa, dropout_threshold=1 << 30, dropout_reserved=1)
+    assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) == 0
+    assert b"dropout_reserved" in L.bpa_last_error()
+    # version 5: the dropout fields past the shorter struct are not read
+    D = _desc(bpa, dropout_reserved=1)
+    D.struct_size = bpa.bpa_attn_desc.dropout_threshold.offset
+    assert L.bpa_workspace_size(bpa.BPA_OP_FWD, ctypes.byref(D)) > 0

@@ -85,3 +85,15 @@ def test_library_checks_the_marshalled_descriptor(bpa):
     base = bpa.bpa_workspace_size(bpa.BPA_OP_BWD, ok)
     det = bpa.bpa_workspace_size(bpa.BPA_OP_BWD, bpa.make_desc(q, k, v, causal=True, deterministic=True))
     assert det == base
+
+
+def test_dropout_threshold_and_seed(bpa):
+    from oracle import oracle
+    q, k, v = _qkv()
+    for p in (0.0, 0.1, 0.5, 0.999999999999):
+        D = bpa.make_desc(q, k, v, dropout_p=p, dropout_seed=2 ** 64 + 7)
+        # the same integer decision rule as the oracle's: round(p * 2^32), capped
+        assert D.dropout_threshold == oracle.dropout_threshold(p)
+        assert D.dropout_seed == 7 and D.dropout_reserved == 0
+    with pytest.raises(ValueError):
+        bpa.make_desc(q, k, v, dropout_p=1.0)
