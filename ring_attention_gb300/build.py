@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbpa.so")
 
-SOURCES = ["fwd_tc.cu", "fwd_tc_drop.cu", "api.cu", "simt.cu", "aux.cu", "bwd_tc.cu", "select.cu", "gather.cu",
+SOURCES = ["fwd_tc.cu", "fwd_tc_drop.cu", "fwd_band.cu", "api.cu", "simt.cu", "aux.cu", "bwd_tc.cu", "select.cu", "gather.cu",
            "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -124,6 +124,9 @@ bpa_status check_select_args(const void* q, const void* k, int32_t dtype, int32_
                              int32_t block_size, int32_t top_n, const int32_t* block_idx_out);
 
 bool fwd_tc_supported(const Problem& P);
+// Narrow key bands with grouped heads take the band forward (fwd_band.cu).
+bool fwd_band_supported(const Problem& P);
+cudaError_t launch_fwd_band(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s);
 bool bwd_tc_supported(const Problem& P);
 bool gather_supported(const Problem& P);
 

@@ -14,6 +14,7 @@ bool fwd_tc_supported(const Problem& P) {
 cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
     const Problem& P = a.P;
     // short key ranges: single-tile CTAs, two per SM; a ring block must hold whole CTAs
+    if (fwd_band_supported(P)) return launch_fwd_band(a, maps, s);
     const bool single = fwd_single_tile(P);
     if (P.drop_thr) return launch_fwd_tc_dropout(a, maps, s, single);
     if (P.d == 128 && P.dv == 64) return single ? launch<128, 64, 1, false>(a, maps, s) : launch<128, 64, 2, false>(a, maps, s);

@@ -107,6 +107,32 @@ def test_backward_bf16(bpa, ora, shape, mask):
     assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
 
 
+BAND_CASES = [  # (B, S, Hq, Hkv, d), mask: windows of at most one tile, grouped heads
+    ((1, 1024, 32, 2, 128), dict(causal=True, window=(128, 0))),
+    ((2, 1000, 8, 4, 128), dict(causal=True, window=(128, 0))),
+    ((1, 700, 4, 2, 64), dict(causal=True, window=(7, 0))),
+    ((2, 300, 4, 1, 128), dict(causal=False, window=(0, 0))),
+    ((1, 520, 6, 3, 128), dict(causal=False, window=(64, 0))),
+    ((1, 640, 4, 2, 64), dict(causal=False, window=(0, 100))),
+    ((1, 130, 2, 1, 128), dict(causal=True, window=(128, 0))),
+]
+
+
+@pytest.mark.parametrize("case", BAND_CASES, ids=lambda c: "x".join(map(str, c[0])) + "_" + _mask_id(c[1]))
+def test_band_forward(bpa, ora, case):
+    # narrow windows with grouped heads take the band kernel (key / value tiles resident
+    # while the group's heads pass, static per-CTA shares): several CTAs share one group,
+    # groups straddle CTAs, ragged tails
+    shape, mask = case
+    B, S, Hq, Hkv, d = shape
+    q, k, v = _inputs(shape, 81 + S, backward=False)
+    o, m, l = bpa.bpa_fwd(dev(q), dev(k), dev(v), **mask)
+    torch.cuda.synchronize()
+    oo, om, ol = ora.attention_fwd(q, k, v, **mask)
+    assert max_abs(host(o), oo) <= BF16_O_MAX_ABS
+    check_stats(m, l, om, ol)
+
+
 def _general_bias(kind, B, Hq, S, seed):
     # bpt.py's bias takes each dim as 1 (broadcast) or full: a bias that depends on the
     # query position ([B, Hq, S, S] or a per-row [B, 1, S, 1]) reaches the backward
