@@ -53,23 +53,32 @@ struct BandCfg {
 };
 
 // One head pair of the sequence: batch entry, kv head, query tile and the pair's first q head.
+// Walked incrementally (no 64-bit division per step: the sequence is (b, kv head, query
+// tile, pair) with the pair innermost).
 struct BandPair {
-    int b, hkv, qt, h0;
+    int b, hkv, qt, hp;
     int64_t group;    // (batch, kv head, query tile) index
+    __device__ __forceinline__ int h0(const Problem& P) const { return hkv * P.G + 2 * hp; }
+    __device__ __forceinline__ void init(const Problem& P, int nqt, int64_t u) {
+        const int hpg = P.G / 2;
+        group = u / hpg;
+        hp = static_cast<int>(u % hpg);
+        qt = static_cast<int>(group % nqt);
+        const int64_t t = group / nqt;
+        hkv = static_cast<int>(t % P.Hkv);
+        b = static_cast<int>(t / P.Hkv);
+    }
+    __device__ __forceinline__ void next(const Problem& P, int nqt) {
+        if (++hp < P.G / 2) return;
+        hp = 0;
+        ++group;
+        if (++qt < nqt) return;
+        qt = 0;
+        if (++hkv < P.Hkv) return;
+        hkv = 0;
+        ++b;
+    }
 };
-
-__device__ __forceinline__ BandPair band_pair(const Problem& P, int nqt, int64_t u) {
-    const int hpg = P.G / 2;
-    BandPair r;
-    r.group = u / hpg;
-    const int hp = static_cast<int>(u % hpg);
-    r.qt = static_cast<int>(r.group % nqt);
-    const int64_t t = r.group / nqt;
-    r.hkv = static_cast<int>(t % P.Hkv);
-    r.b = static_cast<int>(t / P.Hkv);
-    r.h0 = r.hkv * P.G + 2 * hp;
-    return r;
-}
 
 // Key tiles query tile qt sees: lo .. lo + n - 1 (the causal / window bounds of its rows).
 __host__ __device__ __forceinline__ void band_tiles(int S, int causal, int wl, int wr, int qt, int& lo, int& n) {
@@ -259,8 +268,9 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
             int64_t prev_group = -1;
             int qpos = 0;
             bool ok = true;
-            for (int64_t u = u0; ok && u < uend; ++u) {
-                const BandPair T = band_pair(P, nqt, u);
+            BandPair T;
+            T.init(P, nqt, u0);
+            for (int64_t u = u0; ok && u < uend; ++u, T.next(P, nqt)) {
                 // the pair's two query tiles first: they never wait on a key-tile release
                 for (int i = 0; i < 2; ++i, ++qpos) {
                     const int st = qpos % C::NSQ, use = qpos / C::NSQ;
@@ -271,7 +281,7 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
                     mbar_expect_tx(BAR(C::B_QF + st), C::Q_BYTES);
                     for (int sub = 0; sub < D / 64; ++sub)
                         tma_load_4d(sb + C::OFF_Q + st * C::Q_BYTES + sub * C::SUB, &tmQ, BAR(C::B_QF + st), sub * 64,
-                                    T.h0 + i, T.qt * BM, T.b);
+                                    T.h0(P) + i, T.qt * BM, T.b);
                 }
                 if (!ok || T.group == prev_group) continue;
                 prev_group = T.group;
@@ -320,8 +330,9 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
         int qpos = 0, pair = 0;
         bool ok = true;
         int lo = 0, n = 0;
-        for (int64_t u = u0; ok && u < uend; ++u, ++pair) {
-            const BandPair T = band_pair(P, nqt, u);
+        BandPair T;
+        T.init(P, nqt, u0);
+        for (int64_t u = u0; ok && u < uend; ++u, ++pair, T.next(P, nqt)) {
             if (T.group != prev_group) {
                 prev_group = T.group;
                 band_tiles(P.S, P.causal, P.wl, P.wr, T.qt, lo, n);
@@ -336,10 +347,11 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
             }
             // The last pair of its group releases each slot whose tile the next group does not
             // keep, right after the last product that reads it.
-            const bool last_of_group = u + 1 >= uend || band_pair(P, nqt, u + 1).group != T.group;
+            BandPair N = T;
+            N.next(P, nqt);
+            const bool last_of_group = u + 1 >= uend || N.group != T.group;
             Two<bool> release{false, false};
             if (last_of_group && u + 1 < uend) {
-                const BandPair N = band_pair(P, nqt, u + 1);
                 int nlo, nn;
                 band_tiles(P.S, P.causal, P.wl, P.wr, N.qt, nlo, nn);
                 for (int j = 0; j < n; ++j) {
@@ -432,9 +444,10 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
         const float sl2 = P.scale * kLog2e;
         bool aborted = false;
         int cs = 0, pair = 0;                 // S tiles seen, pairs done
-        for (int64_t u = u0; !aborted && u < uend; ++u, ++pair) {
-            const BandPair T = band_pair(P, nqt, u);
-            const int h = T.h0 + wg;
+        BandPair T;
+        T.init(P, nqt, u0);
+        for (int64_t u = u0; !aborted && u < uend; ++u, ++pair, T.next(P, nqt)) {
+            const int h = T.h0(P) + wg;
             const int q = T.qt * BM + t;
             int lo, n;
             band_tiles(P.S, P.causal, P.wl, P.wr, T.qt, lo, n);
