@@ -445,6 +445,16 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
         marks.mark(3, s);
         return e == cudaSuccess ? BPA_OK : cuda_fail(e, "backward launch");
     }
+    if (n == 1 && bwd_band_supported(P)) {
+        // band: the pre-pass zeroes dq, the main kernel adds dQ into it directly
+        a.dq_direct = 1;
+        if ((e = launch_bwd_pre(a, s)) != cudaSuccess) return cuda_fail(e, "backward pre-pass");
+        marks.mark(1, s);
+        if ((e = launch_bwd_tc_band(a, maps, s)) != cudaSuccess) return cuda_fail(e, "backward launch");
+        marks.mark(2, s);
+        marks.mark(3, s);
+        return BPA_OK;
+    }
     a.dq_acc = reinterpret_cast<float*>(ws + L.dq);
     if ((e = launch_bwd_pre(a, s)) != cudaSuccess || (P.dsink && (e = launch_sink_grad(a, s)) != cudaSuccess))
             return cuda_fail(e, "backward pre-pass");

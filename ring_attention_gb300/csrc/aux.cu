@@ -141,6 +141,9 @@ __global__ void k_bwd_pre_bf16v(const BwdArgs a, int zero_dq) {
             }
         }
         for (int o = tpr >> 1; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o, tpr);
+        if (a.dq_direct && live && q < P.S)   // band backward: dq is accumulated in place (d == dv)
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] +
+                                      h * P.qs[2] + sub * 8) = make_uint4(0u, 0u, 0u, 0u);
         if (live && sub == 0) {
             float lse = INFINITY;
             if (q < P.S) {

@@ -77,6 +77,7 @@ struct BwdArgs {
     int Spad;           // S rounded up to 64
     float* dq_acc;      // [B, Hq, Spad / 4, d, 4] float32 (four consecutive queries of a channel together);
                         // deterministic mode: one such slice per 128-key tile, [nkt][B, Hq, Spad / 4, d, 4]
+    int dq_direct;      // band backward: dQ added in bf16 pairs straight into dq (zeroed by the pre-pass)
     float* dk_acc;      // ring carries / block-selected accumulators [B, S, Hkv, d] float32, or nullptr
     float* dv_acc;
     int ring_idx;
@@ -100,6 +101,10 @@ cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_fwd_tc(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s);
 cudaError_t launch_bwd_tc(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s);
+// Band backward (every 64-row query tile seen by at most two key tiles): the tensor-core
+// kernel adding dQ straight into dq; bwd_band_supported says when it applies.
+bool bwd_band_supported(const Problem& P);
+cudaError_t launch_bwd_tc_band(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s);
 cudaError_t launch_gather_fwd(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_gather_bwd(const BwdArgs& a, cudaStream_t s);   // needs dk_acc / dv_acc cleared
 cudaError_t launch_cast_dkdv(const BwdArgs& a, cudaStream_t s);    // dk_acc / dv_acc -> dk / dv (bf16)

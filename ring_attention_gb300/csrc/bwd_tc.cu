@@ -137,7 +137,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32
 // DET: deterministic dQ slices; DROP: attention dropout; NODQ: dK and dV only (the band
 // backward computes dQ in a query-major kernel of its own).  Each is a separate
 // instantiation, so that the default kernel's code stays as it is without the knobs.
-template <int DV, bool DET, bool DROP, bool NODQ = false>
+template <int DV, bool DET, bool DROP, bool NODQ = false, bool DQBF = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_bwd_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -331,6 +331,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tDQ + cq + lane_base, v);
             tc_fence_before();
             mbar_arrive(BAR(B_DQE));
+            if (DQBF) {
+                // band backward: at most two key tiles add to any dq element, so bf16 pair
+                // reductions straight into dq give an order-independent result.  Adjacent
+                // lanes (channels r, r ^ 1) trade one value per two queries: the even lane
+                // adds channels (r, r + 1) of query j, the odd lane those of query j + 1, so
+                // a warp's reduction covers two 64-byte runs of dq.
+                const int q0 = iter_q0(t) + cq;
+                __nv_bfloat16* base = static_cast<__nv_bfloat16*>(a.dq) + W.b * P.qs[0] +
+                                      static_cast<int64_t>(iter_head(t)) * P.qs[2] + (r & ~1);
+                const bool odd = lane & 1;
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 2) {
+                    const float mine0 = __uint_as_float(v[jj]), mine1 = __uint_as_float(v[jj + 1]);
+                    const float got = __shfl_xor_sync(0xffffffffu, odd ? mine0 : mine1, 1);
+                    const int q = q0 + jj + (odd ? 1 : 0);
+                    const float lo = odd ? got : mine0, hi = odd ? mine1 : got;
+                    if (q < P.S) red_add_bf16x2(base + static_cast<int64_t>(q) * P.qs[1], pack_bf16(lo * P.scale, hi * P.scale));
+                }
+                return true;
+            }
             float* dst = a.dq_acc + (static_cast<int64_t>(W.b) * P.Hq + iter_head(t)) * a.Spad * D +
                          (static_cast<int64_t>((iter_q0(t) + cq) >> 2) * D + r) * 4;
             if (DET) {   // this key tile's own slice: written once, added in key order later
@@ -619,6 +639,42 @@ cudaError_t launch_bwd_tc_kv(const BwdArgs& a, const CUtensorMap* maps, cudaStre
     const int grid = nkt * a.P.Hkv * a.P.B;
     k_bwd_tc<128, false, false, true><<<grid, kThreads, L::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
     return cudaGetLastError();
+}
+
+// Band backward: dQ reduced in bf16 pairs into dq (d = dv = 128).
+cudaError_t launch_bwd_tc_band(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
+    using L = BwdCfg<128>;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(k_bwd_tc<128, false, false, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 L::SMEM);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    const int nkt = (a.P.S + BK - 1) / BK;
+    const int grid = nkt * a.P.Hkv * a.P.B;
+    k_bwd_tc<128, false, false, false, true><<<grid, kThreads, L::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
+    return cudaGetLastError();
+}
+
+bool bwd_band_supported(const Problem& P) {
+    if (!bwd_tc_supported(P) || P.dv != D || P.ring_n != 1) return false;
+    if (P.seqlens_q || P.seqlens_kv || P.sink || P.dsink || P.det || P.drop_thr) return false;
+    // the vectorised pre-pass (which zeroes dq) indexes rows in 32 bits
+    if (static_cast<int64_t>(P.B) * P.Hq * ((P.S + 63) / 64 * 64) >= (1ll << 31)) return false;
+    // at most two key tiles may see any 64-row query tile (a window of at most one tile)
+    for (int q0 = 0; q0 < P.S; q0 += BQ) {
+        const int qb = q0 + BQ - 1 < P.S - 1 ? q0 + BQ - 1 : P.S - 1;
+        int klo = 0, khi = P.S - 1;
+        if (P.causal && qb < khi) khi = qb;
+        if (P.wr >= 0 && qb + P.wr < khi) khi = qb + P.wr;
+        if (P.wl >= 0 && q0 - P.wl > klo) klo = q0 - P.wl;
+        if (klo <= khi && khi / BK - klo / BK + 1 > 2) return false;
+    }
+    return true;
 }
 
 bool bwd_tc_supported(const Problem& P) {

@@ -132,6 +132,11 @@ BPA_DEV void red_add_v2(float* dst, float x, float y) {
     asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(reinterpret_cast<uint64_t>(dst)), "f"(x), "f"(y)
                  : "memory");
 }
+// dst[0..1] += (lo, hi) as a bf16 pair (one rounding per addition)
+BPA_DEV void red_add_bf16x2(void* dst, uint32_t v) {
+    asm volatile("red.global.add.noftz.bf16x2 [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(dst)), "r"(v) : "memory");
+}
+
 BPA_DEV void red_add_v4(float* dst, float x, float y, float z, float w) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(reinterpret_cast<uint64_t>(dst)), "f"(x),
                  "f"(y), "f"(z), "f"(w)

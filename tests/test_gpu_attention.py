@@ -133,6 +133,39 @@ def test_band_forward(bpa, ora, case):
     check_stats(m, l, om, ol)
 
 
+BAND_BWD_CASES = [  # (B, S, Hq, Hkv), mask: every 64-row query tile seen by at most two key tiles
+    ((1, 1024, 32, 2), dict(causal=True, window=(128, 0))),
+    ((2, 1000, 8, 4), dict(causal=True, window=(128, 0))),
+    ((1, 700, 4, 4), dict(causal=True, window=(7, 0))),
+    ((2, 300, 4, 1), dict(causal=False, window=(0, 0))),
+    ((1, 520, 6, 3), dict(causal=False, window=(64, 0))),
+    ((1, 640, 4, 2), dict(causal=False, window=(0, 60))),
+    ((1, 130, 2, 1), dict(causal=True, window=(128, 0))),
+]
+
+
+@pytest.mark.parametrize("case", BAND_BWD_CASES, ids=lambda c: "x".join(map(str, c[0])) + "_" + _mask_id(c[1]))
+@pytest.mark.parametrize("bias_kind", ["none", "keys"])
+def test_band_backward(bpa, ora, case, bias_kind):
+    # narrow windows: dQ is added in bf16 pairs straight into dq (at most two key tiles
+    # contribute to any element, so the result does not depend on their order)
+    (B, S, Hq, Hkv), mask = case
+    d = 128
+    q, k, v, do = _inputs((B, S, Hq, Hkv, d), 91 + S)
+    bias = _bias(bias_kind, B, Hq, S, 92)
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    tb = None if bias is None else dev(bias)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, bias=tb, **mask)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, bias=tb, **mask)
+    dq2, dk2, dv2 = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, bias=tb, **mask)
+    torch.cuda.synchronize()
+    rq, rk, rv, *_ = ora.attention_bwd(q, k, v, do, bias=bias, **mask)
+    assert rel_l2(host(dq), rq) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dk), rk) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
+    assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
+
+
 def _general_bias(kind, B, Hq, S, seed):
     # bpt.py's bias takes each dim as 1 (broadcast) or full: a bias that depends on the
     # query position ([B, Hq, S, S] or a per-row [B, 1, S, 1]) reaches the backward
