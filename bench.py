@@ -476,31 +476,60 @@ def main():
     traffic = kernel_traffic("k_bwd_tc")
 
     # ---- end to end through the public API: pinned host -> device -> host --
+    # Every step uploads its inputs from pinned host memory and downloads its outputs.  The
+    # copies run on their own streams against two device buffer sets, so step i + 1's
+    # uploads and step i - 1's downloads overlap step i's kernels; events order the reuse of
+    # each buffer set.
     h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q, k, v, do)]
     for h, t in zip(h_in, (q, k, v, do)):
         h.copy_(t)
     h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, dq, dk, dv)]
-    d_in = [torch.empty_like(t) for t in (q, k, v, do)]
+    d_in = [[torch.empty_like(t) for t in (q, k, v, do)] for _ in range(2)]
+    d_out = [[torch.empty_like(t) for t in (o, dq, dk, dv)] for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
+    s_up, s_run, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of a set uploaded
+    ev_used = [torch.cuda.Event() for _ in range(2)]    # the kernels reading a set's inputs are done
+    ev_done = [torch.cuda.Event() for _ in range(2)]    # outputs of a set written
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # outputs of a set downloaded
+    started = [False, False]
 
-    def e2e_step():
-        for d_, h in zip(d_in, h_in):
-            d_.copy_(h, non_blocking=True)
-        bpa.bpa_fwd(d_in[0], d_in[1], d_in[2], o=o, m=m, l=l, workspace_buf=ws_f, **kw)
-        bpa.bpa_bwd(d_in[0], d_in[1], d_in[2], o, d_in[3], m, l, dq=dq, dk=dk, dv=dv, workspace_buf=ws_b, **kw)
-        for h, d_ in zip(h_out, (o, dq, dk, dv)):
-            h.copy_(d_, non_blocking=True)
+    def e2e_steps(n, t_start=None, t_end=None):
+        if t_start is not None:
+            t_start.record(s_up)
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(s_up):
+                if started[b]:
+                    s_up.wait_event(ev_used[b])
+                for d_, h in zip(d_in[b], h_in):
+                    d_.copy_(h, non_blocking=True)
+                ev_in[b].record(s_up)
+            s_run.wait_event(ev_in[b])
+            if started[b]:
+                s_run.wait_event(ev_out[b])
+            xo, xdq, xdk, xdv = d_out[b]
+            xq, xk, xv, xdo = d_in[b]
+            bpa.bpa_fwd(xq, xk, xv, o=xo, m=m, l=l, workspace_buf=ws_f, stream=s_run, **kw)
+            bpa.bpa_bwd(xq, xk, xv, xo, xdo, m, l, dq=xdq, dk=xdk, dv=xdv, workspace_buf=ws_b, stream=s_run, **kw)
+            ev_used[b].record(s_run)
+            ev_done[b].record(s_run)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(ev_done[b])
+                for h, d_ in zip(h_out, d_out[b]):
+                    h.copy_(d_, non_blocking=True)
+                ev_out[b].record(s_down)
+            started[b] = True
+        if t_end is not None:
+            s_up.wait_stream(s_down)
+            t_end.record(s_up)
 
-    for _ in range(3):
-        e2e_step()
+    e2e_steps(3)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = E(), E()
-    e0.record()
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record()
+    e2e_steps(args.e2e_steps, e0, e1)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     e2e_val = aggregate_tflops(f_fwd + f_bwd, args.e2e_steps, world, e2e_ms)

@@ -98,8 +98,11 @@ typedef struct bpa_attn_desc {
     int32_t ring_size;         /* >= 1: KV super-blocks swept in ring order, S % ring_size == 0 */
     int32_t ring_step_begin;   /* first ring step of this call, 0 <= begin < end */
     int32_t ring_step_end;     /* one past the last step; 0 selects ring_size */
-    const int32_t* block_idx;  /* block-selected mode: [B, Hq, S/sel_block, top_n] from */
-    int32_t sel_block;         /*   bpa_select_blocks (-1 entries are ignored) */
+    const int32_t* block_idx;  /* block-selected mode: [B, Hq, S/sel_block, top_n] from
+                                *   bpa_select_blocks: each entry -1 (ignored) or a block before
+                                *   the query block.  Other entries are ignored too, and the
+                                *   call records BPA_ERR_DEVICE_CHECK for bpa_check */
+    int32_t sel_block;
     int32_t top_n;
     int32_t local_window;      /* keys q - local_window + 1 .. q are always allowed */
     /* Fields below were added in descriptor version 2 (bpa_version() >= 2).  A caller

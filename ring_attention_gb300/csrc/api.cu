@@ -10,6 +10,8 @@
 
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "bpa.h"
 #include "bpa_internal.h"
 #include "common.cuh"
@@ -48,6 +50,20 @@ bpa_status fail(bpa_status st, const char* fmt, ...) {
 bpa_status cuda_fail(cudaError_t e, const char* what) {
     return fail(BPA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
+
+// NVTX range over a scope (header-only NVTX: free unless a profiler is attached), so that a
+// timeline shows each call and each ring step; ncu can select kernels by them (--nvtx).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    NvtxRange(const char* fmt, int i) {
+        char buf[64];
+        snprintf(buf, sizeof buf, fmt, i);
+        nvtxRangePushA(buf);
+    }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -305,6 +321,7 @@ size_t bpa_workspace_size(int32_t op, const bpa_attn_desc* desc) {
 
 bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void* workspace,
                    size_t workspace_bytes, void* stream) {
+    const NvtxRange range("bpa_fwd");
     Problem P;
     bpa_status st = make_problem(desc, P, true);
     if (st != BPA_OK) return st;
@@ -336,6 +353,8 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
     a.sched = counters;
 
     if (P.block_idx) {
+        // entries outside the contract are ignored by the kernels and reported in the status word
+        if ((e = launch_check_blocks(P, a.status, s)) != cudaSuccess) return cuda_fail(e, "block index check");
         e = gather_supported(P) ? launch_gather_fwd(a, s) : launch_fwd_simt(a, s);
         marks.mark(1, s);
         marks.mark(2, s);
@@ -359,6 +378,7 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
     a.acc = reinterpret_cast<float*>(ws + L.acc);
     if (begin == 0 && (e = launch_ring_init(a, s)) != cudaSuccess) return cuda_fail(e, "ring carry init");
     for (int idx = begin; idx < end; ++idx) {
+        const NvtxRange step("bpa_fwd ring step %d", idx);
         a.ring_idx = idx;
         const int li = idx - begin;
         a.sched = counters + li % kCounters;
@@ -375,6 +395,7 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
 
 bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, const float* m, const float* l,
                    void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+    const NvtxRange range("bpa_bwd");
     Problem P;
     bpa_status st = make_problem(desc, P, true);
     if (st != BPA_OK) return st;
@@ -407,6 +428,8 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
     a.lse = reinterpret_cast<float*>(ws + L.lse);
     a.Spad = L.Spad;
     a.status = reinterpret_cast<uint32_t*>(ws);
+    if (P.block_idx && (e = launch_check_blocks(P, a.status, s)) != cudaSuccess)
+        return cuda_fail(e, "block index check");
 
     if (P.block_idx && !P.det && gather_supported(P) && aligned16(dout) && aligned16(dq) && aligned16(dk) && aligned16(dv)) {
         // gathered backward: dQ written per query block, dK / dV reduced into float32 accumulators
@@ -470,6 +493,7 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
             (e = cudaMemsetAsync(a.dv_acc, 0, nv, s)) != cudaSuccess)
             return cuda_fail(e, "clearing the dK / dV carries");
         for (int idx = 0; idx < n; ++idx) {
+            const NvtxRange step("bpa_bwd ring step %d", idx);
             a.ring_idx = idx;
             if ((e = launch_bwd_tc(a, maps, s)) != cudaSuccess) return cuda_fail(e, "ring backward step");
         }
@@ -483,7 +507,7 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
 size_t bpa_select_workspace_size(int32_t B, int32_t S, int32_t H, int32_t d, int32_t block_size) {
     if (B < 1 || S < 1 || H < 1 || d < 1 || block_size < 1 || S % block_size) return 0;
     const size_t sums = sizeof(double) * static_cast<size_t>(B) * H * (S / block_size) * d;
-    return kHeader + 2 * round256(sums);
+    return kHeader + 2 * round256(sums) + round256(sums / 2);
 }
 
 bpa_status bpa_select_blocks(const void* q, const void* k, int32_t dtype, int32_t B, int32_t S, int32_t H,
@@ -519,6 +543,7 @@ bpa_status bpa_select_blocks(const void* q, const void* k, int32_t dtype, int32_
     const size_t sums = sizeof(double) * static_cast<size_t>(B) * H * (S / block_size) * d;
     a.qsum = reinterpret_cast<double*>(ws + kHeader);
     a.ksum = reinterpret_cast<double*>(ws + kHeader + round256(sums));
+    a.kt32 = reinterpret_cast<float*>(ws + kHeader + 2 * round256(sums));
     a.status = reinterpret_cast<uint32_t*>(ws);
     e = launch_select(a, s);
     return e == cudaSuccess ? BPA_OK : cuda_fail(e, "block selection launch");

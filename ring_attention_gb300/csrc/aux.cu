@@ -379,6 +379,32 @@ cudaError_t launch_sink_grad(const BwdArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Block-selected mode: every entry of block_idx [B, Hq, S / sel_block, top_n] must be -1 or a
+// block strictly before its query block (what bpa_select_blocks produces).  Entries outside
+// that range are ignored by the attention kernels and reported here as a device-side check
+// failure (the index array is only read, so a bad entry cannot make an access go astray).
+__global__ void k_check_blocks(const Problem P, uint32_t* status) {
+    const int nblk = P.S / P.sel_block;
+    const int64_t rows = static_cast<int64_t>(P.B) * P.Hq * nblk;
+    for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < rows;
+         r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int i = static_cast<int>(r % nblk);
+        const int32_t* sel = P.block_idx + r * P.top_n;
+        bool bad = false;
+        for (int t = 0; t < P.top_n; ++t) {
+            const int32_t e = sel[t];
+            bad = bad || (e != -1 && (e < 0 || e >= i));
+        }
+        if (bad) report(status, ST_CHECK, 0xB0);
+    }
+}
+
+cudaError_t launch_check_blocks(const Problem& P, uint32_t* status, cudaStream_t s) {
+    const int64_t rows = static_cast<int64_t>(P.B) * P.Hq * (P.S / P.sel_block);
+    k_check_blocks<<<grid_for(rows, 256), 256, 0, s>>>(P, status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s) {
     k_wait_selftest<<<1, 32, 0, s>>>(status, limit_ns);
     return cudaGetLastError();

@@ -93,6 +93,7 @@ struct SelectArgs {
     int32_t* out;
     double* qsum;       // [B, H, nblk, d]
     double* ksum;
+    float* kt32;        // [B, H, d, nblk] float32 copies of the key sums (the pre-filter's)
     uint32_t* status;
 };
 
@@ -117,6 +118,7 @@ cudaError_t launch_pad_stats(const FwdArgs& a, cudaStream_t s);   // m, l of pad
 cudaError_t launch_dq_reduce(const BwdArgs& a, cudaStream_t s);   // deterministic mode: slices -> dq
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s);
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, cudaStream_t s);
+cudaError_t launch_check_blocks(const Problem& P, uint32_t* status, cudaStream_t s);   // block_idx contract
 
 void set_last_error(const char* msg);
 

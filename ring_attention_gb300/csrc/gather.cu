@@ -117,7 +117,8 @@ __device__ __forceinline__ void sum_partials(float (&x)[2][4][4], const float* x
 // with .trans.
 
 // The distinct key blocks query block i visits, ascending: the blocks its local window
-// touches and its selected blocks (entries outside [0, i] are ignored).  Run by one lane.
+// touches and its selected blocks (selected entries outside [0, i) are ignored; a separate
+// check reports them).  Run by one lane.
 __device__ int visit_list(const Problem& P, int64_t unit, int i, int* list) {
     int n = 0;
     const int32_t* sel = P.block_idx + unit * P.top_n;
@@ -130,7 +131,8 @@ __device__ int visit_list(const Problem& P, int64_t unit, int i, int* list) {
     };
     if (P.local_window > 0)
         for (int kb = wfirst; kb <= i; ++kb) add(kb);
-    for (int x = 0; x < P.top_n; ++x) add(sel[x]);
+    for (int x = 0; x < P.top_n; ++x)
+        if (sel[x] < i) add(sel[x]);
     for (int x = 1; x < n; ++x) {   // ascending
         const int key = list[x];
         int y = x - 1;

@@ -63,8 +63,10 @@ __device__ __forceinline__ void ring_range(const Problem& P, bool ring, int idx,
     hi = lo + P.ring_blk - 1;
 }
 
+// Whether key block kb is selected for query q (only blocks before q's own block count).
 __device__ __forceinline__ bool selected(const Problem& P, int b, int h, int q, int kb) {
     const int nblk = P.S / P.sel_block;
+    if (kb >= q / P.sel_block) return false;
     const int32_t* sel = P.block_idx + ((static_cast<int64_t>(b) * P.Hq + h) * nblk + q / P.sel_block) * P.top_n;
     for (int t = 0; t < P.top_n; ++t)
         if (sel[t] == kb) return true;
