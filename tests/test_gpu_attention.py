@@ -297,6 +297,26 @@ def test_select_blocks_nan_scores(bpa, ora):
     np.testing.assert_array_equal(idx.cpu().numpy(), ora.select_blocks(q, k, block_size=bs, top_n=n))
 
 
+def test_select_blocks_near_ties(bpa, ora):
+    # scores that differ far below float32 resolution (2^-30 against a magnitude of ~16):
+    # the float32 pre-filter keeps them all, the float64 contract scores decide; plus exact
+    # ties among them (lower block first) and random blocks the filter drops
+    B, S, H, d, bs, n = 1, 1024, 2, 16, 8, 6
+    rng = np.random.default_rng(58)
+    q = np.zeros((B, S, H, d), np.float32)
+    k = rng.standard_normal((B, S, H, d)).astype(np.float32) * 0.01
+    u = rng.standard_normal(d).astype(np.float32)
+    for i in range(S // bs):
+        q[0, i * bs, :, :] = u
+        if i % 3 == 0:   # a third of the key blocks nearly tie with each other
+            k[0, i * bs:(i + 1) * bs, :, :] = 0.0
+            k[0, i * bs, :, :] = u
+            k[0, i * bs + 1, :, 0] = np.float32(((i * 7) % 11) * 2.0 ** -30)
+    idx = bpa.bpa_select_blocks(dev(q), dev(k), block_size=bs, top_n=n)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), ora.select_blocks(q, k, block_size=bs, top_n=n))
+
+
 def test_select_blocks_ties(bpa, ora):
     # block sums with many exactly equal scores: ties must keep the lower block
     B, S, H, d, bs = 1, 256, 1, 8, 8
@@ -382,6 +402,51 @@ def test_block_selected_backward_planted(bpa, ora, geom):
     check_stats(m, l, rm, rl)
     for got, ref in ((dq, rq), (dk, rk), (dvv, rv)):
         assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_block_index_contract_is_checked_on_the_device(bpa, ora, dtype):
+    # entries that are not -1 or an earlier block (its own block, a later block inside the
+    # tensor, a block past the end, a negative value) are ignored by the kernels and
+    # recorded as a device-side check failure; the index array is only read, so no access
+    # goes outside a buffer even without the check
+    B, H, S, bs, n, lw, d = 1, 2, 256, 32, 4, 32, 64
+    q, k, v, do = draw([(B, S, H, d), (B, S, H, d), (B, S, H, d), (B, S, H, d)], 96, dtype)
+    idx = _planted_selection(B, H, S, bs, n, 97)
+    bad = idx.copy()
+    bad[0, 0, 3, n - 1] = 3            # its own block
+    bad[0, 1, 2, n - 1] = 6            # a later block, inside the tensor
+    bad[0, 1, 5, n - 1] = S // bs + 5  # past the last block
+    bad[0, 0, 7, n - 1] = -7
+    clean = np.where((bad == -1) | ((bad >= 0) & (bad < np.arange(S // bs)[None, None, :, None])), bad, -1)
+    kw = dict(causal=True, sel_block=bs, top_n=n, local_window=lw)
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    D = bpa.make_desc(tq, tk, tv, block_idx=torch.from_numpy(bad).cuda(), **kw)
+    wsf = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_FWD, D), tq.device)
+    wsb = bpa.workspace(bpa.bpa_workspace_size(bpa.BPA_OP_BWD, D), tq.device)
+    ti = torch.from_numpy(bad).cuda()
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, block_idx=ti, workspace_buf=wsf, **kw)
+    dq, dk, dvv = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, block_idx=ti, workspace_buf=wsb, **kw)
+    torch.cuda.synchronize()
+    for ws in (wsf, wsb):
+        with pytest.raises(bpa.BpaError) as err:
+            bpa.bpa_check(ws)
+        assert err.value.status == bpa.BPA_ERR_DEVICE_CHECK
+    rq, rk, rv, ro, rm, rl = ora.attention_bwd(q, k, v, do, block_idx=clean, **kw)
+    if dtype == "f32":
+        for got, ref in ((o, ro), (dq, rq), (dk, rk), (dvv, rv)):
+            assert max_abs(host(got), ref) <= FP32_MAX_ABS
+    else:
+        assert max_abs(host(o), ro) <= BF16_O_MAX_ABS
+        for got, ref in ((dq, rq), (dk, rk), (dvv, rv)):
+            assert rel_l2(host(got), ref) <= BF16_GRAD_REL_L2
+    # a valid selection on the same workspaces clears the status
+    tc = torch.from_numpy(clean).cuda()
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, block_idx=tc, workspace_buf=wsf, **kw)
+    bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, block_idx=tc, workspace_buf=wsb, **kw)
+    torch.cuda.synchronize()
+    bpa.bpa_check(wsf)
+    bpa.bpa_check(wsb)
 
 
 @pytest.mark.parametrize("lw", [0, 20, 64])
