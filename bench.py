@@ -85,7 +85,7 @@ def code_digest(path: str) -> str:
 def kernel_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current code of the kernel (else None)."""
-    src = {"k_bwd_tc": "bwd_tc.cu", "k_fwd_tc": "fwd_tc.cu"}[kernel]
+    src = {"k_bwd_tc": "bwd_tc.cu", "k_fwd_tc": "fwd_tc.cuh"}[kernel]
     path = os.path.join(ROOT, "ring_attention_gb300", "csrc", src)
     digest = code_digest(path)
     table = os.path.join(ROOT, "profiles", "traffic.txt")
