@@ -6,7 +6,27 @@
 //   Qs[i][c] = ((0 + x_0) + x_1) + ... + x_{bs-1}      float64, rows in order
 //   score    = ((0 + a_0*b_0) + a_1*b_1) + ...         float64, channels in
 //              order, every product and sum rounded separately (no FMA)
-//   ranking  : larger score first, the lower block index on equal scores.
+//   ranking  : larger score first, the lower block index on equal scores; a NaN
+//              score below every number, NaNs in block order.
+//
+// GB300 runs float64 at a small fraction of its float32 rate, so the float64 scores
+// are computed only where they can decide the result.  For query block i and every
+// candidate j < i a float32 score s_j (block sums rounded to float32, fused
+// multiply-adds) and a float32 magnitude a_j = sum_c |q_c| |k_c| come first.  With
+// u = 2^-24, d channels and z_j = sum_c (|q_c| + |k_c|) (float32 values),
+//   |s_j - score_j| <= e_j = 2 * 1.01 * ((d + 4) u a_j + 2^-149 z_j) + d * 2^-120
+// covers the float32 rounding of the inputs (relative u, or 2^-150 absolute below the
+// normal range), the float32 accumulation of s_j, a_j and z_j (one rounding per fused
+// step) and the float64 rounding of the contract score, with a factor of two to spare.
+// So score_j lies in [L_j, U_j] = [s_j - e_j, s_j + e_j].  If T is the n-th largest L_j,
+// n blocks score at least T, and any j with U_j < T scores below all of them: it cannot be
+// selected.  The contract scores of the remaining candidates (typically about n) decide
+// the ranking exactly as the definition does.  L_j and U_j are rounded outwards in float32.
+// A row whose float32 values are not all finite takes the contract score of every block.
+// Comparisons use integer keys that order like the scores: float64 comparisons would run
+// on the slow float64 pipe, and they outnumber the arithmetic in the ranking passes.
+#include <climits>
+
 #include "bpa_internal.h"
 #include "common.cuh"
 
@@ -22,7 +42,8 @@ __device__ __forceinline__ double ldd<__nv_bfloat16>(const __nv_bfloat16* p) {
     return static_cast<double>(__bfloat162float(*p));
 }
 
-// grid (nblk, H, B), one thread per channel
+// grid (nblk, H, B), one thread per channel: the float64 block sums of Q and K, and the
+// float32 copy of the key sums, channel-major [B, H, d, nblk] for the pre-filter
 template <typename T>
 __global__ void k_block_sums(const SelectArgs a) {
     const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -31,96 +52,185 @@ __global__ void k_block_sums(const SelectArgs a) {
     const T* K = static_cast<const T*>(a.k);
     for (int c = threadIdx.x; c < a.d; c += blockDim.x) {
         double sq = 0.0, sk = 0.0;
+#pragma unroll 8
         for (int r = 0; r < a.block; ++r) {
             const int64_t s = static_cast<int64_t>(i) * a.block + r;
             sq = __dadd_rn(sq, ldd(Q + b * a.qs[0] + s * a.qs[1] + h * a.qs[2] + c));
             sk = __dadd_rn(sk, ldd(K + b * a.ks[0] + s * a.ks[1] + h * a.ks[2] + c));
         }
-        const int64_t o = ((static_cast<int64_t>(b) * a.H + h) * nblk + i) * a.d + c;
+        const int64_t bh = static_cast<int64_t>(b) * a.H + h;
+        const int64_t o = (bh * nblk + i) * a.d + c;
         a.qsum[o] = sq;
         a.ksum[o] = sk;
+        a.kt32[(bh * a.d + c) * nblk + i] = __double2float_rn(sk);
     }
 }
 
-// Ranking: a larger score first, the lower block on equal scores; a NaN score
-// (non-finite inputs) ranks below every number, NaNs in block order.
-__device__ __forceinline__ bool better(double sa, int ja, double sb, int jb) {
-    const bool na = sa != sa, nb = sb != sb;
-    if (na != nb) return nb;
-    if (na) return ja < jb;
-    return sa > sb || (sa == sb && ja < jb);
+// The ranking, in integers (float64 comparisons run on GB300's slow float64 pipe):
+// a score maps to a signed 64-bit key that orders like the score, with both zeros equal
+// and a NaN below every number; equal keys go to the lower block.
+__device__ __forceinline__ long long rank_key(double s) {
+    const long long bits = __double_as_longlong(s);
+    const long long mag = bits & 0x7FFFFFFFFFFFFFFFll;
+    if (mag > 0x7FF0000000000000ll) return LLONG_MIN;   // NaN
+    if (mag == 0) return 0;                              // +0 and -0
+    return bits >= 0 ? bits : (bits ^ 0x7FFFFFFFFFFFFFFFll);
+}
+
+// A finite float32 as a signed 32-bit key in the same order (for the pre-filter threshold).
+__device__ __forceinline__ int f32_key(float f) {
+    const int bits = __float_as_int(f);
+    return bits >= 0 ? bits : (bits ^ 0x7FFFFFFF);
+}
+
+// The contract score of query block sums qs and key block sums ks.
+// (Unrolled so that several loads are in flight; the additions stay in channel order.)
+__device__ __forceinline__ double contract_dot(const double* qs, const double* ks, int d) {
+    double acc = 0.0;
+#pragma unroll 8
+    for (int c = 0; c < d; ++c) acc = __dadd_rn(acc, __dmul_rn(qs[c], ks[c]));
+    return acc;
 }
 
 constexpr int kSelWarps = 4;
+// Head dims up to this take the float32 pre-filter; wider ones score every block in
+// float64 (measured: at d = 512 the pre-filter's float32 pass costs more than it saves).
+constexpr int kPrefilterMaxD = 128;
 
-// one warp per (b, h, query block i); the scores of the i earlier blocks live
-// in shared memory (kSelWarps * nblk doubles), followed by one "taken" byte
-// per block and warp.
+// The untaken entry with the largest key (the lower index on equal keys); every lane gets it.
+template <typename K>
+__device__ __forceinline__ int warp_best(const K* key, const unsigned char* taken, int n, int lane, K& best) {
+    K bk = 0;
+    int bj = -1;
+    for (int j = lane; j < n; j += 32) {
+        if (taken[j]) continue;
+        const K k = key[j];
+        if (bj < 0 || k > bk) {   // ascending j per lane: a later equal key never wins
+            bk = k;
+            bj = j;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const K ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+        if (oj >= 0 && (bj < 0 || ok > bk || (ok == bk && oj < bj))) {
+            bk = ok;
+            bj = oj;
+        }
+    }
+    best = bk;
+    return bj;
+}
+
+// One warp per (b, h, query block i).  Shared memory per warp: keys[nblk] 64-bit words (the
+// 32-bit keys of the lower bounds L_j, then the 64-bit rank keys of the candidates' contract
+// scores), up[nblk] floats (the upper bounds U_j), taken[nblk] bytes, and the query
+// block's float32 sums q32[d].
 __global__ void __launch_bounds__(kSelWarps * 32) k_select(const SelectArgs a) {
-    extern __shared__ double sc_all[];
+    extern __shared__ long long sm_all[];
     const int nblk = a.S / a.block;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    long long* key64 = sm_all + static_cast<int64_t>(warp) * nblk;
+    int* key32 = reinterpret_cast<int*>(key64);
+    float* up = reinterpret_cast<float*>(sm_all + static_cast<int64_t>(kSelWarps) * nblk) + static_cast<int64_t>(warp) * nblk;
+    float* q32 = reinterpret_cast<float*>(sm_all + static_cast<int64_t>(kSelWarps) * nblk) +
+                 static_cast<int64_t>(kSelWarps) * nblk + static_cast<int64_t>(warp) * a.d;
+    unsigned char* taken = reinterpret_cast<unsigned char*>(q32 + static_cast<int64_t>(kSelWarps - warp) * a.d) +
+                           static_cast<int64_t>(warp) * nblk;
     const int64_t unit = static_cast<int64_t>(blockIdx.x) * kSelWarps + warp;
     if (unit >= static_cast<int64_t>(a.B) * a.H * nblk) return;
     const int i = static_cast<int>(unit % nblk);
     const int64_t bh = unit / nblk;
-    double* sc = sc_all + static_cast<int64_t>(warp) * nblk;
-    unsigned char* taken = reinterpret_cast<unsigned char*>(sc_all + static_cast<int64_t>(kSelWarps) * nblk) +
-                           static_cast<int64_t>(warp) * nblk;
     const double* qs = a.qsum + (bh * nblk + i) * a.d;
-    for (int j = lane; j < i; j += 32) {
-        const double* ks = a.ksum + (bh * nblk + j) * a.d;
-        double acc = 0.0;
-        for (int c = 0; c < a.d; ++c) acc = __dadd_rn(acc, __dmul_rn(qs[c], ks[c]));
-        sc[j] = acc;
-        taken[j] = 0;
-    }
-    __syncwarp();
     const int take = i < a.top_n ? i : a.top_n;
-    int pick0 = -1, pick1 = -1;   // pick t sits in lane t (t < 32) or lane t - 32
-    for (int t = 0; t < take; ++t) {
-        double bs = 0.0;
-        int bj = -1;
-        for (int j = lane; j < i; j += 32) {
-            if (taken[j]) continue;
-            const double s = sc[j];
-            if (bj < 0 || better(s, j, bs, bj)) {
-                bs = s;
-                bj = j;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const double os = __shfl_xor_sync(0xffffffffu, bs, o);
-            const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-            if (oj >= 0 && (bj < 0 || better(os, oj, bs, bj))) {
-                bs = os;
-                bj = oj;
-            }
-        }
-        if (t < 32 && lane == t) pick0 = bj;
-        if (t >= 32 && lane == t - 32) pick1 = bj;
-        __syncwarp();
-        // t < take <= i leaves an untaken candidate, so bj >= 0 here
-        if (lane == 0 && bj >= 0) taken[bj] = 1;
-        __syncwarp();
-    }
     int picks[64];
-    for (int t = 0; t < 32; ++t) {
-        const int x0 = __shfl_sync(0xffffffffu, pick0, t);
-        const int x1 = __shfl_sync(0xffffffffu, pick1, t);
-        picks[t] = x0;
-        picks[t + 32] = x1;
+    if (take > 0) {
+        // ---- float32 pre-filter: L_j and U_j for every earlier block, rounded outwards
+        for (int c = lane; c < a.d; c += 32) q32[c] = __double2float_rn(qs[c]);
+        __syncwarp();
+        const float* kt = a.kt32 + bh * a.d * static_cast<int64_t>(nblk);
+        const float cb = 2.0f * 1.01f * static_cast<float>(a.d + 4) * 5.9604645e-8f * 1.0001f;   // >= 2 * 1.01 * (d + 4) * 2^-24
+        const float zb = 2.0f * 1.01f * 1.4012985e-45f * 2.0f;                                // >= 2 * 1.01 * 2^-149
+        const float eb = static_cast<float>(a.d) * 7.5231638e-37f * 1.0001f;                    // >= d * 2^-120
+        bool finite = a.d <= kPrefilterMaxD;
+        for (int j = lane; j < (a.d <= kPrefilterMaxD ? i : 0); j += 32) {
+            float s = 0.f, m = 0.f, z = 0.f;
+#pragma unroll 8
+            for (int c = 0; c < a.d; ++c) {
+                const float x = q32[c], y = kt[static_cast<int64_t>(c) * nblk + j];
+                s = fmaf(x, y, s);
+                m = fmaf(fabsf(x), fabsf(y), m);
+                z += fabsf(x) + fabsf(y);
+            }
+            const float e = __fmaf_ru(cb, m, __fmaf_ru(zb, z, eb));
+            const float lo = __fsub_rd(s, e), hi = __fadd_ru(s, e);
+            finite = finite && isfinite(lo) && isfinite(hi);
+            key32[j] = isfinite(lo) ? f32_key(lo) : 0;
+            up[j] = hi;
+            taken[j] = 0;
+        }
+        const bool exact_all = !__all_sync(0xffffffffu, finite);   // also every row of a wide head
+        __syncwarp();
+        float T = -INFINITY;   // the take-th largest lower bound
+        if (!exact_all && take < i) {
+            for (int t = 0; t < take; ++t) {
+                int bk;
+                const int bj = warp_best(key32, taken, i, lane, bk);
+                if (lane == 0 && bj >= 0) taken[bj] = 1;
+                __syncwarp();
+                // the key decodes back to the float lower bound
+                const int bits = bk >= 0 ? bk : (bk ^ 0x7FFFFFFF);
+                T = __int_as_float(bits);
+            }
+        }
+        __syncwarp();
+        // ---- contract scores of the candidates (U_j >= T); the rest leave the ranking.  The
+        // candidates are first packed into a list (over the upper bounds, no longer needed),
+        // so that their float64 dot products run side by side, one per lane.
+        for (int j = lane; j < i; j += 32) taken[j] = (exact_all || take >= i || up[j] >= T) ? 0 : 1;
+        __syncwarp();
+        int* list = reinterpret_cast<int*>(up);
+        int count = 0;
+        for (int base = 0; base < i; base += 32) {
+            const int j = base + lane;
+            const bool cand = j < i && !taken[j];
+            const unsigned mask = __ballot_sync(0xffffffffu, cand);
+            if (cand) list[count + __popc(mask & ((1u << lane) - 1u))] = j;
+            count += __popc(mask);
+        }
+        __syncwarp();
+        for (int t = lane; t < count; t += 32) {
+            const int j = list[t];
+            key64[j] = rank_key(contract_dot(qs, a.ksum + (bh * nblk + j) * a.d, a.d));
+        }
+        __syncwarp();
+        // ---- exact ranking among the candidates
+        int pick0 = -1, pick1 = -1;   // pick t sits in lane t (t < 32) or lane t - 32
+        for (int t = 0; t < take; ++t) {
+            long long bk;
+            const int bj = warp_best(key64, taken, i, lane, bk);
+            if (t < 32 && lane == t) pick0 = bj;
+            if (t >= 32 && lane == t - 32) pick1 = bj;
+            __syncwarp();
+            // at least `take` candidates exist, so bj >= 0 here
+            if (lane == 0 && bj >= 0) taken[bj] = 1;
+            __syncwarp();
+        }
+        for (int t = 0; t < 32; ++t) {
+            picks[t] = __shfl_sync(0xffffffffu, pick0, t);
+            picks[t + 32] = __shfl_sync(0xffffffffu, pick1, t);
+        }
     }
     if (lane == 0) {
         for (int x = 1; x < take; ++x) {
-            const int key = picks[x];
+            const int k = picks[x];
             int y = x - 1;
-            while (y >= 0 && picks[y] > key) {
+            while (y >= 0 && picks[y] > k) {
                 picks[y + 1] = picks[y];
                 --y;
             }
-            picks[y + 1] = key;
+            picks[y + 1] = k;
         }
         int32_t* out = a.out + (bh * nblk + i) * a.top_n;
         for (int t = 0; t < a.top_n; ++t) out[t] = t < take ? picks[t] : -1;
@@ -128,6 +238,11 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_select(const SelectArgs a) {
 }
 
 }  // namespace
+
+size_t select_smem_bytes(int nblk, int d) {
+    return static_cast<size_t>(kSelWarps) * (static_cast<size_t>(nblk) * (sizeof(long long) + sizeof(float) + 1) +
+                                             sizeof(float) * static_cast<size_t>(d));
+}
 
 cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
     const int nblk = a.S / a.block;
@@ -140,7 +255,7 @@ cudaError_t launch_select(const SelectArgs& a, cudaStream_t s) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t units = static_cast<int64_t>(a.B) * a.H * nblk;
-    const size_t smem = (sizeof(double) + 1) * kSelWarps * static_cast<size_t>(nblk);
+    const size_t smem = select_smem_bytes(nblk, a.d);
     if (smem > 48 * 1024) {
         e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;

@@ -136,7 +136,7 @@ def test_select_rejects_bad_arguments(bpa):
     assert L.bpa_select_blocks(p, p, 0, 4, 8192, 8, 64, st, st, 33, 8, p, p, 1 << 30, None) == 1
     assert L.bpa_select_blocks(p, p, 0, 4, 8192, 8, 64, st, st, 32, 0, p, p, 1 << 30, None) == 1
     assert L.bpa_select_blocks(p, p, 0, 4, 8192, 8, 64, st, st, 32, 8, p, p, 16, None) == 3
-    assert L.bpa_select_workspace_size(4, 8192, 8, 64, 32) == 256 + 2 * 4 * 8 * 256 * 64 * 8
+    assert L.bpa_select_workspace_size(4, 8192, 8, 64, 32) == 256 + 2 * 4 * 8 * 256 * 64 * 8 + 4 * 8 * 256 * 64 * 4
     # more blocks per sequence than the selection kernel holds
     assert L.bpa_select_blocks(p, p, 0, 1, 4097 * 8, 1, 8, st, st, 8, 4, p, p, 1 << 40, None) == 2
 

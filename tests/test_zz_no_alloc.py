@@ -32,7 +32,7 @@ def _dev(a):
 
 
 def test_noalloc_selection_matches_workspace_entry_point(bpa):
-    B, S, H, d, bs, n = 4, 8192, 8, 64, 32, 8   # 8 MiB of block sums: inside the 16 MiB buffer
+    B, S, H, d, bs, n = 4, 8192, 8, 64, 32, 8   # 10 MiB of block sums: inside the 16 MiB buffer
     first = draw([(B, S, H, d), (B, S, H, d)], 4, "bf16")
     second = draw([(B, S, H, d), (B, S, H, d)], 5, "bf16")
     for q_np, k_np in (first, second):          # two calls in a row share the buffer
