@@ -16,9 +16,10 @@ namespace bpa {
 namespace {
 
 constexpr int kMaxD = 512;
-constexpr int kRows = 16;   // rows per CTA
-constexpr int kWarps = 4;   // warps per CTA
-// KP: channels per lane (lane owns dims lane + 32 i, i < KP): 8 up to 256 channels, 16 above
+constexpr int kWarps = 4;       // warps per CTA
+constexpr int kRows = kWarps;   // rows per CTA: one per warp (small problems still fill the GPU)
+// KP: channels per lane (lane owns dims lane + 32 i, i < KP): 2 up to 64 channels, 4 up to
+// 128, 8 up to 256, 16 above
 
 template <typename T>
 __device__ __forceinline__ float ldf(const T* p);
@@ -471,12 +472,28 @@ cudaError_t bwd_simt_kp(const BwdArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// Channels per lane for the wider of the two head dims.
+static int simt_kp(const Problem& P) {
+    const int w = P.d > P.dv ? P.d : P.dv;
+    return w <= 64 ? 2 : (w <= 128 ? 4 : (w <= 256 ? 8 : 16));
+}
+
 cudaError_t launch_fwd_simt(const FwdArgs& a, cudaStream_t s) {
-    return (a.P.d > 256 || a.P.dv > 256) ? fwd_simt_kp<16>(a, s) : fwd_simt_kp<8>(a, s);
+    switch (simt_kp(a.P)) {
+        case 2: return fwd_simt_kp<2>(a, s);
+        case 4: return fwd_simt_kp<4>(a, s);
+        case 8: return fwd_simt_kp<8>(a, s);
+        default: return fwd_simt_kp<16>(a, s);
+    }
 }
 
 cudaError_t launch_bwd_simt(const BwdArgs& a, cudaStream_t s) {
-    return (a.P.d > 256 || a.P.dv > 256) ? bwd_simt_kp<16>(a, s) : bwd_simt_kp<8>(a, s);
+    switch (simt_kp(a.P)) {
+        case 2: return bwd_simt_kp<2>(a, s);
+        case 4: return bwd_simt_kp<4>(a, s);
+        case 8: return bwd_simt_kp<8>(a, s);
+        default: return bwd_simt_kp<16>(a, s);
+    }
 }
 
 }  // namespace bpa
