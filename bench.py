@@ -226,7 +226,7 @@ def time_extra_workloads(bpa, dev, peak_tf):
         g.manual_seed(seed)
         return torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(dtype)
 
-    def fwd_bwd(w, steps, warmup, deterministic=False):
+    def fwd_bwd(w, steps, warmup, deterministic=False, dropout_p=0.0):
         dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
         q = rnd((w.B, w.S, w.Hq, w.d), dt, w.seed)
         k = rnd((w.B, w.S, w.Hkv, w.d), dt, w.seed + 1)
@@ -238,6 +238,8 @@ def time_extra_workloads(bpa, dev, peak_tf):
             bias[..., w.S - w.pad_tail:] = -1e9
         kw = dict(causal=w.causal, window=w.window, bias=bias, query_chunk=w.query_chunk, key_chunk=w.key_chunk,
                   ring_size=w.ring_size, deterministic=deterministic)
+        if dropout_p:
+            kw.update(dropout_p=dropout_p, dropout_seed=w.seed)
         tok_q = tok_k = w.B * w.S
         if w.seqlens_q:
             lens_q = list(w.seqlens_q)
@@ -287,6 +289,8 @@ def time_extra_workloads(bpa, dev, peak_tf):
     out[VARLEN_CAUSAL.name] = fwd_bwd(VARLEN_CAUSAL, 10, 3)
     # the headline workload with the determinism knob (per-key-tile dQ slices, ordered sum)
     out[GQA_CAUSAL.name + "_deterministic"] = fwd_bwd(GQA_CAUSAL, 10, 3, deterministic=True)
+    # the headline workload with attention dropout (Philox4x32-10 keep decisions in the kernels)
+    out[GQA_CAUSAL.name + "_dropout0.1"] = fwd_bwd(GQA_CAUSAL, 10, 3, dropout_p=0.1)
 
     def block_selected(w):
         q = rnd((w.B, w.S, w.Hq, w.d), torch.bfloat16, w.seed)
