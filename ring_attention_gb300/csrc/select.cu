@@ -20,8 +20,10 @@
 // step) and the float64 rounding of the contract score, with a factor of two to spare.
 // So score_j lies in [L_j, U_j] = [s_j - e_j, s_j + e_j].  If T is the n-th largest L_j,
 // n blocks score at least T, and any j with U_j < T scores below all of them: it cannot be
-// selected.  The contract scores of the remaining candidates (typically about n) decide
-// the ranking exactly as the definition does.  L_j and U_j are rounded outwards in float32.
+// selected.  When exactly n candidates remain they are the selection (every other block
+// scores below each of them, and the output lists the selected blocks in block order), so
+// no contract score is needed; otherwise the contract scores of the candidates decide the
+// ranking exactly as the definition does.  L_j and U_j are rounded outwards in float32.
 // A row whose float32 values are not all finite takes the contract score of every block.
 // Comparisons use integer keys that order like the scores: float64 comparisons would run
 // on the slow float64 pipe, and they outnumber the arithmetic in the ranking passes.
@@ -42,22 +44,79 @@ __device__ __forceinline__ double ldd<__nv_bfloat16>(const __nv_bfloat16* p) {
     return static_cast<double>(__bfloat162float(*p));
 }
 
+// A float32 or bfloat16 value as sign, significand and the exponent of its last bit
+// (value = (-1)^neg * mant * 2^w), with w of a subnormal that of the smallest normal.
+struct Parts {
+    uint32_t mant;
+    int w;
+    bool neg, finite;
+};
+template <typename T>
+__device__ __forceinline__ Parts parts(const T* p);
+template <>
+__device__ __forceinline__ Parts parts<float>(const float* p) {
+    const uint32_t u = __float_as_uint(*p), e = (u >> 23) & 0xFFu, f = u & 0x7FFFFFu;
+    return {e ? (f | 0x800000u) : f, static_cast<int>(e ? e : 1u) - 150, (u >> 31) != 0, e != 0xFFu};
+}
+template <>
+__device__ __forceinline__ Parts parts<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const uint32_t u = __bfloat16_as_ushort(*p), e = (u >> 7) & 0xFFu, f = u & 0x7Fu;
+    return {e ? (f | 0x80u) : f, static_cast<int>(e ? e : 1u) - 134, (u >> 15) != 0, e != 0xFFu};
+}
+template <typename T>
+constexpr int kMantBits = sizeof(T) == 4 ? 24 : 8;
+
+// The float64 sum ((0 + x_0) + x_1) + ... of one channel over the rows of a block, x_r at
+// p + r * stride.  When every nonzero x_r is a multiple of 2^wmin and below 2^(wmax + m) in
+// magnitude (m significand bits) with wmax - wmin + m + ceil(log2 rows) <= 53, every partial
+// sum is a multiple of 2^wmin below 2^(53 + wmin): each float64 addition is exact and the
+// sum equals the exact one, which 64-bit integer additions of the significands (scaled to
+// the common last bit) give without the float64 pipe.  Other columns (a wide exponent
+// range, an infinity or a NaN) take the float64 additions in row order.
+template <typename T>
+__device__ __forceinline__ double column_sum(const T* p, int64_t stride, int rows, int lg_rows) {
+    int wmin = INT_MAX, wmax = INT_MIN;
+    bool finite = true;
+#pragma unroll 8
+    for (int r = 0; r < rows; ++r) {
+        const Parts x = parts(p + r * stride);
+        finite = finite && x.finite;
+        if (x.mant) {
+            wmin = min(wmin, x.w);
+            wmax = max(wmax, x.w);
+        }
+    }
+    if (finite && wmin == INT_MAX) return 0.0;   // all zeros: +0, as the float64 additions give
+    if (finite && wmax - wmin + kMantBits<T> + lg_rows <= 53) {
+        long long acc = 0;
+#pragma unroll 8
+        for (int r = 0; r < rows; ++r) {
+            const Parts x = parts(p + r * stride);
+            if (!x.mant) continue;   // a zero (its w may lie below wmin)
+            const long long m = static_cast<long long>(x.mant) << (x.w - wmin);
+            acc += x.neg ? -m : m;
+        }
+        // |acc| < 2^53: exact as a float64, and the scaling by 2^wmin (a normal float64) too
+        return __dmul_rn(__ll2double_rn(acc), __longlong_as_double(static_cast<long long>(wmin + 1023) << 52));
+    }
+    double s = 0.0;
+#pragma unroll 8
+    for (int r = 0; r < rows; ++r) s = __dadd_rn(s, ldd(p + r * stride));
+    return s;
+}
+
 // grid (nblk, H, B), one thread per channel: the float64 block sums of Q and K, and the
 // float32 copy of the key sums, channel-major [B, H, d, nblk] for the pre-filter
 template <typename T>
 __global__ void k_block_sums(const SelectArgs a) {
     const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int nblk = a.S / a.block;
-    const T* Q = static_cast<const T*>(a.q);
-    const T* K = static_cast<const T*>(a.k);
+    const int lg_rows = a.block > 1 ? 32 - __clz(a.block - 1) : 0;
+    const T* Q = static_cast<const T*>(a.q) + b * a.qs[0] + static_cast<int64_t>(i) * a.block * a.qs[1] + h * a.qs[2];
+    const T* K = static_cast<const T*>(a.k) + b * a.ks[0] + static_cast<int64_t>(i) * a.block * a.ks[1] + h * a.ks[2];
     for (int c = threadIdx.x; c < a.d; c += blockDim.x) {
-        double sq = 0.0, sk = 0.0;
-#pragma unroll 8
-        for (int r = 0; r < a.block; ++r) {
-            const int64_t s = static_cast<int64_t>(i) * a.block + r;
-            sq = __dadd_rn(sq, ldd(Q + b * a.qs[0] + s * a.qs[1] + h * a.qs[2] + c));
-            sk = __dadd_rn(sk, ldd(K + b * a.ks[0] + s * a.ks[1] + h * a.ks[2] + c));
-        }
+        const double sq = column_sum(Q + c, a.qs[1], a.block, lg_rows);
+        const double sk = column_sum(K + c, a.ks[1], a.block, lg_rows);
         const int64_t bh = static_cast<int64_t>(b) * a.H + h;
         const int64_t o = (bh * nblk + i) * a.d + c;
         a.qsum[o] = sq;
@@ -93,9 +152,9 @@ __device__ __forceinline__ double contract_dot(const double* qs, const double* k
 }
 
 constexpr int kSelWarps = 4;
-// Head dims up to this take the float32 pre-filter; wider ones score every block in
-// float64 (measured: at d = 512 the pre-filter's float32 pass costs more than it saves).
-constexpr int kPrefilterMaxD = 128;
+// Head dims up to this take the float32 pre-filter (every head dim the selection accepts);
+// wider ones would score every block in float64.
+constexpr int kPrefilterMaxD = 512;
 
 // The untaken entry with the largest key (the lower index on equal keys); every lane gets it.
 template <typename K>
@@ -154,21 +213,37 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_select(const SelectArgs a) {
         const float zb = 2.0f * 1.01f * 1.4012985e-45f * 2.0f;                                // >= 2 * 1.01 * 2^-149
         const float eb = static_cast<float>(a.d) * 7.5231638e-37f * 1.0001f;                    // >= d * 2^-120
         bool finite = a.d <= kPrefilterMaxD;
-        for (int j = lane; j < (a.d <= kPrefilterMaxD ? i : 0); j += 32) {
-            float s = 0.f, m = 0.f, z = 0.f;
-#pragma unroll 8
+        const int lim = a.d <= kPrefilterMaxD ? i : 0;
+        // four blocks per lane at a time (j0, j0 + 32, j0 + 64, j0 + 96), channels outermost,
+        // so that four independent loads are in flight per channel
+        for (int j0 = lane; j0 < lim; j0 += 128) {
+            float s[4] = {0.f, 0.f, 0.f, 0.f}, m[4] = {0.f, 0.f, 0.f, 0.f}, z[4] = {0.f, 0.f, 0.f, 0.f};
+            int jc[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) jc[w] = min(j0 + 32 * w, lim - 1);   // in range; unused if clamped
+#pragma unroll 4
             for (int c = 0; c < a.d; ++c) {
-                const float x = q32[c], y = kt[static_cast<int64_t>(c) * nblk + j];
-                s = fmaf(x, y, s);
-                m = fmaf(fabsf(x), fabsf(y), m);
-                z += fabsf(x) + fabsf(y);
+                const float x = q32[c];
+                const float* row = kt + static_cast<int64_t>(c) * nblk;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float y = row[jc[w]];
+                    s[w] = fmaf(x, y, s[w]);
+                    m[w] = fmaf(fabsf(x), fabsf(y), m[w]);
+                    z[w] += fabsf(x) + fabsf(y);
+                }
             }
-            const float e = __fmaf_ru(cb, m, __fmaf_ru(zb, z, eb));
-            const float lo = __fsub_rd(s, e), hi = __fadd_ru(s, e);
-            finite = finite && isfinite(lo) && isfinite(hi);
-            key32[j] = isfinite(lo) ? f32_key(lo) : 0;
-            up[j] = hi;
-            taken[j] = 0;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int j = j0 + 32 * w;
+                if (j >= lim) break;
+                const float e = __fmaf_ru(cb, m[w], __fmaf_ru(zb, z[w], eb));
+                const float lo = __fsub_rd(s[w], e), hi = __fadd_ru(s[w], e);
+                finite = finite && isfinite(lo) && isfinite(hi);
+                key32[j] = isfinite(lo) ? f32_key(lo) : 0;
+                up[j] = hi;
+                taken[j] = 0;
+            }
         }
         const bool exact_all = !__all_sync(0xffffffffu, finite);   // also every row of a wide head
         __syncwarp();
@@ -200,6 +275,15 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_select(const SelectArgs a) {
             count += __popc(mask);
         }
         __syncwarp();
+        if (count == take) {
+            // The set is decided without a contract score: the take blocks with the largest
+            // lower bounds have U_j >= L_j >= T, so they are the whole list, and every other
+            // block scores below T, i.e. below each of them (or all blocks are taken).  The
+            // list is in block order, as the output is.
+            int32_t* out = a.out + (bh * nblk + i) * a.top_n;
+            for (int t = lane; t < a.top_n; t += 32) out[t] = t < take ? list[t] : -1;
+            return;
+        }
         for (int t = lane; t < count; t += 32) {
             const int j = list[t];
             key64[j] = rank_key(contract_dot(qs, a.ksum + (bh * nblk + j) * a.d, a.d));

@@ -317,6 +317,41 @@ def test_select_blocks_near_ties(bpa, ora):
     np.testing.assert_array_equal(idx.cpu().numpy(), ora.select_blocks(q, k, block_size=bs, top_n=n))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_select_blocks_sum_rounding(bpa, ora, dtype):
+    # block sums whose float64 additions in row order round (2^60 + 2 - 2^60 = 0, not 2) or
+    # are exact only just inside the range the kernel sums with integers (a span of 42 bits
+    # between the largest and smallest last bit for bfloat16 over 8 rows, 26 for float32)
+    # and just outside it; the ranking depends on every one of these sums
+    B, S, H, d, bs, n = 1, 256, 1, 16, 8, 4
+    big_in, small_in = (2.0 ** 42, 1.0 + 2.0 ** -7) if dtype == "bf16" else (2.0 ** 26, 1.0 + 2.0 ** -23)
+    q = np.zeros((B, S, H, d), np.float32)
+    k = np.zeros((B, S, H, d), np.float32)
+    q[0, ::bs, 0, 0] = 1.0
+    for j in range(S // bs):
+        r = j * bs
+        cls = j % 4
+        if cls == 0:     # rounds away: the contract sum is 0 (the exact sum, 2, would rank first)
+            k[0, r:r + 3, 0, 0] = (2.0 ** 60, 2.0, -(2.0 ** 60))
+        elif cls == 1:   # integer path at its widest span: big + small - big = small exactly
+            k[0, r:r + 3, 0, 0] = (big_in, small_in, -big_in)
+        elif cls == 2:
+            k[0, r + 5, 0, 0] = 1.0
+        else:            # one bit wider: the float64 additions (exact here as well)
+            k[0, r:r + 3, 0, 0] = (2 * big_in, small_in, -2 * big_in)
+        k[0, r + 7, 0, 1 + j % (d - 1)] = 0.25   # a second channel the query does not weigh
+    if dtype == "bf16":
+        q = (q.view(np.uint32) >> 16).astype(np.uint16)
+        k = (k.view(np.uint32) >> 16).astype(np.uint16)
+    idx = bpa.bpa_select_blocks(dev(q), dev(k), block_size=bs, top_n=n)
+    torch.cuda.synchronize()
+    ref = ora.select_blocks(q, k, block_size=bs, top_n=n)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref)
+    # the float64 additions in row order rank the boundary classes first (ties: lower block)
+    # and the rounded-away class last
+    assert ref[0, 0, -1].tolist() == [1, 3, 5, 7]
+
+
 def test_select_blocks_ties(bpa, ora):
     # block sums with many exactly equal scores: ties must keep the lower block
     B, S, H, d, bs = 1, 256, 1, 8, 8
