@@ -16,10 +16,12 @@
 //     flight while the current ones are computed.
 //   - Two softmax warpgroups take alternate heads (the two heads of a pair): the tensor core
 //     works on one head while the other's softmax and epilogue run.
-// Per head the fold is the same as the general kernel's ("bpt.py", scan_kv_block): running
-// max, exp correction, numerator and denominator, lazily rescaled.
-// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256, 256+d), O1 [384, 384+d); P is
-// written over its S tile as bf16 pairs and read by the P V product from TMEM.
+//   - A head's whole band (both key tiles, 256 keys) is scored at once, so its softmax is one
+//     max pass and one exponential pass with the exact row max as the reference: the fold
+//     of "bpt.py" scan_kv_block over the band's key blocks, with nothing to rescale.
+// TMEM (512 columns): region i = [256 i, 256 i + 256) belongs to warpgroup i: S_i (one or two
+// 128-column tiles), then P_i as bf16 pairs over its first 128 columns (read by the P V
+// product from TMEM) and O_i in its columns [128, 128 + d), over scores already read.
 // Roles (320 threads): warps 0-3 / 4-7 softmax of the pair's first / second head (thread =
 // row = TMEM lane), warp 8 TMA producer (lane 0), warp 9 MMA issuer and TMEM owner.
 // Every wait is bounded; on a timeout the CTA drains its copies and products, frees TMEM
@@ -113,14 +115,15 @@ __device__ __forceinline__ int64_t tile_key(const Problem& P, int b, int hkv, in
     return (static_cast<int64_t>(b) * P.Hkv + hkv) * nkt + kt;
 }
 
-// Softmax passes over one row of a 128-key tile, 32 columns at a time (few live registers:
-// a warp runs one chunk after the other).  A chunk whose keys lie outside every row of the
+// Softmax passes over one row of the band's scores (one or two 128-key tiles), 32 columns at
+// a time (few live registers: a warp runs one chunk after the other).  A chunk whose keys lie outside every row of the
 // warp is skipped (its P columns are written as zeros); a chunk inside every row's range
 // needs no elementwise mask.  Scores are in log2 units, x = S * scale * log2(e).
 struct BandRow {
     uint32_t tS;            // TMEM address of this thread's row of S (and of P over it)
     float sl2;              // scale * log2(e)
-    int k0, kmin, kmax;     // first key of the tile, allowed keys of the row
+    int k0, kmin, kmax;     // first key of the band, allowed keys of the row
+    int nch;                // 32-column chunks of S (4 per key tile)
 };
 
 // 0: every key of chunk cc is outside every row's range, 1: inside every row's range,
@@ -136,7 +139,7 @@ __device__ __forceinline__ int chunk_kind(const BandRow& R, int cc) {
 __device__ __forceinline__ float band_row_max(const BandRow& R) {
     float mt = -INFINITY;
 #pragma unroll 1
-    for (int cc = 0; cc < BN / 32; ++cc) {
+    for (int cc = 0; cc < R.nch; ++cc) {
         const int kind = chunk_kind(R, cc);
         if (kind == 0) continue;
         uint32_t r[32];
@@ -159,14 +162,14 @@ __device__ __forceinline__ float band_row_max(const BandRow& R) {
     return mt;
 }
 
-// pass 2: P = exp2(x - mref) as bf16 pairs over the first 64 columns of the row (chunk cc
-// reads S columns [32cc, 32cc + 32) and writes P columns [16cc, 16cc + 16), which were
-// read by an earlier chunk); returns the row sum of P
+// pass 2: P = exp2(x - mref) as bf16 pairs over the first 16 nch columns of the row (chunk
+// cc reads S columns [32cc, 32cc + 32) and writes P columns [16cc, 16cc + 16), which were
+// read by this or an earlier chunk); returns the row sum of P
 __device__ __forceinline__ float band_row_exp(const BandRow& R, float mref) {
     const uint64_t sl2x2 = f2_pack(R.sl2, R.sl2), negm2 = f2_pack(-mref, -mref);
     float sum = 0.f;
 #pragma unroll 1
-    for (int cc = 0; cc < BN / 32; ++cc) {
+    for (int cc = 0; cc < R.nch; ++cc) {
         const int kind = chunk_kind(R, cc);
         uint32_t pk[16];
         if (kind == 0) {
@@ -318,14 +321,14 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
     } else if (warp == C::kMma) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp runs the loop with warp-uniform operands; one elected lane issues.
-        // Per pair (heads t0 = 2p, t1 = 2p + 1 of the CTA's sequence) and key tile j:
-        //   [P_i(j) ready] P_i V_j -> O_i, then S_i(j+1) = Q_i K_(j+1)^T, for i = 0, 1.
-        // Products execute in issue order, so S_i(j+1) overwrites P_i(j) only after
-        // P_i(j) V_j has read it.
+        // Per pair (heads t0 = 2p, t1 = 2p + 1 of the CTA's sequence, warpgroups 0, 1):
+        //   [region i drained]  S_i = Q_i [K_lo .. K_lo+n-1]^T  (one N = 128 product per key tile)
+        //   [P_i ready]         O_i = P_i [V_lo .. V_lo+n-1]
+        // for i = 0, 1.  Region i holds S_i, then P_i over its first 128 columns and O_i in
+        // columns [128, 128 + d): P_i V reads P_i and writes O_i over scores the softmax has read.
         Two<int64_t> res{-1, -1};
         Two<int> loads{0, 0};
         Two<int> seen{0, 0};           // slot loads whose arrival has been observed
-        Two<int> np{0, 0};             // P phases consumed per warpgroup
         int64_t prev_group = -1;
         int qpos = 0, pair = 0;
         bool ok = true;
@@ -349,9 +352,8 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
             // keep, right after the last product that reads it.
             BandPair N = T;
             N.next(P, nqt);
-            const bool last_of_group = u + 1 >= uend || N.group != T.group;
             Two<bool> release{false, false};
-            if (last_of_group && u + 1 < uend) {
+            if (u + 1 < uend && N.group != T.group) {
                 int nlo, nn;
                 band_tiles(P.S, P.causal, P.wl, P.wr, N.qt, nlo, nn);
                 for (int j = 0; j < n; ++j) {
@@ -371,65 +373,46 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
                 }
                 return true;
             };
-            const int st0 = qpos % C::NSQ, st1 = (qpos + 1) % C::NSQ;
-            ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_QF + st0), (qpos / C::NSQ) & 1, abort_flag, a.status, 0x91)) &&
-                 __all_sync(0xffffffffu,
-                            mbar_wait(BAR(C::B_QF + st1), ((qpos + 1) / C::NSQ) & 1, abort_flag, a.status, 0x92)) &&
-                 ensure_tile(0);
-            if (!ok) break;
-            tc_fence_after();
-            const Two<int> stq{st0, st1};
-            auto issue_s = [&](int i, int j) {
-                const int s = (lo + j) & 1;
+            const Two<int> stq{qpos % C::NSQ, (qpos + 1) % C::NSQ};
+            for (int i = 0; ok && i < 2; ++i) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(BAR(C::B_QF + stq.get(i)), ((qpos + i) / C::NSQ) & 1, abort_flag, a.status, 0x91 + i));
+                for (int j = 0; ok && j < n; ++j) ok = ensure_tile(j);
+                // the previous pair's epilogue must have read O_i before S_i overwrites region i
+                if (ok && pair > 0)
+                    ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_OE + i), (pair - 1) & 1, abort_flag, a.status, 0x94));
+                if (!ok) break;
+                tc_fence_after();
                 const uint64_t qd = sdesc_sw128(sb + C::OFF_Q + stq.get(i) * C::Q_BYTES, 16, 1024);
-                const uint64_t kd = sdesc_sw128(sb + C::OFF_K + s * C::KV_BYTES, 16, 1024);
-                const uint32_t d_tmem = tmem + i * BN;
+                for (int j = 0; j < n; ++j) {
+                    const uint64_t kd = sdesc_sw128(sb + C::OFF_K + ((lo + j) & 1) * C::KV_BYTES, 16, 1024);
+                    const uint32_t d_tmem = tmem + i * 256 + j * BN;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::SUB + (kk & 3) * 32;
-                    tc_mma_ss_w(d_tmem, sdesc_advance(qd, off), sdesc_advance(kd, off), C::IDESC_S, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * C::SUB + (kk & 3) * 32;
+                        tc_mma_ss_w(d_tmem, sdesc_advance(qd, off), sdesc_advance(kd, off), C::IDESC_S, kk > 0);
+                    }
                 }
                 tc_commit_w(BAR(C::B_S + i));
-                if (j == n - 1) tc_commit_w(BAR(C::B_QE + stq.get(i)));   // the head's last score product
-            };
-            auto issue_pv = [&](int i, int j) {
-                const int s = (lo + j) & 1;
-                const uint64_t vd = sdesc_sw128(sb + C::OFF_V + s * C::KV_BYTES, C::SUB, 1024);
-                const uint32_t t_p = tmem + i * BN, t_o = tmem + 2 * BN + i * 128;
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    tc_mma_ts_w(t_o, t_p + kk * 8, sdesc_advance(vd, kk * 2048), C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
-            };
-            issue_s(0, 0);
-            issue_s(1, 0);
-            for (int j = 0; ok && j < n; ++j) {
-                for (int i = 0; i < 2; ++i) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_P + i), np.get(i) & 1, abort_flag, a.status, 0x93))) {
-                        ok = false;
-                        break;
-                    }
-                    np.set(i, np.get(i) + 1);
-                    // the previous pair's epilogue must have read O_i before this pair's first P V
-                    if (j == 0 && pair > 0 &&
-                        !__all_sync(0xffffffffu, mbar_wait(BAR(C::B_OE + i), (pair - 1) & 1, abort_flag, a.status, 0x94))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_pv(i, j);
-                    if (j + 1 < n) {
-                        if (!ensure_tile(j + 1)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_s(i, j + 1);
-                    } else {
-                        tc_commit_w(BAR(C::B_O + i));
-                    }
-                }
-                if (ok && release.get(j)) tc_commit_w(BAR(C::B_KVE + ((lo + j) & 1)));
+                tc_commit_w(BAR(C::B_QE + stq.get(i)));   // the head's only score product
             }
+            for (int i = 0; ok && i < 2; ++i) {
+                ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_P + i), pair & 1, abort_flag, a.status, 0x93));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t t_r = tmem + i * 256;
+                for (int j = 0; j < n; ++j) {
+                    const uint64_t vd = sdesc_sw128(sb + C::OFF_V + ((lo + j) & 1) * C::KV_BYTES, C::SUB, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc_mma_ts_w(t_r + 128, t_r + j * (BN / 2) + kk * 8, sdesc_advance(vd, kk * 2048), C::IDESC_PV,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit_w(BAR(C::B_O + i));
+            }
+            if (ok)
+                for (int j = 0; j < n; ++j)
+                    if (release.get(j)) tc_commit_w(BAR(C::B_KVE + ((lo + j) & 1)));
             qpos += 2;
         }
         // drain: all MMAs issued by this warp complete before TMEM is freed
@@ -440,10 +423,10 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
         const int wg = warp >> 2;             // head of the pair taken by this warpgroup
         const int t = threadIdx.x & 127;      // row within the query tile == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + wg * BN + lane_base, tO = tmem + 2 * BN + wg * 128 + lane_base;
+        const uint32_t tS = tmem + wg * 256 + lane_base, tO = tS + 128;
         const float sl2 = P.scale * kLog2e;
         bool aborted = false;
-        int cs = 0, pair = 0;                 // S tiles seen, pairs done
+        int pair = 0;
         BandPair T;
         T.init(P, nqt, u0);
         for (int64_t u = u0; !aborted && u < uend; ++u, ++pair, T.next(P, nqt)) {
@@ -455,44 +438,17 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
             if (P.causal) kmax = min(kmax, q);
             if (P.wr >= 0) kmax = min(kmax, q + P.wr);
             if (P.wl >= 0) kmin = max(kmin, q - P.wl);
-            float m_used = -INFINITY, m_true = -INFINITY, lsum = 0.f;
-            for (int j = 0; j < n; ++j, ++cs) {
-                const int k0 = (lo + j) * BN;
-                if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_S + wg), cs & 1, abort_flag, a.status, 0xA0))) {
-                    aborted = true;
-                    break;
-                }
-                tc_fence_after();
-                const BandRow R{tS, sl2, k0, kmin, kmax};
-                // two passes: the tile max, then P with the (lazily moved) reference
-                const float mt = band_row_max(R);
-                m_true = fmaxf(m_true, mt);
-                float fac = 1.f;
-                bool o_resc = false;
-                if (mt > m_used + kTau) {
-                    fac = m_used == -INFINITY ? 0.f : ex2(m_used - mt);
-                    o_resc = j > 0 && m_used != -INFINITY;
-                    m_used = mt;
-                    lsum *= fac;
-                }
-                if (__any_sync(0xffffffffu, o_resc)) {
-                    // S(j) is complete, so every earlier P V has been added to O
-                    const float f = o_resc ? fac : 1.f;
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t r[32];
-                        tmem_ld32(tO + cc * 32, r);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
-                        tmem_st32(tO + cc * 32, r);
-                    }
-                }
-                const float mref = m_used == -INFINITY ? 0.f : m_used;
-                lsum += band_row_exp(R, mref);
-                tc_fence_before();
-                mbar_arrive(BAR(C::B_P + wg));
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_S + wg), pair & 1, abort_flag, a.status, 0xA0))) {
+                aborted = true;
+                break;
             }
-            if (aborted) break;
+            tc_fence_after();
+            // the whole band in one S: two passes, the row max, then P with it as the reference
+            const BandRow R{tS, sl2, lo * BN, kmin, kmax, n * (BN / 32)};
+            const float mt = band_row_max(R);
+            const float lsum = band_row_exp(R, mt == -INFINITY ? 0.f : mt);
+            tc_fence_before();
+            mbar_arrive(BAR(C::B_P + wg));
             // ------------------------------------------------------------ epilogue
             if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_O + wg), pair & 1, abort_flag, a.status, 0xA1))) {
                 aborted = true;
@@ -501,7 +457,6 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
             tc_fence_after();
             const int qc = min(q, P.S - 1);
             const int64_t mi = (static_cast<int64_t>(T.b) * P.Hq + h) * P.S + qc;
-            const float rel = m_true == -INFINITY ? 0.f : ex2(m_used - m_true);
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.os[0] + static_cast<int64_t>(qc) * P.os[1] +
                                h * P.os[2];
@@ -509,6 +464,11 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t r[32];
                 tmem_ld32(tO + cc * 32, r);
+                if (cc == D / 32 - 1) {
+                    // every column of O_wg has been read: the next pair's S may overwrite the region
+                    tc_fence_before();
+                    mbar_arrive(BAR(C::B_OE + wg));
+                }
                 if (q < P.S) {
                     uint4* dst = reinterpret_cast<uint4*>(O + cc * 32);
 #pragma unroll
@@ -523,12 +483,9 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
                 }
             }
             if (q < P.S) {
-                a.m[mi] = m_true == -INFINITY ? -INFINITY : m_true * kLn2;
-                a.l[mi] = lsum * rel;
+                a.m[mi] = mt == -INFINITY ? -INFINITY : mt * kLn2;
+                a.l[mi] = lsum;
             }
-            // O_wg has been read: the next pair's first P V may overwrite it
-            tc_fence_before();
-            mbar_arrive(BAR(C::B_OE + wg));
         }
     }
 
