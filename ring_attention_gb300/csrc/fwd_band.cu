@@ -116,50 +116,72 @@ __device__ __forceinline__ int64_t tile_key(const Problem& P, int b, int hkv, in
 }
 
 // Softmax passes over one row of the band's scores (one or two 128-key tiles), 32 columns at
-// a time (few live registers: a warp runs one chunk after the other).  A chunk whose keys lie outside every row of the
-// warp is skipped (its P columns are written as zeros); a chunk inside every row's range
-// needs no elementwise mask.  Scores are in log2 units, x = S * scale * log2(e).
+// a time (few live registers: a warp runs one chunk after the other).  A chunk whose keys lie
+// outside every row of the warp is skipped (its P columns are written as zeros); a chunk
+// inside every row's range needs no mask; the others take a per-row bit mask of allowed keys.
+// The allowed range [kmin, kmax] of a row never moves left as the row grows, so lane 0 and
+// lane 31 hold the warp's extreme bounds and a chunk's kind needs no vote.  The maxima and
+// sums run as two independent chains.  Scores are in log2 units, x = S * scale * log2(e).
 struct BandRow {
     uint32_t tS;            // TMEM address of this thread's row of S (and of P over it)
     float sl2;              // scale * log2(e)
     int k0, kmin, kmax;     // first key of the band, allowed keys of the row
     int nch;                // 32-column chunks of S (4 per key tile)
+    int lo_any, hi_any;     // warp-uniform: the union of the warp's rows' ranges
+    int lo_all, hi_all;     // and their intersection
 };
+
+__device__ __forceinline__ BandRow band_row(uint32_t tS, float sl2, int k0, int kmin, int kmax, int nch) {
+    BandRow R{tS, sl2, k0, kmin, kmax, nch, 0, 0, 0, 0};
+    R.lo_any = __shfl_sync(0xffffffffu, kmin, 0);
+    R.hi_any = __shfl_sync(0xffffffffu, kmax, 31);
+    R.lo_all = __shfl_sync(0xffffffffu, kmin, 31);
+    R.hi_all = __shfl_sync(0xffffffffu, kmax, 0);
+    return R;
+}
 
 // 0: every key of chunk cc is outside every row's range, 1: inside every row's range,
 // 2: mixed (warp-uniform)
 __device__ __forceinline__ int chunk_kind(const BandRow& R, int cc) {
     const int a = R.k0 + 32 * cc, z = a + 31;
-    if (__all_sync(0xffffffffu, z < R.kmin || a > R.kmax)) return 0;
-    if (__all_sync(0xffffffffu, a >= R.kmin && z <= R.kmax)) return 1;
+    if (z < R.lo_any || a > R.hi_any) return 0;
+    if (a >= R.lo_all && z <= R.hi_all) return 1;
     return 2;
 }
 
-// pass 1: the row max (log2 units; -inf if the row allows no key of the tile)
+// bit i set: key a + i is allowed for this row
+__device__ __forceinline__ uint32_t row_bits(const BandRow& R, int a) {
+    const int lo = max(R.kmin - a, 0), hi = min(R.kmax - a, 31);
+    if (hi < lo) return 0u;
+    const uint32_t upto = hi == 31 ? 0xffffffffu : ((1u << (hi + 1)) - 1u);
+    return upto & ~((1u << lo) - 1u);
+}
+
+// pass 1: the row max (log2 units; -inf if the row allows no key of the band)
 __device__ __forceinline__ float band_row_max(const BandRow& R) {
-    float mt = -INFINITY;
+    float m0 = -INFINITY, m1 = -INFINITY;   // of raw S (scale > 0: scaled once at the end)
 #pragma unroll 1
     for (int cc = 0; cc < R.nch; ++cc) {
         const int kind = chunk_kind(R, cc);
         if (kind == 0) continue;
         uint32_t r[32];
         tmem_ld32(R.tS + cc * 32, r);
-        float m2 = -INFINITY;
         if (kind == 1) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) m2 = fmax3(m2, __uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            m2 *= R.sl2;   // scale > 0: max of raw S, scaled once
+            for (int i = 0; i < 8; ++i) {
+                m0 = fmax3(m0, __uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]));
+                m1 = fmax3(m1, __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+            }
         } else {
-            const int kb = R.k0 + 32 * cc;
+            const uint32_t bits = row_bits(R, R.k0 + 32 * cc);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const bool ok = kb + i >= R.kmin && kb + i <= R.kmax;
-                m2 = fmaxf(m2, ok ? __uint_as_float(r[i]) * R.sl2 : -INFINITY);
+            for (int i = 0; i < 16; ++i) {
+                m0 = fmaxf(m0, (bits >> (2 * i)) & 1u ? __uint_as_float(r[2 * i]) : -INFINITY);
+                m1 = fmaxf(m1, (bits >> (2 * i + 1)) & 1u ? __uint_as_float(r[2 * i + 1]) : -INFINITY);
             }
         }
-        mt = fmaxf(mt, m2);
     }
-    return mt;
+    return fmaxf(m0, m1) * R.sl2;
 }
 
 // pass 2: P = exp2(x - mref) as bf16 pairs over the first 16 nch columns of the row (chunk
@@ -167,7 +189,7 @@ __device__ __forceinline__ float band_row_max(const BandRow& R) {
 // read by this or an earlier chunk); returns the row sum of P
 __device__ __forceinline__ float band_row_exp(const BandRow& R, float mref) {
     const uint64_t sl2x2 = f2_pack(R.sl2, R.sl2), negm2 = f2_pack(-mref, -mref);
-    float sum = 0.f;
+    uint64_t ra = 0, rb = 0;   // two chains of float32 pair sums
 #pragma unroll 1
     for (int cc = 0; cc < R.nch; ++cc) {
         const int kind = chunk_kind(R, cc);
@@ -178,31 +200,31 @@ __device__ __forceinline__ float band_row_exp(const BandRow& R, float mref) {
         } else {
             uint32_t r[32];
             tmem_ld32(R.tS + cc * 32, r);
-            uint64_t rs2 = 0;
-            const int kb = R.k0 + 32 * cc;
+            const uint32_t bits = kind == 1 ? 0xffffffffu : row_bits(R, R.k0 + 32 * cc);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 float x0, x1;
                 f2_unpack(ffma2(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sl2x2, negm2), x0,
                           x1);
-                if (kind == 2) {
-                    x0 = (kb + 2 * i >= R.kmin && kb + 2 * i <= R.kmax) ? x0 : -INFINITY;
-                    x1 = (kb + 2 * i + 1 >= R.kmin && kb + 2 * i + 1 <= R.kmax) ? x1 : -INFINITY;
-                }
+                x0 = (bits >> (2 * i)) & 1u ? x0 : -INFINITY;
+                x1 = (bits >> (2 * i + 1)) & 1u ? x1 : -INFINITY;
                 const uint64_t p2 = f2_pack(ex2(x0), ex2(x1));
-                rs2 = fadd2(rs2, p2);
+                if (i & 1)
+                    rb = fadd2(rb, p2);
+                else
+                    ra = fadd2(ra, p2);
                 float p0, p1;
                 f2_unpack(p2, p0, p1);
                 pk[i] = pack_bf16(p0, p1);
             }
-            float a0, a1;
-            f2_unpack(rs2, a0, a1);
-            sum += a0 + a1;
         }
         tmem_st16_nowait(R.tS + cc * 16, pk);
     }
     tmem_st_wait();
-    return sum;
+    float a0, a1, b0, b1;
+    f2_unpack(ra, a0, a1);
+    f2_unpack(rb, b0, b1);
+    return (a0 + a1) + (b0 + b1);
 }
 
 template <int D>
@@ -444,7 +466,7 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
             }
             tc_fence_after();
             // the whole band in one S: two passes, the row max, then P with it as the reference
-            const BandRow R{tS, sl2, lo * BN, kmin, kmax, n * (BN / 32)};
+            const BandRow R = band_row(tS, sl2, lo * BN, kmin, kmax, n * (BN / 32));
             const float mt = band_row_max(R);
             const float lsum = band_row_exp(R, mt == -INFINITY ? 0.f : mt);
             tc_fence_before();
