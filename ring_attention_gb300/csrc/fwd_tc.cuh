@@ -2,10 +2,11 @@
 // (64, 64), (128, 128) or (128, 64)).
 //
 // Persistent: one CTA per SM (two for the one-tile variant) takes work items from a
-// counter, heaviest first; an item is two consecutive 128-row query tiles of one
-// (batch, q head).  For each item the CTA walks the 128-key tiles the masks (and the
-// batch entry's sequence lengths) allow, folding each into a running (max, numerator,
-// denominator) carry per query row ("bpt.py", _blockwise_attention_fwd / scan_kv_block):
+// counter, heaviest first; an item is two 128-row query tiles: the same rows of two q heads
+// of one kv head (even group sizes), else two consecutive row tiles of one (batch, q head).
+// For each item the CTA walks the 128-key tiles the masks (and the batch entry's sequence
+// lengths) allow, folding each into a running (max, numerator, denominator) carry per query
+// row ("bpt.py", _blockwise_attention_fwd / scan_kv_block):
 //     m' = max(m, rowmax S);  P = exp(S - m');  num = num * exp(m - m') + P V;
 //     den = den * exp(m - m') + rowsum P
 // Both query tiles share every K / V tile that is loaded.
@@ -86,7 +87,8 @@ struct FwdCfg {
 };
 
 struct Tile {
-    int b, h, hkv, q0;       // q0: first row of query tile 0
+    int b, h, hkv, q0;       // h, q0: head and first row of query tile 0
+    int dh, dq;              // query tile 1: head h + dh, first row q0 + dq
     int rlo, rhi;            // key range of this launch (ring super-block or whole sequence)
     int kt0;                 // first key tile visited by the CTA
     int n;                   // key tiles visited by the CTA
@@ -94,21 +96,48 @@ struct Tile {
     int lq, off;             // valid query rows of the batch entry, offset of the causal / window diagonal
 };
 
-// Work item `item` (heaviest causal query pairs first) -> its query tiles and key range.
+// The two query tiles of a work item are the same rows of two q heads that share a kv head
+// when the group size is even (the tiles then see the same key tiles, so neither finishes
+// alone, and a per-head key bias would differ between them, so none may be staged per key
+// tile); otherwise two consecutive row tiles of one q head.
+template <int NQ>
+__host__ __device__ __forceinline__ bool head_pairs(const Problem& P) {
+    return NQ == 2 && P.G % 2 == 0 && (P.bias == nullptr || P.bs[1] == 0);
+}
+
+template <int NQ>
+__host__ __device__ __forceinline__ int fwd_items(const Problem& P) {
+    return head_pairs<NQ>(P) ? ((P.S + BM - 1) / BM) * (P.Hq / 2) * P.B
+                             : ((P.S + NQ * BM - 1) / (NQ * BM)) * P.Hq * P.B;
+}
+
+// Work item `item` (heaviest causal query rows first) -> its query tiles and key range.
 template <int NQ>
 __device__ __forceinline__ Tile decode_tile(const FwdArgs& a, int item) {
     const Problem& P = a.P;
-    const int nqp = (P.S + NQ * BM - 1) / (NQ * BM);
+    const bool hp = head_pairs<NQ>(P);
+    const int per_g = hp ? P.G / 2 : P.G;   // items per (row block, batch entry, kv head)
     int r = item;
-    const int gi = r % P.G;
-    r /= P.G;
+    const int gi = r % per_g;
+    r /= per_g;
     Tile t;
     t.hkv = r % P.Hkv;
     r /= P.Hkv;
     t.b = r % P.B;
-    const int qp = nqp - 1 - r / P.B;   // heaviest (causal) query pairs first
-    t.h = t.hkv * P.G + gi;
-    t.q0 = qp * NQ * BM;
+    if (hp) {
+        const int qt = (P.S + BM - 1) / BM - 1 - r / P.B;   // heaviest (causal) rows first
+        t.h = t.hkv * P.G + 2 * gi;
+        t.q0 = qt * BM;
+        t.dh = 1;
+        t.dq = 0;
+    } else {
+        const int nqp = (P.S + NQ * BM - 1) / (NQ * BM);
+        const int qp = nqp - 1 - r / P.B;
+        t.h = t.hkv * P.G + gi;
+        t.q0 = qp * NQ * BM;
+        t.dh = 0;
+        t.dq = BM;
+    }
     const Lens len = lens_of(P, t.b);   // full lengths unless the problem has sequence lengths
     t.lq = len.lq;
     t.off = len.off;
@@ -124,7 +153,7 @@ __device__ __forceinline__ Tile decode_tile(const FwdArgs& a, int item) {
     int ulo = 1 << 30, uhi = -1;
 #pragma unroll
     for (int i = 0; i < NQ; ++i) {
-        const int qa = t.q0 + i * BM, qb = min(qa + BM - 1, t.lq - 1);
+        const int qa = t.q0 + i * t.dq, qb = min(qa + BM - 1, t.lq - 1);
         int lo = t.rlo, hi = t.rhi;
         if (qa >= t.lq) hi = -1;
         if (P.causal) hi = min(hi, qb + t.off);
@@ -283,8 +312,8 @@ __device__ __forceinline__ float row_exp(const RowCtx& R, float mref) {
 // reference (mt > reference + kTau); otherwise it recomputes P with row_exp.
 template <int BIAS, bool EDGE, bool DROP = false>
 __device__ __forceinline__ float row_exp_1p(const RowCtx& R, float mref, uint32_t (&pk)[BN / 2], float& mt) {
-    uint64_t rs2 = 0;   // two float32 partial sums
-    float mx = -INFINITY;
+    uint64_t ra = 0, rb = 0;   // two chains of float32 pair sums (even / odd pairs)
+    float ma = -INFINITY, mb = -INFINITY;   // and of maxima
     const uint64_t sl2x2 = f2_pack(R.sl2, R.sl2), negm2 = f2_pack(-mref, -mref);
 #pragma unroll
     for (int cc = 0; cc < BN / 32; ++cc) {
@@ -295,6 +324,7 @@ __device__ __forceinline__ float row_exp_1p(const RowCtx& R, float mref, uint32_
             const int col = cc * 32 + 2 * i;
             const float s0 = __uint_as_float(cur[2 * i]), s1 = __uint_as_float(cur[2 * i + 1]);
             float x0, x1;   // x - mref
+            float& mx = (i & 1) ? mb : ma;
             if (!BIAS && !EDGE) {
                 mx = fmax3(mx, s0, s1);   // scale > 0: max of raw S, scaled once
                 f2_unpack(ffma2(f2_pack(s0, s1), sl2x2, negm2), x0, x1);
@@ -309,16 +339,21 @@ __device__ __forceinline__ float row_exp_1p(const RowCtx& R, float mref, uint32_
                 mx = fmax3(mx, x0, x1);
             }
             const uint64_t p2 = f2_pack(ex2(x0), ex2(x1));
-            rs2 = fadd2(rs2, p2);
+            if (i & 1)
+                rb = fadd2(rb, p2);
+            else
+                ra = fadd2(ra, p2);
             float p0, p1;
             f2_unpack(p2, p0, p1);
             pk[cc * 16 + i] = pack_bf16(p0, p1);
         }
     }
+    const float mx = fmaxf(ma, mb);
     mt = (!BIAS && !EDGE) ? mx * R.sl2 : mx + mref;
-    float a, b;
-    f2_unpack(rs2, a, b);
-    return a + b;
+    float a0, a1, b0, b1;
+    f2_unpack(ra, a0, a1);
+    f2_unpack(rb, b0, b1);
+    return (a0 + a1) + (b0 + b1);
 }
 
 // DROP: the attention-dropout instantiation (a separate kernel, so that the softmax of the
@@ -340,7 +375,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
     const Problem& P = a.P;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int* item_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);   // two slots
-    const int n_items = ((P.S + NQ * BM - 1) / (NQ * BM)) * P.Hq * P.B;
+    const int n_items = fwd_items<NQ>(P);
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(C::B_Q), 1);
@@ -417,8 +452,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
                 mbar_expect_tx(BAR(C::B_Q), NQ * C::Q_BYTES);
                 for (int i = 0; i < NQ; ++i)
                     for (int sub = 0; sub < D / 64; ++sub)
-                        tma_load_4d(sb + C::OFF_Q + i * C::Q_BYTES + sub * C::SUB, &tmQ, BAR(C::B_Q), sub * 64, T.h,
-                                    T.q0 + i * BM, T.b);
+                        tma_load_4d(sb + C::OFF_Q + i * C::Q_BYTES + sub * C::SUB, &tmQ, BAR(C::B_Q), sub * 64,
+                                    T.h + i * T.dh, T.q0 + i * T.dq, T.b);
                 ++kw;
                 const float* kbias_src = key_bias ? P.bias + T.b * P.bs[0] + T.h * P.bs[1] : nullptr;
                 bool ok = true;
@@ -606,14 +641,15 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
             const int item = read_item(k, lane == 0);
             if (item >= n_items) break;
             const Tile T = decode_tile<NQ>(a, item);
-            const int q = T.q0 + qt * BM + t;
+            const int q = T.q0 + qt * T.dq + t;
+            const int h = T.h + qt * T.dh;        // q head of this warpgroup's tile
             int kmin = T.rlo, kmax = min(T.rhi, P.S - 1);
             if (P.causal) kmax = min(kmax, q + T.off);
             if (P.wr >= 0) kmax = min(kmax, q + T.off + P.wr);
             if (P.wl >= 0) kmin = max(kmin, q + T.off - P.wl);
             if (q >= T.lq) kmax = -1;             // padding row: nothing allowed
             const float* bias_row =
-                P.bias ? P.bias + T.b * P.bs[0] + T.h * P.bs[1] + static_cast<int64_t>(min(q, P.S - 1)) * P.bs[2]
+                P.bias ? P.bias + T.b * P.bs[0] + h * P.bs[1] + static_cast<int64_t>(min(q, P.S - 1)) * P.bs[2]
                        : nullptr;
             float m_used = -INFINITY, m_true = -INFINITY, lsum = 0.f;
             const int jlo = T.lo[qt], jhi = T.n > 0 ? T.hi[qt] : -1;
@@ -642,7 +678,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
             if constexpr (DROP) {
 #pragma unroll
                 for (int w = 0; w < 4; ++w)
-                    R.keep[w] = dropout_keep32(P.drop_thr, P.drop_k0, P.drop_k1, T.b, T.h, q, k0 + 32 * w);
+                    R.keep[w] = dropout_keep32(P.drop_thr, P.drop_k0, P.drop_k1, T.b, h, q, k0 + 32 * w);
                 mode = 6 + (bias_row ? (key_bias ? 1 : 2) : 0);
             }
             // after the first tile: one pass with the reference the row already has, P kept in
@@ -744,7 +780,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
 
             // -------------------------------------------------------- epilogue
             const int qc = min(q, P.S - 1);
-            const int64_t mi = (static_cast<int64_t>(T.b) * P.Hq + T.h) * P.S + qc;
+            const int64_t mi = (static_cast<int64_t>(T.b) * P.Hq + h) * P.S + qc;
             const bool has_work = jlo <= jhi;
             // with a sink every row takes it here; padding rows of variable-length problems get
             // their m, l reset by a pass after the kernel (their O is 0 either way), which keeps
@@ -758,7 +794,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
                 float m_fin = m_true;
                 float den = lsum;   // softmax denominator relative to m_used
                 if (sink_row) {
-                    const float3 r = with_sink(__ldg(P.sink + T.h), lsum, m_used, m_true);
+                    const float3 r = with_sink(__ldg(P.sink + h), lsum, m_used, m_true);
                     den = r.x;
                     m_fin = r.y;
                     l_true = r.z;
@@ -767,7 +803,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
                 if (!a.acc) {
                     const float inv = den > 0.f ? 1.f / den : 0.f;
                     __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.os[0] +
-                                       static_cast<int64_t>(qc) * P.os[1] + T.h * P.os[2];
+                                       static_cast<int64_t>(qc) * P.os[1] + h * P.os[2];
     #pragma unroll 1
                     for (int cc = 0; cc < DV / 32; ++cc) {
                         uint32_t r[32];
@@ -799,7 +835,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
                     const float mn = fmaxf(mc, m_nat);
                     const float fa = mc == -INFINITY ? 0.f : ex2((mc - mn) * kLog2e);
                     const float fb = m_nat == -INFINITY ? 0.f : ex2((m_nat - mn) * kLog2e) * rel;
-                    float* Cr = a.acc + ((static_cast<int64_t>(T.b) * P.S + qc) * P.Hq + T.h) * DV;
+                    float* Cr = a.acc + ((static_cast<int64_t>(T.b) * P.S + qc) * P.Hq + h) * DV;
     #pragma unroll 1
                     for (int cc = 0; cc < DV / 32; ++cc) {
                         uint32_t r[32];
@@ -825,9 +861,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DV, NQ>::kThreads, NQ == 1 ? 2 : 1)
             } else if (!aborted && !has_work && !a.acc && q < P.S) {
                 // no key allowed for this tile: O = 0, m = -inf, l = 0 (with a sink: m = sink, l = 1)
                 __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.os[0] +
-                                   static_cast<int64_t>(q) * P.os[1] + T.h * P.os[2];
+                                   static_cast<int64_t>(q) * P.os[1] + h * P.os[2];
                 for (int cc = 0; cc < DV; cc += 8) *reinterpret_cast<uint4*>(O + cc) = make_uint4(0, 0, 0, 0);
-                a.m[mi] = sink_row ? __ldg(P.sink + T.h) : -INFINITY;   // only the sink: m = sink, l = 1
+                a.m[mi] = sink_row ? __ldg(P.sink + h) : -INFINITY;   // only the sink: m = sink, l = 1
                 a.l[mi] = sink_row ? 1.f : 0.f;
             }
 
@@ -871,8 +907,7 @@ cudaError_t launch(const FwdArgs& a, const CUtensorMap* maps, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) sm_count[dev] = sms;
     }
-    const int nqp = (a.P.S + NQ * BM - 1) / (NQ * BM);
-    const int64_t items = static_cast<int64_t>(nqp) * a.P.Hq * a.P.B;
+    const int64_t items = fwd_items<NQ>(a.P);
     const int grid = static_cast<int>(std::min<int64_t>(items, static_cast<int64_t>(sms) * (NQ == 1 ? 2 : 1)));
     k_fwd_tc<D, DV, NQ, DROP><<<grid, C::kThreads, C::SMEM, s>>>(maps[0], maps[1], maps[2], a);
     return cudaGetLastError();
