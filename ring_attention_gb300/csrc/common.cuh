@@ -377,6 +377,13 @@ BPA_DEV void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uin
                  : "memory");
 }
 
+// 32 bytes (eight 32-bit words) to global memory in one access; p must be 32-byte aligned.
+BPA_DEV void st_global_v8(void* p, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 BPA_DEV void st_shared_u32(uint32_t addr, uint32_t a) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
 }
