@@ -510,14 +510,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             }
                         } else {
-                            uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+                            uint32_t w[16];
 #pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                dst[i] = make_uint4(
-                                    pack_bf16(__uint_as_float(v[8 * i + 0]) * f, __uint_as_float(v[8 * i + 1]) * f),
-                                    pack_bf16(__uint_as_float(v[8 * i + 2]) * f, __uint_as_float(v[8 * i + 3]) * f),
-                                    pack_bf16(__uint_as_float(v[8 * i + 4]) * f, __uint_as_float(v[8 * i + 5]) * f),
-                                    pack_bf16(__uint_as_float(v[8 * i + 6]) * f, __uint_as_float(v[8 * i + 7]) * f));
+                            for (int i = 0; i < 16; ++i)
+                                w[i] = pack_bf16(__uint_as_float(v[2 * i]) * f, __uint_as_float(v[2 * i + 1]) * f);
+                            if ((reinterpret_cast<uintptr_t>(out) & 31u) == 0) {   // whole 32-byte sectors
+                                st_global_v8(out + c * 32, w);
+                                st_global_v8(out + c * 32 + 16, w + 8);
+                            } else {
+                                uint4* dst = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                            }
                         }
                     }
                 }

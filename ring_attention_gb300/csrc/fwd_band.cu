@@ -482,6 +482,7 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o) + T.b * P.os[0] + static_cast<int64_t>(qc) * P.os[1] +
                                h * P.os[2];
+            const bool al32 = (reinterpret_cast<uintptr_t>(O) & 31u) == 0;
 #pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t r[32];
@@ -492,15 +493,17 @@ __global__ void __launch_bounds__(BandCfg<D>::kThreads, 1)
                     mbar_arrive(BAR(C::B_OE + wg));
                 }
                 if (q < P.S) {
-                    uint4* dst = reinterpret_cast<uint4*>(O + cc * 32);
+                    uint32_t w[16];
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4) {
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(r[v4 * 8 + 0]) * inv, __uint_as_float(r[v4 * 8 + 1]) * inv);
-                        w.y = pack_bf16(__uint_as_float(r[v4 * 8 + 2]) * inv, __uint_as_float(r[v4 * 8 + 3]) * inv);
-                        w.z = pack_bf16(__uint_as_float(r[v4 * 8 + 4]) * inv, __uint_as_float(r[v4 * 8 + 5]) * inv);
-                        w.w = pack_bf16(__uint_as_float(r[v4 * 8 + 6]) * inv, __uint_as_float(r[v4 * 8 + 7]) * inv);
-                        dst[v4] = w;
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack_bf16(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+                    if (al32) {   // whole 32-byte sectors per store
+                        st_global_v8(O + cc * 32, w);
+                        st_global_v8(O + cc * 32 + 16, w + 8);
+                    } else {
+                        uint4* dst = reinterpret_cast<uint4*>(O + cc * 32);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) dst[v4] = make_uint4(w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2], w[4 * v4 + 3]);
                     }
                 }
             }
