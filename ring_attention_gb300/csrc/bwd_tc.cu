@@ -50,8 +50,10 @@ namespace {
 constexpr int D = 128;        // head dim
 constexpr int BK = 128;       // keys per CTA
 constexpr int BQ = 64;        // queries per tile
-constexpr int NS = 4;         // Q / dO stages (measured: three stages plus a second dS^T buffer in
-                              // the freed space made the GQA causal backward 8 % slower)
+constexpr int NS = 4;         // Q / dO stages.  Measured: a second dS^T buffer (so that the softmax
+                              // warps may write tile it while dQ^T(it - 1) still reads the other)
+                              // made the backward slower, 8 % on the GQA causal workload (with three
+                              // stages to make room) and 12 % on the MLA one (four stages)
 constexpr int kThreads = 352;
 constexpr int kSoftmax = 256;    // threads of the two softmax warpgroups
 
