@@ -284,6 +284,17 @@ def test_select_blocks_bit_exact(bpa, ora, dims):
     np.testing.assert_array_equal(idx.cpu().numpy(), ora.select_blocks(q, k, block_size=bs, top_n=n))
 
 
+@pytest.mark.parametrize("dims", [(1, 512, 2, 24, 64, 4, "bf16"),    # blocks of 64 rows: the column kernel
+                                  (1, 256, 3, 7, 16, 3, "bf16"),     # odd head dim: one channel per thread
+                                  (2, 512, 2, 40, 32, 5, "f32")])    # float32 inputs
+def test_select_blocks_bit_exact_sum_paths(bpa, ora, dims):
+    B, S, H, d, bs, n, dt = dims
+    q, k = draw([(B, S, H, d), (B, S, H, d)], 53 + d, dt)
+    idx = bpa.bpa_select_blocks(dev(q), dev(k), block_size=bs, top_n=n)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), ora.select_blocks(q, k, block_size=bs, top_n=n))
+
+
 def test_select_blocks_nan_scores(bpa, ora):
     # a NaN in a key block (every score against it NaN) and one in a query block (all its
     # scores NaN): NaN ranks below every number, and no kernel access leaves its buffers
