@@ -126,6 +126,14 @@ __global__ void k_bwd_pre_bf16v(const BwdArgs a, int zero_dq) {
         const int bh = rr / spad;
         const int h = bh % P.Hq;
         const int b = bh / P.Hq;
+        // the row's saved statistics are fetched first, so that they are in flight together
+        // with O and dO
+        float lv = 0.f, mv = 0.f;
+        if (live && sub == 0 && q < P.S) {
+            const int64_t mi = static_cast<int64_t>(bh) * P.S + q;
+            lv = a.l[mi];
+            mv = a.m[mi];
+        }
         float s = 0.f;
         if (live && q < P.S) {
             const int64_t off = b * P.os[0] + static_cast<int64_t>(q) * P.os[1] + h * P.os[2] + sub * 8;
@@ -145,12 +153,7 @@ __global__ void k_bwd_pre_bf16v(const BwdArgs a, int zero_dq) {
             *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + b * P.qs[0] + static_cast<int64_t>(q) * P.qs[1] +
                                       h * P.qs[2] + sub * 8) = make_uint4(0u, 0u, 0u, 0u);
         if (live && sub == 0) {
-            float lse = INFINITY;
-            if (q < P.S) {
-                const int64_t mi = static_cast<int64_t>(bh) * P.S + q;
-                const float lv = a.l[mi];
-                if (lv > 0.f) lse = a.m[mi] + logf(lv);
-            }
+            const float lse = q < P.S && lv > 0.f ? mv + logf(lv) : INFINITY;
             a.Dvec[r] = q < P.S ? s : 0.f;
             a.lse[r] = lse;
         }
