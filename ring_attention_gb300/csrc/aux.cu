@@ -165,6 +165,14 @@ __global__ void k_bwd_pre_bf16v(const BwdArgs a, int zero_dq) {
         for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4; i += nthreads)
             z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    if (a.hsplit > 1) {   // split band backward: its halves add dK, dV into zeroed (contiguous) dk, dv
+        const int64_t nk = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.d / 8, nv = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.dv / 8;
+        const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+        for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nk + nv; i += nthreads) {
+            uint4* z = i < nk ? static_cast<uint4*>(a.dk) + i : static_cast<uint4*>(a.dv) + (i - nk);
+            *z = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
 }
 
 // float32 [B, S, H, d] accumulator -> bf16 tensor with strides (s0, s1, s2); d % 8 == 0:

@@ -78,6 +78,8 @@ struct BwdArgs {
     float* dq_acc;      // [B, Hq, Spad / 4, d, 4] float32 (four consecutive queries of a channel together);
                         // deterministic mode: one such slice per 128-key tile, [nkt][B, Hq, Spad / 4, d, 4]
     int dq_direct;      // band backward: dQ added in bf16 pairs straight into dq (zeroed by the pre-pass)
+    int hsplit;         // band backward: CTAs per key tile, each taking G / hsplit q heads (1 or 2); with 2
+                        // the halves add dK, dV in bf16 pairs into dk, dv (zeroed by the pre-pass)
     float* dk_acc;      // ring carries / block-selected accumulators [B, S, Hkv, d] float32, or nullptr
     float* dv_acc;
     int ring_idx;

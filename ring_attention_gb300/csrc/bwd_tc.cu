@@ -91,6 +91,7 @@ struct Work {
     int q_lo, q_hi;      // query rows that may see this key tile (ring block included)
     int qt_lo, n_qt, n_it;
     int lk, off;         // valid keys of the batch entry, offset of the causal / window diagonal
+    int g0, gn;          // q heads of the group this CTA walks: g0 .. g0 + gn - 1
 };
 
 // The work of key tile kt of (batch b, kv head hkv): the query rows that may see it.
@@ -118,6 +119,8 @@ __device__ __forceinline__ Work decode_tile_of(const BwdArgs& a, int b, int hkv,
     w.q_hi = hi;
     w.qt_lo = lo / BQ;
     w.n_qt = lo <= hi ? hi / BQ - w.qt_lo + 1 : 0;
+    w.g0 = 0;
+    w.gn = P.G;
     w.n_it = w.n_qt * P.G;
     return w;
 }
@@ -127,14 +130,22 @@ __device__ __forceinline__ Work decode_tile_of(const BwdArgs& a, int b, int hkv,
 // tiles and dQ accumulator rows in L2 (DRAM traffic 953 -> 426 / 534 MB per launch on the GQA
 // causal workload) but balance the causal work worse (+5 % / +1.5 % time); the kernel is
 // tensor-bound, so the interleaved order stays.
+// With a head split, CTA pairs (2 r, 2 r + 1) share key tile r and take one half of the group's
+// q heads each (the band backward: shorter, equal CTAs fill the last wave better).
 __device__ __forceinline__ Work decode(const BwdArgs& a) {
     const Problem& P = a.P;
-    int r = blockIdx.x;
+    const int hs = a.hsplit > 1 ? 2 : 1;
+    int r = blockIdx.x / hs;
+    const int half = blockIdx.x % hs;
     const int b = r % P.B;
     r /= P.B;
     const int hkv = r % P.Hkv;
     const int kt = r / P.Hkv;
-    return decode_tile_of(a, b, hkv, kt);
+    Work w = decode_tile_of(a, b, hkv, kt);
+    w.gn = P.G / hs;
+    w.g0 = half * w.gn;
+    w.n_it = w.n_qt * w.gn;
+    return w;
 }
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
@@ -202,8 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Query tiles from the last one down, the group's q heads innermost: the CTAs of one
     // (batch, kv head) then walk the same query tiles at about the same time, so a Q / dO
     // tile and its dQ accumulator rows are fetched once into L2 and shared.
-    auto iter_head = [&](int it) { return W.hkv * P.G + it % P.G; };
-    auto iter_q0 = [&](int it) { return (W.qt_lo + W.n_qt - 1 - it / P.G) * BQ; };
+    auto iter_head = [&](int it) { return W.hkv * P.G + W.g0 + it % W.gn; };
+    auto iter_q0 = [&](int it) { return (W.qt_lo + W.n_qt - 1 - it / W.gn) * BQ; };
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
@@ -516,7 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
                                 w[i] = pack_bf16(__uint_as_float(v[2 * i]) * f, __uint_as_float(v[2 * i + 1]) * f);
-                            if ((reinterpret_cast<uintptr_t>(out) & 31u) == 0) {   // whole 32-byte sectors
+                            if (DQBF && a.hsplit > 1) {
+                                // two halves add into the zeroed dk / dv: 0 + x + y in either order
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) red_add_bf16x2(out + c * 32 + 2 * i, w[i]);
+                            } else if ((reinterpret_cast<uintptr_t>(out) & 31u) == 0) {   // whole 32-byte sectors
                                 st_global_v8(out + c * 32, w);
                                 st_global_v8(out + c * 32 + 16, w + 8);
                             } else {
@@ -640,7 +655,7 @@ cudaError_t launch_bwd_tc_band(const BwdArgs& a, const CUtensorMap* maps, cudaSt
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
     const int nkt = (a.P.S + BK - 1) / BK;
-    const int grid = nkt * a.P.Hkv * a.P.B;
+    const int grid = nkt * a.P.Hkv * a.P.B * (a.hsplit > 1 ? 2 : 1);
     k_bwd_tc<128, false, false, true><<<grid, kThreads, L::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
     return cudaGetLastError();
 }
