@@ -468,17 +468,20 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
         marks.mark(3, s);
         return e == cudaSuccess ? BPA_OK : cuda_fail(e, "backward launch");
     }
+    // With contiguous, 16-byte aligned dk / dv the q heads of a group are split over two CTAs
+    // per key tile, which add their dK, dV halves into dk, dv (zeroed by the pre-pass): exactly
+    // two contributions per element, so the result does not depend on their order.
+    const bool kv_dense = P.ks[2] == P.d && P.ks[1] == static_cast<int64_t>(P.Hkv) * P.d &&
+                          P.ks[0] == static_cast<int64_t>(P.S) * P.Hkv * P.d && P.vs[2] == P.dv &&
+                          P.vs[1] == static_cast<int64_t>(P.Hkv) * P.dv &&
+                          P.vs[0] == static_cast<int64_t>(P.S) * P.Hkv * P.dv &&
+                          ((reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15u) == 0;
+    const int split_kv = kv_dense && P.G % 2 == 0 && P.d % 8 == 0 && P.dv % 8 == 0 ? 2 : 1;
     if (n == 1 && bwd_band_supported(P)) {
-        // band: the pre-pass zeroes dq, the main kernel adds dQ into it directly.  With
-        // contiguous, 16-byte aligned dk / dv the q heads of a group are split over two CTAs
-        // per key tile, which add their dK, dV halves into dk, dv (zeroed by the pre-pass too).
+        // band: the pre-pass zeroes dq, the main kernel adds dQ into it directly (dK, dV split
+        // as below)
         a.dq_direct = 1;
-        const bool kv_dense = P.ks[2] == P.d && P.ks[1] == static_cast<int64_t>(P.Hkv) * P.d &&
-                              P.ks[0] == static_cast<int64_t>(P.S) * P.Hkv * P.d && P.vs[2] == P.dv &&
-                              P.vs[1] == static_cast<int64_t>(P.Hkv) * P.dv &&
-                              P.vs[0] == static_cast<int64_t>(P.S) * P.Hkv * P.dv &&
-                              ((reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15u) == 0;
-        a.hsplit = kv_dense && P.G % 2 == 0 && P.d % 8 == 0 && P.dv % 8 == 0 ? 2 : 1;
+        a.hsplit = split_kv;
         if ((e = launch_bwd_pre(a, s)) != cudaSuccess) return cuda_fail(e, "backward pre-pass");
         marks.mark(1, s);
         if ((e = launch_bwd_tc_band(a, maps, s)) != cudaSuccess) return cuda_fail(e, "backward launch");
@@ -487,6 +490,9 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
         return BPA_OK;
     }
     a.dq_acc = reinterpret_cast<float*>(ws + L.dq);
+    // (measured: with four q heads per group the half-length CTAs lost 8 %, with sixteen they
+    // gained 4 %; the ring steps carry dK, dV in float32 instead)
+    a.hsplit = n == 1 && P.G >= 8 ? split_kv : 1;
     if ((e = launch_bwd_pre(a, s)) != cudaSuccess || (P.dsink && (e = launch_sink_grad(a, s)) != cudaSuccess))
             return cuda_fail(e, "backward pre-pass");
     marks.mark(1, s);

@@ -66,6 +66,19 @@ __global__ void k_ring_finalize(const FwdArgs a) {
 }
 
 // one warp per (b, h, q) row of the padded [B, Hq, Spad] statistics
+// A backward split over two CTAs per key tile adds its dK, dV halves (bf16 pairs) into dk, dv,
+// which must start at zero (contiguous bf16 [B, S, Hkv, d] and [.., dv], 16-byte aligned).
+__device__ __forceinline__ void zero_split_kv(const BwdArgs& a) {
+    if (a.hsplit <= 1) return;
+    const Problem& P = a.P;
+    const int64_t nk = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.d / 8, nv = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.dv / 8;
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nk + nv; i += nthreads) {
+        uint4* z = i < nk ? static_cast<uint4*>(a.dk) + i : static_cast<uint4*>(a.dv) + (i - nk);
+        *z = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 template <typename T>
 __global__ void k_bwd_pre(const BwdArgs a, int zero_dq) {
     const Problem& P = a.P;
@@ -103,6 +116,7 @@ __global__ void k_bwd_pre(const BwdArgs a, int zero_dq) {
         for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4; i += stride)
             z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    zero_split_kv(a);
 }
 
 // bf16 rows, d % 8 == 0 and d / 8 a power of two (<= 32): each thread loads 16 bytes
@@ -165,14 +179,7 @@ __global__ void k_bwd_pre_bf16v(const BwdArgs a, int zero_dq) {
         for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4; i += nthreads)
             z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (a.hsplit > 1) {   // split band backward: its halves add dK, dV into zeroed (contiguous) dk, dv
-        const int64_t nk = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.d / 8, nv = static_cast<int64_t>(P.B) * P.S * P.Hkv * P.dv / 8;
-        const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-        for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nk + nv; i += nthreads) {
-            uint4* z = i < nk ? static_cast<uint4*>(a.dk) + i : static_cast<uint4*>(a.dv) + (i - nk);
-            *z = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
+    zero_split_kv(a);
 }
 
 // float32 [B, S, H, d] accumulator -> bf16 tensor with strides (s0, s1, s2); d % 8 == 0:

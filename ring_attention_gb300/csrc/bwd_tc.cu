@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
                                 w[i] = pack_bf16(__uint_as_float(v[2 * i]) * f, __uint_as_float(v[2 * i + 1]) * f);
-                            if (DQBF && a.hsplit > 1) {
+                            if (a.hsplit > 1) {
                                 // two halves add into the zeroed dk / dv: 0 + x + y in either order
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) red_add_bf16x2(out + c * 32 + 2 * i, w[i]);
@@ -575,7 +575,7 @@ cudaError_t launch_dv(const BwdArgs& a, const CUtensorMap* maps, cudaStream_t s)
         if (dev >= 0 && dev < 64) configured[var][dev] = true;
     }
     const int nkt = (a.P.S + BK - 1) / BK;
-    const int grid = nkt * a.P.Hkv * a.P.B;
+    const int grid = nkt * a.P.Hkv * a.P.B * (a.hsplit > 1 ? 2 : 1);
     kern<<<grid, kThreads, L::SMEM, s>>>(maps[0], maps[1], maps[2], maps[3], a);
     return cudaGetLastError();
 }
