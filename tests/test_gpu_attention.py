@@ -166,6 +166,45 @@ def test_band_backward(bpa, ora, case, bias_kind):
     assert torch.equal(dq, dq2) and torch.equal(dk, dk2) and torch.equal(dv, dv2)
 
 
+SPLIT_CASES = [  # (B, S, Hq, Hkv, d), mask: groups of eight or more q heads split over two CTAs
+    ((1, 300, 16, 2, 128), dict(causal=True, window=(-1, -1))),
+    ((2, 257, 8, 1, 128), dict(causal=True, window=(100, 0))),    # the band backward
+    ((1, 600, 8, 1, 128), dict(causal=True, window=(300, 0))),
+    ((1, 384, 16, 1, 128), dict(causal=False, window=(-1, -1))),
+]
+
+
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda c: "x".join(map(str, c[0])) + "_" + _mask_id(c[1]))
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_backward_head_split(bpa, ora, case, deterministic):
+    # a kv head with at least eight q heads: two CTAs per key tile take half the heads each and
+    # add their dK, dV halves in bf16 pairs into the zeroed dk, dv (two contributions, so the
+    # result is repeatable); a strided dk / dv view keeps the single-CTA path
+    shape, mask = case
+    q, k, v, do = _inputs(shape, 97 + shape[1])
+    tq, tk, tv, tdo = dev(q), dev(k), dev(v), dev(do)
+    o, m, l = bpa.bpa_fwd(tq, tk, tv, **mask)
+    dq, dk, dv = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, deterministic=deterministic, **mask)
+    dq2, dk2, dv2 = bpa.bpa_bwd(tq, tk, tv, o, tdo, m, l, deterministic=deterministic, **mask)
+    # k, v (and so dk, dv) as views with a row stride of 2 d: not contiguous, no split
+    big_k = torch.zeros(shape[0], shape[1], shape[3], 2 * shape[4], dtype=tk.dtype, device=tk.device)
+    big_v = torch.zeros_like(big_k)
+    big_k[..., :shape[4]] = tk
+    big_v[..., :shape[4]] = tv
+    _, dk3, dv3 = bpa.bpa_bwd(tq, big_k[..., :shape[4]], big_v[..., :shape[4]], o, tdo, m, l,
+                              deterministic=deterministic, **mask)
+    torch.cuda.synchronize()
+    rq, rk, rv, *_ = ora.attention_bwd(q, k, v, do, **mask)
+    assert rel_l2(host(dq), rq) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dk), rk) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dv), rv) <= BF16_GRAD_REL_L2
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    if deterministic:
+        assert torch.equal(dq, dq2)
+    assert rel_l2(host(dk3), rk) <= BF16_GRAD_REL_L2
+    assert rel_l2(host(dv3), rv) <= BF16_GRAD_REL_L2
+
+
 def _general_bias(kind, B, Hq, S, seed):
     # bpt.py's bias takes each dim as 1 (broadcast) or full: a bias that depends on the
     # query position ([B, Hq, S, S] or a per-row [B, 1, S, 1]) reaches the backward
