@@ -312,10 +312,11 @@ __device__ __forceinline__ int warp_best(const K* key, const unsigned char* take
     return bj;
 }
 
-// One warp per (b, h, query block i).  Shared memory per warp: keys[nblk] 64-bit words (the
-// 32-bit keys of the lower bounds L_j, then the 64-bit rank keys of the candidates' contract
-// scores), up[nblk] floats (the upper bounds U_j), taken[nblk] bytes, and the query
-// block's float32 sums q32[d].
+// One warp per (b, h, query block i); a CTA of nw warps takes query blocks nw y .. nw y + nw - 1
+// of one (b, h) = blockIdx.x.  Shared memory per warp: keys[nblk] 64-bit words (the 32-bit keys
+// of the lower bounds L_j, then the 64-bit rank keys of the candidates' contract scores),
+// up[nblk] floats (the upper bounds U_j), taken[nblk] bytes, and the query block's float32 sums
+// q32[d]; per CTA the staged tile of float32 key sums.
 __global__ void __launch_bounds__(kSelMaxWarps * 32) k_select(const SelectArgs a) {
     extern __shared__ long long sm_all[];
     const int nblk = a.S / a.block;
