@@ -212,6 +212,8 @@ __global__ void __launch_bounds__(Geom<NW>::QB_F * NW * 32) k_gather_fwd(const F
         const int kb = S.list[x];
         bool selected = false;
         for (int y = 0; y < P.top_n; ++y) selected |= selrow[y] == kb;
+        // a selected block wholly before query block i with no window bounds: no key is masked
+        const bool full = !DROP && selected && kb < i && P.wl < 0 && P.wr < 0;
         // stage K and V of the block: 32 rows x 8 chunks of 16 B each, 8 chunks per lane
         __syncwarp();
 #pragma unroll
@@ -262,6 +264,16 @@ __global__ void __launch_bounds__(Geom<NW>::QB_F * NW * 32) k_gather_fwd(const F
             for (int hh = 0; hh < 2; ++hh) {
                 const int q = BS * i + mt * 16 + g + hh * 8;
                 float mx = -INFINITY;
+                if (full) {   // a selected block wholly before the query block: every key allowed
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float v = s[mt][nt][hh * 2 + e] * sl2;
+                            s[mt][nt][hh * 2 + e] = v;
+                            mx = fmaxf(mx, v);
+                        }
+                } else {
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     uint32_t dw[2] = {0u, 0u};   // draws of keys (e = 0, 1), dropout only
@@ -281,6 +293,7 @@ __global__ void __launch_bounds__(Geom<NW>::QB_F * NW * 32) k_gather_fwd(const F
                         s[mt][nt][hh * 2 + e] = v;
                         mx = fmaxf(mx, v);
                     }
+                }
                 }
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -552,6 +565,8 @@ __global__ void __launch_bounds__(Geom<NW>::QB_B * NW * 32) k_gather_bwd(const B
         const int kb = W.list[x];
         bool selected = false;
         for (int y = 0; y < P.top_n; ++y) selected |= selrow[y] == kb;
+        // a selected block wholly before query block i with no window bounds: no key is masked
+        const bool full = !DROP && selected && kb < i && P.wl < 0 && P.wr < 0;
         __syncwarp();   // the previous block's reads of K, V and the P / dS tiles are done
         stage_rows(sk, K + static_cast<int64_t>(BS) * kb * P.ks[1], P.ks[1], lane);
         stage_rows(sv, V + static_cast<int64_t>(BS) * kb * P.vs[1], P.vs[1], lane);
@@ -574,6 +589,16 @@ __global__ void __launch_bounds__(Geom<NW>::QB_B * NW * 32) k_gather_bwd(const B
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int q = BS * i + mt * 16 + g + hh * 8;
+                if (full) {   // a selected block wholly before the query block: every key allowed
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float p = ex2(s[mt][nt][hh * 2 + e] * sl2 - lse2[mt][hh]);
+                            s[mt][nt][hh * 2 + e] = p;
+                            dp[mt][nt][hh * 2 + e] = p * (dp[mt][nt][hh * 2 + e] - Drow[mt][hh]);
+                        }
+                } else {
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     uint32_t dw[2] = {0u, 0u};   // draws of keys (e = 0, 1), dropout only
@@ -592,6 +617,7 @@ __global__ void __launch_bounds__(Geom<NW>::QB_B * NW * 32) k_gather_bwd(const B
                         s[mt][nt][hh * 2 + e] = p;
                         dp[mt][nt][hh * 2 + e] = p * (dp[mt][nt][hh * 2 + e] - Drow[mt][hh]);
                     }
+                }
                 }
             }
         store_tile32(sp, s, lane);
