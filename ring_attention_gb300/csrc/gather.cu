@@ -147,7 +147,7 @@ __device__ int visit_list(const Problem& P, int64_t unit, int i, int* list) {
 
 // DROP: the attention-dropout instantiation (dropped entries leave the softmax)
 template <int NW, bool DROP>
-__global__ void __launch_bounds__(Geom<NW>::QB_F * NW * 32) k_gather_fwd(const FwdArgs a) {
+__global__ void __launch_bounds__(Geom<NW>::QB_F * NW * 32, NW == 1 ? 3 : 1) k_gather_fwd(const FwdArgs a) {
     using G = Geom<NW>;
     const Problem& P = a.P;
     extern __shared__ __align__(128) uint8_t gsm[];
