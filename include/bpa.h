@@ -204,7 +204,7 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l,
  * dq, dk, dv have the dtype of the inputs and the strides of q, k, v; o and
  * dout are [B, S, Hq, dv] with o_strides.  dq, dk, dv must not overlap any input:
  * some paths zero them first and add partial results into them (narrow windows: dq;
- * contiguous dk, dv with eight or more q heads per kv head, or narrow windows: dk, dv,
+ * contiguous dk, dv with narrow windows or with eight or more q heads per kv head: dk, dv,
  * from two CTAs per key tile, so the two-term sums are the same on every call).
  * Block-selected mode (ring_size 1) is supported: the selection is held
  * fixed ("AnnAttention", faiss_block_attention.py, which trains through the
