@@ -393,6 +393,18 @@ bpa_status bpa_fwd(const bpa_attn_desc* desc, void* o, float* m, float* l, void*
     return BPA_OK;
 }
 
+// SMs of the current device (cached per device; 1 if it cannot be read)
+static int sm_count_current() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) return 1;
+    if (dev >= 0 && dev < 64) cached[dev] = sms;
+    return sms;
+}
+
 bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, const float* m, const float* l,
                    void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
     const NvtxRange range("bpa_bwd");
@@ -476,7 +488,13 @@ bpa_status bpa_bwd(const bpa_attn_desc* desc, const void* o, const void* dout, c
                           P.vs[1] == static_cast<int64_t>(P.Hkv) * P.dv &&
                           P.vs[0] == static_cast<int64_t>(P.S) * P.Hkv * P.dv &&
                           ((reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 15u) == 0;
-    const int split_kv = kv_dense && P.G % 2 == 0 && P.d % 8 == 0 && P.dv % 8 == 0 ? 2 : 1;
+    // ... and only where the halves fill the last wave better: ceil(2 c / sms) < 2 ceil(c / sms)
+    // for c key-tile CTAs (measured: at B 1 of the sliding-window workload, 256 CTAs in two
+    // waves either way, the split cost 8 %)
+    const int sms = sm_count_current();
+    const int64_t ctas = static_cast<int64_t>((P.S + 127) / 128) * P.Hkv * P.B;
+    const bool fills = (2 * ctas + sms - 1) / sms < 2 * ((ctas + sms - 1) / sms);
+    const int split_kv = kv_dense && fills && P.G % 2 == 0 && P.d % 8 == 0 && P.dv % 8 == 0 ? 2 : 1;
     if (n == 1 && bwd_band_supported(P)) {
         // band: the pre-pass zeroes dq, the main kernel adds dQ into it directly (dK, dV split
         // as below)
